@@ -1,0 +1,417 @@
+"""Benchmark of the fused MoE layer (forward + backward) on GB300.
+
+One step = forward + backward of the whole layer (routing, dispatch, gate/up +
+SwiGLU, down + combine, and the backward's dgrads, wgrads, router gradient and
+un-permute) over one batch of synthetic inputs already resident in HBM.
+Prints one JSON line.  ``--impl reference`` times the CPU oracle instead.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    torchrun --nproc-per-node N bench.py --gpus N ...   (independent replicas)
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth_inputs as si  # noqa: E402
+
+METRIC = "MoE layer fwd+bwd tokens/s and TFLOP/s on 1×GB300 (% of tensor-core peak)"
+DEFAULT_WORKLOAD = "qwen3_235b"
+
+# algorithmic FLOPs per launch of each GEMM kernel (P = T*k rows)
+def gemm_flops(sh):
+    P, T, H, F, E = sh.P, sh.T, sh.H, sh.F, sh.E
+    return {
+        "router_gemm_topk": 2 * T * H * E,
+        "gate_up_gemm_swiglu": 4 * P * H * F,
+        "down_gemm_scatter": 2 * P * F * H,
+        "down_dgrad_swiglu_bwd": 2 * P * H * F,
+        "down_wgrad": 2 * P * F * H,
+        "gate_up_dgrad_scatter": 4 * P * H * F,
+        "gate_up_wgrad": 4 * P * H * F,
+        "router_wgrad": 2 * T * H * E,
+    }
+
+
+# algorithmic bytes per launch of the memory-bound kernels
+def kernel_bytes(sh):
+    P, T, H, k = sh.P, sh.T, sh.H, sh.top_k
+    row = 2 * H
+    return {
+        "gather_x": T * row + P * row + 4 * P,
+        "gather_dy": T * row + P * row + 4 * P,
+        "combine": P * row + T * row,
+        "unpermute_dx": P * row + T * row + 8 * P,
+    }
+
+
+def layer_flops(sh):
+    fwd = 6 * sh.P * sh.H * sh.F + 2 * sh.T * sh.H * sh.E
+    bwd = 12 * sh.P * sh.H * sh.F + 4 * sh.T * sh.H * sh.E
+    return fwd, bwd
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[3 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available() and args.impl == "ours":
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample_time(sh, inp_cpu, n_tokens: int):
+    """Times the CPU oracle (as it stands) on the first n_tokens tokens of the
+    workload: routing, forward and the full backward (expert weight
+    gradients are computed expert by expert and dropped)."""
+    from oracle import moe_oracle as mo
+    x = inp_cpu["x"][:n_tokens]
+    dY = inp_cpu["dY"][:n_tokens]
+    t0 = time.perf_counter()
+    g = mo.backward(x, inp_cpu["W_r"], inp_cpu["W_gate"], inp_cpu["W_up"], inp_cpu["W_down"],
+                    sh.top_k, dY, logit_bias=inp_cpu["logit_bias"], keep_weight_grads=False)
+    dt = time.perf_counter() - t0
+    assert np.isfinite(g["dx"]).all()
+    return dt
+
+
+def host_copy_for_oracle(inp):
+    """fp32 numpy copies of the (bf16) inputs; the oracle widens them to fp64."""
+    out = {}
+    for k in ("x", "W_r", "W_gate", "W_up", "W_down", "dY"):
+        out[k] = inp[k].float().cpu().numpy()
+    out["logit_bias"] = None if inp["logit_bias"] is None else inp["logit_bias"].cpu().numpy()
+    return out
+
+
+def blas_threads() -> int:
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(sh, inp, budget_s: float = 20.0):
+    """Oracle throughput on a bounded sample of the same workload."""
+    inp_cpu = host_copy_for_oracle(inp)
+    n = 8
+    dt = oracle_sample_time(sh, inp_cpu, n)
+    # grow the sample to about budget_s / 2 of work, then time it once more
+    target = int(n * max(1.0, (budget_s / 2) / max(dt, 1e-3)))
+    n2 = max(n, min(sh.T, target))
+    if n2 > n:
+        n, dt = n2, oracle_sample_time(sh, inp_cpu, n2)
+    return {"value": n / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"first {n} of {sh.T} tokens of {sh.name}: route + fwd + full bwd in "
+                      f"numpy fp64 ({dt:.1f} s)"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, sh, world, rank, local):
+    from mixture_experts_layer_17_gb300 import (MoeLayer, moe_launch_count, moe_profile_enable,
+                                                moe_profile_read)
+    dev = torch.device("cuda", local)
+    shr = si.shape(sh.name) if sh.name in si.WORKLOADS else sh
+    import dataclasses
+    shr = dataclasses.replace(shr, seed=shr.seed + 1000 * rank) if rank else shr
+    inp = si.make_inputs(shr, dev)
+    layer = MoeLayer(sh.T, sh.H, sh.F, sh.E, sh.top_k, sh.precision, device=dev)
+    grads = {"dx": torch.empty_like(inp["x"]), "dW_r": torch.empty_like(inp["W_r"]),
+             "dW_gate": torch.empty_like(inp["W_gate"]), "dW_up": torch.empty_like(inp["W_up"]),
+             "dW_down": torch.empty_like(inp["W_down"])}
+    y = torch.empty_like(inp["x"])
+    W = (inp["W_r"], inp["W_gate"], inp["W_up"], inp["W_down"])
+
+    def step(x, dY):
+        layer.forward(x, W[0], W[1], W[2], W[3], inp["logit_bias"], y=y)
+        layer.backward(x, W[0], W[1], W[2], W[3], dY, grads=grads)
+
+    for _ in range(args.warmup):
+        step(inp["x"], inp["dY"])
+    torch.cuda.synchronize()
+    assert layer.device_status("fwd") == 0 and layer.device_status("bwd") == 0
+
+    # ---- device-resident timed region (per-kernel events recorded live)
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    moe_profile_read()
+    moe_profile_enable(True)
+    launches0 = moe_launch_count()
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        layer.forward(inp["x"], W[0], W[1], W[2], W[3], inp["logit_bias"], y=y)
+        ev[i][1].record(stream)
+        layer.backward(inp["x"], W[0], W[1], W[2], W[3], inp["dY"], grads=grads)
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    launches = moe_launch_count() - launches0
+    moe_profile_enable(False)
+    prof = moe_profile_read()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    ms_per_step = total_ms / args.steps
+    assert layer.device_status("fwd") == 0 and layer.device_status("bwd") == 0
+
+    # ---- end to end through the API with pinned host buffers
+    hx = inp["x"].cpu().pin_memory()
+    hdY = inp["dY"].cpu().pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    hdx = torch.empty_like(hx).pin_memory()
+    dx_dev = torch.empty_like(inp["x"])
+    dY_dev = torch.empty_like(inp["dY"])
+    x_dev = torch.empty_like(inp["x"])
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        x_dev.copy_(hx, non_blocking=True)
+        dY_dev.copy_(hdY, non_blocking=True)
+        layer.forward(x_dev, W[0], W[1], W[2], W[3], inp["logit_bias"], y=y)
+        layer.backward(x_dev, W[0], W[1], W[2], W[3], dY_dev, grads=grads)
+        hy.copy_(y, non_blocking=True)
+        hdx.copy_(grads["dx"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+
+    fwd_fl, bwd_fl = layer_flops(sh)
+    flops = gemm_flops(sh)
+    byts = kernel_bytes(sh)
+    peaks = load_peaks()
+    kernels = {name: {"launches": n, "avg_ms": ms / max(n, 1), "share": None}
+               for name, (n, ms) in prof.items()}
+    ktotal = sum(v["avg_ms"] * v["launches"] for v in kernels.values())
+    for v in kernels.values():
+        v["share"] = v["avg_ms"] * v["launches"] / ktotal if ktotal else None
+    dom = max(kernels, key=lambda n: kernels[n]["avg_ms"] * kernels[n]["launches"])
+    if dom in flops:
+        ach = flops[dom] / (kernels[dom]["avg_ms"] * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak,
+                "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                "peak_source": f"{peaks['source']} bf16 sustained"}
+    else:
+        ach = byts.get(dom, 0) / (kernels[dom]["avg_ms"] * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                "frac": ach / peak, "traffic": None, "peak_source": f"{peaks['source']} hbm"}
+    per_kernel = {}
+    for name, v in sorted(kernels.items(), key=lambda kv: -kv[1]["share"]):
+        d = {"launches": v["launches"], "avg_ms": round(v["avg_ms"], 4),
+             "share": round(v["share"], 4)}
+        if name in flops:
+            d["tflops"] = round(flops[name] / (v["avg_ms"] * 1e-3) / 1e12, 1)
+            d["frac_bf16_sustained"] = round(d["tflops"] / peaks["bf16_tflops_sustained"], 3)
+        if name in byts:
+            d["gbs"] = round(byts[name] / (v["avg_ms"] * 1e-3) / 1e9, 1)
+            d["frac_hbm"] = round(d["gbs"] / peaks["hbm_gbs"], 3)
+        per_kernel[name] = d
+
+    tokens_per_s = world * sh.T / (ms_per_step * 1e-3)
+    line = {
+        "metric": METRIC,
+        "value": tokens_per_s,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, random init)",
+        "config": {"workload": sh.name, "T": sh.T, "H": sh.H, "F": sh.F, "E": sh.E,
+                   "top_k": sh.top_k, "precision": sh.precision,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (no flush): weights and activations exceed 129 MB"},
+        "tflops": world * (fwd_fl + bwd_fl) / (ms_per_step * 1e-3) / 1e12,
+        "fwd_ms": fwd_ms,
+        "bwd_ms": bwd_ms,
+        "full_layer_ms": 2 * fwd_ms + bwd_ms,
+        "full_layer_tflops": (2 * fwd_fl + bwd_fl) / ((2 * fwd_ms + bwd_ms) * 1e-3) / 1e12,
+        "frac_bf16_sustained": (fwd_fl + bwd_fl) / (ms_per_step * 1e-3) / 1e12
+        / peaks["bf16_tflops_sustained"],
+        "clocks": clk,
+        "e2e": {"value": world * sh.T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * hx.numel() * 2, "d2h_bytes_per_step": 2 * hx.numel() * 2},
+        "gpu_launches": launches,
+        "roofline": roof,
+        "kernels": per_kernel,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(sh, inp, args.cpu_budget)
+    return line
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args, sh, world, rank):
+    """The CPU oracle timed on the host cores, each step a bounded sample."""
+    if rank != 0:
+        return None
+    inp = si.make_inputs(sh, "cpu")
+    inp_cpu = host_copy_for_oracle(inp)
+    n = 8
+    dt = oracle_sample_time(sh, inp_cpu, n)
+    per_step_budget = max(1.0, args.cpu_budget / max(1, args.steps + args.warmup))
+    n = max(8, min(sh.T, int(n * per_step_budget / max(dt, 1e-3))))
+    for _ in range(args.warmup):
+        oracle_sample_time(sh, inp_cpu, n)
+    times = [oracle_sample_time(sh, inp_cpu, n) for _ in range(args.steps)]
+    sec = sum(times) / len(times)
+    value = n / sec
+    sample = f"first {n} of {sh.T} tokens of {sh.name} per step: route + fwd + full bwd, numpy fp64"
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": sh.name, "T": sh.T, "H": sh.H, "F": sh.F,
+                                        "E": sh.E, "top_k": sh.top_k, "precision": sh.precision},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(si.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    sh = si.shape(args.workload)
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        line = run_reference(args, sh, world, rank)
+    else:
+        line = run_ours(args, sh, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

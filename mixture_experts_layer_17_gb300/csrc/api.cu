@@ -1,0 +1,742 @@
+// C ABI of libmoe (declared in include/moe.h): argument validation, workspace
+// layout, TMA descriptor creation and the launch sequences of the routing,
+// forward and backward passes.  Host code only; all arithmetic runs in the
+// kernels of gemm_*.cu and elementwise.cu.
+#include <atomic>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kernels.h"
+#include "moe.h"
+
+namespace {
+
+using namespace moe;
+
+// ---------------------------------------------------------------- device info
+
+struct DevInfo {
+  bool queried = false;
+  bool supported = false;
+  int sms = 0;
+};
+
+std::mutex g_dev_mu;
+DevInfo g_dev[64];
+
+moe_status_t current_device(DevInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.queried) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);
+    d.sms = sms;
+    d.queried = true;
+  }
+  *out = d;
+  return d.supported ? MOE_OK : MOE_ERR_UNSUPPORTED_DEVICE;
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major matrix [rows, cols] with the given row
+// stride; boxes of box_rows x box_cols (box_cols * 2 = 128 bytes) with the
+// 128-byte swizzle.  Reads outside the matrix return zeros.
+bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+              uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------- profiling
+
+struct Pending {
+  const char* name;
+  cudaEvent_t start;
+  cudaEvent_t stop;
+};
+struct Totals {
+  int64_t launches = 0;
+  double ms = 0.0;
+};
+
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<Pending> g_pending;
+std::map<std::string, Totals> g_totals;
+std::vector<std::string> g_names;   // storage behind names handed out by moe_profile_read
+std::atomic<int64_t> g_launches{0};
+
+// Runs one kernel launch: optional profiling events, launch counting, and
+// (with MOE_FLAG_SYNC_CHECK) a synchronising error check.
+template <class Fn>
+moe_status_t run(const char* name, cudaStream_t s, uint32_t flags, Fn&& fn) {
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  bool prof;
+  {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    prof = g_prof_on;
+  }
+  if (prof) {
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    cudaEventRecord(e0, s);
+  }
+  cudaError_t err = fn();
+  g_launches.fetch_add(1);
+  if (prof) {
+    cudaEventRecord(e1, s);
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_pending.push_back({name, e0, e1});
+  }
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  if (flags & MOE_FLAG_SYNC_CHECK) {
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+#define MOE_TRY(expr)                 \
+  do {                                \
+    moe_status_t _st = (expr);        \
+    if (_st != MOE_OK) return _st;    \
+  } while (0)
+
+// ---------------------------------------------------------------- layout
+
+constexpr uint64_t kNormalWaitNs = 2000000000ull;   // 2 s: no legitimate wait comes close
+constexpr uint64_t kTestWaitNs = 20000000ull;       // 20 ms for MOE_FLAG_TEST_TIMEOUT
+
+size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
+
+struct Carver {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t at = off;
+    off = align256(off + bytes);
+    return at;
+  }
+};
+
+int next_pow2_at_least16(int v) {
+  int p = 16;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+struct Layout {
+  int64_t T, P, T_pad;
+  int H, F, E, k;
+  int ntiles;        // router tiles of 128 tokens
+  int router_bn;     // N of the router GEMM (power of two >= E, >= 16)
+  int dgrad_bn;      // N tile of the down dgrad (256 if F % 256 == 0, else 128)
+  int nparts;        // dw partials per row = F / dgrad_bn
+  int wr_split, wr_kbps, wr_mtiles, wr_ntiles;
+  // forward / route workspace
+  size_t f_status, f_hist, f_base, f_a, f_scratch;
+  size_t r_wrt, r_row_slot, r_w_row, r_mtile, r_order, f_total;
+  // context
+  size_t c_idx, c_w, c_counts, c_offsets, c_perm, c_slot, c_row_slot, c_w_row, c_mtile,
+      c_order, c_wrt, c_xperm, c_h, c_total;
+  // backward workspace
+  size_t b_status, b_dyp, b_dh, b_aw, b_dwp, b_dl, b_dlt, b_scratch, b_wrp, b_total;
+};
+
+Layout make_layout(const moe_config_t& c, int sms) {
+  Layout L;
+  L.T = c.T;
+  L.H = c.H;
+  L.F = c.F;
+  L.E = c.E;
+  L.k = c.top_k;
+  L.P = L.T * L.k;
+  L.T_pad = (L.T + 7) / 8 * 8;
+  L.ntiles = static_cast<int>((L.T + kBM - 1) / kBM);
+  L.router_bn = next_pow2_at_least16(L.E);
+  L.dgrad_bn = (L.F % 256 == 0) ? 256 : 128;
+  L.nparts = L.F / L.dgrad_bn;
+  L.wr_mtiles = (L.E + kBM - 1) / kBM;
+  L.wr_ntiles = L.H / 256;
+  const int total_kb = static_cast<int>((L.T + kBK - 1) / kBK);
+  int split = sms / (L.wr_mtiles * L.wr_ntiles);
+  split = split < 1 ? 1 : (split > total_kb ? total_kb : split);
+  L.wr_kbps = (total_kb + split - 1) / split;
+  L.wr_split = (total_kb + L.wr_kbps - 1) / L.wr_kbps;
+  const size_t P = static_cast<size_t>(L.P), T = static_cast<size_t>(L.T);
+  const size_t H = L.H, F = L.F, E = L.E;
+
+  Carver f;
+  L.f_status = f.take(sizeof(DeviceStatus));
+  L.f_hist = f.take(sizeof(int) * L.ntiles * E);
+  L.f_base = f.take(sizeof(int) * L.ntiles * E);
+  L.r_wrt = f.take(2 * E * H);
+  L.r_row_slot = f.take(sizeof(int) * P);
+  L.r_w_row = f.take(sizeof(float) * P);
+  L.r_mtile = f.take(sizeof(int) * (E + 1));
+  L.r_order = f.take(sizeof(int) * E);
+  L.f_a = f.take(2 * P * F);
+  L.f_scratch = f.take(2 * P * H);
+  L.f_total = f.off;
+
+  Carver x;
+  L.c_idx = x.take(sizeof(int) * P);
+  L.c_w = x.take(sizeof(float) * P);
+  L.c_counts = x.take(sizeof(int) * E);
+  L.c_offsets = x.take(sizeof(int) * (E + 1));
+  L.c_perm = x.take(sizeof(int) * P);
+  L.c_slot = x.take(sizeof(int) * P);
+  L.c_row_slot = x.take(sizeof(int) * P);
+  L.c_w_row = x.take(sizeof(float) * P);
+  L.c_mtile = x.take(sizeof(int) * (E + 1));
+  L.c_order = x.take(sizeof(int) * E);
+  L.c_wrt = x.take(2 * E * H);
+  L.c_xperm = x.take(2 * P * H);
+  L.c_h = x.take(2 * P * 2 * F);
+  L.c_total = x.off;
+
+  Carver b;
+  L.b_status = b.take(sizeof(DeviceStatus));
+  L.b_dyp = b.take(2 * P * H);
+  L.b_dh = b.take(2 * P * 2 * F);
+  L.b_aw = b.take(2 * P * F);
+  L.b_dwp = b.take(sizeof(float) * P * L.nparts);
+  L.b_dl = b.take(sizeof(float) * P);
+  L.b_dlt = b.take(2 * E * static_cast<size_t>(L.T_pad));
+  L.b_scratch = b.take(2 * P * H);
+  L.b_wrp = b.take(sizeof(float) * L.wr_split * E * H);
+  L.b_total = b.off;
+  (void)T;
+  return L;
+}
+
+moe_status_t validate(const moe_config_t* c) {
+  if (c == nullptr) return MOE_ERR_INVALID_ARG;
+  if (c->flags & ~(MOE_FLAG_SYNC_CHECK | MOE_FLAG_TEST_TIMEOUT)) return MOE_ERR_INVALID_ARG;
+  if (c->precision < MOE_BF16 || c->precision > MOE_FP8_BWD) return MOE_ERR_INVALID_ARG;
+  if (c->T < 1 || c->H < 256 || c->H % 256 != 0 || c->H > 65536 || c->F < 128 ||
+      c->F % 128 != 0 || c->F > 65536 || c->E < 1 || c->E > 256 || c->top_k < 1 ||
+      c->top_k > 16 || c->top_k > c->E)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->T * static_cast<int64_t>(c->top_k) >= (static_cast<int64_t>(1) << 31) - 256)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+template <class T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+GemmArgs base_args(DeviceStatus* st, uint32_t flags) {
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.status = st;
+  a.wait_limit_ns = kNormalWaitNs;
+  a.flags = 0;
+  (void)flags;
+  return a;
+}
+
+int grid_for(int64_t tiles, int sms) {
+  if (tiles < 1) return 1;
+  return static_cast<int>(tiles < sms ? tiles : sms);
+}
+
+}  // namespace
+
+namespace {
+
+struct RouteBufs {
+  const uint16_t* x;
+  const uint16_t* W_r;
+  const float* bias;
+  float* logits;
+  int* idx;
+  float* w;
+  int* counts;
+  int* offsets;
+  int* perm;
+  int* slot;
+  int* row_slot;
+  float* w_row;
+  int* mtile;
+  int* order;
+  uint16_t* wrt;
+  int* hist;
+  int* base;
+  DeviceStatus* st;
+};
+
+// F1-F5: router GEMM with the fused top-k epilogue, expert scan, permutation.
+moe_status_t run_routing(const moe_config_t& c, const Layout& L, const RouteBufs& b, int sms,
+                         cudaStream_t s) {
+  MOE_TRY(run("transpose_router_weight", s, c.flags,
+              [&] { return launch_transpose_bf16(b.W_r, b.wrt, L.H, L.E, s); }));
+  GemmArgs a = base_args(b.st, c.flags);
+  if (!make_map(&a.mapA, b.x, L.H, L.T, 2ull * L.H, 64, 128) ||
+      !make_map(&a.mapB0, b.wrt, L.H, L.E, 2ull * L.H, 64, L.router_bn))
+    return MOE_ERR_CUDA;
+  a.mapB1 = a.mapB0;
+  a.M = static_cast<int>(L.T);
+  a.N = L.router_bn;
+  a.K = L.H;
+  a.n_tiles = 1;
+  a.in0 = b.bias;
+  a.out0 = b.logits;
+  a.out1 = b.idx;
+  a.out2 = b.w;
+  a.out3 = b.hist;
+  a.E = L.E;
+  a.top_k = L.k;
+  a.T = L.T;
+  MOE_TRY(run("router_gemm_topk", s, c.flags, [&] {
+    return launch_router_fwd(L.router_bn, a, grid_for(L.ntiles, sms), s);
+  }));
+  MOE_TRY(run("expert_scan", s, c.flags, [&] {
+    return launch_scan(b.hist, L.ntiles, L.E, b.counts, b.offsets, b.base, b.mtile, b.order, s);
+  }));
+  MOE_TRY(run("permute", s, c.flags, [&] {
+    return launch_permute(b.idx, b.w, b.base, L.T, L.k, L.E, b.perm, b.slot, b.row_slot,
+                          b.w_row, s);
+  }));
+  return MOE_OK;
+}
+
+int64_t grouped_m_tile_bound(const Layout& L) { return (L.P + kBM - 1) / kBM + L.E; }
+
+bool all_aligned16(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (p == nullptr || !aligned(p, 16)) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t st) {
+  switch (st) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_UNSUPPORTED_DEVICE: return "MOE_ERR_UNSUPPORTED_DEVICE";
+    case MOE_ERR_NOT_IMPLEMENTED: return "MOE_ERR_NOT_IMPLEMENTED";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* fwd_ws, size_t* ctx_bytes,
+                                size_t* bwd_ws) {
+  MOE_TRY(validate(cfg));
+  DevInfo d;
+  MOE_TRY(current_device(&d));
+  const Layout L = make_layout(*cfg, d.sms);
+  if (fwd_ws) *fwd_ws = L.f_total;
+  if (ctx_bytes) *ctx_bytes = L.c_total;
+  if (bwd_ws) *bwd_ws = L.b_total;
+  return MOE_OK;
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const moe_bf16_t* x, const moe_bf16_t* W_r,
+                       const float* logit_bias, float* logits, int32_t* topk_idx, float* topk_w,
+                       int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* slot_row,
+                       void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  if (!all_aligned16({x, W_r}) || topk_idx == nullptr || topk_w == nullptr ||
+      counts == nullptr || offsets == nullptr || perm_token == nullptr || slot_row == nullptr ||
+      ws == nullptr || !aligned(ws, 256) || !aligned(logit_bias, 4) || !aligned(logits, 4))
+    return MOE_ERR_INVALID_ARG;
+  DevInfo d;
+  MOE_TRY(current_device(&d));
+  const Layout L = make_layout(*cfg, d.sms);
+  if (ws_bytes < L.f_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DeviceStatus* st = at<DeviceStatus>(ws, L.f_status);
+  if (cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s) != cudaSuccess) return MOE_ERR_CUDA;
+  RouteBufs b{x, W_r, logit_bias, logits, topk_idx, topk_w, counts, offsets, perm_token,
+              slot_row, at<int>(ws, L.r_row_slot), at<float>(ws, L.r_w_row),
+              at<int>(ws, L.r_mtile), at<int>(ws, L.r_order), at<uint16_t>(ws, L.r_wrt),
+              at<int>(ws, L.f_hist), at<int>(ws, L.f_base), st};
+  return run_routing(*cfg, L, b, d.sms, s);
+}
+
+moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe_bf16_t* W_r,
+                         const float* logit_bias, const moe_bf16_t* W_gate,
+                         const moe_bf16_t* W_up, const moe_bf16_t* W_down, moe_bf16_t* y,
+                         void* ctx, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->precision == MOE_MXFP8) return MOE_ERR_NOT_IMPLEMENTED;
+  if (!all_aligned16({x, W_r, W_gate, W_up, W_down, y}) || ctx == nullptr || ws == nullptr ||
+      !aligned(ctx, 256) || !aligned(ws, 256) || !aligned(logit_bias, 4))
+    return MOE_ERR_INVALID_ARG;
+  DevInfo d;
+  MOE_TRY(current_device(&d));
+  const Layout L = make_layout(*cfg, d.sms);
+  if (ws_bytes < L.f_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint32_t fl = cfg->flags;
+  DeviceStatus* st = at<DeviceStatus>(ws, L.f_status);
+  if (cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  int* idx = at<int>(ctx, L.c_idx);
+  int* offsets = at<int>(ctx, L.c_offsets);
+  int* slot = at<int>(ctx, L.c_slot);
+  int* row_slot = at<int>(ctx, L.c_row_slot);
+  float* w_row = at<float>(ctx, L.c_w_row);
+  int* mtile = at<int>(ctx, L.c_mtile);
+  uint16_t* xperm = at<uint16_t>(ctx, L.c_xperm);
+  uint16_t* h = at<uint16_t>(ctx, L.c_h);
+  uint16_t* act = at<uint16_t>(ws, L.f_a);
+  uint16_t* scratch = at<uint16_t>(ws, L.f_scratch);
+
+  RouteBufs b{x, W_r, logit_bias, nullptr, idx, at<float>(ctx, L.c_w),
+              at<int>(ctx, L.c_counts), offsets, at<int>(ctx, L.c_perm), slot, row_slot,
+              w_row, mtile, at<int>(ctx, L.c_order), at<uint16_t>(ctx, L.c_wrt),
+              at<int>(ws, L.f_hist), at<int>(ws, L.f_base), st};
+  MOE_TRY(run_routing(*cfg, L, b, d.sms, s));
+
+  // F6: dispatch x to the expert-major rows
+  MOE_TRY(run("gather_x", s, fl,
+              [&] { return launch_gather_rows(x, slot, xperm, L.T, L.H, L.k, s); }));
+
+  // F7 + F8: gate/up GEMM with SwiGLU
+  {
+    GemmArgs a = base_args(st, fl);
+    if (!make_map(&a.mapA, xperm, L.H, L.P, 2ull * L.H, 64, 128) ||
+        !make_map(&a.mapB0, W_gate, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 64) ||
+        !make_map(&a.mapB1, W_up, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 64))
+      return MOE_ERR_CUDA;
+    a.K = L.H;
+    a.N = 2 * L.F;
+    a.n_tiles = L.F / 128;
+    a.num_groups = L.E;
+    a.b_group_rows = L.H;
+    a.offsets = offsets;
+    a.mtile_off = mtile;
+    a.out0 = act;
+    a.out1 = h;
+    a.ld0 = L.F;
+    if (fl & MOE_FLAG_TEST_TIMEOUT) {
+      a.flags = 2u;
+      a.wait_limit_ns = kTestWaitNs;
+    }
+    const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
+    MOE_TRY(run("gate_up_gemm_swiglu", s, fl, [&] { return launch_gate_up_fwd(a, grid, s); }));
+  }
+  // F9 + F10: down GEMM with the weighted scatter, then the k-way combine
+  {
+    GemmArgs a = base_args(st, fl);
+    if (!make_map(&a.mapA, act, L.F, L.P, 2ull * L.F, 64, 128) ||
+        !make_map(&a.mapB0, W_down, L.H, static_cast<uint64_t>(L.E) * L.F, 2ull * L.H, 64, 64))
+      return MOE_ERR_CUDA;
+    a.mapB1 = a.mapB0;
+    a.K = L.F;
+    a.N = L.H;
+    a.n_tiles = L.H / 256;
+    a.num_groups = L.E;
+    a.b_group_rows = L.F;
+    a.offsets = offsets;
+    a.mtile_off = mtile;
+    a.in0 = w_row;
+    a.in1 = row_slot;
+    a.out0 = scratch;
+    a.ld0 = L.H;
+    const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
+    MOE_TRY(run("down_gemm_scatter", s, fl, [&] { return launch_down_fwd(a, grid, s); }));
+  }
+  MOE_TRY(run("combine", s, fl, [&] { return launch_combine(scratch, y, L.T, L.H, L.k, s); }));
+  return MOE_OK;
+}
+
+moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const moe_bf16_t* W_r,
+                          const moe_bf16_t* W_gate, const moe_bf16_t* W_up,
+                          const moe_bf16_t* W_down, const void* ctx_in, const moe_bf16_t* dY,
+                          moe_bf16_t* dx, moe_bf16_t* dW_r, moe_bf16_t* dW_gate,
+                          moe_bf16_t* dW_up, moe_bf16_t* dW_down, void* ws, size_t ws_bytes,
+                          moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->precision != MOE_BF16) return MOE_ERR_NOT_IMPLEMENTED;
+  if (!all_aligned16({x, W_r, W_gate, W_up, W_down, dY, dx, dW_r, dW_gate, dW_up, dW_down}) ||
+      ctx_in == nullptr || ws == nullptr || !aligned(ctx_in, 256) || !aligned(ws, 256))
+    return MOE_ERR_INVALID_ARG;
+  DevInfo d;
+  MOE_TRY(current_device(&d));
+  const Layout L = make_layout(*cfg, d.sms);
+  if (ws_bytes < L.b_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint32_t fl = cfg->flags;
+  void* ctx = const_cast<void*>(ctx_in);
+  DeviceStatus* st = at<DeviceStatus>(ws, L.b_status);
+  if (cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  const int* idx = at<int>(ctx, L.c_idx);
+  const float* w = at<float>(ctx, L.c_w);
+  const int* offsets = at<int>(ctx, L.c_offsets);
+  const int* slot = at<int>(ctx, L.c_slot);
+  const int* row_slot = at<int>(ctx, L.c_row_slot);
+  const float* w_row = at<float>(ctx, L.c_w_row);
+  const int* mtile = at<int>(ctx, L.c_mtile);
+  const int* order = at<int>(ctx, L.c_order);
+  const uint16_t* wrt = at<uint16_t>(ctx, L.c_wrt);
+  const uint16_t* xperm = at<uint16_t>(ctx, L.c_xperm);
+  const uint16_t* h = at<uint16_t>(ctx, L.c_h);
+  uint16_t* dyp = at<uint16_t>(ws, L.b_dyp);
+  uint16_t* dh = at<uint16_t>(ws, L.b_dh);
+  uint16_t* aw = at<uint16_t>(ws, L.b_aw);
+  float* dwp = at<float>(ws, L.b_dwp);
+  float* dl = at<float>(ws, L.b_dl);
+  uint16_t* dlt = at<uint16_t>(ws, L.b_dlt);
+  uint16_t* scratch = at<uint16_t>(ws, L.b_scratch);
+  float* wrp = at<float>(ws, L.b_wrp);
+  (void)W_r;
+
+  // B1: dispatch dY to the expert-major rows
+  MOE_TRY(run("gather_dy", s, fl,
+              [&] { return launch_gather_rows(dY, slot, dyp, L.T, L.H, L.k, s); }));
+
+  // B2-B4: down dgrad with the SwiGLU backward and router-weight partials
+  {
+    GemmArgs a = base_args(st, fl);
+    if (!make_map(&a.mapA, dyp, L.H, L.P, 2ull * L.H, 64, 128) ||
+        !make_map(&a.mapB0, W_down, L.H, static_cast<uint64_t>(L.E) * L.F, 2ull * L.H, 64,
+                  L.dgrad_bn))
+      return MOE_ERR_CUDA;
+    a.mapB1 = a.mapB0;
+    a.K = L.H;
+    a.N = L.F;
+    a.n_tiles = L.nparts;
+    a.num_groups = L.E;
+    a.b_group_rows = L.F;
+    a.offsets = offsets;
+    a.mtile_off = mtile;
+    a.in0 = h;
+    a.in1 = w_row;
+    a.out0 = dh;
+    a.out1 = aw;
+    a.out2 = dwp;
+    a.ld0 = L.F;
+    if (fl & MOE_FLAG_TEST_TIMEOUT) {
+      a.flags = 2u;
+      a.wait_limit_ns = kTestWaitNs;
+    }
+    const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
+    MOE_TRY(run("down_dgrad_swiglu_bwd", s, fl,
+                [&] { return launch_down_dgrad(L.dgrad_bn, a, grid, s); }));
+  }
+  // B9: router softmax / top-k backward
+  if (cudaMemsetAsync(dlt, 0, 2ull * L.E * L.T_pad, s) != cudaSuccess) return MOE_ERR_CUDA;
+  MOE_TRY(run("router_bwd", s, fl, [&] {
+    return launch_router_bwd(dwp, L.nparts, slot, w, idx, L.T, L.k, dl, dlt, L.T_pad, s);
+  }));
+  // B5: down wgrad over ragged K
+  {
+    GemmArgs a = base_args(st, fl);
+    if (!make_map(&a.mapA, aw, L.F, L.P, 2ull * L.F, 64, 64) ||
+        !make_map(&a.mapB0, dyp, L.H, L.P, 2ull * L.H, 64, 64))
+      return MOE_ERR_CUDA;
+    a.mapB1 = a.mapB0;
+    a.M = L.F;
+    a.N = L.H;
+    a.m_tiles = L.F / 128;
+    a.n_tiles = L.H / 256;
+    a.num_groups = L.E;
+    a.offsets = offsets;
+    a.group_order = order;
+    a.out0 = dW_down;
+    a.ld0 = L.H;
+    const int grid = grid_for(static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles, d.sms);
+    MOE_TRY(run("down_wgrad", s, fl, [&] { return launch_down_wgrad(a, grid, s); }));
+  }
+  // B6 + B7: gate/up dgrad with the scatter, then the un-permute (+ router dgrad)
+  {
+    GemmArgs a = base_args(st, fl);
+    if (!make_map(&a.mapA, dh, 2ull * L.F, L.P, 4ull * L.F, 64, 128) ||
+        !make_map(&a.mapB0, W_gate, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 256) ||
+        !make_map(&a.mapB1, W_up, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 256))
+      return MOE_ERR_CUDA;
+    a.K = 2 * L.F;
+    a.k_half = L.F;
+    a.N = L.H;
+    a.n_tiles = L.H / 256;
+    a.num_groups = L.E;
+    a.b_group_rows = L.H;
+    a.offsets = offsets;
+    a.mtile_off = mtile;
+    a.in1 = row_slot;
+    a.out0 = scratch;
+    a.ld0 = L.H;
+    const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
+    MOE_TRY(run("gate_up_dgrad_scatter", s, fl, [&] { return launch_gate_up_dgrad(a, grid, s); }));
+  }
+  MOE_TRY(run("unpermute_dx", s, fl, [&] {
+    return launch_unpermute(scratch, dl, idx, wrt, dx, L.T, L.H, L.k, s);
+  }));
+  // B8: gate/up wgrad over ragged K
+  {
+    GemmArgs a = base_args(st, fl);
+    if (!make_map(&a.mapA, xperm, L.H, L.P, 2ull * L.H, 64, 64) ||
+        !make_map(&a.mapB0, dh, 2ull * L.F, L.P, 4ull * L.F, 64, 64))
+      return MOE_ERR_CUDA;
+    a.mapB1 = a.mapB0;
+    a.M = L.H;
+    a.N = 2 * L.F;
+    a.m_tiles = L.H / 128;
+    a.n_tiles = (2 * L.F) / 256;
+    a.num_groups = L.E;
+    a.offsets = offsets;
+    a.group_order = order;
+    a.out0 = dW_gate;
+    a.out1 = dW_up;
+    a.ld0 = L.F;
+    const int grid = grid_for(static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles, d.sms);
+    MOE_TRY(run("gate_up_wgrad", s, fl, [&] { return launch_gate_up_wgrad(a, grid, s); }));
+  }
+  // B10: router weight gradient dW_r = x^T dl (split-K, then reduce + transpose)
+  {
+    GemmArgs a = base_args(st, fl);
+    if (!make_map(&a.mapA, dlt, L.T, L.E, 2ull * L.T_pad, 64, 128) ||
+        !make_map(&a.mapB0, x, L.H, L.T, 2ull * L.H, 64, 64))
+      return MOE_ERR_CUDA;
+    a.mapB1 = a.mapB0;
+    a.M = L.E;
+    a.N = L.H;
+    a.K = static_cast<int>(L.T);
+    a.m_tiles = L.wr_mtiles;
+    a.n_tiles = L.wr_ntiles;
+    a.k_split = L.wr_split;
+    a.kb_per_split = L.wr_kbps;
+    a.out0 = wrp;
+    a.ld0 = L.H;
+    const int grid =
+        grid_for(static_cast<int64_t>(L.wr_split) * L.wr_mtiles * L.wr_ntiles, d.sms);
+    MOE_TRY(run("router_wgrad", s, fl, [&] { return launch_router_wgrad(a, grid, s); }));
+  }
+  MOE_TRY(run("router_wgrad_reduce", s, fl,
+              [&] { return launch_wr_reduce(wrp, L.wr_split, L.E, L.H, dW_r, s); }));
+  return MOE_OK;
+}
+
+moe_status_t moe_gemm_bf16(int64_t M, int64_t N, int64_t K, const moe_bf16_t* A, int a_kmajor,
+                           const moe_bf16_t* B, int b_kmajor, float* D, void* ws,
+                           size_t ws_bytes, moe_stream_t stream) {
+  if (M < 1 || K < 1 || N < 256 || N % 256 != 0 || M >= (1ll << 31) || N >= (1ll << 31) ||
+      K >= (1ll << 31))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  const int64_t a_row = a_kmajor ? K : M;
+  const int64_t b_row = b_kmajor ? K : N;
+  if (a_row % 8 != 0 || b_row % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!all_aligned16({A, B, D}) || ws == nullptr || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < sizeof(DeviceStatus)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  DevInfo d;
+  MOE_TRY(current_device(&d));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DeviceStatus* st = static_cast<DeviceStatus*>(ws);
+  if (cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s) != cudaSuccess) return MOE_ERR_CUDA;
+  GemmArgs a = base_args(st, 0);
+  const bool ok_a = a_kmajor ? make_map(&a.mapA, A, K, M, 2ull * K, 64, 128)
+                             : make_map(&a.mapA, A, M, K, 2ull * M, 64, 64);
+  const bool ok_b = b_kmajor ? make_map(&a.mapB0, B, K, N, 2ull * K, 64, 256)
+                             : make_map(&a.mapB0, B, N, K, 2ull * N, 64, 64);
+  if (!ok_a || !ok_b) return MOE_ERR_CUDA;
+  a.mapB1 = a.mapB0;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.n_tiles = static_cast<int>(N / 256);
+  a.out0 = D;
+  a.ld0 = static_cast<int>(N);
+  const int64_t tiles = ((M + kBM - 1) / kBM) * a.n_tiles;
+  return run("dense_gemm", s, 0, [&] {
+    return launch_dense(!a_kmajor, !b_kmajor, a, grid_for(tiles, d.sms), s);
+  });
+}
+
+moe_status_t moe_get_device_status(const void* ws, moe_stream_t stream) {
+  if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int code = 0;
+  if (cudaMemcpyAsync(&code, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  return static_cast<moe_status_t>(code);
+}
+
+void moe_profile_enable(int on) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof_on = on != 0;
+}
+
+int moe_profile_read(const char** names, int64_t* launches, double* total_ms, int cap) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  for (const Pending& p : g_pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(p.stop) == cudaSuccess &&
+        cudaEventElapsedTime(&ms, p.start, p.stop) == cudaSuccess) {
+      Totals& t = g_totals[p.name];
+      t.launches += 1;
+      t.ms += ms;
+    }
+    cudaEventDestroy(p.start);
+    cudaEventDestroy(p.stop);
+  }
+  g_pending.clear();
+  g_names.clear();
+  for (const auto& kv : g_totals) g_names.push_back(kv.first);
+  int n = 0;
+  for (const auto& kv : g_totals) {
+    if (n < cap) {
+      if (names) names[n] = g_names[n].c_str();
+      if (launches) launches[n] = kv.second.launches;
+      if (total_ms) total_ms[n] = kv.second.ms;
+    }
+    ++n;
+  }
+  g_totals.clear();
+  return n;
+}
+
+int64_t moe_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

@@ -1,0 +1,310 @@
+// Memory-bound kernels of the MoE layer: expert counts and offsets (scan),
+// the deterministic expert-major permutation, the token -> row gathers
+// (dispatch of x and dY), the k-way combine, the router softmax/top-k
+// backward, the un-permute with the router's input gradient, and two small
+// transposes.  Every index result is deterministic.
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+// ---------------------------------------------------------------- transpose
+
+// out[c, r] = in[r, c] for a bf16 matrix [rows, cols]
+__global__ void transpose_bf16_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out,
+                                      int rows, int cols) {
+  __shared__ uint16_t tile[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) tile[i][threadIdx.x] = in[static_cast<int64_t>(r) * cols + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int c = c0 + i, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) out[static_cast<int64_t>(c) * rows + r] = tile[threadIdx.x][i];
+  }
+}
+
+// ---------------------------------------------------------------- F3/F4: scan
+
+// One block of 256 threads (thread = expert).  From the per-tile histograms
+// hist[tiles, E] it writes counts[E], offsets[E+1] (exclusive prefix sum),
+// block_base[tiles, E] (first row of each tile's tokens inside each expert's
+// segment), mtile_off[E+1] (prefix of ceil(count / 128), the grouped-GEMM
+// m-tiles) and group_order[E] (experts by descending count, ties by id).
+__global__ void scan_kernel(const int* __restrict__ hist, int ntiles, int E,
+                            int* __restrict__ counts, int* __restrict__ offsets,
+                            int* __restrict__ block_base, int* __restrict__ mtile_off,
+                            int* __restrict__ group_order) {
+  __shared__ int s_cnt[256];
+  __shared__ int s_off[257];
+  __shared__ int s_mt[257];
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < E) {
+    for (int b = 0; b < ntiles; ++b) {
+      const int h = hist[static_cast<int64_t>(b) * E + e];
+      block_base[static_cast<int64_t>(b) * E + e] = run;
+      run += h;
+    }
+  }
+  s_cnt[e] = (e < E) ? run : 0;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0, acc_mt = 0;
+    for (int i = 0; i < E; ++i) {
+      s_off[i] = acc;
+      s_mt[i] = acc_mt;
+      acc += s_cnt[i];
+      acc_mt += (s_cnt[i] + 127) / 128;
+    }
+    s_off[E] = acc;
+    s_mt[E] = acc_mt;
+  }
+  __syncthreads();
+  if (e < E) {
+    counts[e] = run;
+    offsets[e] = s_off[e];
+    mtile_off[e] = s_mt[e];
+    for (int b = 0; b < ntiles; ++b) block_base[static_cast<int64_t>(b) * E + e] += s_off[e];
+    int rank = 0;
+    for (int i = 0; i < E; ++i) rank += (s_cnt[i] > run) || (s_cnt[i] == run && i < e);
+    group_order[rank] = e;
+  }
+  if (e == 0) {
+    offsets[E] = s_off[E];
+    mtile_off[E] = s_mt[E];
+  }
+}
+
+// ---------------------------------------------------------------- F5: permutation
+
+// Block = the 128 tokens of one router tile.  A (token, slot) pair routed to
+// expert e goes to row block_base[tile, e] + (number of earlier tokens of the
+// tile routed to e); per-warp lane masks give that count without atomics on
+// global memory, so rows are expert-major with ascending token inside an
+// expert.
+__global__ void permute_kernel(const int* __restrict__ idx, const float* __restrict__ w,
+                               const int* __restrict__ block_base, int64_t T, int k, int E,
+                               int* __restrict__ perm_token, int* __restrict__ slot_row,
+                               int* __restrict__ row_slot, float* __restrict__ w_row) {
+  __shared__ unsigned mask[4][256];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < 4 * 256; i += blockDim.x) (&mask[0][0])[i] = 0u;
+  __syncthreads();
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * 128 + tid;
+  const bool valid = t < T;
+  if (valid)
+    for (int j = 0; j < k; ++j) atomicOr(&mask[warp][idx[t * k + j]], 1u << lane);
+  __syncthreads();
+  if (!valid) return;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int j = 0; j < k; ++j) {
+    const int e = idx[t * k + j];
+    int before = __popc(mask[warp][e] & lt);
+    for (int q = 0; q < warp; ++q) before += __popc(mask[q][e]);
+    const int r = block_base[static_cast<int64_t>(blockIdx.x) * E + e] + before;
+    perm_token[r] = static_cast<int>(t);
+    slot_row[t * k + j] = r;
+    row_slot[r] = static_cast<int>(t * k + j);
+    w_row[r] = w[t * k + j];
+  }
+}
+
+// ---------------------------------------------------------------- F6/B1: dispatch
+
+// dst[slot_row[t, j]] = src[t] for every slot j: one warp per token reads the
+// token's row once (16-byte vectors) and writes its k copies.
+__global__ void gather_rows_kernel(const uint16_t* __restrict__ src, const int* __restrict__ slot_row,
+                                   uint16_t* __restrict__ dst, int64_t T, int H, int k) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int lane = threadIdx.x & 31;
+  int64_t rows[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) rows[j] = (j < k) ? static_cast<int64_t>(slot_row[t * k + j]) * H : 0;
+  const uint16_t* s = src + t * H;
+  const int nchunks = H >> 3;
+#pragma unroll 4
+  for (int c = lane; c < nchunks; c += 32) {
+    const uint4 v = ld_global_nc_v4(s + c * 8);
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (j < k) st_global_v4(dst + rows[j] + c * 8, v.x, v.y, v.z, v.w);
+  }
+}
+
+MOE_DEV void add_bf16x8(const uint4& v, float (&acc)[8], float scale = 1.0f) {
+  float a, b;
+  unpack_bf16x2(v.x, a, b); acc[0] = fmaf(scale, a, acc[0]); acc[1] = fmaf(scale, b, acc[1]);
+  unpack_bf16x2(v.y, a, b); acc[2] = fmaf(scale, a, acc[2]); acc[3] = fmaf(scale, b, acc[3]);
+  unpack_bf16x2(v.z, a, b); acc[4] = fmaf(scale, a, acc[4]); acc[5] = fmaf(scale, b, acc[5]);
+  unpack_bf16x2(v.w, a, b); acc[6] = fmaf(scale, a, acc[6]); acc[7] = fmaf(scale, b, acc[7]);
+}
+
+// ---------------------------------------------------------------- F10: combine
+
+// y[t] = sum_j scratch[t*k + j]; scratch rows already carry the router weight.
+__global__ void combine_kernel(const uint16_t* __restrict__ scratch, uint16_t* __restrict__ y,
+                               int64_t T, int H, int k) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int cpr = H >> 3;
+  if (i >= T * cpr) return;
+  const int64_t t = i / cpr;
+  const int c = static_cast<int>(i - t * cpr) * 8;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const uint16_t* base = scratch + t * k * H + c;
+  for (int j = 0; j < k; ++j) add_bf16x8(ld_global_nc_v4(base + static_cast<int64_t>(j) * H), acc);
+  st_global_v4(y + t * H + c, pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+               pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+}
+
+// ---------------------------------------------------------------- B9: router backward
+
+// dw[t, j] = sum of the down-dgrad epilogue partials of row slot_row[t, j];
+// dl[t, j] = w_j (dw_j - sum_i w_i dw_i) (gradient of the renormalised softmax
+// at the selected logits); dlT[e, t] = dl for the dense router weight GEMM.
+__global__ void router_bwd_kernel(const float* __restrict__ dw_part, int nparts,
+                                  const int* __restrict__ slot_row, const float* __restrict__ w,
+                                  const int* __restrict__ idx, int64_t T, int k,
+                                  float* __restrict__ dl, uint16_t* __restrict__ dlT, int64_t T_pad) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  float dwv[16], wv[16];
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    dwv[j] = 0.f;
+    wv[j] = 0.f;
+    if (j < k) {
+      const int64_t r = slot_row[t * k + j];
+      float d = 0.f;
+      for (int n = 0; n < nparts; ++n) d += dw_part[r * nparts + n];
+      dwv[j] = d;
+      wv[j] = w[t * k + j];
+      s = fmaf(wv[j], d, s);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (j < k) {
+      const float g = wv[j] * (dwv[j] - s);
+      dl[t * k + j] = g;
+      __nv_bfloat16 b = __float2bfloat16_rn(g);
+      dlT[static_cast<int64_t>(idx[t * k + j]) * T_pad + t] = *reinterpret_cast<uint16_t*>(&b);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- B7: un-permute
+
+// dx[t] = sum_j scratch[t*k + j] + sum_j dl[t, j] * W_r^T[idx[t, j]]
+// (the expert input gradients plus the router's input gradient dl · W_r^T,
+// whose only non-zero terms are the k selected experts).
+__global__ void unpermute_kernel(const uint16_t* __restrict__ scratch, const float* __restrict__ dl,
+                                 const int* __restrict__ idx, const uint16_t* __restrict__ WrT,
+                                 uint16_t* __restrict__ dx, int64_t T, int H, int k) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int cpr = H >> 3;
+  if (i >= T * cpr) return;
+  const int64_t t = i / cpr;
+  const int c = static_cast<int>(i - t * cpr) * 8;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const uint16_t* base = scratch + t * k * H + c;
+  for (int j = 0; j < k; ++j) {
+    add_bf16x8(ld_global_nc_v4(base + static_cast<int64_t>(j) * H), acc);
+    const int e = idx[t * k + j];
+    add_bf16x8(ld_global_nc_v4(WrT + static_cast<int64_t>(e) * H + c), acc, dl[t * k + j]);
+  }
+  st_global_v4(dx + t * H + c, pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+               pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+}
+
+// ---------------------------------------------------------------- B10: dW_r
+
+// dW_r[h, e] = sum over splits of part[s, e, h] (fp32), written as bf16 [H, E].
+__global__ void wr_reduce_kernel(const float* __restrict__ part, int S, int E, int H,
+                                 uint16_t* __restrict__ dWr) {
+  __shared__ float tile[32][33];
+  const int h0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int e = e0 + i, h = h0 + threadIdx.x;
+    float s = 0.f;
+    if (e < E && h < H)
+      for (int sp = 0; sp < S; ++sp) s += part[(static_cast<int64_t>(sp) * E + e) * H + h];
+    tile[i][threadIdx.x] = s;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int h = h0 + i, e = e0 + threadIdx.x;
+    if (h < H && e < E) {
+      __nv_bfloat16 b = __float2bfloat16_rn(tile[threadIdx.x][i]);
+      dWr[static_cast<int64_t>(h) * E + e] = *reinterpret_cast<uint16_t*>(&b);
+    }
+  }
+}
+
+inline unsigned blocks_for(int64_t n, int per) { return static_cast<unsigned>((n + per - 1) / per); }
+
+}  // namespace
+
+cudaError_t launch_transpose_bf16(const uint16_t* in, uint16_t* out, int rows, int cols,
+                                  cudaStream_t s) {
+  dim3 grid(blocks_for(cols, 32), blocks_for(rows, 32));
+  transpose_bf16_kernel<<<grid, dim3(32, 8), 0, s>>>(in, out, rows, cols);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan(const int* hist, int ntiles, int E, int* counts, int* offsets,
+                        int* block_base, int* mtile_off, int* group_order, cudaStream_t s) {
+  scan_kernel<<<1, 256, 0, s>>>(hist, ntiles, E, counts, offsets, block_base, mtile_off,
+                                group_order);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const int* idx, const float* w, const int* block_base, int64_t T,
+                           int k, int E, int* perm_token, int* slot_row, int* row_slot,
+                           float* w_row, cudaStream_t s) {
+  permute_kernel<<<blocks_for(T, 128), 128, 0, s>>>(idx, w, block_base, T, k, E, perm_token,
+                                                    slot_row, row_slot, w_row);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const uint16_t* src, const int* slot_row, uint16_t* dst,
+                               int64_t T, int H, int k, cudaStream_t s) {
+  gather_rows_kernel<<<blocks_for(T, 8), 256, 0, s>>>(src, slot_row, dst, T, H, k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const uint16_t* scratch, uint16_t* y, int64_t T, int H, int k,
+                           cudaStream_t s) {
+  combine_kernel<<<blocks_for(T * (H / 8), 256), 256, 0, s>>>(scratch, y, T, H, k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_bwd(const float* dw_part, int nparts, const int* slot_row,
+                              const float* w, const int* idx, int64_t T, int k, float* dl,
+                              uint16_t* dlT, int64_t T_pad, cudaStream_t s) {
+  router_bwd_kernel<<<blocks_for(T, 128), 128, 0, s>>>(dw_part, nparts, slot_row, w, idx, T, k,
+                                                       dl, dlT, T_pad);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpermute(const uint16_t* scratch, const float* dl, const int* idx,
+                             const uint16_t* WrT, uint16_t* dx, int64_t T, int H, int k,
+                             cudaStream_t s) {
+  unpermute_kernel<<<blocks_for(T * (H / 8), 256), 256, 0, s>>>(scratch, dl, idx, WrT, dx, T, H,
+                                                                k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wr_reduce(const float* part, int S, int E, int H, uint16_t* dWr,
+                             cudaStream_t s) {
+  dim3 grid(blocks_for(H, 32), blocks_for(E, 32));
+  wr_reduce_kernel<<<grid, dim3(32, 8), 0, s>>>(part, S, E, H, dWr);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

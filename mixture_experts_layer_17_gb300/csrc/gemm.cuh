@@ -1,0 +1,421 @@
+// Persistent, warp-specialised tcgen05 GEMM engine for the MoE layer.
+//
+// One CTA per SM walks a static list of 128 x BN output tiles.  Per CTA:
+//   warp 0      TMA producer: fills a ring of STAGES shared-memory stages
+//               (A: 128 x 64 bf16, B: BN x 64 bf16, 128-byte swizzle);
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN, K=16)
+//               into a double-buffered TMEM accumulator and commits stage and
+//               accumulator barriers;
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (thread = output row),
+//               the problem's fused element-wise work, and global stores.
+// The problem policy (struct P) supplies the tile schedule, the TMA loads and
+// the epilogue; the engine is shared by every GEMM of the layer:
+//   router logits + top-k, expert gate/up with SwiGLU, expert down with the
+//   weighted scatter, their dgrads (SwiGLU backward, router-weight gradient)
+//   and their wgrads over ragged per-expert token counts.
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kBM = 128;          // rows of an output tile (TMEM lanes)
+constexpr int kBK = 64;           // bf16 elements of K per stage (128 bytes)
+constexpr int kThreads = 192;     // 6 warps
+constexpr uint32_t kChunkBytes = 64 * 128;   // one MN-major 64 x 64 bf16 chunk
+
+struct GemmArgs {
+  CUtensorMap mapA;
+  CUtensorMap mapB0;
+  CUtensorMap mapB1;
+  int M;               // dense: output rows; grouped-K / split-K: output rows per group
+  int N;               // output columns
+  int K;               // reduction length (dense, grouped-M, split-K)
+  int n_tiles;         // ceil(N / BN)
+  int m_tiles;         // grouped-K / split-K: ceil(M / 128)
+  int num_groups;      // experts
+  int k_split;         // split-K: number of K chunks
+  int kb_per_split;    // split-K: k-blocks per chunk
+  int b_group_rows;    // rows of one expert in B's 2-D tensor map
+  int k_half;          // gate/up dgrad: K index where B switches from W_gate to W_up
+  const int* offsets;  // [E + 1] row offsets of the permuted layout
+  const int* mtile_off;     // [E + 1] prefix of ceil(count / 128)
+  const int* group_order;   // grouped-K: experts in processing order
+  void* out0;
+  void* out1;
+  void* out2;
+  void* out3;
+  const void* in0;
+  const void* in1;
+  const void* in2;
+  int64_t T;
+  int E;
+  int top_k;
+  int ld0;
+  int ld1;
+  DeviceStatus* status;
+  uint64_t wait_limit_ns;
+  uint32_t flags;      // bit 1: inject a wait that nothing signals (timeout test)
+};
+
+struct TileInfo {
+  int e;        // expert (group), -1 for dense problems
+  int m0;       // first output row (grouped-M: row of the permuted layout)
+  int n0;       // first output column
+  int rows;     // valid output rows in the tile
+  int kb0;      // first k-block
+  int num_kb;   // k-blocks
+  int k_last;   // valid K rows in the last k-block (grouped-K)
+  int krow0;    // first K row of the group (grouped-K)
+  int mt;       // m-tile index (dense)
+};
+
+// ------------------------------------------------------------ schedules
+
+// Grouped-M: rows of expert e are [offsets[e], offsets[e+1]); its m-tiles are
+// numbered from mtile_off[e].  Tiles are ordered (expert, n-tile, m-tile) so
+// that CTAs running at the same time share the expert's weight panel in L2.
+MOE_DEV int grouped_m_num_tiles(const GemmArgs& a) {
+  return __ldg(a.mtile_off + a.num_groups) * a.n_tiles;
+}
+
+MOE_DEV TileInfo grouped_m_tile(const GemmArgs& a, int t, int BN) {
+  const int q = t / a.n_tiles;
+  int lo = 0, hi = a.num_groups - 1;   // largest e with mtile_off[e] <= q
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(a.mtile_off + mid) <= q) lo = mid; else hi = mid - 1;
+  }
+  const int e = lo;
+  const int mbase = __ldg(a.mtile_off + e);
+  const int mt_e = __ldg(a.mtile_off + e + 1) - mbase;
+  const int local = t - mbase * a.n_tiles;
+  const int nt = local / mt_e;
+  const int mt = local - nt * mt_e;
+  const int r0 = __ldg(a.offsets + e);
+  const int r1 = __ldg(a.offsets + e + 1);
+  TileInfo ti;
+  ti.e = e;
+  ti.m0 = r0 + mt * kBM;
+  ti.n0 = nt * BN;
+  ti.rows = min(kBM, r1 - ti.m0);
+  ti.kb0 = 0;
+  ti.num_kb = (a.K + kBK - 1) / kBK;
+  ti.k_last = kBK;
+  ti.krow0 = 0;
+  ti.mt = mt;
+  return ti;
+}
+
+// Grouped-K (weight gradients): every expert owns m_tiles x n_tiles output
+// tiles; its K range is its token rows [offsets[e], offsets[e+1]).
+MOE_DEV int grouped_k_num_tiles(const GemmArgs& a) {
+  return a.num_groups * a.m_tiles * a.n_tiles;
+}
+
+MOE_DEV TileInfo grouped_k_tile(const GemmArgs& a, int t, int BN) {
+  const int per = a.m_tiles * a.n_tiles;
+  const int gi = t / per;
+  const int local = t - gi * per;
+  const int mt = local / a.n_tiles;
+  const int nt = local - mt * a.n_tiles;
+  const int e = a.group_order != nullptr ? __ldg(a.group_order + gi) : gi;
+  const int r0 = __ldg(a.offsets + e);
+  const int cnt = __ldg(a.offsets + e + 1) - r0;
+  TileInfo ti;
+  ti.e = e;
+  ti.m0 = mt * kBM;
+  ti.n0 = nt * BN;
+  ti.rows = min(kBM, a.M - ti.m0);
+  ti.kb0 = 0;
+  ti.num_kb = (cnt + kBK - 1) / kBK;
+  ti.k_last = cnt - (ti.num_kb - 1) * kBK;
+  ti.krow0 = r0;
+  ti.mt = mt;
+  return ti;
+}
+
+MOE_DEV int dense_num_tiles(const GemmArgs& a) {
+  return ((a.M + kBM - 1) / kBM) * a.n_tiles;
+}
+
+MOE_DEV TileInfo dense_tile(const GemmArgs& a, int t, int BN) {
+  const int mt = t / a.n_tiles;
+  const int nt = t - mt * a.n_tiles;
+  TileInfo ti;
+  ti.e = -1;
+  ti.m0 = mt * kBM;
+  ti.n0 = nt * BN;
+  ti.rows = min(kBM, a.M - ti.m0);
+  ti.kb0 = 0;
+  ti.num_kb = (a.K + kBK - 1) / kBK;
+  ti.k_last = kBK;
+  ti.krow0 = 0;
+  ti.mt = mt;
+  return ti;
+}
+
+// Split-K: tiles (split, m-tile, n-tile); each split reduces kb_per_split
+// k-blocks and writes an fp32 partial.
+MOE_DEV int split_k_num_tiles(const GemmArgs& a) { return a.k_split * a.m_tiles * a.n_tiles; }
+
+MOE_DEV TileInfo split_k_tile(const GemmArgs& a, int t, int BN) {
+  const int per = a.m_tiles * a.n_tiles;
+  const int ks = t / per;
+  const int local = t - ks * per;
+  const int mt = local / a.n_tiles;
+  const int nt = local - mt * a.n_tiles;
+  const int total_kb = (a.K + kBK - 1) / kBK;
+  TileInfo ti;
+  ti.e = ks;
+  ti.m0 = mt * kBM;
+  ti.n0 = nt * BN;
+  ti.rows = min(kBM, a.M - ti.m0);
+  ti.kb0 = ks * a.kb_per_split;
+  ti.num_kb = max(0, min(total_kb, ti.kb0 + a.kb_per_split) - ti.kb0);
+  ti.k_last = kBK;
+  ti.krow0 = 0;
+  ti.mt = mt;
+  return ti;
+}
+
+// ------------------------------------------------------------ engine
+
+template <int BN>
+struct StageCfg {
+  static constexpr uint32_t kABytes = kBM * kBK * 2;
+  static constexpr uint32_t kBBytes = BN * kBK * 2;
+  static constexpr int kStages = (BN >= 256) ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
+};
+
+template <class P>
+constexpr size_t gemm_smem_bytes() {
+  using C = StageCfg<P::BN>;
+  return 1024 + static_cast<size_t>(C::kStages) * (C::kABytes + C::kBBytes) + 256 +
+         P::kExtraSmem;
+}
+
+template <class P>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs args) {
+  constexpr int BN = P::BN;
+  using C = StageCfg<BN>;
+  constexpr int S = C::kStages;
+  constexpr uint32_t kA = C::kABytes;
+  constexpr uint32_t kB = C::kBBytes;
+  constexpr uint32_t kIdesc = make_idesc_bf16(kBM, BN, P::kAMN, P::kBMN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * kA;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sB + S * kB);
+  uint64_t* empty_bar = full_bar + S;
+  uint64_t* tfull_bar = empty_bar + S;     // [2]
+  uint64_t* tempty_bar = tfull_bar + 2;    // [2]
+  uint64_t* drain_bar = tempty_bar + 2;    // [1]
+  uint64_t* never_bar = drain_bar + 1;     // [1] nothing ever arrives here
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(never_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* zero_flag = abort_flag + 1;   // stays 0: drains are never cut short
+  uint8_t* extra = reinterpret_cast<uint8_t*>(full_bar) + 256;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar + s, 1);
+      mbar_init(empty_bar + s, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tfull_bar + i, 1);
+      mbar_init(tempty_bar + i, 4);
+    }
+    mbar_init(drain_bar, 1);
+    mbar_init(never_bar, 1);
+    *abort_flag = 0;
+    *zero_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_holder, C::kTmemCols);
+  }
+  P::init_extra(args, extra);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int num_tiles = P::num_tiles(args);
+  const uint64_t limit = args.wait_limit_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&args.mapA);
+      prefetch_tmap(&args.mapB0);
+      prefetch_tmap(&args.mapB1);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, parity_mask = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        const TileInfo ti = P::tile(args, t);
+        for (int kb = 0; kb < ti.num_kb; ++kb) {
+          if (!mbar_wait_bounded(empty_bar + stage, phase ^ 1u, abort_flag, limit)) {
+            if (!*abort_flag) record_timeout(args.status, kWaitProducerEmpty);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar + stage, kA + kB);
+          P::load(args, ti, kb, sA + stage * kA, sB + stage * kB, full_bar + stage);
+          issued_mask |= 1u << stage;
+          parity_mask = (parity_mask & ~(1u << stage)) | (phase << stage);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // let every load already in flight land before the CTA exits
+        for (int s = 0; s < S; ++s) {
+          if (issued_mask & (1u << s)) {
+            mbar_wait_bounded(full_bar + s, (parity_mask >> s) & 1u, zero_flag, 100000000ull);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    bool committed_any = false;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      const TileInfo ti = P::tile(args, t);
+      if (ti.num_kb == 0) continue;
+      if (!mbar_wait_bounded(tempty_bar + acc, acc_phase ^ 1u, abort_flag, limit)) {
+        if (!*abort_flag) record_timeout(args.status, kWaitMmaTmemEmpty);
+        *abort_flag = 1;
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      for (int kb = 0; kb < ti.num_kb; ++kb) {
+        if (!mbar_wait_bounded(full_bar + stage, phase, abort_flag, limit)) {
+          if (!*abort_flag) record_timeout(args.status, kWaitMmaFull);
+          *abort_flag = 1;
+          ok = false;
+          break;
+        }
+        if (P::kTailZero && kb == ti.num_kb - 1 && ti.k_last < kBK) {
+          // rows [k_last, 64) of every 64 x 128-byte chunk belong to the next
+          // expert (or lie past the tensor): clear them before the MMA reads
+          const uint32_t nbytes = static_cast<uint32_t>(kBK - ti.k_last) * 128u;
+          const uint32_t off = static_cast<uint32_t>(ti.k_last) * 128u;
+          for (int c = 0; c < static_cast<int>(kA / kChunkBytes) + static_cast<int>(kB / kChunkBytes); ++c) {
+            uint8_t* base = (c < static_cast<int>(kA / kChunkBytes))
+                                ? sA + stage * kA + c * kChunkBytes
+                                : sB + stage * kB + (c - kA / kChunkBytes) * kChunkBytes;
+            for (uint32_t b = lane * 16u; b < nbytes; b += 32u * 16u) {
+              *reinterpret_cast<uint4*>(base + off + b) = make_uint4(0, 0, 0, 0);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + stage * kA);
+          const uint32_t b_base = smem_u32(sB + stage * kB);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t adesc =
+                P::kAMN ? make_smem_desc(a_base + k * 2048, kChunkBytes, 1024)
+                        : make_smem_desc(a_base + k * 32, 16, 1024);
+            const uint64_t bdesc =
+                P::kBMN ? make_smem_desc(b_base + k * 2048, kChunkBytes, 1024)
+                        : make_smem_desc(b_base + k * 32, 16, 1024);
+            mma_bf16(d_tmem, adesc, bdesc, kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(empty_bar + stage);
+          committed_any = true;
+        }
+        __syncwarp();
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) {
+        const bool inject = (args.flags & 2u) != 0 && t == static_cast<int>(blockIdx.x);
+        if (!inject) mma_commit(tfull_bar + acc);
+      }
+      __syncwarp();
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    // wait until every MMA this thread issued has completed
+    if (lane == 0 && committed_any) {
+      mma_commit(drain_bar);
+      mbar_wait_bounded(drain_bar, 0, zero_flag, 100000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ epilogue (warps 2-5)
+    const int quarter = warp & 3;            // TMEM lane quarter of this warp
+    const int r = quarter * 32 + lane;       // row of the tile this thread owns
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool first = true;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      const TileInfo ti = P::tile(args, t);
+      if (ti.num_kb == 0) {
+        P::epilogue_empty(args, ti, r, extra);
+        continue;
+      }
+      if (first && (args.flags & 2u) != 0) {
+        // test hook: a wait on a barrier that nothing signals
+        if (!mbar_wait_bounded(never_bar, 0, abort_flag, limit)) {
+          record_timeout(args.status, kWaitInjected);
+          *abort_flag = 1;
+          break;
+        }
+      }
+      first = false;
+      if (!mbar_wait_bounded(tfull_bar + acc, acc_phase, abort_flag, limit)) {
+        if (!*abort_flag) record_timeout(args.status, kWaitEpiTmemFull);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      P::epilogue(args, ti, tmem_base + lane_off + static_cast<uint32_t>(acc * BN), r, extra);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar + acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) {
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+}  // namespace moe

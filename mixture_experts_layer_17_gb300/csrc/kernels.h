@@ -1,0 +1,64 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gemm.cuh"
+
+namespace moe {
+
+// tcgen05 GEMMs (gemm_*.cu); `grid` CTAs of kThreads threads, persistent.
+cudaError_t launch_router_fwd(int bn, const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_gate_up_fwd(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_down_fwd(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_down_dgrad(int bn, const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_gate_up_dgrad(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_down_wgrad(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_gate_up_wgrad(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_router_wgrad(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_dense(bool a_mn, bool b_mn, const GemmArgs& a, int grid, cudaStream_t s);
+
+// memory-bound kernels (elementwise.cu)
+cudaError_t launch_transpose_bf16(const uint16_t* in, uint16_t* out, int rows, int cols,
+                                  cudaStream_t s);
+cudaError_t launch_scan(const int* hist, int ntiles, int E, int* counts, int* offsets,
+                        int* block_base, int* mtile_off, int* group_order, cudaStream_t s);
+cudaError_t launch_permute(const int* idx, const float* w, const int* block_base, int64_t T,
+                           int k, int E, int* perm_token, int* slot_row, int* row_slot,
+                           float* w_row, cudaStream_t s);
+cudaError_t launch_gather_rows(const uint16_t* src, const int* slot_row, uint16_t* dst,
+                               int64_t T, int H, int k, cudaStream_t s);
+cudaError_t launch_combine(const uint16_t* scratch, uint16_t* y, int64_t T, int H, int k,
+                           cudaStream_t s);
+cudaError_t launch_router_bwd(const float* dw_part, int nparts, const int* slot_row,
+                              const float* w, const int* idx, int64_t T, int k, float* dl,
+                              uint16_t* dlT, int64_t T_pad, cudaStream_t s);
+cudaError_t launch_unpermute(const uint16_t* scratch, const float* dl, const int* idx,
+                             const uint16_t* WrT, uint16_t* dx, int64_t T, int H, int k,
+                             cudaStream_t s);
+cudaError_t launch_wr_reduce(const float* part, int S, int E, int H, uint16_t* dWr,
+                             cudaStream_t s);
+
+// Launches gemm_kernel<P>, raising the dynamic shared-memory limit once per
+// device.
+template <class P>
+cudaError_t launch_gemm(const GemmArgs& a, int grid, cudaStream_t s) {
+  constexpr size_t smem = gemm_smem_bytes<P>();
+  static_assert(smem <= 232448, "shared memory per CTA exceeds 227 KB");
+  static unsigned long long configured = 0ull;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(configured & bit)) {
+    e = cudaFuncSetAttribute(gemm_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured |= bit;
+  }
+  gemm_kernel<P><<<grid, kThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,239 @@
+// The GEMMs of the MoE layer as policies of the tcgen05 engine (gemm.cuh).
+//
+// Notation: T tokens, H hidden, F expert width, E experts, k = top_k,
+// P = T * k rows of the expert-major permuted layout.  Operand tiles are
+// loaded by TMA with the 128-byte swizzle, either K-major (box 64 x rows) or
+// MN-major (chunks of 64 MN-elements x 64 K-rows, 8 KB each).
+#pragma once
+
+#include "gemm.cuh"
+
+namespace moe {
+
+MOE_DEV void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// ------------------------------------------------------------------------
+// F1 + F2 (+ histogram): router logits x·W_r (+ logit_bias), top-k selection
+// with ties to the lower expert id, softmax weights renormalised over the
+// selected experts, and the expert histogram of this 128-token tile.
+//   mapA  = x [T, H] K-major, box {64, 128}
+//   mapB0 = W_r^T [E, H] K-major, box {64, BN}  (rows >= E read as zero)
+//   in0 = logit_bias f32 [E] or null;  out0 = logits f32 [T, E] or null
+//   out1 = topk_idx i32 [T, k];  out2 = topk_w f32 [T, k];  out3 = hist i32 [tiles, E]
+// ------------------------------------------------------------------------
+template <int BN_>
+struct RouterProblem {
+  static constexpr int BN = BN_;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = false;
+  static constexpr bool kTailZero = false;
+  static constexpr size_t kExtraSmem = 256 * sizeof(int);
+  static constexpr int kMaxK = 16;
+
+  MOE_DEV static int num_tiles(const GemmArgs& a) { return dense_num_tiles(a); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return dense_tile(a, t, BN); }
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t* extra) {
+    int* h = reinterpret_cast<int*>(extra);
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) h[i] = 0;
+  }
+  MOE_DEV static void load(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
+                           uint8_t* sB, uint64_t* bar) {
+    tma_load_2d(sA, &a.mapA, kb * kBK, ti.m0, bar);
+    tma_load_2d(sB, &a.mapB0, kb * kBK, 0, bar);
+  }
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, uint8_t*) {}
+
+  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
+                               uint8_t* extra) {
+    int* hist = reinterpret_cast<int*>(extra);
+    const int E = a.E;
+    const int k = a.top_k;
+    const bool valid = r < ti.rows;
+    const int64_t t = static_cast<int64_t>(ti.m0) + r;
+    const float* bias = static_cast<const float*>(a.in0);
+    float* logits = static_cast<float*>(a.out0);
+    float topv[kMaxK];
+    int topi[kMaxK];
+#pragma unroll
+    for (int i = 0; i < kMaxK; ++i) {
+      topv[i] = -INFINITY;
+      topi[i] = 0x7fffffff;
+    }
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 16) {
+      float v[16];
+      tmem_ld16(taddr + c, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int e = c + i;
+        if (e < E) {
+          float l = v[i];
+          if (bias != nullptr) l += __ldg(bias + e);
+          v[i] = l;
+          // insert (l, e) into the list ordered by (-logit, id)
+          float cv = l;
+          int ci = e;
+#pragma unroll
+          for (int s = 0; s < kMaxK; ++s) {
+            if (s < k) {
+              const bool better = (cv > topv[s]) || (cv == topv[s] && ci < topi[s]);
+              if (better) {
+                const float tv = topv[s];
+                const int tt = topi[s];
+                topv[s] = cv;
+                topi[s] = ci;
+                cv = tv;
+                ci = tt;
+              }
+            }
+          }
+        }
+      }
+      if (valid && logits != nullptr) {
+        float* dst = logits + t * E + c;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (c + i < E) dst[i] = v[i];
+      }
+    }
+    if (valid) {
+      const float m = topv[0];
+      float ex[kMaxK];
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        ex[j] = (j < k) ? expf(topv[j] - m) : 0.f;
+        sum += ex[j];
+      }
+      const float inv = 1.0f / sum;
+      int* idx_out = static_cast<int*>(a.out1) + t * k;
+      float* w_out = static_cast<float*>(a.out2) + t * k;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j < k) {
+          idx_out[j] = topi[j];
+          w_out[j] = ex[j] * inv;
+          atomicAdd(hist + topi[j], 1);
+        }
+      }
+    }
+    epi_bar_sync();
+    int* hist_out = static_cast<int*>(a.out3) + static_cast<int64_t>(ti.mt) * E;
+    for (int e = r; e < E; e += 128) {
+      hist_out[e] = hist[e];
+      hist[e] = 0;
+    }
+    epi_bar_sync();
+  }
+};
+
+// ------------------------------------------------------------------------
+// F7 + F8: expert gate/up GEMM with the SwiGLU epilogue.
+//   Tile = 128 permuted rows x (128 gate columns | 128 up columns) of expert e.
+//   mapA  = x_perm [P, H] K-major, box {64, 128}
+//   mapB0 = W_gate as [E*H, F] MN-major, box {64, 64};  mapB1 = W_up, same
+//   out0 = a [P, F] bf16 (silu(h_g) * h_u);  out1 = h [P, 2F] bf16 (h_g | h_u)
+//   ld0 = F;  K = H;  n_tiles = F / 128;  b_group_rows = H
+// ------------------------------------------------------------------------
+struct GateUpFwdProblem {
+  static constexpr int BN = 256;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = true;
+  static constexpr bool kTailZero = false;
+  static constexpr size_t kExtraSmem = 0;
+
+  MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile(a, t, 128); }
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
+  MOE_DEV static void load(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
+                           uint8_t* sB, uint64_t* bar) {
+    const int k0 = kb * kBK;
+    const int brow = ti.e * a.b_group_rows + k0;
+    tma_load_2d(sA, &a.mapA, k0, ti.m0, bar);
+    tma_load_2d(sB, &a.mapB0, ti.n0, brow, bar);
+    tma_load_2d(sB + kChunkBytes, &a.mapB0, ti.n0 + 64, brow, bar);
+    tma_load_2d(sB + 2 * kChunkBytes, &a.mapB1, ti.n0, brow, bar);
+    tma_load_2d(sB + 3 * kChunkBytes, &a.mapB1, ti.n0 + 64, brow, bar);
+  }
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, uint8_t*) {}
+  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
+                               uint8_t*) {
+    const bool valid = r < ti.rows;
+    const int64_t row = static_cast<int64_t>(ti.m0) + r;
+    const int F = a.ld0;
+    __nv_bfloat16* act = static_cast<__nv_bfloat16*>(a.out0) + row * F + ti.n0;
+    __nv_bfloat16* hg = static_cast<__nv_bfloat16*>(a.out1) + row * 2 * F + ti.n0;
+    __nv_bfloat16* hu = hg + F;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 16) {
+      float g[16], u[16];
+      tmem_ld16(taddr + c, g);
+      tmem_ld16(taddr + 128 + c, u);
+      tmem_ld_wait();
+      if (valid) {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = g[i] * sigmoidf_fast(g[i]) * u[i];
+        store_bf16x16(act + c, v);
+        store_bf16x16(hg + c, g);
+        store_bf16x16(hu + c, u);
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------------------
+// F9 + F10 (first half): expert down GEMM; the epilogue scales each row by its
+// router weight and scatters it to the (token, slot)-ordered scratch, which
+// the combine kernel then sums over the k slots.
+//   mapA  = a [P, F] K-major, box {64, 128}
+//   mapB0 = W_down as [E*F, H] MN-major, box {64, 64}
+//   in0 = w_row f32 [P];  in1 = row_slot i32 [P];  out0 = scratch bf16 [P, H]
+//   ld0 = H;  K = F;  n_tiles = H / 256;  b_group_rows = F
+// ------------------------------------------------------------------------
+struct DownFwdProblem {
+  static constexpr int BN = 256;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = true;
+  static constexpr bool kTailZero = false;
+  static constexpr size_t kExtraSmem = 0;
+
+  MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile(a, t, BN); }
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
+  MOE_DEV static void load(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
+                           uint8_t* sB, uint64_t* bar) {
+    const int k0 = kb * kBK;
+    const int brow = ti.e * a.b_group_rows + k0;
+    tma_load_2d(sA, &a.mapA, k0, ti.m0, bar);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * kChunkBytes, &a.mapB0, ti.n0 + 64 * c, brow, bar);
+  }
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, uint8_t*) {}
+  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
+                               uint8_t*) {
+    const bool valid = r < ti.rows;
+    const int64_t row = static_cast<int64_t>(ti.m0) + r;
+    float w = 0.f;
+    __nv_bfloat16* dst = nullptr;
+    if (valid) {
+      w = __ldg(static_cast<const float*>(a.in0) + row);
+      const int slot = __ldg(static_cast<const int*>(a.in1) + row);
+      dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 + ti.n0;
+    }
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 16) {
+      float v[16];
+      tmem_ld16(taddr + c, v);
+      tmem_ld_wait();
+      if (valid) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] *= w;
+        store_bf16x16(dst + c, v);
+      }
+    }
+  }
+};
+
+}  // namespace moe

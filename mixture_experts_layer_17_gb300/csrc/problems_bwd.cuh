@@ -1,0 +1,338 @@
+// Backward-pass GEMMs of the MoE layer and the dense test GEMM, as policies of
+// the tcgen05 engine.  Notation as in problems.cuh.
+#pragma once
+
+#include "problems.cuh"
+
+namespace moe {
+
+// ------------------------------------------------------------------------
+// B2 + B3 + B4: down dgrad g = dY_perm · W_down^T with the fused epilogue
+//   a  = silu(h_g) * h_u                 (recomputed from the saved h)
+//   dw partial = sum_f g * a             (router-weight gradient, one partial
+//                                         per 128/256-column tile)
+//   da = w * g;  dh_g = da * h_u * silu'(h_g);  dh_u = da * silu(h_g)
+//   aw = w * a                           (A operand of the down wgrad)
+//   mapA  = dY_perm [P, H] K-major, box {64, 128}
+//   mapB0 = W_down as [E*F, H] K-major, box {64, BN}
+//   in0 = h bf16 [P, 2F];  in1 = w_row f32 [P]
+//   out0 = dh bf16 [P, 2F];  out1 = aw bf16 [P, F];  out2 = dw_part f32 [P, n_tiles]
+//   ld0 = F;  K = H;  n_tiles = F / BN;  b_group_rows = F
+// ------------------------------------------------------------------------
+template <int BN_>
+struct DownDgradProblem {
+  static constexpr int BN = BN_;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = false;
+  static constexpr bool kTailZero = false;
+  static constexpr size_t kExtraSmem = 0;
+
+  MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile(a, t, BN); }
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
+  MOE_DEV static void load(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
+                           uint8_t* sB, uint64_t* bar) {
+    const int k0 = kb * kBK;
+    tma_load_2d(sA, &a.mapA, k0, ti.m0, bar);
+    tma_load_2d(sB, &a.mapB0, k0, ti.e * a.b_group_rows + ti.n0, bar);
+  }
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, uint8_t*) {}
+  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
+                               uint8_t*) {
+    const bool valid = r < ti.rows;
+    const int64_t row = static_cast<int64_t>(ti.m0) + r;
+    const int F = a.ld0;
+    const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(a.in0) + row * 2 * F + ti.n0;
+    __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(a.out0) + row * 2 * F + ti.n0;
+    __nv_bfloat16* aw = static_cast<__nv_bfloat16*>(a.out1) + row * F + ti.n0;
+    const float w = valid ? __ldg(static_cast<const float*>(a.in1) + row) : 0.f;
+    float dw = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 16) {
+      float g[16];
+      tmem_ld16(taddr + c, g);
+      tmem_ld_wait();
+      if (valid) {
+        float hg[16], hu[16], dhg[16], dhu[16], awv[16];
+        load_bf16x16(h + c, hg);
+        load_bf16x16(h + F + c, hu);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float s = sigmoidf_fast(hg[i]);
+          const float silu = hg[i] * s;
+          const float act = silu * hu[i];
+          dw = fmaf(g[i], act, dw);
+          const float da = w * g[i];
+          dhg[i] = da * hu[i] * s * (1.0f + hg[i] * (1.0f - s));
+          dhu[i] = da * silu;
+          awv[i] = w * act;
+        }
+        store_bf16x16(dh + c, dhg);
+        store_bf16x16(dh + F + c, dhu);
+        store_bf16x16(aw + c, awv);
+      }
+    }
+    if (valid) static_cast<float*>(a.out2)[row * a.n_tiles + ti.n0 / BN] = dw;
+  }
+};
+
+// ------------------------------------------------------------------------
+// B6 (+ B7 first half): gate/up dgrad dx_perm = dh_g · W_gate^T + dh_u · W_up^T
+// over K = 2F; the epilogue scatters rows to the (token, slot)-ordered scratch.
+//   mapA  = dh [P, 2F] K-major, box {64, 128}
+//   mapB0 = W_gate as [E*H, F] K-major, box {64, 256};  mapB1 = W_up, same
+//   in1 = row_slot i32 [P];  out0 = scratch bf16 [P, H]
+//   ld0 = H;  K = 2F;  k_half = F;  n_tiles = H / 256;  b_group_rows = H
+// ------------------------------------------------------------------------
+struct GateUpDgradProblem {
+  static constexpr int BN = 256;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = false;
+  static constexpr bool kTailZero = false;
+  static constexpr size_t kExtraSmem = 0;
+
+  MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile(a, t, BN); }
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
+  MOE_DEV static void load(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
+                           uint8_t* sB, uint64_t* bar) {
+    const int k0 = kb * kBK;
+    const int brow = ti.e * a.b_group_rows + ti.n0;
+    tma_load_2d(sA, &a.mapA, k0, ti.m0, bar);
+    if (k0 < a.k_half)
+      tma_load_2d(sB, &a.mapB0, k0, brow, bar);
+    else
+      tma_load_2d(sB, &a.mapB1, k0 - a.k_half, brow, bar);
+  }
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, uint8_t*) {}
+  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
+                               uint8_t*) {
+    const bool valid = r < ti.rows;
+    const int64_t row = static_cast<int64_t>(ti.m0) + r;
+    __nv_bfloat16* dst = nullptr;
+    if (valid) {
+      const int slot = __ldg(static_cast<const int*>(a.in1) + row);
+      dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 + ti.n0;
+    }
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 16) {
+      float v[16];
+      tmem_ld16(taddr + c, v);
+      tmem_ld_wait();
+      if (valid) store_bf16x16(dst + c, v);
+    }
+  }
+};
+
+// Stores a 128 x 256 fp32 accumulator tile as bf16 rows (weight gradients).
+MOE_DEV void store_tile_bf16(uint32_t taddr, bool valid, __nv_bfloat16* dst) {
+#pragma unroll 1
+  for (int c = 0; c < 256; c += 16) {
+    float v[16];
+    tmem_ld16(taddr + c, v);
+    tmem_ld_wait();
+    if (valid) store_bf16x16(dst + c, v);
+  }
+}
+
+MOE_DEV void zero_row_bf16(__nv_bfloat16* dst, int n) {
+  for (int c = 0; c < n; c += 8) st_global_v4(dst + c, 0u, 0u, 0u, 0u);
+}
+
+// ------------------------------------------------------------------------
+// B5: down wgrad dW_down[e] = (w·a)_e^T · dY_perm_e, K = tokens of expert e.
+//   mapA  = aw [P, F] MN-major, box {64, 64}      (M = F)
+//   mapB0 = dY_perm [P, H] MN-major, box {64, 64} (N = H)
+//   out0 = dW_down bf16 [E, F, H];  M = F;  N = H;  ld0 = H
+// ------------------------------------------------------------------------
+struct DownWgradProblem {
+  static constexpr int BN = 256;
+  static constexpr bool kAMN = true;
+  static constexpr bool kBMN = true;
+  static constexpr bool kTailZero = true;
+  static constexpr size_t kExtraSmem = 0;
+
+  MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_k_num_tiles(a); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_k_tile(a, t, BN); }
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
+  MOE_DEV static void load(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
+                           uint8_t* sB, uint64_t* bar) {
+    const int krow = ti.krow0 + kb * kBK;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) tma_load_2d(sA + c * kChunkBytes, &a.mapA, ti.m0 + 64 * c, krow, bar);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * kChunkBytes, &a.mapB0, ti.n0 + 64 * c, krow, bar);
+  }
+  MOE_DEV static __nv_bfloat16* out_row(const GemmArgs& a, const TileInfo& ti, int r) {
+    return static_cast<__nv_bfloat16*>(a.out0) +
+           (static_cast<int64_t>(ti.e) * a.M + ti.m0 + r) * a.ld0 + ti.n0;
+  }
+  MOE_DEV static void epilogue_empty(const GemmArgs& a, const TileInfo& ti, int r, uint8_t*) {
+    if (r < ti.rows) zero_row_bf16(out_row(a, ti, r), BN);
+  }
+  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
+                               uint8_t*) {
+    const bool valid = r < ti.rows;
+    store_tile_bf16(taddr, valid, valid ? out_row(a, ti, r) : nullptr);
+  }
+};
+
+// ------------------------------------------------------------------------
+// B8: gate/up wgrad dW_gate[e] = x_perm_e^T · dh_g,e and dW_up[e] = x_perm_e^T ·
+// dh_u,e, K = tokens of expert e; N runs over the 2F columns of dh.
+//   mapA  = x_perm [P, H] MN-major, box {64, 64}  (M = H)
+//   mapB0 = dh [P, 2F] MN-major, box {64, 64}     (N = 2F)
+//   out0 = dW_gate, out1 = dW_up bf16 [E, H, F];  M = H;  N = 2F;  ld0 = F
+// ------------------------------------------------------------------------
+struct GateUpWgradProblem {
+  static constexpr int BN = 256;
+  static constexpr bool kAMN = true;
+  static constexpr bool kBMN = true;
+  static constexpr bool kTailZero = true;
+  static constexpr size_t kExtraSmem = 0;
+
+  MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_k_num_tiles(a); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_k_tile(a, t, BN); }
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
+  MOE_DEV static void load(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
+                           uint8_t* sB, uint64_t* bar) {
+    const int krow = ti.krow0 + kb * kBK;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) tma_load_2d(sA + c * kChunkBytes, &a.mapA, ti.m0 + 64 * c, krow, bar);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * kChunkBytes, &a.mapB0, ti.n0 + 64 * c, krow, bar);
+  }
+  // 16-column chunk starting at global column gc of the [gate | up] range
+  MOE_DEV static __nv_bfloat16* out_ptr(const GemmArgs& a, const TileInfo& ti, int r, int gc) {
+    const int F = a.ld0;
+    __nv_bfloat16* base = static_cast<__nv_bfloat16*>(gc < F ? a.out0 : a.out1);
+    const int col = gc < F ? gc : gc - F;
+    return base + (static_cast<int64_t>(ti.e) * a.M + ti.m0 + r) * F + col;
+  }
+  MOE_DEV static void epilogue_empty(const GemmArgs& a, const TileInfo& ti, int r, uint8_t*) {
+    if (r >= ti.rows) return;
+    for (int c = 0; c < BN; c += 16) {
+      __nv_bfloat16* p = out_ptr(a, ti, r, ti.n0 + c);
+      st_global_v4(p, 0u, 0u, 0u, 0u);
+      st_global_v4(p + 8, 0u, 0u, 0u, 0u);
+    }
+  }
+  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
+                               uint8_t*) {
+    const bool valid = r < ti.rows;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 16) {
+      float v[16];
+      tmem_ld16(taddr + c, v);
+      tmem_ld_wait();
+      if (valid) store_bf16x16(out_ptr(a, ti, r, ti.n0 + c), v);
+    }
+  }
+};
+
+// ------------------------------------------------------------------------
+// B10 (weight half): dW_r^T = dl^T · x as a split-K GEMM over the tokens;
+// each split writes an fp32 partial that a small kernel reduces and transposes.
+//   mapA  = dl^T [E, T_pad] K-major bf16, box {64, 128}  (M = E, rows >= E zero)
+//   mapB0 = x [T, H] MN-major, box {64, 64}               (N = H)
+//   out0 = partials f32 [k_split, E, H];  M = E;  N = H;  K = T;  ld0 = H
+// ------------------------------------------------------------------------
+struct RouterWgradProblem {
+  static constexpr int BN = 256;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = true;
+  static constexpr bool kTailZero = false;
+  static constexpr size_t kExtraSmem = 0;
+
+  MOE_DEV static int num_tiles(const GemmArgs& a) { return split_k_num_tiles(a); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return split_k_tile(a, t, BN); }
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
+  MOE_DEV static void load(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
+                           uint8_t* sB, uint64_t* bar) {
+    const int k0 = (ti.kb0 + kb) * kBK;
+    tma_load_2d(sA, &a.mapA, k0, ti.m0, bar);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * kChunkBytes, &a.mapB0, ti.n0 + 64 * c, k0, bar);
+  }
+  MOE_DEV static float* out_row(const GemmArgs& a, const TileInfo& ti, int r) {
+    return static_cast<float*>(a.out0) +
+           (static_cast<int64_t>(ti.e) * a.M + ti.m0 + r) * a.ld0 + ti.n0;
+  }
+  MOE_DEV static void epilogue_empty(const GemmArgs& a, const TileInfo& ti, int r, uint8_t*) {
+    if (r >= ti.rows) return;
+    float* p = out_row(a, ti, r);
+    for (int c = 0; c < BN; c += 4) st_global_v4(p + c, 0u, 0u, 0u, 0u);
+  }
+  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
+                               uint8_t*) {
+    const bool valid = r < ti.rows;
+    float* p = valid ? out_row(a, ti, r) : nullptr;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 16) {
+      float v[16];
+      tmem_ld16(taddr + c, v);
+      tmem_ld_wait();
+      if (valid) {
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          st_global_v4(p + c + i, __float_as_uint(v[i]), __float_as_uint(v[i + 1]),
+                       __float_as_uint(v[i + 2]), __float_as_uint(v[i + 3]));
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------------------
+// Dense GEMM D[M, N] (fp32) = sum_k A(m, k) B(n, k) for moe_gemm_bf16.
+//   A K-major: [M, K], box {64, 128};  A MN-major: [K, M], box {64, 64}
+//   B K-major: [N, K], box {64, 256};  B MN-major: [K, N], box {64, 64}
+//   out0 = D f32 [M, N];  ld0 = N
+// ------------------------------------------------------------------------
+template <bool A_MN, bool B_MN>
+struct DenseProblem {
+  static constexpr int BN = 256;
+  static constexpr bool kAMN = A_MN;
+  static constexpr bool kBMN = B_MN;
+  static constexpr bool kTailZero = false;
+  static constexpr size_t kExtraSmem = 0;
+
+  MOE_DEV static int num_tiles(const GemmArgs& a) { return dense_num_tiles(a); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return dense_tile(a, t, BN); }
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
+  MOE_DEV static void load(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
+                           uint8_t* sB, uint64_t* bar) {
+    const int k0 = kb * kBK;
+    if (A_MN) {
+      tma_load_2d(sA, &a.mapA, ti.m0, k0, bar);
+      tma_load_2d(sA + kChunkBytes, &a.mapA, ti.m0 + 64, k0, bar);
+    } else {
+      tma_load_2d(sA, &a.mapA, k0, ti.m0, bar);
+    }
+    if (B_MN) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * kChunkBytes, &a.mapB0, ti.n0 + 64 * c, k0, bar);
+    } else {
+      tma_load_2d(sB, &a.mapB0, k0, ti.n0, bar);
+    }
+  }
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, uint8_t*) {}
+  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
+                               uint8_t*) {
+    const bool valid = r < ti.rows;
+    float* p = static_cast<float*>(a.out0) + (static_cast<int64_t>(ti.m0) + r) * a.ld0 + ti.n0;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 16) {
+      float v[16];
+      tmem_ld16(taddr + c, v);
+      tmem_ld_wait();
+      if (valid) {
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          st_global_v4(p + c + i, __float_as_uint(v[i]), __float_as_uint(v[i + 1]),
+                       __float_as_uint(v[i + 2]), __float_as_uint(v[i + 3]));
+      }
+    }
+  }
+};
+
+}  // namespace moe

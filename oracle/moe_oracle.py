@@ -410,23 +410,31 @@ def iter_expert_backward(fwd, x, dY, W_gate, W_up, W_down,
 
 
 def backward(x, W_r, W_gate, W_up, W_down, top_k: int, dY, logit_bias=None,
-             precision: Optional[str] = None, fwd=None, idx=None) -> Dict[str, np.ndarray]:
+             precision: Optional[str] = None, fwd=None, idx=None,
+             keep_weight_grads: bool = True) -> Dict[str, np.ndarray]:
     """Full VJP of the layer at dY: dx, dW_r, dW_gate, dW_up, dW_down, and the
-    router intermediates dw [T,k] and dl [T,E]."""
+    router intermediates dw [T,k] and dl [T,E].  With keep_weight_grads=False
+    the expert weight gradients are computed expert by expert and dropped, so
+    the token-local results (dx, dw, dl) of a token subset of a large layer
+    fit in host memory."""
     x = np.asarray(x, np.float64)
     if fwd is None:
         fwd = forward(x, W_r, W_gate, W_up, W_down, top_k, logit_bias, precision, idx=idx)
     T, H = x.shape
     E, _, F = W_gate.shape
     P = T * top_k
-    dW_gate = np.zeros((E, H, F))
-    dW_up = np.zeros((E, H, F))
-    dW_down = np.zeros((E, F, H))
+    if keep_weight_grads:
+        dW_gate = np.zeros((E, H, F))
+        dW_up = np.zeros((E, H, F))
+        dW_down = np.zeros((E, F, H))
+    else:
+        dW_gate = dW_up = dW_down = None
     dw_rows = np.zeros(P)
     dx_rows = np.zeros((P, H))
     for e, g in iter_expert_backward(fwd, x, dY, W_gate, W_up, W_down, precision):
         r0, r1 = g["rows"]
-        dW_gate[e], dW_up[e], dW_down[e] = g["dW_gate"], g["dW_up"], g["dW_down"]
+        if keep_weight_grads:
+            dW_gate[e], dW_up[e], dW_down[e] = g["dW_gate"], g["dW_up"], g["dW_down"]
         dw_rows[r0:r1] = g["dw_row"]
         dx_rows[r0:r1] = g["dx_row"]
     dw = dw_rows[fwd["slot_row"]]                        # [T, k]

@@ -1,0 +1,80 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads and
+exports every entry point include/moe.h declares, status strings, and argument
+validation (which runs before any CUDA call)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mixture_experts_layer_17_gb300 import build, libmoe
+    if not os.path.exists(build.LIB_PATH):
+        build.build()
+    return libmoe.load()
+
+
+def _declared_symbols():
+    with open(os.path.join(ROOT, "include", "moe.h")) as fh:
+        text = fh.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_symbols():
+    from mixture_experts_layer_17_gb300 import libmoe
+    assert _declared_symbols() == sorted(libmoe.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    from mixture_experts_layer_17_gb300 import libmoe
+    for code, name in libmoe.STATUS.items():
+        assert libmoe.moe_status_string(code) == name
+    assert libmoe.moe_status_string(99) == "MOE_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("shape, code", [
+    ((128, 256, 128, 8, 2), None),          # valid: reaches the device query
+    ((128, 200, 128, 8, 2), 2),             # H not a multiple of 256
+    ((128, 256, 100, 8, 2), 2),             # F not a multiple of 128
+    ((128, 256, 128, 8, 9), 2),             # top_k > E
+    ((128, 256, 128, 300, 2), 2),           # E > 256
+    ((128, 256, 128, 32, 17), 2),           # top_k > 16
+    ((0, 256, 128, 8, 2), 2),               # T < 1
+])
+def test_shape_validation(lib, shape, code):
+    from mixture_experts_layer_17_gb300 import libmoe
+    cfg = libmoe.make_config(*shape)
+    f, c, b = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    st = lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(f), ctypes.byref(c),
+                                ctypes.byref(b))
+    if code is None:
+        assert st in (0, 4, 6)       # OK on a GB300; CUDA / device error without one
+    else:
+        assert st == code
+
+
+def test_null_and_flag_validation(lib):
+    from mixture_experts_layer_17_gb300 import libmoe
+    assert lib.moe_workspace_size(None, None, None, None) == 1
+    cfg = libmoe.make_config(128, 256, 128, 8, 2, flags=0x100)
+    assert lib.moe_workspace_size(ctypes.byref(cfg), None, None, None) == 1
+    cfg = libmoe.make_config(128, 256, 128, 8, 2)
+    cfg.precision = 7
+    assert lib.moe_workspace_size(ctypes.byref(cfg), None, None, None) == 1
+    cfg = libmoe.make_config(128, 256, 128, 8, 2)
+    # null tensors are rejected before any CUDA call
+    assert lib.moe_forward(ctypes.byref(cfg), *([None] * 9), 0, None) == 1
+    assert lib.moe_route(ctypes.byref(cfg), *([None] * 10), 0, None) == 1
+    assert lib.moe_backward(ctypes.byref(cfg), *([None] * 13), 0, None) == 1
+    assert lib.moe_gemm_bf16(128, 100, 64, None, 1, None, 1, None, None, 0, None) == 2
