@@ -148,6 +148,35 @@ moe_status_t moe_gemm_bf16(int64_t M, int64_t N, int64_t K, const moe_bf16_t* A,
                            const moe_bf16_t* B, int b_kmajor, float* D, void* ws,
                            size_t ws_bytes, moe_stream_t stream);
 
+/* Routing without a caller-provided workspace.
+ *
+ * Same computation and outputs as moe_route, for callers that cannot call
+ * cudaMalloc: hosts whose device memory is owned entirely by another
+ * allocator or runtime (a framework's memory pool, a fixed budget carved out
+ * at start-up), and plain C callers that have no device allocator of their
+ * own.  The pages describe no such call; it has no counterpart there.
+ *
+ * Its scratch is a fixed array of MOE_NOALLOC_SCRATCH_BYTES inside the
+ * library; every GPU that loads the library holds that array until the
+ * process exits.  A configuration that needs more scratch than that is
+ * rejected with MOE_ERR_WORKSPACE_TOO_SMALL before anything is queued (at
+ * E = 128, H = 4096, top_k = 8 the limit is about T = 100,000 tokens).
+ * The call allocates no device memory and calls no allocating routine.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array and it keeps the last call's
+ * contents: calls whose GPU work overlaps (on different streams, or from
+ * different host threads) race on it and must be serialised by the caller.
+ * device_status (nullable, 4 bytes of device memory) receives the call's
+ * device status code (MOE_OK or MOE_ERR_TIMEOUT) once the work has run. */
+#define MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
+moe_status_t moe_route_noalloc(const moe_config_t* cfg, const moe_bf16_t* x,
+                               const moe_bf16_t* W_r, const float* logit_bias, float* logits,
+                               int32_t* topk_idx, float* topk_w, int32_t* counts,
+                               int32_t* offsets, int32_t* perm_token, int32_t* slot_row,
+                               int32_t* device_status, moe_stream_t stream);
+
 /* Reads the device status word of a workspace after the work queued on
  * `stream` has finished (this call synchronises the stream).  Returns
  * MOE_OK, MOE_ERR_TIMEOUT, or MOE_ERR_CUDA if the read itself failed. */

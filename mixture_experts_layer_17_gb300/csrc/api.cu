@@ -740,3 +740,95 @@ int moe_profile_read(const char** names, int64_t* launches, double* total_ms, in
 int64_t moe_launch_count(void) { return g_launches.load(); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- routing without a workspace
+//
+// moe_route_noalloc: the routing pass with its scratch in a file-scope device
+// array instead of a caller workspace, for callers that cannot allocate
+// device memory.  Host code must not hand the array's name to a kernel (on
+// the host it is only a stand-in symbol); its device address is looked up
+// once per device with cudaGetSymbolAddress.
+
+namespace {
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64] = {};
+
+// Device address of g_noalloc_scratch on the current device (looked up on
+// first use, with that device current).
+moe_status_t noalloc_scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return MOE_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return MOE_OK;
+}
+
+// Scratch of the routing pass alone: status word, per-tile histograms and
+// bases, W_r^T, the row -> (token, slot) map, row weights, m-tile prefix and
+// expert order.
+struct RouteScratch {
+  size_t status, hist, base, wrt, row_slot, w_row, mtile, order, total;
+};
+
+RouteScratch route_scratch_layout(const Layout& L) {
+  const size_t P = static_cast<size_t>(L.P), E = L.E, H = L.H;
+  Carver c;
+  RouteScratch r;
+  r.status = c.take(sizeof(DeviceStatus));
+  r.hist = c.take(sizeof(int) * L.ntiles * E);
+  r.base = c.take(sizeof(int) * L.ntiles * E);
+  r.wrt = c.take(2 * E * H);
+  r.row_slot = c.take(sizeof(int) * P);
+  r.w_row = c.take(sizeof(float) * P);
+  r.mtile = c.take(sizeof(int) * (E + 1));
+  r.order = c.take(sizeof(int) * E);
+  r.total = c.off;
+  return r;
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_route_noalloc(const moe_config_t* cfg, const moe_bf16_t* x,
+                                          const moe_bf16_t* W_r, const float* logit_bias,
+                                          float* logits, int32_t* topk_idx, float* topk_w,
+                                          int32_t* counts, int32_t* offsets,
+                                          int32_t* perm_token, int32_t* slot_row,
+                                          int32_t* device_status, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  if (!all_aligned16({x, W_r}) || topk_idx == nullptr || topk_w == nullptr ||
+      counts == nullptr || offsets == nullptr || perm_token == nullptr || slot_row == nullptr ||
+      !aligned(logit_bias, 4) || !aligned(logits, 4) || !aligned(device_status, 4))
+    return MOE_ERR_INVALID_ARG;
+  DevInfo d;
+  MOE_TRY(current_device(&d));
+  const Layout L = make_layout(*cfg, d.sms);
+  const RouteScratch R = route_scratch_layout(L);
+  if (R.total > static_cast<size_t>(MOE_NOALLOC_SCRATCH_BYTES)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  void* base = nullptr;
+  MOE_TRY(noalloc_scratch_address(&base));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DeviceStatus* st = at<DeviceStatus>(base, R.status);
+  // the array keeps the previous call's contents: only the status word has to
+  // start at zero (every other scratch value is written before it is read)
+  if (cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s) != cudaSuccess) return MOE_ERR_CUDA;
+  RouteBufs b{x, W_r, logit_bias, logits, topk_idx, topk_w, counts, offsets, perm_token,
+              slot_row, at<int>(base, R.row_slot), at<float>(base, R.w_row),
+              at<int>(base, R.mtile), at<int>(base, R.order), at<uint16_t>(base, R.wrt),
+              at<int>(base, R.hist), at<int>(base, R.base), st};
+  MOE_TRY(run_routing(*cfg, L, b, d.sms, s));
+  if (device_status != nullptr &&
+      cudaMemcpyAsync(device_status, &st->code, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) !=
+          cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}

@@ -28,7 +28,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
 # every symbol include/moe.h declares
 EXPORTED = ("moe_workspace_size", "moe_route", "moe_forward", "moe_backward", "moe_gemm_bf16",
             "moe_get_device_status", "moe_status_string", "moe_profile_enable",
-            "moe_profile_read", "moe_launch_count")
+            "moe_profile_read", "moe_launch_count", "moe_route_noalloc")
 
 
 class MoeConfig(ctypes.Structure):
@@ -69,6 +69,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_profile_read": [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(_i64),
                              ctypes.POINTER(ctypes.c_double), _i32],
         "moe_launch_count": [],
+        "moe_route_noalloc": [cfgp] + [_vp] * 11 + [_vp],
     }
     for name, argtypes in sig.items():
         fn = getattr(lib, name)
@@ -124,6 +125,19 @@ def moe_route(cfg: MoeConfig, x, W_r, logit_bias, logits, topk_idx, topk_w, coun
                             _ptr(counts, i32), _ptr(offsets, i32), _ptr(perm_token, i32),
                             _ptr(slot_row, i32), _ptr(ws), ws.numel() * ws.element_size(),
                             _stream(stream)), "moe_route")
+
+
+def moe_route_noalloc(cfg: MoeConfig, x, W_r, logit_bias, logits, topk_idx, topk_w, counts,
+                      offsets, perm_token, slot_row, device_status=None, stream=None) -> None:
+    """moe_route without a workspace: the library's fixed scratch array is used
+    instead, for callers that cannot allocate device memory."""
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    _check(load().moe_route_noalloc(ctypes.byref(cfg), _ptr(x, bf), _ptr(W_r, bf),
+                                    _ptr(logit_bias, f32), _ptr(logits, f32), _ptr(topk_idx, i32),
+                                    _ptr(topk_w, f32), _ptr(counts, i32), _ptr(offsets, i32),
+                                    _ptr(perm_token, i32), _ptr(slot_row, i32),
+                                    _ptr(device_status, i32), _stream(stream)),
+           "moe_route_noalloc")
 
 
 def moe_forward(cfg: MoeConfig, x, W_r, logit_bias, W_gate, W_up, W_down, y, ctx, ws,
