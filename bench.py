@@ -58,6 +58,32 @@ def kernel_bytes(sh):
     }
 
 
+def csrc_hash() -> str:
+    """Hash of the kernel sources: a stored ncu traffic figure is only used
+    while the kernels it was taken on are unchanged."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mixture_experts_layer_17_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel: str, workload: str):
+    """dram__bytes_read.sum + dram__bytes_write.sum per launch from the
+    committed ncu capture (profiles/dram_traffic.json), or None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        table = json.load(fh)
+    rec = table.get(f"{kernel}@{workload}")
+    if rec is None or rec.get("csrc_hash") != csrc_hash():
+        return None
+    return rec["bytes_per_launch"]
+
+
 def layer_flops(sh):
     fwd = 6 * sh.P * sh.H * sh.F + 2 * sh.T * sh.H * sh.E
     bwd = 12 * sh.P * sh.H * sh.F + 4 * sh.T * sh.H * sh.E
@@ -93,7 +119,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -241,6 +267,7 @@ def run_ours(args, sh, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     clocks.start()
+    time.sleep(1.0)          # let nvidia-smi start sampling before the timed region
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -301,13 +328,13 @@ def run_ours(args, sh, world, rank, local):
         ach = flops[dom] / (kernels[dom]["avg_ms"] * 1e-3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak,
-                "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": ach / peak, "traffic": stored_traffic(dom, sh.name),
                 "peak_source": f"{peaks['source']} bf16 sustained"}
     else:
         ach = byts.get(dom, 0) / (kernels[dom]["avg_ms"] * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
         roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
-                "frac": ach / peak, "traffic": None, "peak_source": f"{peaks['source']} hbm"}
+                "frac": ach / peak, "traffic": stored_traffic(dom, sh.name), "peak_source": f"{peaks['source']} hbm"}
     per_kernel = {}
     for name, v in sorted(kernels.items(), key=lambda kv: -kv[1]["share"]):
         d = {"launches": v["launches"], "avg_ms": round(v["avg_ms"], 4),
@@ -392,15 +419,21 @@ def run_reference(args, sh, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(si.WORKLOADS))
+    ap.add_argument("--shape", default=None,
+                    help="T,H,F,E,top_k: a custom shape (profiling aid) instead of --workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--cpu-budget", type=float, default=30.0)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    sh = si.shape(args.workload)
+    if args.shape:
+        T, H, F, E, k = (int(v) for v in args.shape.split(","))
+        sh = si.custom_shape(T, H, F, E, k, seed=5, name=f"custom_{T}x{H}x{F}x{E}x{k}")
+    else:
+        sh = si.shape(args.workload)
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         line = run_reference(args, sh, world, rank)

@@ -167,7 +167,7 @@ struct Layout {
   int ntiles;        // router tiles of 128 tokens
   int router_bn;     // N of the router GEMM (power of two >= E, >= 16)
   int dgrad_bn;      // N tile of the down dgrad (256 if F % 256 == 0, else 128)
-  int nparts;        // dw partials per row = F / dgrad_bn
+  int nparts;        // dw partials per row = 2 * F / dgrad_bn
   int wr_split, wr_kbps, wr_mtiles, wr_ntiles;
   // forward / route workspace
   size_t f_status, f_hist, f_base, f_a, f_scratch;
@@ -191,7 +191,7 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.ntiles = static_cast<int>((L.T + kBM - 1) / kBM);
   L.router_bn = next_pow2_at_least16(L.E);
   L.dgrad_bn = (L.F % 256 == 0) ? 256 : 128;
-  L.nparts = L.F / L.dgrad_bn;
+  L.nparts = (L.F / L.dgrad_bn) * 2;   // one partial per n-tile and epilogue column half
   L.wr_mtiles = (L.E + kBM - 1) / kBM;
   L.wr_ntiles = L.H / 256;
   const int total_kb = static_cast<int>((L.T + kBK - 1) / kBK);
@@ -546,7 +546,7 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
     a.mapB1 = a.mapB0;
     a.K = L.H;
     a.N = L.F;
-    a.n_tiles = L.nparts;
+    a.n_tiles = L.F / L.dgrad_bn;
     a.num_groups = L.E;
     a.b_group_rows = L.F;
     a.offsets = offsets;

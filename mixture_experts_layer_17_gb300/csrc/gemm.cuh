@@ -6,7 +6,8 @@
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN, K=16)
 //               into a double-buffered TMEM accumulator and commits stage and
 //               accumulator barriers;
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (thread = output row),
+//   warps 2..   epilogue (one or two warpgroups): tcgen05.ld of the
+//               accumulator (thread = output row, warpgroup = column half),
 //               the problem's fused element-wise work, and global stores.
 // The problem policy (struct P) supplies the tile schedule, the TMA loads and
 // the epilogue; the engine is shared by every GEMM of the layer:
@@ -21,7 +22,10 @@ namespace moe {
 
 constexpr int kBM = 128;          // rows of an output tile (TMEM lanes)
 constexpr int kBK = 64;           // bf16 elements of K per stage (128 bytes)
-constexpr int kThreads = 192;     // 6 warps
+// Threads of a CTA: warp 0 (TMA), warp 1 (MMA) and kEpiGroups warpgroups of
+// epilogue warps; group g owns columns [g*BN/G, (g+1)*BN/G) of every tile.
+template <class P>
+constexpr int gemm_threads() { return 64 + 128 * P::kEpiGroups; }
 constexpr uint32_t kChunkBytes = 64 * 128;   // one MN-major 64 x 64 bf16 chunk
 
 struct GemmArgs {
@@ -197,7 +201,7 @@ constexpr size_t gemm_smem_bytes() {
 }
 
 template <class P>
-__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmArgs args) {
+__global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid_constant__ GemmArgs args) {
   constexpr int BN = P::BN;
   using C = StageCfg<BN>;
   constexpr int S = C::kStages;
@@ -231,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull_bar + i, 1);
-      mbar_init(tempty_bar + i, 4);
+      mbar_init(tempty_bar + i, 4 * P::kEpiGroups);
     }
     mbar_init(drain_bar, 1);
     mbar_init(never_bar, 1);
@@ -371,8 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------ epilogue (warps 2-5)
+    // ------------------------------------------------ epilogue (warps 2..)
     const int quarter = warp & 3;            // TMEM lane quarter of this warp
+    const int group = (warp - 2) >> 2;       // column group of this warp
     const int r = quarter * 32 + lane;       // row of the tile this thread owns
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     int acc = 0;
@@ -381,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
       const TileInfo ti = P::tile(args, t);
       if (ti.num_kb == 0) {
-        P::epilogue_empty(args, ti, r, extra);
+        P::epilogue_empty(args, ti, r, group, extra);
         continue;
       }
       if (first && (args.flags & 2u) != 0) {
@@ -399,7 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         break;
       }
       tc_fence_after();
-      P::epilogue(args, ti, tmem_base + lane_off + static_cast<uint32_t>(acc * BN), r, extra);
+      P::epilogue(args, ti, tmem_base + lane_off + static_cast<uint32_t>(acc * BN), r, group,
+                  extra);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar + acc);

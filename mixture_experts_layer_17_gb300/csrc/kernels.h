@@ -57,7 +57,7 @@ cudaError_t launch_gemm(const GemmArgs& a, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured |= bit;
   }
-  gemm_kernel<P><<<grid, kThreads, smem, s>>>(a);
+  gemm_kernel<P><<<grid, gemm_threads<P>(), smem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -28,6 +28,7 @@ struct RouterProblem {
   static constexpr bool kBMN = false;
   static constexpr bool kTailZero = false;
   static constexpr size_t kExtraSmem = 256 * sizeof(int);
+  static constexpr int kEpiGroups = 1;      // a thread needs its whole row for the top-k
   static constexpr int kMaxK = 16;
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return dense_num_tiles(a); }
@@ -41,10 +42,10 @@ struct RouterProblem {
     tma_load_2d(sA, &a.mapA, kb * kBK, ti.m0, bar);
     tma_load_2d(sB, &a.mapB0, kb * kBK, 0, bar);
   }
-  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, uint8_t*) {}
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
 
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               uint8_t* extra) {
+                               int, uint8_t* extra) {
     int* hist = reinterpret_cast<int*>(extra);
     const int E = a.E;
     const int k = a.top_k;
@@ -142,6 +143,7 @@ struct GateUpFwdProblem {
   static constexpr bool kBMN = true;
   static constexpr bool kTailZero = false;
   static constexpr size_t kExtraSmem = 0;
+  static constexpr int kEpiGroups = 2;
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
   MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile(a, t, 128); }
@@ -156,9 +158,9 @@ struct GateUpFwdProblem {
     tma_load_2d(sB + 2 * kChunkBytes, &a.mapB1, ti.n0, brow, bar);
     tma_load_2d(sB + 3 * kChunkBytes, &a.mapB1, ti.n0 + 64, brow, bar);
   }
-  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, uint8_t*) {}
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               uint8_t*) {
+                               int group, uint8_t*) {
     const bool valid = r < ti.rows;
     const int64_t row = static_cast<int64_t>(ti.m0) + r;
     const int F = a.ld0;
@@ -166,7 +168,7 @@ struct GateUpFwdProblem {
     __nv_bfloat16* hg = static_cast<__nv_bfloat16*>(a.out1) + row * 2 * F + ti.n0;
     __nv_bfloat16* hu = hg + F;
 #pragma unroll 1
-    for (int c = 0; c < 128; c += 16) {
+    for (int c = group * 64; c < group * 64 + 64; c += 16) {
       float g[16], u[16];
       tmem_ld16(taddr + c, g);
       tmem_ld16(taddr + 128 + c, u);
@@ -198,6 +200,7 @@ struct DownFwdProblem {
   static constexpr bool kBMN = true;
   static constexpr bool kTailZero = false;
   static constexpr size_t kExtraSmem = 0;
+  static constexpr int kEpiGroups = 2;
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
   MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile(a, t, BN); }
@@ -210,9 +213,9 @@ struct DownFwdProblem {
 #pragma unroll
     for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * kChunkBytes, &a.mapB0, ti.n0 + 64 * c, brow, bar);
   }
-  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, uint8_t*) {}
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               uint8_t*) {
+                               int group, uint8_t*) {
     const bool valid = r < ti.rows;
     const int64_t row = static_cast<int64_t>(ti.m0) + r;
     float w = 0.f;
@@ -223,7 +226,7 @@ struct DownFwdProblem {
       dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 + ti.n0;
     }
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
+    for (int c = group * (BN / 2); c < (group + 1) * (BN / 2); c += 16) {
       float v[16];
       tmem_ld16(taddr + c, v);
       tmem_ld_wait();

@@ -16,7 +16,8 @@ namespace moe {
 //   mapA  = dY_perm [P, H] K-major, box {64, 128}
 //   mapB0 = W_down as [E*F, H] K-major, box {64, BN}
 //   in0 = h bf16 [P, 2F];  in1 = w_row f32 [P]
-//   out0 = dh bf16 [P, 2F];  out1 = aw bf16 [P, F];  out2 = dw_part f32 [P, n_tiles]
+//   out0 = dh bf16 [P, 2F];  out1 = aw bf16 [P, F];
+//   out2 = dw_part f32 [P, 2 * n_tiles] (one partial per n-tile and column half)
 //   ld0 = F;  K = H;  n_tiles = F / BN;  b_group_rows = F
 // ------------------------------------------------------------------------
 template <int BN_>
@@ -26,6 +27,7 @@ struct DownDgradProblem {
   static constexpr bool kBMN = false;
   static constexpr bool kTailZero = false;
   static constexpr size_t kExtraSmem = 0;
+  static constexpr int kEpiGroups = 2;
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
   MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile(a, t, BN); }
@@ -36,26 +38,50 @@ struct DownDgradProblem {
     tma_load_2d(sA, &a.mapA, k0, ti.m0, bar);
     tma_load_2d(sB, &a.mapB0, k0, ti.e * a.b_group_rows + ti.n0, bar);
   }
-  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, uint8_t*) {}
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
+  // One thread = one row, one column half.  The global loads of the saved h
+  // for chunk c + 16 are issued before chunk c is computed, so their latency
+  // overlaps the arithmetic and stores of chunk c.
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               uint8_t*) {
+                               int group, uint8_t*) {
+    constexpr int kHalf = BN / 2;
     const bool valid = r < ti.rows;
-    const int64_t row = static_cast<int64_t>(ti.m0) + r;
+    const int64_t row = static_cast<int64_t>(ti.m0) + (valid ? r : 0);
     const int F = a.ld0;
+    const int c0 = group * kHalf;
     const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(a.in0) + row * 2 * F + ti.n0;
     __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(a.out0) + row * 2 * F + ti.n0;
     __nv_bfloat16* aw = static_cast<__nv_bfloat16*>(a.out1) + row * F + ti.n0;
     const float w = valid ? __ldg(static_cast<const float*>(a.in1) + row) : 0.f;
     float dw = 0.f;
+    uint4 ng0 = make_uint4(0, 0, 0, 0), ng1 = ng0, nu0 = ng0, nu1 = ng0;
+    if (valid) {
+      ng0 = ld_global_v4(h + c0);
+      ng1 = ld_global_v4(h + c0 + 8);
+      nu0 = ld_global_v4(h + F + c0);
+      nu1 = ld_global_v4(h + F + c0 + 8);
+    }
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
+    for (int c = c0; c < c0 + kHalf; c += 16) {
+      const uint4 g0 = ng0, g1 = ng1, u0 = nu0, u1 = nu1;
+      if (valid && c + 16 < c0 + kHalf) {
+        ng0 = ld_global_v4(h + c + 16);
+        ng1 = ld_global_v4(h + c + 24);
+        nu0 = ld_global_v4(h + F + c + 16);
+        nu1 = ld_global_v4(h + F + c + 24);
+      }
       float g[16];
       tmem_ld16(taddr + c, g);
       tmem_ld_wait();
       if (valid) {
         float hg[16], hu[16], dhg[16], dhu[16], awv[16];
-        load_bf16x16(h + c, hg);
-        load_bf16x16(h + F + c, hu);
+        const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          unpack_bf16x2(gw[i], hg[2 * i], hg[2 * i + 1]);
+          unpack_bf16x2(uw[i], hu[2 * i], hu[2 * i + 1]);
+        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float s = sigmoidf_fast(hg[i]);
@@ -72,7 +98,10 @@ struct DownDgradProblem {
         store_bf16x16(aw + c, awv);
       }
     }
-    if (valid) static_cast<float*>(a.out2)[row * a.n_tiles + ti.n0 / BN] = dw;
+    // one router-weight partial per (row, n-tile, column half)
+    if (valid)
+      static_cast<float*>(a.out2)[row * (a.n_tiles * kEpiGroups) + (ti.n0 / BN) * kEpiGroups +
+                                  group] = dw;
   }
 };
 
@@ -90,6 +119,7 @@ struct GateUpDgradProblem {
   static constexpr bool kBMN = false;
   static constexpr bool kTailZero = false;
   static constexpr size_t kExtraSmem = 0;
+  static constexpr int kEpiGroups = 2;
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
   MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile(a, t, BN); }
@@ -104,9 +134,9 @@ struct GateUpDgradProblem {
     else
       tma_load_2d(sB, &a.mapB1, k0 - a.k_half, brow, bar);
   }
-  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, uint8_t*) {}
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               uint8_t*) {
+                               int group, uint8_t*) {
     const bool valid = r < ti.rows;
     const int64_t row = static_cast<int64_t>(ti.m0) + r;
     __nv_bfloat16* dst = nullptr;
@@ -115,7 +145,7 @@ struct GateUpDgradProblem {
       dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 + ti.n0;
     }
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
+    for (int c = group * (BN / 2); c < (group + 1) * (BN / 2); c += 16) {
       float v[16];
       tmem_ld16(taddr + c, v);
       tmem_ld_wait();
@@ -124,10 +154,10 @@ struct GateUpDgradProblem {
   }
 };
 
-// Stores a 128 x 256 fp32 accumulator tile as bf16 rows (weight gradients).
-MOE_DEV void store_tile_bf16(uint32_t taddr, bool valid, __nv_bfloat16* dst) {
+// Stores columns [c0, c1) of a fp32 accumulator row as bf16 (weight gradients).
+MOE_DEV void store_tile_bf16(uint32_t taddr, bool valid, __nv_bfloat16* dst, int c0, int c1) {
 #pragma unroll 1
-  for (int c = 0; c < 256; c += 16) {
+  for (int c = c0; c < c1; c += 16) {
     float v[16];
     tmem_ld16(taddr + c, v);
     tmem_ld_wait();
@@ -151,6 +181,7 @@ struct DownWgradProblem {
   static constexpr bool kBMN = true;
   static constexpr bool kTailZero = true;
   static constexpr size_t kExtraSmem = 0;
+  static constexpr int kEpiGroups = 2;
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_k_num_tiles(a); }
   MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_k_tile(a, t, BN); }
@@ -167,13 +198,15 @@ struct DownWgradProblem {
     return static_cast<__nv_bfloat16*>(a.out0) +
            (static_cast<int64_t>(ti.e) * a.M + ti.m0 + r) * a.ld0 + ti.n0;
   }
-  MOE_DEV static void epilogue_empty(const GemmArgs& a, const TileInfo& ti, int r, uint8_t*) {
-    if (r < ti.rows) zero_row_bf16(out_row(a, ti, r), BN);
+  MOE_DEV static void epilogue_empty(const GemmArgs& a, const TileInfo& ti, int r, int group,
+                                     uint8_t*) {
+    if (r < ti.rows) zero_row_bf16(out_row(a, ti, r) + group * (BN / 2), BN / 2);
   }
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               uint8_t*) {
+                               int group, uint8_t*) {
     const bool valid = r < ti.rows;
-    store_tile_bf16(taddr, valid, valid ? out_row(a, ti, r) : nullptr);
+    store_tile_bf16(taddr, valid, valid ? out_row(a, ti, r) : nullptr, group * (BN / 2),
+                    (group + 1) * (BN / 2));
   }
 };
 
@@ -190,6 +223,7 @@ struct GateUpWgradProblem {
   static constexpr bool kBMN = true;
   static constexpr bool kTailZero = true;
   static constexpr size_t kExtraSmem = 0;
+  static constexpr int kEpiGroups = 2;
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_k_num_tiles(a); }
   MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_k_tile(a, t, BN); }
@@ -209,19 +243,20 @@ struct GateUpWgradProblem {
     const int col = gc < F ? gc : gc - F;
     return base + (static_cast<int64_t>(ti.e) * a.M + ti.m0 + r) * F + col;
   }
-  MOE_DEV static void epilogue_empty(const GemmArgs& a, const TileInfo& ti, int r, uint8_t*) {
+  MOE_DEV static void epilogue_empty(const GemmArgs& a, const TileInfo& ti, int r, int group,
+                                     uint8_t*) {
     if (r >= ti.rows) return;
-    for (int c = 0; c < BN; c += 16) {
+    for (int c = group * (BN / 2); c < (group + 1) * (BN / 2); c += 16) {
       __nv_bfloat16* p = out_ptr(a, ti, r, ti.n0 + c);
       st_global_v4(p, 0u, 0u, 0u, 0u);
       st_global_v4(p + 8, 0u, 0u, 0u, 0u);
     }
   }
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               uint8_t*) {
+                               int group, uint8_t*) {
     const bool valid = r < ti.rows;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
+    for (int c = group * (BN / 2); c < (group + 1) * (BN / 2); c += 16) {
       float v[16];
       tmem_ld16(taddr + c, v);
       tmem_ld_wait();
@@ -243,6 +278,7 @@ struct RouterWgradProblem {
   static constexpr bool kBMN = true;
   static constexpr bool kTailZero = false;
   static constexpr size_t kExtraSmem = 0;
+  static constexpr int kEpiGroups = 2;
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return split_k_num_tiles(a); }
   MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return split_k_tile(a, t, BN); }
@@ -258,17 +294,19 @@ struct RouterWgradProblem {
     return static_cast<float*>(a.out0) +
            (static_cast<int64_t>(ti.e) * a.M + ti.m0 + r) * a.ld0 + ti.n0;
   }
-  MOE_DEV static void epilogue_empty(const GemmArgs& a, const TileInfo& ti, int r, uint8_t*) {
+  MOE_DEV static void epilogue_empty(const GemmArgs& a, const TileInfo& ti, int r, int group,
+                                     uint8_t*) {
     if (r >= ti.rows) return;
     float* p = out_row(a, ti, r);
-    for (int c = 0; c < BN; c += 4) st_global_v4(p + c, 0u, 0u, 0u, 0u);
+    for (int c = group * (BN / 2); c < (group + 1) * (BN / 2); c += 4)
+      st_global_v4(p + c, 0u, 0u, 0u, 0u);
   }
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               uint8_t*) {
+                               int group, uint8_t*) {
     const bool valid = r < ti.rows;
     float* p = valid ? out_row(a, ti, r) : nullptr;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
+    for (int c = group * (BN / 2); c < (group + 1) * (BN / 2); c += 16) {
       float v[16];
       tmem_ld16(taddr + c, v);
       tmem_ld_wait();
@@ -295,6 +333,7 @@ struct DenseProblem {
   static constexpr bool kBMN = B_MN;
   static constexpr bool kTailZero = false;
   static constexpr size_t kExtraSmem = 0;
+  static constexpr int kEpiGroups = 2;
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return dense_num_tiles(a); }
   MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return dense_tile(a, t, BN); }
@@ -315,13 +354,13 @@ struct DenseProblem {
       tma_load_2d(sB, &a.mapB0, k0, ti.n0, bar);
     }
   }
-  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, uint8_t*) {}
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               uint8_t*) {
+                               int group, uint8_t*) {
     const bool valid = r < ti.rows;
     float* p = static_cast<float*>(a.out0) + (static_cast<int64_t>(ti.m0) + r) * a.ld0 + ti.n0;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
+    for (int c = group * (BN / 2); c < (group + 1) * (BN / 2); c += 16) {
       float v[16];
       tmem_ld16(taddr + c, v);
       tmem_ld_wait();
