@@ -64,7 +64,7 @@ typedef enum {
   MOE_ERR_CUDA = 4,                 /* a CUDA runtime call failed           */
   MOE_ERR_TIMEOUT = 5,              /* a device-side bounded wait ran out   */
   MOE_ERR_UNSUPPORTED_DEVICE = 6,   /* not an sm_103 GPU                    */
-  MOE_ERR_NOT_IMPLEMENTED = 7       /* precision mode not built yet         */
+  MOE_ERR_NOT_IMPLEMENTED = 7       /* reserved: a feature this build lacks */
 } moe_status_t;
 
 /* flags */
@@ -176,6 +176,17 @@ moe_status_t moe_route_noalloc(const moe_config_t* cfg, const moe_bf16_t* x,
                                int32_t* topk_idx, float* topk_w, int32_t* counts,
                                int32_t* offsets, int32_t* perm_token, int32_t* slot_row,
                                int32_t* device_status, moe_stream_t stream);
+
+/* Dense MXFP8 GEMM on the block-scaled engine: quantises A [M, K] and B [N, K]
+ * (bf16, row-major) to E4M3 with an E8M0 scale per 32 elements along K (the
+ * OCP MX rule of the precision modes above), then D[M, N] (fp32, row-major) =
+ * sum_k A_q(m, k) B_q(n, k) with fp32 accumulation.  Limits: M >= 1; N and K
+ * multiples of 128.  Workspace: call with ws = NULL to receive the size in
+ * *ws_bytes; otherwise *ws_bytes is the workspace size (256-byte aligned).
+ * Used to test the engine's MXFP8 path in isolation. */
+moe_status_t moe_gemm_mxfp8(int64_t M, int64_t N, int64_t K, const moe_bf16_t* A,
+                            const moe_bf16_t* B, float* D, void* ws, size_t* ws_bytes,
+                            moe_stream_t stream);
 
 /* Reads the device status word of a workspace after the work queued on
  * `stream` has finished (this call synchronises the stream).  Returns

@@ -84,6 +84,21 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D byte (E4M3) tensor map: [rows, cols] bytes, 128 x 128-byte boxes with
+// the 128-byte swizzle.
+bool make_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                 uint64_t row_stride_bytes, uint32_t box_rows = 128) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------- profiling
 
 struct Pending {
@@ -177,6 +192,11 @@ struct Layout {
       c_order, c_wrt, c_xperm, c_h, c_total;
   // backward workspace
   size_t b_status, b_dyp, b_dh, b_aw, b_dwp, b_dl, b_dlt, b_scratch, b_wrp, b_total;
+  // MXFP8 buffers (E4M3 data + scale atoms); present only when the precision uses them
+  int64_t mt_max;    // upper bound of the 128-row m-tiles (= K-tiles of the padded token layout)
+  size_t fq_x, fs_x, fq_a, fs_a, fq_wgu, fs_wgu, fq_wd, fs_wd;
+  size_t bq_dy, bs_dy, bq_wdh, bs_wdh, bq_dh, bs_dh, bq_wg, bs_wg, bq_wu, bs_wu;
+  size_t bq_awt, bs_awt, bq_dyt, bs_dyt, bq_xt, bs_xt, bq_dht, bs_dht;
 };
 
 Layout make_layout(const moe_config_t& c, int sms) {
@@ -191,7 +211,8 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.ntiles = static_cast<int>((L.T + kBM - 1) / kBM);
   L.router_bn = next_pow2_at_least16(L.E);
   L.dgrad_bn = (L.F % 256 == 0) ? 256 : 128;
-  L.nparts = (L.F / L.dgrad_bn) * 2;   // one partial per n-tile and epilogue column half
+  // one router-weight partial per n-tile and epilogue column half (MXFP8 tiles are 128 wide)
+  L.nparts = (c.precision == MOE_BF16 ? L.F / L.dgrad_bn : L.F / 128) * 2;
   L.wr_mtiles = (L.E + kBM - 1) / kBM;
   L.wr_ntiles = L.H / 256;
   const int total_kb = static_cast<int>((L.T + kBK - 1) / kBK);
@@ -213,6 +234,18 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.r_order = f.take(sizeof(int) * E);
   L.f_a = f.take(2 * P * F);
   L.f_scratch = f.take(2 * P * H);
+  L.mt_max = (L.P + kBM - 1) / kBM + L.E;
+  const size_t mt = static_cast<size_t>(L.mt_max);
+  if (c.precision == MOE_MXFP8) {
+    L.fq_x = f.take(P * H);
+    L.fs_x = f.take(mt * (H / 128) * 512);
+    L.fq_a = f.take(P * F);
+    L.fs_a = f.take(mt * (F / 128) * 512);
+    L.fq_wgu = f.take(E * H * 2 * F);
+    L.fs_wgu = f.take(E * (2 * F / 128) * (H / 128) * 512);
+    L.fq_wd = f.take(E * F * H);
+    L.fs_wd = f.take(E * (H / 128) * (F / 128) * 512);
+  }
   L.f_total = f.off;
 
   Carver x;
@@ -241,6 +274,27 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.b_dlt = b.take(2 * E * static_cast<size_t>(L.T_pad));
   L.b_scratch = b.take(2 * P * H);
   L.b_wrp = b.take(sizeof(float) * L.wr_split * E * H);
+  if (c.precision != MOE_BF16) {
+    const size_t Pp = 128 * mt;   // padded token rows
+    L.bq_dy = b.take(P * H);
+    L.bs_dy = b.take(mt * (H / 128) * 512);
+    L.bq_wdh = b.take(E * F * H);
+    L.bs_wdh = b.take(E * (F / 128) * (H / 128) * 512);
+    L.bq_dh = b.take(P * 2 * F);
+    L.bs_dh = b.take(mt * (2 * F / 128) * 512);
+    L.bq_wg = b.take(E * H * F);
+    L.bs_wg = b.take(E * (H / 128) * (F / 128) * 512);
+    L.bq_wu = b.take(E * H * F);
+    L.bs_wu = b.take(E * (H / 128) * (F / 128) * 512);
+    L.bq_awt = b.take(Pp * F);
+    L.bs_awt = b.take(mt * (F / 128) * 512);
+    L.bq_dyt = b.take(Pp * H);
+    L.bs_dyt = b.take(mt * (H / 128) * 512);
+    L.bq_xt = b.take(Pp * H);
+    L.bs_xt = b.take(mt * (H / 128) * 512);
+    L.bq_dht = b.take(Pp * 2 * F);
+    L.bs_dht = b.take(mt * (2 * F / 128) * 512);
+  }
   L.b_total = b.off;
   (void)T;
   return L;
@@ -349,6 +403,273 @@ bool all_aligned16(std::initializer_list<const void*> ps) {
   return true;
 }
 
+
+// ---------------------------------------------------------------- MXFP8 passes
+
+// F7 + F8 and F9 in MXFP8: quantise the gate/up operands (x_perm along H;
+// W_gate / W_up along H, interleaved per 128 columns), the block-scaled
+// gate/up GEMM with SwiGLU, quantise a along F and W_down along F, then the
+// block-scaled down GEMM with the weighted scatter.
+moe_status_t forward_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t fl,
+                              DeviceStatus* st, const uint16_t* xperm, const uint16_t* W_gate,
+                              const uint16_t* W_up, const uint16_t* W_down, const int* offsets,
+                              const int* mtile, const float* w_row, const int* row_slot,
+                              uint16_t* act, uint16_t* h, uint16_t* scratch, void* ws) {
+  uint8_t* xq = at<uint8_t>(ws, L.fq_x);
+  uint8_t* sx = at<uint8_t>(ws, L.fs_x);
+  uint8_t* aq = at<uint8_t>(ws, L.fq_a);
+  uint8_t* sa = at<uint8_t>(ws, L.fs_a);
+  uint8_t* wgu = at<uint8_t>(ws, L.fq_wgu);
+  uint8_t* swgu = at<uint8_t>(ws, L.fs_wgu);
+  uint8_t* wd = at<uint8_t>(ws, L.fq_wd);
+  uint8_t* swd = at<uint8_t>(ws, L.fs_wd);
+  MOE_TRY(run("mx_quant_x", s, fl, [&] {
+    return launch_quant_rows_permuted(xperm, L.P, L.H, xq, sx, offsets, mtile, L.E, s);
+  }));
+  MOE_TRY(run("mx_quant_w_gate_up", s, fl, [&] {
+    return launch_quant_cols_gate_up(W_gate, W_up, L.E, L.H, L.F, wgu, swgu, s);
+  }));
+  {
+    GemmArgs a = base_args(st, fl);
+    if (!make_map_u8(&a.mapA, xq, L.H, L.P, L.H) ||
+        !make_map_u8(&a.mapB0, wgu, 2ull * L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F))
+      return MOE_ERR_CUDA;
+    a.mapB1 = a.mapB0;
+    a.K = L.H;
+    a.N = 2 * L.F;
+    a.n_tiles = 2 * L.F / 128;
+    a.num_groups = L.E;
+    a.b_group_rows = L.H;
+    a.offsets = offsets;
+    a.mtile_off = mtile;
+    a.out0 = act;
+    a.out1 = h;
+    a.ld0 = L.F;
+    a.sfA = sx;
+    a.kt_a = L.H / 128;
+    a.sfB0 = swgu;
+    a.kt_b = L.H / 128;
+    if (fl & MOE_FLAG_TEST_TIMEOUT) {
+      a.flags = 2u;
+      a.wait_limit_ns = kTestWaitNs;
+    }
+    const int grid = grid_for(((L.P + kBM - 1) / kBM + L.E) * a.n_tiles, sms);
+    MOE_TRY(run("gate_up_gemm_swiglu_mx", s, fl, [&] { return launch_gate_up_fwd_mx(a, grid, s); }));
+  }
+  MOE_TRY(run("mx_quant_a", s, fl, [&] {
+    return launch_quant_rows_permuted(act, L.P, L.F, aq, sa, offsets, mtile, L.E, s);
+  }));
+  MOE_TRY(run("mx_quant_w_down_f", s, fl, [&] {
+    return launch_quant_cols_weights(W_down, L.E, L.F, L.H, wd, swd, s);
+  }));
+  {
+    GemmArgs a = base_args(st, fl);
+    if (!make_map_u8(&a.mapA, aq, L.F, L.P, L.F) ||
+        !make_map_u8(&a.mapB0, wd, L.H, static_cast<uint64_t>(L.E) * L.F, L.H))
+      return MOE_ERR_CUDA;
+    a.mapB1 = a.mapB0;
+    a.K = L.F;
+    a.N = L.H;
+    a.n_tiles = L.H / 128;
+    a.num_groups = L.E;
+    a.b_group_rows = L.F;
+    a.offsets = offsets;
+    a.mtile_off = mtile;
+    a.in0 = w_row;
+    a.in1 = row_slot;
+    a.out0 = scratch;
+    a.ld0 = L.H;
+    a.sfA = sa;
+    a.kt_a = L.F / 128;
+    a.sfB0 = swd;
+    a.kt_b = L.F / 128;
+    const int grid = grid_for(((L.P + kBM - 1) / kBM + L.E) * a.n_tiles, sms);
+    MOE_TRY(run("down_gemm_scatter_mx", s, fl, [&] { return launch_down_fwd_mx(a, grid, s); }));
+  }
+  return MOE_OK;
+}
+
+
+struct BwdBufs {
+  const uint16_t *W_gate, *W_up, *W_down, *dyp, *xperm, *h;
+  const int *offsets, *mtile, *order, *slot, *row_slot;
+  const float *w_row, *w;
+  const int* idx;
+  const uint16_t* wrt;
+  uint16_t *dh, *aw;
+  float *dwp, *dl;
+  uint16_t *dlt, *scratch, *dx, *dW_gate, *dW_up, *dW_down;
+  void* ws;
+};
+
+// B2-B9 in MXFP8 (precision mxfp8 and fp8_bwd): every expert GEMM of the
+// backward runs block-scaled on operands quantised along its K: dY_perm and
+// W_down along H (down dgrad), dh along F and W_gate / W_up along F (gate/up
+// dgrad), and w*a, dY_perm, x_perm, dh along the tokens of each expert (the
+// weight gradients, segments padded to 128 rows).
+moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t fl,
+                                      DeviceStatus* st, const BwdBufs& b) {
+  void* ws = b.ws;
+  uint8_t* dyq = at<uint8_t>(ws, L.bq_dy);
+  uint8_t* sdy = at<uint8_t>(ws, L.bs_dy);
+  uint8_t* wdh = at<uint8_t>(ws, L.bq_wdh);
+  uint8_t* swdh = at<uint8_t>(ws, L.bs_wdh);
+  uint8_t* dhq = at<uint8_t>(ws, L.bq_dh);
+  uint8_t* sdh = at<uint8_t>(ws, L.bs_dh);
+  uint8_t* wg = at<uint8_t>(ws, L.bq_wg);
+  uint8_t* swg = at<uint8_t>(ws, L.bs_wg);
+  uint8_t* wu = at<uint8_t>(ws, L.bq_wu);
+  uint8_t* swu = at<uint8_t>(ws, L.bs_wu);
+  uint8_t* awt = at<uint8_t>(ws, L.bq_awt);
+  uint8_t* sawt = at<uint8_t>(ws, L.bs_awt);
+  uint8_t* dyt = at<uint8_t>(ws, L.bq_dyt);
+  uint8_t* sdyt = at<uint8_t>(ws, L.bs_dyt);
+  uint8_t* xt = at<uint8_t>(ws, L.bq_xt);
+  uint8_t* sxt = at<uint8_t>(ws, L.bs_xt);
+  uint8_t* dht = at<uint8_t>(ws, L.bq_dht);
+  uint8_t* sdht = at<uint8_t>(ws, L.bs_dht);
+  const uint64_t Pp = 128ull * static_cast<uint64_t>(L.mt_max);
+  const int64_t mtiles = (L.P + kBM - 1) / kBM + L.E;
+
+  // B2-B4: down dgrad
+  MOE_TRY(run("mx_quant_dy", s, fl, [&] {
+    return launch_quant_rows_permuted(b.dyp, L.P, L.H, dyq, sdy, b.offsets, b.mtile, L.E, s);
+  }));
+  MOE_TRY(run("mx_quant_w_down_h", s, fl, [&] {
+    return launch_quant_rows_dense(b.W_down, static_cast<int64_t>(L.E) * L.F, L.H, wdh, swdh, s);
+  }));
+  {
+    GemmArgs a = base_args(st, fl);
+    if (!make_map_u8(&a.mapA, dyq, L.H, L.P, L.H) ||
+        !make_map_u8(&a.mapB0, wdh, L.H, static_cast<uint64_t>(L.E) * L.F, L.H))
+      return MOE_ERR_CUDA;
+    a.mapB1 = a.mapB0;
+    a.K = L.H;
+    a.N = L.F;
+    a.n_tiles = L.F / 128;
+    a.num_groups = L.E;
+    a.b_group_rows = L.F;
+    a.offsets = b.offsets;
+    a.mtile_off = b.mtile;
+    a.in0 = b.h;
+    a.in1 = b.w_row;
+    a.out0 = b.dh;
+    a.out1 = b.aw;
+    a.out2 = b.dwp;
+    a.ld0 = L.F;
+    a.sfA = sdy;
+    a.kt_a = L.H / 128;
+    a.sfB0 = swdh;
+    a.kt_b = L.H / 128;
+    if (fl & MOE_FLAG_TEST_TIMEOUT) {
+      a.flags = 2u;
+      a.wait_limit_ns = kTestWaitNs;
+    }
+    const int grid = grid_for(mtiles * a.n_tiles, sms);
+    MOE_TRY(run("down_dgrad_swiglu_bwd_mx", s, fl, [&] { return launch_down_dgrad_mx(a, grid, s); }));
+  }
+  // B9: router softmax / top-k backward
+  if (cudaMemsetAsync(b.dlt, 0, 2ull * L.E * L.T_pad, s) != cudaSuccess) return MOE_ERR_CUDA;
+  MOE_TRY(run("router_bwd", s, fl, [&] {
+    return launch_router_bwd(b.dwp, L.nparts, b.slot, b.w, b.idx, L.T, L.k, b.dl, b.dlt, L.T_pad, s);
+  }));
+  // B5: down wgrad over the padded token layout
+  MOE_TRY(run("mx_quant_aw_tokens", s, fl, [&] {
+    return launch_quant_cols_tokens(b.aw, L.mt_max, L.F, awt, sawt, b.offsets, b.mtile, L.E, s);
+  }));
+  MOE_TRY(run("mx_quant_dy_tokens", s, fl, [&] {
+    return launch_quant_cols_tokens(b.dyp, L.mt_max, L.H, dyt, sdyt, b.offsets, b.mtile, L.E, s);
+  }));
+  {
+    GemmArgs a = base_args(st, fl);
+    if (!make_map_u8(&a.mapA, awt, L.F, Pp, L.F) || !make_map_u8(&a.mapB0, dyt, L.H, Pp, L.H))
+      return MOE_ERR_CUDA;
+    a.mapB1 = a.mapB0;
+    a.M = L.F;
+    a.N = L.H;
+    a.m_tiles = L.F / 128;
+    a.n_tiles = L.H / 128;
+    a.num_groups = L.E;
+    a.offsets = b.offsets;
+    a.mtile_off = b.mtile;
+    a.group_order = b.order;
+    a.out0 = b.dW_down;
+    a.ld0 = L.H;
+    a.sfA = sawt;
+    a.sfB0 = sdyt;
+    const int grid = grid_for(static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles, sms);
+    MOE_TRY(run("down_wgrad_mx", s, fl, [&] { return launch_down_wgrad_mx(a, grid, s); }));
+  }
+  // B6 + B7: gate/up dgrad, then the un-permute
+  MOE_TRY(run("mx_quant_dh", s, fl, [&] {
+    return launch_quant_rows_permuted(b.dh, L.P, 2 * L.F, dhq, sdh, b.offsets, b.mtile, L.E, s);
+  }));
+  MOE_TRY(run("mx_quant_w_gate_f", s, fl, [&] {
+    return launch_quant_rows_dense(b.W_gate, static_cast<int64_t>(L.E) * L.H, L.F, wg, swg, s);
+  }));
+  MOE_TRY(run("mx_quant_w_up_f", s, fl, [&] {
+    return launch_quant_rows_dense(b.W_up, static_cast<int64_t>(L.E) * L.H, L.F, wu, swu, s);
+  }));
+  {
+    GemmArgs a = base_args(st, fl);
+    if (!make_map_u8(&a.mapA, dhq, 2ull * L.F, L.P, 2ull * L.F) ||
+        !make_map_u8(&a.mapB0, wg, L.F, static_cast<uint64_t>(L.E) * L.H, L.F) ||
+        !make_map_u8(&a.mapB1, wu, L.F, static_cast<uint64_t>(L.E) * L.H, L.F))
+      return MOE_ERR_CUDA;
+    a.K = 2 * L.F;
+    a.k_half = L.F;
+    a.N = L.H;
+    a.n_tiles = L.H / 128;
+    a.num_groups = L.E;
+    a.b_group_rows = L.H;
+    a.offsets = b.offsets;
+    a.mtile_off = b.mtile;
+    a.in1 = b.row_slot;
+    a.out0 = b.scratch;
+    a.ld0 = L.H;
+    a.sfA = sdh;
+    a.kt_a = 2 * L.F / 128;
+    a.sfB0 = swg;
+    a.sfB1 = swu;
+    a.kt_b = L.F / 128;
+    const int grid = grid_for(mtiles * a.n_tiles, sms);
+    MOE_TRY(run("gate_up_dgrad_scatter_mx", s, fl, [&] { return launch_gate_up_dgrad_mx(a, grid, s); }));
+  }
+  MOE_TRY(run("unpermute_dx", s, fl, [&] {
+    return launch_unpermute(b.scratch, b.dl, b.idx, b.wrt, b.dx, L.T, L.H, L.k, s);
+  }));
+  // B8: gate/up wgrad over the padded token layout
+  MOE_TRY(run("mx_quant_x_tokens", s, fl, [&] {
+    return launch_quant_cols_tokens(b.xperm, L.mt_max, L.H, xt, sxt, b.offsets, b.mtile, L.E, s);
+  }));
+  MOE_TRY(run("mx_quant_dh_tokens", s, fl, [&] {
+    return launch_quant_cols_tokens(b.dh, L.mt_max, 2 * L.F, dht, sdht, b.offsets, b.mtile, L.E, s);
+  }));
+  {
+    GemmArgs a = base_args(st, fl);
+    if (!make_map_u8(&a.mapA, xt, L.H, Pp, L.H) ||
+        !make_map_u8(&a.mapB0, dht, 2ull * L.F, Pp, 2ull * L.F))
+      return MOE_ERR_CUDA;
+    a.mapB1 = a.mapB0;
+    a.M = L.H;
+    a.N = 2 * L.F;
+    a.m_tiles = L.H / 128;
+    a.n_tiles = 2 * L.F / 128;
+    a.num_groups = L.E;
+    a.offsets = b.offsets;
+    a.mtile_off = b.mtile;
+    a.group_order = b.order;
+    a.out0 = b.dW_gate;
+    a.out1 = b.dW_up;
+    a.ld0 = L.F;
+    a.sfA = sxt;
+    a.sfB0 = sdht;
+    const int grid = grid_for(static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles, sms);
+    MOE_TRY(run("gate_up_wgrad_mx", s, fl, [&] { return launch_gate_up_wgrad_mx(a, grid, s); }));
+  }
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -407,7 +728,6 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
                          const moe_bf16_t* W_up, const moe_bf16_t* W_down, moe_bf16_t* y,
                          void* ctx, void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(validate(cfg));
-  if (cfg->precision == MOE_MXFP8) return MOE_ERR_NOT_IMPLEMENTED;
   if (!all_aligned16({x, W_r, W_gate, W_up, W_down, y}) || ctx == nullptr || ws == nullptr ||
       !aligned(ctx, 256) || !aligned(ws, 256) || !aligned(logit_bias, 4))
     return MOE_ERR_INVALID_ARG;
@@ -441,50 +761,55 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
   MOE_TRY(run("gather_x", s, fl,
               [&] { return launch_gather_rows(x, slot, xperm, L.T, L.H, L.k, s); }));
 
-  // F7 + F8: gate/up GEMM with SwiGLU
-  {
-    GemmArgs a = base_args(st, fl);
-    if (!make_map(&a.mapA, xperm, L.H, L.P, 2ull * L.H, 64, 128) ||
-        !make_map(&a.mapB0, W_gate, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 64) ||
-        !make_map(&a.mapB1, W_up, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 64))
-      return MOE_ERR_CUDA;
-    a.K = L.H;
-    a.N = 2 * L.F;
-    a.n_tiles = L.F / 128;
-    a.num_groups = L.E;
-    a.b_group_rows = L.H;
-    a.offsets = offsets;
-    a.mtile_off = mtile;
-    a.out0 = act;
-    a.out1 = h;
-    a.ld0 = L.F;
-    if (fl & MOE_FLAG_TEST_TIMEOUT) {
-      a.flags = 2u;
-      a.wait_limit_ns = kTestWaitNs;
+  if (cfg->precision == MOE_MXFP8) {
+    MOE_TRY(forward_gemms_mx(L, d.sms, s, fl, st, xperm, W_gate, W_up, W_down, offsets, mtile,
+                             w_row, row_slot, act, h, scratch, ws));
+  } else {
+    // F7 + F8: gate/up GEMM with SwiGLU
+    {
+      GemmArgs a = base_args(st, fl);
+      if (!make_map(&a.mapA, xperm, L.H, L.P, 2ull * L.H, 64, 128) ||
+          !make_map(&a.mapB0, W_gate, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 64) ||
+          !make_map(&a.mapB1, W_up, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 64))
+        return MOE_ERR_CUDA;
+      a.K = L.H;
+      a.N = 2 * L.F;
+      a.n_tiles = L.F / 128;
+      a.num_groups = L.E;
+      a.b_group_rows = L.H;
+      a.offsets = offsets;
+      a.mtile_off = mtile;
+      a.out0 = act;
+      a.out1 = h;
+      a.ld0 = L.F;
+      if (fl & MOE_FLAG_TEST_TIMEOUT) {
+        a.flags = 2u;
+        a.wait_limit_ns = kTestWaitNs;
+      }
+      const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
+      MOE_TRY(run("gate_up_gemm_swiglu", s, fl, [&] { return launch_gate_up_fwd(a, grid, s); }));
     }
-    const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
-    MOE_TRY(run("gate_up_gemm_swiglu", s, fl, [&] { return launch_gate_up_fwd(a, grid, s); }));
-  }
-  // F9 + F10: down GEMM with the weighted scatter, then the k-way combine
-  {
-    GemmArgs a = base_args(st, fl);
-    if (!make_map(&a.mapA, act, L.F, L.P, 2ull * L.F, 64, 128) ||
-        !make_map(&a.mapB0, W_down, L.H, static_cast<uint64_t>(L.E) * L.F, 2ull * L.H, 64, 64))
-      return MOE_ERR_CUDA;
-    a.mapB1 = a.mapB0;
-    a.K = L.F;
-    a.N = L.H;
-    a.n_tiles = L.H / 256;
-    a.num_groups = L.E;
-    a.b_group_rows = L.F;
-    a.offsets = offsets;
-    a.mtile_off = mtile;
-    a.in0 = w_row;
-    a.in1 = row_slot;
-    a.out0 = scratch;
-    a.ld0 = L.H;
-    const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
-    MOE_TRY(run("down_gemm_scatter", s, fl, [&] { return launch_down_fwd(a, grid, s); }));
+    // F9 + F10: down GEMM with the weighted scatter, then the k-way combine
+    {
+      GemmArgs a = base_args(st, fl);
+      if (!make_map(&a.mapA, act, L.F, L.P, 2ull * L.F, 64, 128) ||
+          !make_map(&a.mapB0, W_down, L.H, static_cast<uint64_t>(L.E) * L.F, 2ull * L.H, 64, 64))
+        return MOE_ERR_CUDA;
+      a.mapB1 = a.mapB0;
+      a.K = L.F;
+      a.N = L.H;
+      a.n_tiles = L.H / 256;
+      a.num_groups = L.E;
+      a.b_group_rows = L.F;
+      a.offsets = offsets;
+      a.mtile_off = mtile;
+      a.in0 = w_row;
+      a.in1 = row_slot;
+      a.out0 = scratch;
+      a.ld0 = L.H;
+      const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
+      MOE_TRY(run("down_gemm_scatter", s, fl, [&] { return launch_down_fwd(a, grid, s); }));
+    }
   }
   MOE_TRY(run("combine", s, fl, [&] { return launch_combine(scratch, y, L.T, L.H, L.k, s); }));
   return MOE_OK;
@@ -497,7 +822,6 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
                           moe_bf16_t* dW_up, moe_bf16_t* dW_down, void* ws, size_t ws_bytes,
                           moe_stream_t stream) {
   MOE_TRY(validate(cfg));
-  if (cfg->precision != MOE_BF16) return MOE_ERR_NOT_IMPLEMENTED;
   if (!all_aligned16({x, W_r, W_gate, W_up, W_down, dY, dx, dW_r, dW_gate, dW_up, dW_down}) ||
       ctx_in == nullptr || ws == nullptr || !aligned(ctx_in, 256) || !aligned(ws, 256))
     return MOE_ERR_INVALID_ARG;
@@ -536,102 +860,109 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
   MOE_TRY(run("gather_dy", s, fl,
               [&] { return launch_gather_rows(dY, slot, dyp, L.T, L.H, L.k, s); }));
 
-  // B2-B4: down dgrad with the SwiGLU backward and router-weight partials
-  {
-    GemmArgs a = base_args(st, fl);
-    if (!make_map(&a.mapA, dyp, L.H, L.P, 2ull * L.H, 64, 128) ||
-        !make_map(&a.mapB0, W_down, L.H, static_cast<uint64_t>(L.E) * L.F, 2ull * L.H, 64,
-                  L.dgrad_bn))
-      return MOE_ERR_CUDA;
-    a.mapB1 = a.mapB0;
-    a.K = L.H;
-    a.N = L.F;
-    a.n_tiles = L.F / L.dgrad_bn;
-    a.num_groups = L.E;
-    a.b_group_rows = L.F;
-    a.offsets = offsets;
-    a.mtile_off = mtile;
-    a.in0 = h;
-    a.in1 = w_row;
-    a.out0 = dh;
-    a.out1 = aw;
-    a.out2 = dwp;
-    a.ld0 = L.F;
-    if (fl & MOE_FLAG_TEST_TIMEOUT) {
-      a.flags = 2u;
-      a.wait_limit_ns = kTestWaitNs;
+  if (cfg->precision != MOE_BF16) {
+    const BwdBufs bb{W_gate, W_up, W_down, dyp, xperm, h, offsets, mtile, order, slot,
+                     row_slot, w_row, w, idx, wrt, dh, aw, dwp, dl, dlt, scratch, dx,
+                     dW_gate, dW_up, dW_down, ws};
+    MOE_TRY(backward_expert_gemms_mx(L, d.sms, s, fl, st, bb));
+  } else {
+    // B2-B4: down dgrad with the SwiGLU backward and router-weight partials
+    {
+      GemmArgs a = base_args(st, fl);
+      if (!make_map(&a.mapA, dyp, L.H, L.P, 2ull * L.H, 64, 128) ||
+          !make_map(&a.mapB0, W_down, L.H, static_cast<uint64_t>(L.E) * L.F, 2ull * L.H, 64,
+                    L.dgrad_bn))
+        return MOE_ERR_CUDA;
+      a.mapB1 = a.mapB0;
+      a.K = L.H;
+      a.N = L.F;
+      a.n_tiles = L.F / L.dgrad_bn;
+      a.num_groups = L.E;
+      a.b_group_rows = L.F;
+      a.offsets = offsets;
+      a.mtile_off = mtile;
+      a.in0 = h;
+      a.in1 = w_row;
+      a.out0 = dh;
+      a.out1 = aw;
+      a.out2 = dwp;
+      a.ld0 = L.F;
+      if (fl & MOE_FLAG_TEST_TIMEOUT) {
+        a.flags = 2u;
+        a.wait_limit_ns = kTestWaitNs;
+      }
+      const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
+      MOE_TRY(run("down_dgrad_swiglu_bwd", s, fl,
+                  [&] { return launch_down_dgrad(L.dgrad_bn, a, grid, s); }));
     }
-    const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
-    MOE_TRY(run("down_dgrad_swiglu_bwd", s, fl,
-                [&] { return launch_down_dgrad(L.dgrad_bn, a, grid, s); }));
-  }
-  // B9: router softmax / top-k backward
-  if (cudaMemsetAsync(dlt, 0, 2ull * L.E * L.T_pad, s) != cudaSuccess) return MOE_ERR_CUDA;
-  MOE_TRY(run("router_bwd", s, fl, [&] {
-    return launch_router_bwd(dwp, L.nparts, slot, w, idx, L.T, L.k, dl, dlt, L.T_pad, s);
-  }));
-  // B5: down wgrad over ragged K
-  {
-    GemmArgs a = base_args(st, fl);
-    if (!make_map(&a.mapA, aw, L.F, L.P, 2ull * L.F, 64, 64) ||
-        !make_map(&a.mapB0, dyp, L.H, L.P, 2ull * L.H, 64, 64))
-      return MOE_ERR_CUDA;
-    a.mapB1 = a.mapB0;
-    a.M = L.F;
-    a.N = L.H;
-    a.m_tiles = L.F / 128;
-    a.n_tiles = L.H / 256;
-    a.num_groups = L.E;
-    a.offsets = offsets;
-    a.group_order = order;
-    a.out0 = dW_down;
-    a.ld0 = L.H;
-    const int grid = grid_for(static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles, d.sms);
-    MOE_TRY(run("down_wgrad", s, fl, [&] { return launch_down_wgrad(a, grid, s); }));
-  }
-  // B6 + B7: gate/up dgrad with the scatter, then the un-permute (+ router dgrad)
-  {
-    GemmArgs a = base_args(st, fl);
-    if (!make_map(&a.mapA, dh, 2ull * L.F, L.P, 4ull * L.F, 64, 128) ||
-        !make_map(&a.mapB0, W_gate, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 256) ||
-        !make_map(&a.mapB1, W_up, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 256))
-      return MOE_ERR_CUDA;
-    a.K = 2 * L.F;
-    a.k_half = L.F;
-    a.N = L.H;
-    a.n_tiles = L.H / 256;
-    a.num_groups = L.E;
-    a.b_group_rows = L.H;
-    a.offsets = offsets;
-    a.mtile_off = mtile;
-    a.in1 = row_slot;
-    a.out0 = scratch;
-    a.ld0 = L.H;
-    const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
-    MOE_TRY(run("gate_up_dgrad_scatter", s, fl, [&] { return launch_gate_up_dgrad(a, grid, s); }));
-  }
-  MOE_TRY(run("unpermute_dx", s, fl, [&] {
-    return launch_unpermute(scratch, dl, idx, wrt, dx, L.T, L.H, L.k, s);
-  }));
-  // B8: gate/up wgrad over ragged K
-  {
-    GemmArgs a = base_args(st, fl);
-    if (!make_map(&a.mapA, xperm, L.H, L.P, 2ull * L.H, 64, 64) ||
-        !make_map(&a.mapB0, dh, 2ull * L.F, L.P, 4ull * L.F, 64, 64))
-      return MOE_ERR_CUDA;
-    a.mapB1 = a.mapB0;
-    a.M = L.H;
-    a.N = 2 * L.F;
-    a.m_tiles = L.H / 128;
-    a.n_tiles = (2 * L.F) / 256;
-    a.num_groups = L.E;
-    a.offsets = offsets;
-    a.group_order = order;
-    a.out0 = dW_gate;
-    a.out1 = dW_up;
-    a.ld0 = L.F;
-    const int grid = grid_for(static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles, d.sms);
-    MOE_TRY(run("gate_up_wgrad", s, fl, [&] { return launch_gate_up_wgrad(a, grid, s); }));
+    // B9: router softmax / top-k backward
+    if (cudaMemsetAsync(dlt, 0, 2ull * L.E * L.T_pad, s) != cudaSuccess) return MOE_ERR_CUDA;
+    MOE_TRY(run("router_bwd", s, fl, [&] {
+      return launch_router_bwd(dwp, L.nparts, slot, w, idx, L.T, L.k, dl, dlt, L.T_pad, s);
+    }));
+    // B5: down wgrad over ragged K
+    {
+      GemmArgs a = base_args(st, fl);
+      if (!make_map(&a.mapA, aw, L.F, L.P, 2ull * L.F, 64, 64) ||
+          !make_map(&a.mapB0, dyp, L.H, L.P, 2ull * L.H, 64, 64))
+        return MOE_ERR_CUDA;
+      a.mapB1 = a.mapB0;
+      a.M = L.F;
+      a.N = L.H;
+      a.m_tiles = L.F / 128;
+      a.n_tiles = L.H / 256;
+      a.num_groups = L.E;
+      a.offsets = offsets;
+      a.group_order = order;
+      a.out0 = dW_down;
+      a.ld0 = L.H;
+      const int grid = grid_for(static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles, d.sms);
+      MOE_TRY(run("down_wgrad", s, fl, [&] { return launch_down_wgrad(a, grid, s); }));
+    }
+    // B6 + B7: gate/up dgrad with the scatter, then the un-permute (+ router dgrad)
+    {
+      GemmArgs a = base_args(st, fl);
+      if (!make_map(&a.mapA, dh, 2ull * L.F, L.P, 4ull * L.F, 64, 128) ||
+          !make_map(&a.mapB0, W_gate, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 256) ||
+          !make_map(&a.mapB1, W_up, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 256))
+        return MOE_ERR_CUDA;
+      a.K = 2 * L.F;
+      a.k_half = L.F;
+      a.N = L.H;
+      a.n_tiles = L.H / 256;
+      a.num_groups = L.E;
+      a.b_group_rows = L.H;
+      a.offsets = offsets;
+      a.mtile_off = mtile;
+      a.in1 = row_slot;
+      a.out0 = scratch;
+      a.ld0 = L.H;
+      const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
+      MOE_TRY(run("gate_up_dgrad_scatter", s, fl, [&] { return launch_gate_up_dgrad(a, grid, s); }));
+    }
+    MOE_TRY(run("unpermute_dx", s, fl, [&] {
+      return launch_unpermute(scratch, dl, idx, wrt, dx, L.T, L.H, L.k, s);
+    }));
+    // B8: gate/up wgrad over ragged K
+    {
+      GemmArgs a = base_args(st, fl);
+      if (!make_map(&a.mapA, xperm, L.H, L.P, 2ull * L.H, 64, 64) ||
+          !make_map(&a.mapB0, dh, 2ull * L.F, L.P, 4ull * L.F, 64, 64))
+        return MOE_ERR_CUDA;
+      a.mapB1 = a.mapB0;
+      a.M = L.H;
+      a.N = 2 * L.F;
+      a.m_tiles = L.H / 128;
+      a.n_tiles = (2 * L.F) / 256;
+      a.num_groups = L.E;
+      a.offsets = offsets;
+      a.group_order = order;
+      a.out0 = dW_gate;
+      a.out1 = dW_up;
+      a.ld0 = L.F;
+      const int grid = grid_for(static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles, d.sms);
+      MOE_TRY(run("gate_up_wgrad", s, fl, [&] { return launch_gate_up_wgrad(a, grid, s); }));
+    }
   }
   // B10: router weight gradient dW_r = x^T dl (split-K, then reduce + transpose)
   {
@@ -691,6 +1022,55 @@ moe_status_t moe_gemm_bf16(int64_t M, int64_t N, int64_t K, const moe_bf16_t* A,
   return run("dense_gemm", s, 0, [&] {
     return launch_dense(!a_kmajor, !b_kmajor, a, grid_for(tiles, d.sms), s);
   });
+}
+
+moe_status_t moe_gemm_mxfp8(int64_t M, int64_t N, int64_t K, const moe_bf16_t* A,
+                            const moe_bf16_t* B, float* D, void* ws, size_t* ws_bytes,
+                            moe_stream_t stream) {
+  if (ws_bytes == nullptr) return MOE_ERR_INVALID_ARG;
+  if (M < 1 || N < 128 || K < 128 || N % 128 != 0 || K % 128 != 0 || M >= (1ll << 31) ||
+      N >= (1ll << 31) || K >= (1ll << 31))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  const size_t mt = static_cast<size_t>((M + 127) / 128), nt = static_cast<size_t>(N / 128);
+  const size_t kt = static_cast<size_t>(K / 128);
+  Carver c;
+  const size_t o_st = c.take(sizeof(DeviceStatus));
+  const size_t o_aq = c.take(static_cast<size_t>(M) * K);
+  const size_t o_bq = c.take(static_cast<size_t>(N) * K);
+  const size_t o_sa = c.take(mt * kt * 512);
+  const size_t o_sb = c.take(nt * kt * 512);
+  if (ws == nullptr) {
+    *ws_bytes = c.off;
+    return MOE_OK;
+  }
+  if (*ws_bytes < c.off) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (!all_aligned16({A, B, D}) || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  DevInfo d;
+  MOE_TRY(current_device(&d));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DeviceStatus* st = at<DeviceStatus>(ws, o_st);
+  if (cudaMemsetAsync(st, 0, sizeof(DeviceStatus), s) != cudaSuccess) return MOE_ERR_CUDA;
+  uint8_t* aq = at<uint8_t>(ws, o_aq);
+  uint8_t* bq = at<uint8_t>(ws, o_bq);
+  uint8_t* sa = at<uint8_t>(ws, o_sa);
+  uint8_t* sb = at<uint8_t>(ws, o_sb);
+  MOE_TRY(run("mx_quant_dense_a", s, 0, [&] { return launch_quant_rows_dense(A, M, static_cast<int>(K), aq, sa, s); }));
+  MOE_TRY(run("mx_quant_dense_b", s, 0, [&] { return launch_quant_rows_dense(B, N, static_cast<int>(K), bq, sb, s); }));
+  GemmArgs a = base_args(st, 0);
+  if (!make_map_u8(&a.mapA, aq, K, M, K) || !make_map_u8(&a.mapB0, bq, K, N, K)) return MOE_ERR_CUDA;
+  a.mapB1 = a.mapB0;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.n_tiles = static_cast<int>(nt);
+  a.out0 = D;
+  a.ld0 = static_cast<int>(N);
+  a.sfA = sa;
+  a.kt_a = static_cast<int>(kt);
+  a.sfB0 = sb;
+  a.kt_b = static_cast<int>(kt);
+  const int64_t tiles = static_cast<int64_t>(mt * nt);
+  return run("dense_gemm_mx", s, 0, [&] { return launch_dense_mx(a, grid_for(tiles, d.sms), s); });
 }
 
 moe_status_t moe_get_device_status(const void* ws, moe_stream_t stream) {

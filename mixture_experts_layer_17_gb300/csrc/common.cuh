@@ -278,3 +278,84 @@ MOE_DEV void load_bf16x16(const void* p, float (&v)[16]) {
 MOE_DEV float sigmoidf_fast(float z) { return 1.0f / (1.0f + __expf(-z)); }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------- MXFP8
+
+#include <cuda_fp8.h>
+
+namespace moe {
+
+// 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of
+// 16), completion through the mbarrier's transaction count.
+MOE_DEV void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gmem_src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Copies one 512-byte scale-factor atom (128 MN-rows x 4 K-blocks of 32,
+// row r at byte 16*(r%32) + 4*(r/32) + kblock) from shared memory into four
+// TMEM columns, replicated to the four lane quarters.  The TMEM column must be
+// a multiple of 4.
+MOE_DEV void sf_copy_to_tmem(uint32_t tmem_col_addr, const void* smem_atom) {
+  const uint64_t desc = static_cast<uint64_t>((smem_u32(smem_atom) & 0x3FFFFu) >> 4) |
+                        (static_cast<uint64_t>(128u >> 4) << 16) |
+                        (static_cast<uint64_t>(128u >> 4) << 32) | (1ull << 46);
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tmem_col_addr), "l"(desc)
+               : "memory");
+}
+
+// D[tmem] (+)= (A * 2^sfA) (B * 2^sfB)^T for one K = 32 block of E4M3 operands
+// with E8M0 block scales (OCP MX), cta_group::1.  sf_id in the instruction
+// descriptor picks the K-block byte inside the 4-block scale column group.
+MOE_DEV void mma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                      uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with E4M3 A/B, UE8M0 scales:
+// bits 4-5 B scale id, 7-9 A format (0 = E4M3), 10-12 B format, 15/16 majors,
+// 17-22 N >> 3, 23 scale format (1 = UE8M0), 24-28 M >> 4, 29-30 A scale id.
+__host__ __device__ constexpr uint32_t make_idesc_mxf8(int M, int N, bool a_mn, bool b_mn) {
+  return ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((static_cast<uint32_t>(N) >> 3) << 17) | (1u << 23) |
+         ((static_cast<uint32_t>(M) >> 4) << 24);
+}
+
+MOE_DEV uint32_t idesc_with_sf_id(uint32_t idesc, uint32_t sf_id) {
+  return idesc | (sf_id << 4) | (sf_id << 29);
+}
+
+// OCP MX shared exponent of a block with absolute maximum amax:
+// floor(log2(amax)) - 8 (8 = exponent of E4M3's largest power of two),
+// clamped to E8M0's [-127, 127]; an all-zero block takes -127.
+MOE_DEV int mx_exponent(float amax) {
+  if (!(amax > 0.f)) return -127;
+  int e;
+  frexpf(amax, &e);            // amax = m * 2^e, m in [0.5, 1)
+  const int x = (e - 1) - 8;
+  return x < -127 ? -127 : (x > 127 ? 127 : x);
+}
+
+// Four fp32 values scaled by 2^-X, rounded to nearest even E4M3 with
+// saturation to +-448, packed little-endian into one word.
+MOE_DEV uint32_t to_e4m3x4(float a, float b, float c, float d, float inv_scale) {
+  const __nv_fp8x2_storage_t lo =
+      __nv_cvt_float2_to_fp8x2(make_float2(a * inv_scale, b * inv_scale), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi =
+      __nv_cvt_float2_to_fp8x2(make_float2(c * inv_scale, d * inv_scale), __NV_SATFINITE, __NV_E4M3);
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// byte offset of (MN row r in [0,128), K-block kb in [0,4)) inside an atom
+MOE_DEV int sf_atom_offset(int r, int kb) { return 16 * (r & 31) + 4 * (r >> 5) + kb; }
+
+}  // namespace moe

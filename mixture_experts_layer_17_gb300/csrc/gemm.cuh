@@ -16,6 +16,8 @@
 //   and their wgrads over ragged per-expert token counts.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace moe {
@@ -57,6 +59,11 @@ struct GemmArgs {
   int top_k;
   int ld0;
   int ld1;
+  const uint8_t* sfA;   // MXFP8: scale atoms of A
+  const uint8_t* sfB0;  // MXFP8: scale atoms of B (first map)
+  const uint8_t* sfB1;  // MXFP8: scale atoms of B (second map)
+  int kt_a;             // MXFP8: K-tiles (of 128) per atom row of A
+  int kt_b;             // MXFP8: K-tiles (of 128) per atom row of B
   DeviceStatus* status;
   uint64_t wait_limit_ns;
   uint32_t flags;      // bit 1: inject a wait that nothing signals (timeout test)
@@ -185,36 +192,64 @@ MOE_DEV TileInfo split_k_tile(const GemmArgs& a, int t, int BN) {
 
 // ------------------------------------------------------------ engine
 
-template <int BN>
+// Problems with `static constexpr bool kMX = true` run on MXFP8 operands.
+template <class P, class = void>
+struct IsMX : std::false_type {};
+template <class P>
+struct IsMX<P, std::void_t<decltype(P::kMX)>> : std::integral_constant<bool, P::kMX> {};
+
+// Stage geometry.  bf16: a stage holds K = 64 (128 bytes per row).  MXFP8: a
+// stage holds K = 128 E4M3 (128 bytes per row) plus one 512-byte scale atom
+// for A and BN/128 for B; accumulators use TMEM columns [0, 2*BN) and the
+// stage's scales are copied to columns 256 + 8*stage (A) and +4 (B).
+template <class P, bool MX = IsMX<P>::value>
 struct StageCfg {
+  static constexpr int BN = P::BN;
   static constexpr uint32_t kABytes = kBM * kBK * 2;
   static constexpr uint32_t kBBytes = BN * kBK * 2;
+  static constexpr uint32_t kSFBytes = 0;
   static constexpr int kStages = (BN >= 256) ? 4 : (BN >= 128 ? 6 : 8);
   static constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
 };
 
 template <class P>
+struct StageCfg<P, true> {
+  static constexpr int BN = P::BN;
+  static_assert(BN == 128, "MXFP8 tiles are 128 x 128");
+  static constexpr uint32_t kABytes = kBM * 128;
+  static constexpr uint32_t kBBytes = BN * 128;
+  static constexpr uint32_t kSFBytes = 512 + (BN / 128) * 512;
+  static constexpr int kStages = 6;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kSFCol0 = 256;
+};
+
+template <class P>
 constexpr size_t gemm_smem_bytes() {
-  using C = StageCfg<P::BN>;
-  return 1024 + static_cast<size_t>(C::kStages) * (C::kABytes + C::kBBytes) + 256 +
+  using C = StageCfg<P>;
+  return 1024 + static_cast<size_t>(C::kStages) * (C::kABytes + C::kBBytes + C::kSFBytes) + 256 +
          P::kExtraSmem;
 }
 
 template <class P>
 __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid_constant__ GemmArgs args) {
   constexpr int BN = P::BN;
-  using C = StageCfg<BN>;
+  constexpr bool kMX = IsMX<P>::value;
+  using C = StageCfg<P>;
   constexpr int S = C::kStages;
   constexpr uint32_t kA = C::kABytes;
   constexpr uint32_t kB = C::kBBytes;
-  constexpr uint32_t kIdesc = make_idesc_bf16(kBM, BN, P::kAMN, P::kBMN);
+  constexpr uint32_t kSF = C::kSFBytes;
+  constexpr uint32_t kIdesc = kMX ? make_idesc_mxf8(kBM, BN, P::kAMN, P::kBMN)
+                                  : make_idesc_bf16(kBM, BN, P::kAMN, P::kBMN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + S * kA;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sB + S * kB);
+  uint8_t* sSF = sB + S * kB;              // MXFP8 only: [S][kSF] scale atoms
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sSF + S * kSF);
   uint64_t* empty_bar = full_bar + S;
   uint64_t* tfull_bar = empty_bar + S;     // [2]
   uint64_t* tempty_bar = tfull_bar + 2;    // [2]
@@ -273,8 +308,12 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar + stage, kA + kB);
-          P::load(args, ti, kb, sA + stage * kA, sB + stage * kB, full_bar + stage);
+          mbar_arrive_expect_tx(full_bar + stage, kA + kB + kSF);
+          if constexpr (kMX)
+            P::load_mx(args, ti, kb, sA + stage * kA, sB + stage * kB, sSF + stage * kSF,
+                       full_bar + stage);
+          else
+            P::load(args, ti, kb, sA + stage * kA, sB + stage * kB, full_bar + stage);
           issued_mask |= 1u << stage;
           parity_mask = (parity_mask & ~(1u << stage)) | (phase << stage);
           if (++stage == S) {
@@ -334,22 +373,48 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
           fence_proxy_async_smem();
           __syncwarp();
         }
-        if (lane == 0) {
-          tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + stage * kA);
-          const uint32_t b_base = smem_u32(sB + stage * kB);
+        if constexpr (kMX) {
+          if (lane == 0) {
+            tc_fence_after();
+            // scales of this stage -> TMEM (4-column aligned slots), then four
+            // K = 32 block-scaled MMAs selecting the K-block with sf_id
+            const uint32_t sf_t = tmem_base + StageCfg<P, true>::kSFCol0 + 8u * stage;
+            sf_copy_to_tmem(sf_t, sSF + stage * kSF);
+            sf_copy_to_tmem(sf_t + 4, sSF + stage * kSF + 512);
+            const uint32_t a_base = smem_u32(sA + stage * kA);
+            const uint32_t b_base = smem_u32(sB + stage * kB);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t adesc =
-                P::kAMN ? make_smem_desc(a_base + k * 2048, kChunkBytes, 1024)
-                        : make_smem_desc(a_base + k * 32, 16, 1024);
-            const uint64_t bdesc =
-                P::kBMN ? make_smem_desc(b_base + k * 2048, kChunkBytes, 1024)
-                        : make_smem_desc(b_base + k * 32, 16, 1024);
-            mma_bf16(d_tmem, adesc, bdesc, kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t adesc =
+                  P::kAMN ? make_smem_desc(a_base + k * 4096, 16384, 1024)
+                          : make_smem_desc(a_base + k * 32, 16, 1024);
+              const uint64_t bdesc =
+                  P::kBMN ? make_smem_desc(b_base + k * 4096, 16384, 1024)
+                          : make_smem_desc(b_base + k * 32, 16, 1024);
+              mma_mxf8(d_tmem, adesc, bdesc, idesc_with_sf_id(kIdesc, k), sf_t, sf_t + 4,
+                       (kb > 0 || k > 0) ? 1u : 0u);
+            }
+            mma_commit(empty_bar + stage);
+            committed_any = true;
           }
-          mma_commit(empty_bar + stage);
-          committed_any = true;
+        } else {
+          if (lane == 0) {
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(sA + stage * kA);
+            const uint32_t b_base = smem_u32(sB + stage * kB);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint64_t adesc =
+                  P::kAMN ? make_smem_desc(a_base + k * 2048, kChunkBytes, 1024)
+                          : make_smem_desc(a_base + k * 32, 16, 1024);
+              const uint64_t bdesc =
+                  P::kBMN ? make_smem_desc(b_base + k * 2048, kChunkBytes, 1024)
+                          : make_smem_desc(b_base + k * 32, 16, 1024);
+              mma_bf16(d_tmem, adesc, bdesc, kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
+            }
+            mma_commit(empty_bar + stage);
+            committed_any = true;
+          }
         }
         __syncwarp();
         if (++stage == S) {

@@ -19,6 +19,29 @@ cudaError_t launch_gate_up_wgrad(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_router_wgrad(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_dense(bool a_mn, bool b_mn, const GemmArgs& a, int grid, cudaStream_t s);
 
+// MXFP8 GEMMs (gemm_mx.cu)
+cudaError_t launch_gate_up_fwd_mx(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_down_fwd_mx(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_down_dgrad_mx(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_gate_up_dgrad_mx(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_down_wgrad_mx(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_gate_up_wgrad_mx(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_dense_mx(const GemmArgs& a, int grid, cudaStream_t s);
+
+// MXFP8 quantisers (mx_quant.cu): E4M3 data + 512-byte scale atoms
+cudaError_t launch_quant_rows_dense(const uint16_t* src, int64_t R, int C, uint8_t* dst,
+                                    uint8_t* sf, cudaStream_t s);
+cudaError_t launch_quant_rows_permuted(const uint16_t* src, int64_t P, int C, uint8_t* dst,
+                                       uint8_t* sf, const int* offsets, const int* mtile_off,
+                                       int E, cudaStream_t s);
+cudaError_t launch_quant_cols_weights(const uint16_t* src, int E, int R, int C, uint8_t* dst,
+                                      uint8_t* sf, cudaStream_t s);
+cudaError_t launch_quant_cols_gate_up(const uint16_t* W_gate, const uint16_t* W_up, int E, int H,
+                                      int F, uint8_t* dst, uint8_t* sf, cudaStream_t s);
+cudaError_t launch_quant_cols_tokens(const uint16_t* src, int64_t max_ktiles, int C, uint8_t* dst,
+                                     uint8_t* sf, const int* offsets, const int* mtile_off, int E,
+                                     cudaStream_t s);
+
 // memory-bound kernels (elementwise.cu)
 cudaError_t launch_transpose_bf16(const uint16_t* in, uint16_t* out, int rows, int cols,
                                   cudaStream_t s);

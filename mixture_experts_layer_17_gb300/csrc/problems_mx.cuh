@@ -1,0 +1,321 @@
+// MXFP8 GEMMs of the MoE layer: E4M3 operands with E8M0 scales per 32
+// elements along K, block-scaled tcgen05 MMA, 128 x 128 output tiles, K = 128
+// per stage.  Scale atoms (512 bytes: 128 MN-rows x 4 K-blocks) are fetched
+// with 1-D bulk copies beside the operand tiles:
+//   activations along features (K-major, rows of the permuted layout): atom
+//     ((mtile_off[e] + m-tile) * kt_a + k-tile);
+//   weights: atom ((expert * n_tiles + n-tile) * kt_b + k-tile);
+//   activations along tokens (MN-major, expert segments padded to 128 rows):
+//     atom (k-tile * tiles_of_MN + MN-tile), k-tile = mtile_off[e] + local.
+// Epilogues match the bf16 problems (problems.cuh, problems_bwd.cuh).
+#pragma once
+
+#include "problems_bwd.cuh"
+
+namespace moe {
+
+MOE_DEV const uint8_t* sf_atom(const uint8_t* base, int64_t index) { return base + index * 512; }
+
+// grouped-M tile with 128-element (fp8) K stages
+MOE_DEV TileInfo grouped_m_tile_mx(const GemmArgs& a, int t, int nstep) {
+  TileInfo ti = grouped_m_tile(a, t, nstep);
+  ti.num_kb = a.K / 128;
+  return ti;
+}
+
+// grouped-K tile over the 128-row padded token layout: expert e's K range is
+// k-tiles [mtile_off[e], mtile_off[e+1]) (an expert without tokens has none).
+MOE_DEV TileInfo grouped_k_tile_mx(const GemmArgs& a, int t, int BN) {
+  const int per = a.m_tiles * a.n_tiles;
+  const int gi = t / per;
+  const int local = t - gi * per;
+  const int mt = local / a.n_tiles;
+  const int nt = local - mt * a.n_tiles;
+  const int e = a.group_order != nullptr ? __ldg(a.group_order + gi) : gi;
+  const int k0 = __ldg(a.mtile_off + e);
+  TileInfo ti;
+  ti.e = e;
+  ti.m0 = mt * kBM;
+  ti.n0 = nt * BN;
+  ti.rows = min(kBM, a.M - ti.m0);
+  ti.kb0 = k0;
+  ti.num_kb = __ldg(a.mtile_off + e + 1) - k0;
+  ti.k_last = 128;
+  ti.krow0 = 128 * k0;
+  ti.mt = mt;
+  return ti;
+}
+
+// ------------------------------------------------------------------------
+// F7 + F8 in MXFP8: A = x_perm E4M3 [P, H]; B = W_gate|W_up quantised along H
+// and interleaved per 128-column tile as [64 gate | 64 up] ([E*H, 2F], MN-major).
+// Tile = 128 rows x (64 gate + 64 up) columns; outputs as GateUpFwdProblem.
+// ------------------------------------------------------------------------
+struct GateUpFwdMXProblem {
+  static constexpr int BN = 128;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = true;
+  static constexpr bool kTailZero = false;
+  static constexpr bool kMX = true;
+  static constexpr size_t kExtraSmem = 0;
+  static constexpr int kEpiGroups = 2;
+
+  MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile_mx(a, t, 64); }
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
+  MOE_DEV static void load_mx(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
+                              uint8_t* sB, uint8_t* sSF, uint64_t* bar) {
+    const int k0 = kb * 128;
+    const int nt = ti.n0 / 64;
+    tma_load_2d(sA, &a.mapA, k0, ti.m0, bar);
+    tma_load_2d(sB, &a.mapB0, nt * 128, ti.e * a.b_group_rows + k0, bar);
+    bulk_load(sSF, sf_atom(a.sfA, (static_cast<int64_t>(__ldg(a.mtile_off + ti.e)) + ti.mt) * a.kt_a + kb), 512, bar);
+    bulk_load(sSF + 512, sf_atom(a.sfB0, (static_cast<int64_t>(ti.e) * a.n_tiles + nt) * a.kt_b + kb), 512, bar);
+  }
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
+  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
+                               int group, uint8_t*) {
+    const bool valid = r < ti.rows;
+    const int64_t row = static_cast<int64_t>(ti.m0) + r;
+    const int F = a.ld0;
+    const int f0 = ti.n0 + 32 * group;
+    __nv_bfloat16* act = static_cast<__nv_bfloat16*>(a.out0) + row * F + f0;
+    __nv_bfloat16* hg = static_cast<__nv_bfloat16*>(a.out1) + row * 2 * F + f0;
+    __nv_bfloat16* hu = hg + F;
+#pragma unroll 1
+    for (int c = 0; c < 32; c += 16) {
+      float g[16], u[16];
+      tmem_ld16(taddr + 32 * group + c, g);
+      tmem_ld16(taddr + 64 + 32 * group + c, u);
+      tmem_ld_wait();
+      if (valid) {
+        float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = g[i] * sigmoidf_fast(g[i]) * u[i];
+        store_bf16x16(act + c, v);
+        store_bf16x16(hg + c, g);
+        store_bf16x16(hu + c, u);
+      }
+    }
+  }
+};
+
+// F9 + F10 in MXFP8: A = a E4M3 [P, F]; B = W_down quantised along F
+// ([E*F, H], MN-major); weighted scatter epilogue.
+struct DownFwdMXProblem {
+  static constexpr int BN = 128;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = true;
+  static constexpr bool kTailZero = false;
+  static constexpr bool kMX = true;
+  static constexpr size_t kExtraSmem = 0;
+  static constexpr int kEpiGroups = 2;
+
+  MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile_mx(a, t, BN); }
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
+  MOE_DEV static void load_mx(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
+                              uint8_t* sB, uint8_t* sSF, uint64_t* bar) {
+    const int k0 = kb * 128;
+    const int nt = ti.n0 / BN;
+    tma_load_2d(sA, &a.mapA, k0, ti.m0, bar);
+    tma_load_2d(sB, &a.mapB0, ti.n0, ti.e * a.b_group_rows + k0, bar);
+    bulk_load(sSF, sf_atom(a.sfA, (static_cast<int64_t>(__ldg(a.mtile_off + ti.e)) + ti.mt) * a.kt_a + kb), 512, bar);
+    bulk_load(sSF + 512, sf_atom(a.sfB0, (static_cast<int64_t>(ti.e) * a.n_tiles + nt) * a.kt_b + kb), 512, bar);
+  }
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
+  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
+                               int group, uint8_t*) {
+    const bool valid = r < ti.rows;
+    const int64_t row = static_cast<int64_t>(ti.m0) + r;
+    float w = 0.f;
+    __nv_bfloat16* dst = nullptr;
+    if (valid) {
+      w = __ldg(static_cast<const float*>(a.in0) + row);
+      const int slot = __ldg(static_cast<const int*>(a.in1) + row);
+      dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 + ti.n0;
+    }
+#pragma unroll 1
+    for (int c = group * 64; c < group * 64 + 64; c += 16) {
+      float v[16];
+      tmem_ld16(taddr + c, v);
+      tmem_ld_wait();
+      if (valid) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] *= w;
+        store_bf16x16(dst + c, v);
+      }
+    }
+  }
+};
+
+// B2-B4 in MXFP8: A = dY_perm E4M3 [P, H]; B = W_down quantised along H
+// ([E*F, H], K-major); the SwiGLU-backward epilogue of DownDgradProblem<128>.
+struct DownDgradMXProblem : DownDgradProblem<128> {
+  static constexpr bool kMX = true;
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile_mx(a, t, 128); }
+  MOE_DEV static void load_mx(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
+                              uint8_t* sB, uint8_t* sSF, uint64_t* bar) {
+    const int k0 = kb * 128;
+    const int nt = ti.n0 / 128;
+    tma_load_2d(sA, &a.mapA, k0, ti.m0, bar);
+    tma_load_2d(sB, &a.mapB0, k0, ti.e * a.b_group_rows + ti.n0, bar);
+    bulk_load(sSF, sf_atom(a.sfA, (static_cast<int64_t>(__ldg(a.mtile_off + ti.e)) + ti.mt) * a.kt_a + kb), 512, bar);
+    bulk_load(sSF + 512, sf_atom(a.sfB0, (static_cast<int64_t>(ti.e) * a.n_tiles + nt) * a.kt_b + kb), 512, bar);
+  }
+};
+
+// B6 in MXFP8: A = dh E4M3 [P, 2F] (each half quantised along F); B = W_gate
+// then W_up quantised along F ([E*H, F], K-major); scatter epilogue.
+struct GateUpDgradMXProblem {
+  static constexpr int BN = 128;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = false;
+  static constexpr bool kTailZero = false;
+  static constexpr bool kMX = true;
+  static constexpr size_t kExtraSmem = 0;
+  static constexpr int kEpiGroups = 2;
+
+  MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile_mx(a, t, BN); }
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
+  MOE_DEV static void load_mx(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
+                              uint8_t* sB, uint8_t* sSF, uint64_t* bar) {
+    const int k0 = kb * 128;
+    const int nt = ti.n0 / BN;
+    const int brow = ti.e * a.b_group_rows + ti.n0;
+    tma_load_2d(sA, &a.mapA, k0, ti.m0, bar);
+    bulk_load(sSF, sf_atom(a.sfA, (static_cast<int64_t>(__ldg(a.mtile_off + ti.e)) + ti.mt) * a.kt_a + kb), 512, bar);
+    const int64_t wrow = static_cast<int64_t>(ti.e) * a.n_tiles + nt;
+    if (k0 < a.k_half) {
+      tma_load_2d(sB, &a.mapB0, k0, brow, bar);
+      bulk_load(sSF + 512, sf_atom(a.sfB0, wrow * a.kt_b + kb), 512, bar);
+    } else {
+      tma_load_2d(sB, &a.mapB1, k0 - a.k_half, brow, bar);
+      bulk_load(sSF + 512, sf_atom(a.sfB1, wrow * a.kt_b + kb - a.kt_b), 512, bar);
+    }
+  }
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
+  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
+                               int group, uint8_t*) {
+    const bool valid = r < ti.rows;
+    const int64_t row = static_cast<int64_t>(ti.m0) + r;
+    __nv_bfloat16* dst = nullptr;
+    if (valid) {
+      const int slot = __ldg(static_cast<const int*>(a.in1) + row);
+      dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 + ti.n0;
+    }
+#pragma unroll 1
+    for (int c = group * 64; c < group * 64 + 64; c += 16) {
+      float v[16];
+      tmem_ld16(taddr + c, v);
+      tmem_ld_wait();
+      if (valid) store_bf16x16(dst + c, v);
+    }
+  }
+};
+
+// Weight gradients in MXFP8 over the padded token layout (both operands
+// MN-major, quantised along tokens per expert segment).
+//   Down:    A = w*a [P_pad, F] (M = F), B = dY_perm [P_pad, H] (N = H) -> dW_down [E, F, H]
+//   Gate/up: A = x_perm [P_pad, H] (M = H), B = dh [P_pad, 2F] (N = 2F) -> dW_gate, dW_up
+template <bool kGateUp>
+struct WgradMXProblem {
+  static constexpr int BN = 128;
+  static constexpr bool kAMN = true;
+  static constexpr bool kBMN = true;
+  static constexpr bool kTailZero = false;
+  static constexpr bool kMX = true;
+  static constexpr size_t kExtraSmem = 0;
+  static constexpr int kEpiGroups = 2;
+
+  MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_k_num_tiles(a); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_k_tile_mx(a, t, BN); }
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
+  MOE_DEV static void load_mx(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
+                              uint8_t* sB, uint8_t* sSF, uint64_t* bar) {
+    const int kt = ti.kb0 + kb;
+    const int krow = 128 * kt;
+    tma_load_2d(sA, &a.mapA, ti.m0, krow, bar);
+    tma_load_2d(sB, &a.mapB0, ti.n0, krow, bar);
+    bulk_load(sSF, sf_atom(a.sfA, static_cast<int64_t>(kt) * a.m_tiles + ti.mt), 512, bar);
+    bulk_load(sSF + 512, sf_atom(a.sfB0, static_cast<int64_t>(kt) * a.n_tiles + ti.n0 / BN), 512, bar);
+  }
+  MOE_DEV static __nv_bfloat16* out_ptr(const GemmArgs& a, const TileInfo& ti, int r, int gc) {
+    if (kGateUp) {
+      const int F = a.ld0;
+      __nv_bfloat16* base = static_cast<__nv_bfloat16*>(gc < F ? a.out0 : a.out1);
+      const int col = gc < F ? gc : gc - F;
+      return base + (static_cast<int64_t>(ti.e) * a.M + ti.m0 + r) * F + col;
+    }
+    return static_cast<__nv_bfloat16*>(a.out0) +
+           (static_cast<int64_t>(ti.e) * a.M + ti.m0 + r) * a.ld0 + gc;
+  }
+  MOE_DEV static void epilogue_empty(const GemmArgs& a, const TileInfo& ti, int r, int group,
+                                     uint8_t*) {
+    if (r >= ti.rows) return;
+    for (int c = group * 64; c < group * 64 + 64; c += 16) {
+      __nv_bfloat16* p = out_ptr(a, ti, r, ti.n0 + c);
+      st_global_v4(p, 0u, 0u, 0u, 0u);
+      st_global_v4(p + 8, 0u, 0u, 0u, 0u);
+    }
+  }
+  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
+                               int group, uint8_t*) {
+    const bool valid = r < ti.rows;
+#pragma unroll 1
+    for (int c = group * 64; c < group * 64 + 64; c += 16) {
+      float v[16];
+      tmem_ld16(taddr + c, v);
+      tmem_ld_wait();
+      if (valid) store_bf16x16(out_ptr(a, ti, r, ti.n0 + c), v);
+    }
+  }
+};
+
+// Dense MXFP8 GEMM for moe_gemm_mxfp8: A [M, K] and B [N, K] E4M3 (K-major),
+// atoms (m-tile * kt + k-tile) and (n-tile * kt + k-tile); D fp32 [M, N].
+struct DenseMXProblem {
+  static constexpr int BN = 128;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = false;
+  static constexpr bool kTailZero = false;
+  static constexpr bool kMX = true;
+  static constexpr size_t kExtraSmem = 0;
+  static constexpr int kEpiGroups = 2;
+
+  MOE_DEV static int num_tiles(const GemmArgs& a) { return dense_num_tiles(a); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) {
+    TileInfo ti = dense_tile(a, t, BN);
+    ti.num_kb = (a.K + 127) / 128;
+    return ti;
+  }
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
+  MOE_DEV static void load_mx(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
+                              uint8_t* sB, uint8_t* sSF, uint64_t* bar) {
+    tma_load_2d(sA, &a.mapA, kb * 128, ti.m0, bar);
+    tma_load_2d(sB, &a.mapB0, kb * 128, ti.n0, bar);
+    bulk_load(sSF, sf_atom(a.sfA, static_cast<int64_t>(ti.mt) * a.kt_a + kb), 512, bar);
+    bulk_load(sSF + 512, sf_atom(a.sfB0, static_cast<int64_t>(ti.n0 / BN) * a.kt_b + kb), 512, bar);
+  }
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
+  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
+                               int group, uint8_t*) {
+    const bool valid = r < ti.rows;
+    float* p = static_cast<float*>(a.out0) + (static_cast<int64_t>(ti.m0) + r) * a.ld0 + ti.n0;
+#pragma unroll 1
+    for (int c = group * 64; c < group * 64 + 64; c += 16) {
+      float v[16];
+      tmem_ld16(taddr + c, v);
+      tmem_ld_wait();
+      if (valid) {
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          st_global_v4(p + c + i, __float_as_uint(v[i]), __float_as_uint(v[i + 1]),
+                       __float_as_uint(v[i + 2]), __float_as_uint(v[i + 3]));
+      }
+    }
+  }
+};
+
+}  // namespace moe

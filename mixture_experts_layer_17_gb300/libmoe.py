@@ -28,7 +28,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
 # every symbol include/moe.h declares
 EXPORTED = ("moe_workspace_size", "moe_route", "moe_forward", "moe_backward", "moe_gemm_bf16",
             "moe_get_device_status", "moe_status_string", "moe_profile_enable",
-            "moe_profile_read", "moe_launch_count", "moe_route_noalloc")
+            "moe_profile_read", "moe_launch_count", "moe_route_noalloc", "moe_gemm_mxfp8")
 
 
 class MoeConfig(ctypes.Structure):
@@ -70,6 +70,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                              ctypes.POINTER(ctypes.c_double), _i32],
         "moe_launch_count": [],
         "moe_route_noalloc": [cfgp] + [_vp] * 11 + [_vp],
+        "moe_gemm_mxfp8": [_i64, _i64, _i64, _vp, _vp, _vp, _vp, ctypes.POINTER(_sz), _vp],
     }
     for name, argtypes in sig.items():
         fn = getattr(lib, name)
@@ -169,6 +170,22 @@ def moe_gemm_bf16(A, a_kmajor: bool, B, b_kmajor: bool, D, ws, stream=None) -> N
                                 int(bool(b_kmajor)), _ptr(D, torch.float32), _ptr(ws),
                                 ws.numel() * ws.element_size(), _stream(stream)),
            "moe_gemm_bf16")
+
+
+def moe_gemm_mxfp8(A, B, D, stream=None) -> None:
+    """D[M,N] = sum_k A_q(m,k) B_q(n,k) with A [M,K], B [N,K] bf16 quantised to
+    MXFP8 along K by the library; D fp32 [M,N].  Sizes and owns its workspace."""
+    M, K = A.shape
+    N = B.shape[0]
+    lib = load()
+    need = _sz(0)
+    _check(lib.moe_gemm_mxfp8(M, N, K, None, None, None, None, ctypes.byref(need), None),
+           "moe_gemm_mxfp8")
+    ws = torch.empty(max(need.value, 256), dtype=torch.uint8, device=A.device)
+    have = _sz(ws.numel())
+    bf = torch.bfloat16
+    _check(lib.moe_gemm_mxfp8(M, N, K, _ptr(A, bf), _ptr(B, bf), _ptr(D, torch.float32),
+                              _ptr(ws), ctypes.byref(have), _stream(stream)), "moe_gemm_mxfp8")
 
 
 def moe_get_device_status(ws, stream=None) -> int:
