@@ -357,15 +357,19 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
           ok = false;
           break;
         }
+        // grouped-K tail: the last k-block holds k_last valid K rows; only
+        // ceil(k_last / 16) MMAs are issued and A's rows [k_last, next multiple
+        // of 16) - the next expert's tokens - are cleared.  B's rows there hold
+        // finite values of the next expert (or TMA zero fill), so the zero A
+        // rows remove their contribution.
+        int n_mma = kBK / 16;
         if (P::kTailZero && kb == ti.num_kb - 1 && ti.k_last < kBK) {
-          // rows [k_last, 64) of every 64 x 128-byte chunk belong to the next
-          // expert (or lie past the tensor): clear them before the MMA reads
-          const uint32_t nbytes = static_cast<uint32_t>(kBK - ti.k_last) * 128u;
+          n_mma = (ti.k_last + 15) >> 4;
+          const uint32_t k16 = static_cast<uint32_t>(n_mma) * 16u;
+          const uint32_t nbytes = (k16 - static_cast<uint32_t>(ti.k_last)) * 128u;
           const uint32_t off = static_cast<uint32_t>(ti.k_last) * 128u;
-          for (int c = 0; c < static_cast<int>(kA / kChunkBytes) + static_cast<int>(kB / kChunkBytes); ++c) {
-            uint8_t* base = (c < static_cast<int>(kA / kChunkBytes))
-                                ? sA + stage * kA + c * kChunkBytes
-                                : sB + stage * kB + (c - kA / kChunkBytes) * kChunkBytes;
+          for (int c = 0; c < static_cast<int>(kA / kChunkBytes); ++c) {
+            uint8_t* base = sA + stage * kA + c * kChunkBytes;
             for (uint32_t b = lane * 16u; b < nbytes; b += 32u * 16u) {
               *reinterpret_cast<uint4*>(base + off + b) = make_uint4(0, 0, 0, 0);
             }
@@ -404,6 +408,7 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
             const uint32_t b_base = smem_u32(sB + stage * kB);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
+              if (k >= n_mma) break;
               const uint64_t adesc =
                   P::kAMN ? make_smem_desc(a_base + k * 2048, kChunkBytes, 1024)
                           : make_smem_desc(a_base + k * 32, 16, 1024);

@@ -88,14 +88,17 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, int64_t R, i
 enum ColMode { kColsWeights = 0, kColsGateUp = 1, kColsTokens = 2 };
 
 template <int MODE>
-__global__ void quant_cols_kernel(const uint16_t* __restrict__ src0,
+__global__ void __launch_bounds__(64) quant_cols_kernel(const uint16_t* __restrict__ src0,
                                   const uint16_t* __restrict__ src1, int R, int C_in,
                                   uint8_t* __restrict__ dst, uint8_t* __restrict__ sf,
                                   const int* __restrict__ offsets,
                                   const int* __restrict__ mtile_off, int E) {
+  // 64 threads: thread = (32-row block rb in 0..3, group of 8 columns cg in 0..15);
+  // each reads 32 rows x 16 bytes, keeps 8 running maxima, writes 32 x 8 bytes.
   const int kg = blockIdx.x;           // K-tile (global)
   const int ct = blockIdx.y;           // 128-column tile of the output
-  const int c_loc = threadIdx.x & 127;
+  const int cg = threadIdx.x & 15;
+  const int rb = threadIdx.x >> 4;
   const int C_out = (MODE == kColsGateUp) ? 2 * C_in : C_in;
   int64_t src_row0, dst_row0;
   int valid;                           // valid rows of this K-tile
@@ -114,7 +117,7 @@ __global__ void quant_cols_kernel(const uint16_t* __restrict__ src0,
     valid = min(128, static_cast<int>(__ldg(offsets + lo + 1) - src_row0));
     dst_row0 = 128ll * kg;
     atom = static_cast<int64_t>(kg) * (C_out >> 7) + ct;
-    src_col = ct * 128 + c_loc;
+    src_col = ct * 128 + cg * 8;
   } else {
     const int kt_per = R >> 7;
     const int e = kg / kt_per;
@@ -124,37 +127,52 @@ __global__ void quant_cols_kernel(const uint16_t* __restrict__ src0,
     valid = 128;
     atom = (static_cast<int64_t>(e) * (C_out >> 7) + ct) * kt_per + kt;
     if (MODE == kColsGateUp) {
-      src = (c_loc < 64) ? src0 : src1;
-      src_col = ct * 64 + (c_loc & 63);
+      src = (cg < 8) ? src0 : src1;    // output columns 0..63 gate, 64..127 up
+      src_col = ct * 64 + (cg & 7) * 8;
     } else {
-      src_col = ct * 128 + c_loc;
+      src_col = ct * 128 + cg * 8;
     }
   }
-  const int out_col = ct * 128 + c_loc;
-  for (int rb = threadIdx.x >> 7; rb < 4; rb += blockDim.x >> 7) {
-    float v[32];
-    float amax = 0.f;
+  const int out_col = ct * 128 + cg * 8;
+  // pass 1: column maxima of the 32-row block; pass 2 re-reads the same
+  // 512 bytes per thread (cache-resident) and converts
+  float amax[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const uint16_t* base = src + src_row0 * C_in + src_col;
 #pragma unroll 8
-    for (int i = 0; i < 32; ++i) {
-      const int rr = rb * 32 + i;
-      float x = 0.f;
-      if (rr < valid) {
-        const uint16_t bits = src[(src_row0 + rr) * C_in + src_col];
-        x = __uint_as_float(static_cast<uint32_t>(bits) << 16);
+  for (int i = 0; i < 32; ++i) {
+    const int rr = rb * 32 + i;
+    if (rr < valid) {
+      const uint4 u = ld_global_v4(base + static_cast<int64_t>(rr) * C_in);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float lo, hi;
+        unpack_bf16x2(w[q], lo, hi);
+        amax[2 * q] = fmaxf(amax[2 * q], fabsf(lo));
+        amax[2 * q + 1] = fmaxf(amax[2 * q + 1], fabsf(hi));
       }
-      v[i] = x;
-      amax = fmaxf(amax, fabsf(x));
     }
-    const int X = mx_exponent(amax);
-    const float inv = ldexpf(1.0f, -X);
+  }
+  float inv[8];
 #pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-      const uint32_t w = to_e4m3x4(v[i], v[i + 1], v[i + 2], v[i + 3], inv);
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        dst[(dst_row0 + rb * 32 + i + q) * C_out + out_col] = static_cast<uint8_t>(w >> (8 * q));
-    }
-    sf[atom * 512 + sf_atom_offset(c_loc, rb)] = static_cast<uint8_t>(X + 127);
+  for (int j = 0; j < 8; ++j) {
+    const int X = mx_exponent(amax[j]);
+    inv[j] = ldexpf(1.0f, -X);
+    sf[atom * 512 + sf_atom_offset(cg * 8 + j, rb)] = static_cast<uint8_t>(X + 127);
+  }
+#pragma unroll 8
+  for (int i = 0; i < 32; ++i) {
+    const int rr = rb * 32 + i;
+    uint4 u = make_uint4(0, 0, 0, 0);
+    if (rr < valid) u = ld_global_v4(base + static_cast<int64_t>(rr) * C_in);
+    float v[8];
+    unpack_bf16x2(u.x, v[0], v[1]);
+    unpack_bf16x2(u.y, v[2], v[3]);
+    unpack_bf16x2(u.z, v[4], v[5]);
+    unpack_bf16x2(u.w, v[6], v[7]);
+    const uint32_t lo = to_e4m3x4(v[0] * inv[0], v[1] * inv[1], v[2] * inv[2], v[3] * inv[3], 1.0f);
+    const uint32_t hi = to_e4m3x4(v[4] * inv[4], v[5] * inv[5], v[6] * inv[6], v[7] * inv[7], 1.0f);
+    *reinterpret_cast<uint2*>(dst + (dst_row0 + rb * 32 + i) * C_out + out_col) = make_uint2(lo, hi);
   }
 }
 
@@ -178,7 +196,7 @@ cudaError_t launch_quant_rows_permuted(const uint16_t* src, int64_t P, int C, ui
 cudaError_t launch_quant_cols_weights(const uint16_t* src, int E, int R, int C, uint8_t* dst,
                                       uint8_t* sf, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(E * (R / 128)), static_cast<unsigned>(C / 128));
-  quant_cols_kernel<kColsWeights><<<grid, 256, 0, s>>>(src, nullptr, R, C, dst, sf, nullptr,
+  quant_cols_kernel<kColsWeights><<<grid, 64, 0, s>>>(src, nullptr, R, C, dst, sf, nullptr,
                                                        nullptr, E);
   return cudaGetLastError();
 }
@@ -186,7 +204,7 @@ cudaError_t launch_quant_cols_weights(const uint16_t* src, int E, int R, int C, 
 cudaError_t launch_quant_cols_gate_up(const uint16_t* W_gate, const uint16_t* W_up, int E, int H,
                                       int F, uint8_t* dst, uint8_t* sf, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(E * (H / 128)), static_cast<unsigned>(2 * F / 128));
-  quant_cols_kernel<kColsGateUp><<<grid, 256, 0, s>>>(W_gate, W_up, H, F, dst, sf, nullptr,
+  quant_cols_kernel<kColsGateUp><<<grid, 64, 0, s>>>(W_gate, W_up, H, F, dst, sf, nullptr,
                                                       nullptr, E);
   return cudaGetLastError();
 }
@@ -195,7 +213,7 @@ cudaError_t launch_quant_cols_tokens(const uint16_t* src, int64_t max_ktiles, in
                                      uint8_t* sf, const int* offsets, const int* mtile_off, int E,
                                      cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(max_ktiles), static_cast<unsigned>(C / 128));
-  quant_cols_kernel<kColsTokens><<<grid, 256, 0, s>>>(src, nullptr, 0, C, dst, sf, offsets,
+  quant_cols_kernel<kColsTokens><<<grid, 64, 0, s>>>(src, nullptr, 0, C, dst, sf, offsets,
                                                       mtile_off, E);
   return cudaGetLastError();
 }

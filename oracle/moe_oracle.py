@@ -165,29 +165,18 @@ def e4m3_decode(code: np.ndarray) -> np.ndarray:
     return np.where((e == 15) & (m == 7), np.nan, val)
 
 
-def _e4m3_grid() -> np.ndarray:
-    """All finite non-negative E4M3 values, ascending."""
-    v = e4m3_decode(np.arange(0, 0x7F))
-    return np.unique(v[np.isfinite(v)])
-
-
-_E4M3_POS = _e4m3_grid()
-
-
 def e4m3_round(v: np.ndarray) -> np.ndarray:
-    """Round to the nearest E4M3 value (ties to even mantissa), saturating at
-    +-448.  Brute force over the 127 non-negative values."""
+    """Round to the nearest E4M3 value, ties to even mantissa, saturating at
+    +-448.  E4M3 has 3 mantissa bits, so inside the binade [2^e, 2^(e+1)) the
+    representable values are multiples of 2^(e-3); subnormals share the step
+    2^-9 of the lowest binade (e = -6).  Rounding |v| / step half-to-even is
+    mantissa-parity rounding because every binade starts at the even multiple 8."""
     v = np.asarray(v, np.float64)
     a = np.minimum(np.abs(v), E4M3_MAX)
-    grid = _E4M3_POS
-    hi = np.clip(np.searchsorted(grid, a, side="left"), 0, len(grid) - 1)
-    lo = np.clip(hi - 1, 0, len(grid) - 1)
-    glo, ghi = grid[lo], grid[hi]
-    dlo, dhi = a - glo, ghi - a
-    # index parity = mantissa parity for consecutive codes: even code wins ties
-    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
-    r = np.where(pick_hi, ghi, glo)
-    r = np.where(a == glo, glo, r)
+    _, ex = np.frexp(a)                     # a = m * 2^ex, m in [0.5, 1)
+    e = np.maximum(ex.astype(np.int64) - 1, -6)
+    step = np.exp2((e - 3).astype(np.float64))
+    r = np.minimum(np.rint(a / step) * step, E4M3_MAX)
     return np.sign(v) * r
 
 
@@ -503,4 +492,43 @@ def expert_weight_grad_columns(e: int, cols, x, dY, W_gate, W_up, W_down, rows_t
         out["dW_gate_col"].append(xe.T @ (da * hu * silu_grad(hg)))
         out["dW_up_col"].append(xe.T @ (da * silu(hg)))
         out["dW_down_row"].append((rows_w * a) @ dYe)
+    return {k: np.array(v) for k, v in out.items()}
+
+
+def expert_weight_grad_columns_mx(e: int, cols, x, dY, W_gate, W_up, W_down, rows_tokens,
+                                  rows_w, precision: str) -> Dict[str, np.ndarray]:
+    """expert_weight_grad_columns with the MXFP8 quantisation points of
+    ``precision`` ('mxfp8' or 'fp8_bwd'): columns f of dW_gate[e] / dW_up[e]
+    and rows f of dW_down[e].
+
+    Forward (mxfp8 only): x rows and W_gate / W_up columns along H, a along F
+    (the whole row of a is needed for that block, so full rows of h are formed).
+    Backward: dY rows and W_down rows along H for g; the weight gradients take
+    x, dh, w*a and dY quantised along the expert's tokens (blocks of 32 from the
+    segment start, zero-padded), which only needs whole token columns."""
+    qf = _q(precision, "fwd")
+    xe = np.asarray(x[rows_tokens], np.float64)
+    dYe = np.asarray(dY[rows_tokens], np.float64)
+    Wg = np.asarray(W_gate[e], np.float64)
+    Wu = np.asarray(W_up[e], np.float64)
+    Wd = np.asarray(W_down[e], np.float64)
+    seg = np.array([0, xe.shape[0]])
+    xf = mx_round_trip(xe, 1) if qf else xe
+    Wgf = mx_round_trip(Wg, 0) if qf else Wg
+    Wuf = mx_round_trip(Wu, 0) if qf else Wu
+    hg = xf @ Wgf
+    hu = xf @ Wuf
+    a = swiglu(hg, hu)
+    g = mx_round_trip(dYe, 1) @ mx_round_trip(Wd, 1).T
+    xq = mx_round_trip_segments(xe, seg)
+    dYq = mx_round_trip_segments(dYe, seg)
+    out = {"dW_gate_col": [], "dW_up_col": [], "dW_down_row": []}
+    for f in cols:
+        da = rows_w * g[:, f]
+        dhg = (da * hu[:, f] * silu_grad(hg[:, f]))[:, None]
+        dhu = (da * silu(hg[:, f]))[:, None]
+        aw = (rows_w * a[:, f])[:, None]
+        out["dW_gate_col"].append(xq.T @ mx_round_trip_segments(dhg, seg)[:, 0])
+        out["dW_up_col"].append(xq.T @ mx_round_trip_segments(dhu, seg)[:, 0])
+        out["dW_down_row"].append(mx_round_trip_segments(aw, seg)[:, 0] @ dYq)
     return {k: np.array(v) for k, v in out.items()}

@@ -389,3 +389,22 @@ def test_mxfp8_forward_is_close_to_exact_and_equals_manual_quantisation():
     for name in ("dx", "dW_gate", "dW_up", "dW_down"):
         rel = np.linalg.norm(gb[name] - ge[name]) / np.linalg.norm(ge[name])
         assert 1e-4 < rel < 0.1, name
+
+
+@pytest.mark.parametrize("precision", ["mxfp8", "fp8_bwd"])
+def test_mx_weight_grad_columns_match_full_backward(precision):
+    rng = np.random.default_rng(18)
+    x, W_r, Wg, Wu, Wd, dY = _rand_layer(rng, 70, 64, 64, 3, 2, std=0.1)
+    g = mo.backward(x, W_r, Wg, Wu, Wd, 2, dY, precision=precision)
+    fwd = g["fwd"]
+    for e in range(3):
+        r0, r1 = fwd["offsets"][e], fwd["offsets"][e + 1]
+        cols = [0, 17, 63]
+        c = mo.expert_weight_grad_columns_mx(e, cols, x, dY, Wg, Wu, Wd, fwd["perm_token"][r0:r1],
+                                             fwd["w_row"][r0:r1], precision)
+        np.testing.assert_allclose(c["dW_gate_col"], g["dW_gate"][e][:, cols].T, rtol=1e-10,
+                                   atol=1e-12)
+        np.testing.assert_allclose(c["dW_up_col"], g["dW_up"][e][:, cols].T, rtol=1e-10,
+                                   atol=1e-12)
+        np.testing.assert_allclose(c["dW_down_row"], g["dW_down"][e][cols, :], rtol=1e-10,
+                                   atol=1e-12)
