@@ -240,7 +240,7 @@ def run_ours(args, sh, world, rank, local):
     import dataclasses
     shr = dataclasses.replace(shr, seed=shr.seed + 1000 * rank) if rank else shr
     inp = si.make_inputs(shr, dev)
-    layer = MoeLayer(sh.T, sh.H, sh.F, sh.E, sh.top_k, sh.precision, device=dev)
+    layer = MoeLayer(sh.T, sh.H, sh.F, sh.E, sh.top_k, sh.precision, flags=args.flags, device=dev)
     grads = {"dx": torch.empty_like(inp["x"]), "dW_r": torch.empty_like(inp["W_r"]),
              "dW_gate": torch.empty_like(inp["W_gate"]), "dW_up": torch.empty_like(inp["W_up"]),
              "dW_down": torch.empty_like(inp["W_down"])}
@@ -423,6 +423,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(si.WORKLOADS))
+    ap.add_argument("--flags", type=lambda v: int(v, 0), default=0,
+                    help="moe_config_t flags (e.g. 0x4: single-CTA tiles only; 0x8: CTA pairs)")
     ap.add_argument("--shape", default=None,
                     help="T,H,F,E,top_k: a custom shape (profiling aid) instead of --workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")

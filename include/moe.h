@@ -76,6 +76,13 @@ typedef enum {
                                          timeout path can be exercised; the call
                                          then reports MOE_ERR_TIMEOUT through
                                          moe_get_device_status                   */
+#define MOE_FLAG_CTA_PAIRS_OFF  0x4u  /* run every expert GEMM on single-CTA 128-row
+                                         tiles                                    */
+#define MOE_FLAG_CTA_PAIRS_ON   0x8u  /* use CTA-pair 256-row tiles (cta_group::2)
+                                         wherever the shape allows; by default,
+                                         when experts average >= 512 rows, pairs
+                                         run the gate/up dgrad, the down forward
+                                         and the two expert weight gradients      */
 
 typedef struct {
   int64_t T;           /* tokens                                   */
@@ -160,7 +167,7 @@ moe_status_t moe_gemm_bf16(int64_t M, int64_t N, int64_t K, const moe_bf16_t* A,
  * library; every GPU that loads the library holds that array until the
  * process exits.  A configuration that needs more scratch than that is
  * rejected with MOE_ERR_WORKSPACE_TOO_SMALL before anything is queued (at
- * E = 128, H = 4096, top_k = 8 the limit is about T = 100,000 tokens).
+ * E = 128, H = 4096, top_k = 8 the limit is about T = 75,000 tokens).
  * The call allocates no device memory and calls no allocating routine.
  *
  * The first call on a device looks up the array's device address (once per

@@ -178,6 +178,8 @@ int next_pow2_at_least16(int v) {
 
 struct Layout {
   int64_t T, P, T_pad;
+  int64_t Pa;        // rows of the padded internal layout: P + 64 * E (64-row aligned segments)
+  bool pair_gu_fwd, pair_down_fwd, pair_down_dgrad, pair_gu_dgrad, pair_down_wgrad, pair_gu_wgrad;
   int H, F, E, k;
   int ntiles;        // router tiles of 128 tokens
   int router_bn;     // N of the router GEMM (power of two >= E, >= 16)
@@ -186,10 +188,10 @@ struct Layout {
   int wr_split, wr_kbps, wr_mtiles, wr_ntiles;
   // forward / route workspace
   size_t f_status, f_hist, f_base, f_a, f_scratch;
-  size_t r_wrt, r_row_slot, r_w_row, r_mtile, r_order, f_total;
+  size_t r_wrt, r_row_slot, r_w_row, r_mtile, r_order, r_poff, r_mtile2, r_slotpad, f_total;
   // context
   size_t c_idx, c_w, c_counts, c_offsets, c_perm, c_slot, c_row_slot, c_w_row, c_mtile,
-      c_order, c_wrt, c_xperm, c_h, c_total;
+      c_order, c_wrt, c_xperm, c_h, c_poff, c_mtile2, c_slotpad, c_total;
   // backward workspace
   size_t b_status, b_dyp, b_dh, b_aw, b_dwp, b_dl, b_dlt, b_scratch, b_wrp, b_total;
   // MXFP8 buffers (E4M3 data + scale atoms); present only when the precision uses them
@@ -207,7 +209,27 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.E = c.E;
   L.k = c.top_k;
   L.P = L.T * L.k;
+  L.Pa = L.P + 64ll * L.E;
   L.T_pad = (L.T + 7) / 8 * 8;
+  // CTA pairs (256-row tiles, cta_group::2): each CTA stages half of B, so six
+  // stages fit and the operand-latency lookahead grows by half; a pair tile
+  // of a grouped-M GEMM wastes more rows at the end of each expert.  Measured
+  // on the 235B shape (1024 rows per expert), pairs win for the gate/up dgrad,
+  // the down forward and both weight gradients, and lose for the gate/up
+  // forward and the down dgrad; with ~256 rows per expert they lose
+  // everywhere.  MOE_FLAG_CTA_PAIRS_ON / _OFF override the choice.
+  const bool pairs_on = (c.flags & MOE_FLAG_CTA_PAIRS_ON) != 0;
+  const bool pairs_off = (c.flags & MOE_FLAG_CTA_PAIRS_OFF) != 0;
+  const bool bf = c.precision != MOE_MXFP8;        // bf16 forward GEMMs
+  const bool bb = c.precision == MOE_BF16;         // bf16 backward GEMMs
+  const bool big = L.P >= 512ll * L.E;             // experts average >= 512 rows
+  const bool pp = !pairs_off && (pairs_on || big);
+  L.pair_gu_fwd = bf && !pairs_off && pairs_on;
+  L.pair_down_fwd = bf && pp;
+  L.pair_down_dgrad = bb && !pairs_off && pairs_on && (L.F % 256 == 0);
+  L.pair_gu_dgrad = bb && pp;
+  L.pair_down_wgrad = bb && pp && (L.F % 256 == 0);
+  L.pair_gu_wgrad = bb && pp;
   L.ntiles = static_cast<int>((L.T + kBM - 1) / kBM);
   L.router_bn = next_pow2_at_least16(L.E);
   L.dgrad_bn = (L.F % 256 == 0) ? 256 : 128;
@@ -221,6 +243,7 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.wr_kbps = (total_kb + split - 1) / split;
   L.wr_split = (total_kb + L.wr_kbps - 1) / L.wr_kbps;
   const size_t P = static_cast<size_t>(L.P), T = static_cast<size_t>(L.T);
+  const size_t Pa = static_cast<size_t>(L.Pa);
   const size_t H = L.H, F = L.F, E = L.E;
 
   Carver f;
@@ -228,18 +251,21 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.f_hist = f.take(sizeof(int) * L.ntiles * E);
   L.f_base = f.take(sizeof(int) * L.ntiles * E);
   L.r_wrt = f.take(2 * E * H);
-  L.r_row_slot = f.take(sizeof(int) * P);
-  L.r_w_row = f.take(sizeof(float) * P);
+  L.r_row_slot = f.take(sizeof(int) * Pa);
+  L.r_w_row = f.take(sizeof(float) * Pa);
   L.r_mtile = f.take(sizeof(int) * (E + 1));
   L.r_order = f.take(sizeof(int) * E);
-  L.f_a = f.take(2 * P * F);
+  L.r_poff = f.take(sizeof(int) * (E + 1));
+  L.r_mtile2 = f.take(sizeof(int) * (E + 1));
+  L.r_slotpad = f.take(sizeof(int) * P);
+  L.f_a = f.take(2 * Pa * F);
   L.f_scratch = f.take(2 * P * H);
   L.mt_max = (L.P + kBM - 1) / kBM + L.E;
   const size_t mt = static_cast<size_t>(L.mt_max);
   if (c.precision == MOE_MXFP8) {
-    L.fq_x = f.take(P * H);
+    L.fq_x = f.take(Pa * H);
     L.fs_x = f.take(mt * (H / 128) * 512);
-    L.fq_a = f.take(P * F);
+    L.fq_a = f.take(Pa * F);
     L.fs_a = f.take(mt * (F / 128) * 512);
     L.fq_wgu = f.take(E * H * 2 * F);
     L.fs_wgu = f.take(E * (2 * F / 128) * (H / 128) * 512);
@@ -255,32 +281,35 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.c_offsets = x.take(sizeof(int) * (E + 1));
   L.c_perm = x.take(sizeof(int) * P);
   L.c_slot = x.take(sizeof(int) * P);
-  L.c_row_slot = x.take(sizeof(int) * P);
-  L.c_w_row = x.take(sizeof(float) * P);
+  L.c_row_slot = x.take(sizeof(int) * Pa);
+  L.c_w_row = x.take(sizeof(float) * Pa);
   L.c_mtile = x.take(sizeof(int) * (E + 1));
   L.c_order = x.take(sizeof(int) * E);
   L.c_wrt = x.take(2 * E * H);
-  L.c_xperm = x.take(2 * P * H);
-  L.c_h = x.take(2 * P * 2 * F);
+  L.c_xperm = x.take(2 * Pa * H);
+  L.c_h = x.take(2 * Pa * 2 * F);
+  L.c_poff = x.take(sizeof(int) * (E + 1));
+  L.c_mtile2 = x.take(sizeof(int) * (E + 1));
+  L.c_slotpad = x.take(sizeof(int) * P);
   L.c_total = x.off;
 
   Carver b;
   L.b_status = b.take(sizeof(DeviceStatus));
-  L.b_dyp = b.take(2 * P * H);
-  L.b_dh = b.take(2 * P * 2 * F);
-  L.b_aw = b.take(2 * P * F);
-  L.b_dwp = b.take(sizeof(float) * P * L.nparts);
+  L.b_dyp = b.take(2 * Pa * H);
+  L.b_dh = b.take(2 * Pa * 2 * F);
+  L.b_aw = b.take(2 * Pa * F);
+  L.b_dwp = b.take(sizeof(float) * Pa * L.nparts);
   L.b_dl = b.take(sizeof(float) * P);
   L.b_dlt = b.take(2 * E * static_cast<size_t>(L.T_pad));
   L.b_scratch = b.take(2 * P * H);
   L.b_wrp = b.take(sizeof(float) * L.wr_split * E * H);
   if (c.precision != MOE_BF16) {
     const size_t Pp = 128 * mt;   // padded token rows
-    L.bq_dy = b.take(P * H);
+    L.bq_dy = b.take(Pa * H);
     L.bs_dy = b.take(mt * (H / 128) * 512);
     L.bq_wdh = b.take(E * F * H);
     L.bs_wdh = b.take(E * (F / 128) * (H / 128) * 512);
-    L.bq_dh = b.take(P * 2 * F);
+    L.bq_dh = b.take(Pa * 2 * F);
     L.bs_dh = b.take(mt * (2 * F / 128) * 512);
     L.bq_wg = b.take(E * H * F);
     L.bs_wg = b.take(E * (H / 128) * (F / 128) * 512);
@@ -302,7 +331,11 @@ Layout make_layout(const moe_config_t& c, int sms) {
 
 moe_status_t validate(const moe_config_t* c) {
   if (c == nullptr) return MOE_ERR_INVALID_ARG;
-  if (c->flags & ~(MOE_FLAG_SYNC_CHECK | MOE_FLAG_TEST_TIMEOUT)) return MOE_ERR_INVALID_ARG;
+  if (c->flags & ~(MOE_FLAG_SYNC_CHECK | MOE_FLAG_TEST_TIMEOUT | MOE_FLAG_CTA_PAIRS_OFF |
+                   MOE_FLAG_CTA_PAIRS_ON))
+    return MOE_ERR_INVALID_ARG;
+  if ((c->flags & MOE_FLAG_CTA_PAIRS_OFF) && (c->flags & MOE_FLAG_CTA_PAIRS_ON))
+    return MOE_ERR_INVALID_ARG;
   if (c->precision < MOE_BF16 || c->precision > MOE_FP8_BWD) return MOE_ERR_INVALID_ARG;
   if (c->T < 1 || c->H < 256 || c->H % 256 != 0 || c->H > 65536 || c->F < 128 ||
       c->F % 128 != 0 || c->F > 65536 || c->E < 1 || c->E > 256 || c->top_k < 1 ||
@@ -358,6 +391,9 @@ struct RouteBufs {
   int* hist;
   int* base;
   DeviceStatus* st;
+  int* poff;       // padded segment starts
+  int* mtile2;     // pair-tile prefix
+  int* slot_pad;   // (t, j) -> row of the padded layout
 };
 
 // F1-F5: router GEMM with the fused top-k epilogue, expert scan, permutation.
@@ -386,16 +422,25 @@ moe_status_t run_routing(const moe_config_t& c, const Layout& L, const RouteBufs
     return launch_router_fwd(L.router_bn, a, grid_for(L.ntiles, sms), s);
   }));
   MOE_TRY(run("expert_scan", s, c.flags, [&] {
-    return launch_scan(b.hist, L.ntiles, L.E, b.counts, b.offsets, b.base, b.mtile, b.order, s);
+    return launch_scan(b.hist, L.ntiles, L.E, b.counts, b.offsets, b.poff, b.base, b.mtile,
+                       b.mtile2, b.order, s);
   }));
   MOE_TRY(run("permute", s, c.flags, [&] {
-    return launch_permute(b.idx, b.w, b.base, L.T, L.k, L.E, b.perm, b.slot, b.row_slot,
-                          b.w_row, s);
+    return launch_permute(b.idx, b.w, b.base, b.offsets, b.poff, L.T, L.k, L.E, b.perm, b.slot,
+                          b.slot_pad, b.row_slot, b.w_row, s);
   }));
   return MOE_OK;
 }
 
 int64_t grouped_m_tile_bound(const Layout& L) { return (L.P + kBM - 1) / kBM + L.E; }
+int64_t grouped_m_pair_bound(const Layout& L) { return (L.P + 2 * kBM - 1) / (2 * kBM) + L.E; }
+
+// even grid of at most sms CTAs for `pair_tiles` CTA-pair tiles
+int grid_for_pairs(int64_t pair_tiles, int sms) {
+  const int64_t cap = sms & ~1;
+  const int64_t g = 2 * (pair_tiles < 1 ? 1 : pair_tiles);
+  return static_cast<int>(g < cap ? g : cap);
+}
 
 bool all_aligned16(std::initializer_list<const void*> ps) {
   for (const void* p : ps)
@@ -408,12 +453,14 @@ bool all_aligned16(std::initializer_list<const void*> ps) {
 
 // F7 + F8 and F9 in MXFP8: quantise the gate/up operands (x_perm along H;
 // W_gate / W_up along H, interleaved per 128 columns), the block-scaled
-// gate/up GEMM with SwiGLU, quantise a along F and W_down along F, then the
-// block-scaled down GEMM with the weighted scatter.
+// gate/up GEMM with SwiGLU whose epilogue quantises a along F from fp32,
+// quantise W_down along F, then the block-scaled down GEMM with the weighted
+// scatter.
 moe_status_t forward_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t fl,
                               DeviceStatus* st, const uint16_t* xperm, const uint16_t* W_gate,
                               const uint16_t* W_up, const uint16_t* W_down, const int* offsets,
-                              const int* mtile, const float* w_row, const int* row_slot,
+                              const int* counts, const int* mtile, const float* w_row,
+                              const int* row_slot,
                               uint16_t* act, uint16_t* h, uint16_t* scratch, void* ws) {
   uint8_t* xq = at<uint8_t>(ws, L.fq_x);
   uint8_t* sx = at<uint8_t>(ws, L.fs_x);
@@ -424,14 +471,14 @@ moe_status_t forward_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t
   uint8_t* wd = at<uint8_t>(ws, L.fq_wd);
   uint8_t* swd = at<uint8_t>(ws, L.fs_wd);
   MOE_TRY(run("mx_quant_x", s, fl, [&] {
-    return launch_quant_rows_permuted(xperm, L.P, L.H, xq, sx, offsets, mtile, L.E, s);
+    return launch_quant_rows_permuted(xperm, L.Pa, L.H, xq, sx, offsets, mtile, L.E, s);
   }));
   MOE_TRY(run("mx_quant_w_gate_up", s, fl, [&] {
     return launch_quant_cols_gate_up(W_gate, W_up, L.E, L.H, L.F, wgu, swgu, s);
   }));
   {
     GemmArgs a = base_args(st, fl);
-    if (!make_map_u8(&a.mapA, xq, L.H, L.P, L.H) ||
+    if (!make_map_u8(&a.mapA, xq, L.H, L.Pa, L.H) ||
         !make_map_u8(&a.mapB0, wgu, 2ull * L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F))
       return MOE_ERR_CUDA;
     a.mapB1 = a.mapB0;
@@ -441,9 +488,11 @@ moe_status_t forward_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t
     a.num_groups = L.E;
     a.b_group_rows = L.H;
     a.offsets = offsets;
+    a.counts = counts;
     a.mtile_off = mtile;
-    a.out0 = act;
+    a.out0 = aq;    // a quantised to E4M3 in the epilogue
     a.out1 = h;
+    a.out2 = sa;    // its scale atoms
     a.ld0 = L.F;
     a.sfA = sx;
     a.kt_a = L.H / 128;
@@ -456,15 +505,12 @@ moe_status_t forward_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t
     const int grid = grid_for(((L.P + kBM - 1) / kBM + L.E) * a.n_tiles, sms);
     MOE_TRY(run("gate_up_gemm_swiglu_mx", s, fl, [&] { return launch_gate_up_fwd_mx(a, grid, s); }));
   }
-  MOE_TRY(run("mx_quant_a", s, fl, [&] {
-    return launch_quant_rows_permuted(act, L.P, L.F, aq, sa, offsets, mtile, L.E, s);
-  }));
   MOE_TRY(run("mx_quant_w_down_f", s, fl, [&] {
     return launch_quant_cols_weights(W_down, L.E, L.F, L.H, wd, swd, s);
   }));
   {
     GemmArgs a = base_args(st, fl);
-    if (!make_map_u8(&a.mapA, aq, L.F, L.P, L.F) ||
+    if (!make_map_u8(&a.mapA, aq, L.F, L.Pa, L.F) ||
         !make_map_u8(&a.mapB0, wd, L.H, static_cast<uint64_t>(L.E) * L.F, L.H))
       return MOE_ERR_CUDA;
     a.mapB1 = a.mapB0;
@@ -474,6 +520,7 @@ moe_status_t forward_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t
     a.num_groups = L.E;
     a.b_group_rows = L.F;
     a.offsets = offsets;
+    a.counts = counts;
     a.mtile_off = mtile;
     a.in0 = w_row;
     a.in1 = row_slot;
@@ -492,7 +539,7 @@ moe_status_t forward_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t
 
 struct BwdBufs {
   const uint16_t *W_gate, *W_up, *W_down, *dyp, *xperm, *h;
-  const int *offsets, *mtile, *order, *slot, *row_slot;
+  const int *offsets, *counts, *mtile, *order, *slot, *row_slot;   // offsets: padded starts
   const float *w_row, *w;
   const int* idx;
   const uint16_t* wrt;
@@ -533,14 +580,14 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
 
   // B2-B4: down dgrad
   MOE_TRY(run("mx_quant_dy", s, fl, [&] {
-    return launch_quant_rows_permuted(b.dyp, L.P, L.H, dyq, sdy, b.offsets, b.mtile, L.E, s);
+    return launch_quant_rows_permuted(b.dyp, L.Pa, L.H, dyq, sdy, b.offsets, b.mtile, L.E, s);
   }));
   MOE_TRY(run("mx_quant_w_down_h", s, fl, [&] {
     return launch_quant_rows_dense(b.W_down, static_cast<int64_t>(L.E) * L.F, L.H, wdh, swdh, s);
   }));
   {
     GemmArgs a = base_args(st, fl);
-    if (!make_map_u8(&a.mapA, dyq, L.H, L.P, L.H) ||
+    if (!make_map_u8(&a.mapA, dyq, L.H, L.Pa, L.H) ||
         !make_map_u8(&a.mapB0, wdh, L.H, static_cast<uint64_t>(L.E) * L.F, L.H))
       return MOE_ERR_CUDA;
     a.mapB1 = a.mapB0;
@@ -550,12 +597,15 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     a.num_groups = L.E;
     a.b_group_rows = L.F;
     a.offsets = b.offsets;
+    a.counts = b.counts;
     a.mtile_off = b.mtile;
     a.in0 = b.h;
     a.in1 = b.w_row;
     a.out0 = b.dh;
     a.out1 = b.aw;
     a.out2 = b.dwp;
+    a.out3 = dhq;   // dh quantised to E4M3 along F in the epilogue
+    a.out4 = sdh;
     a.ld0 = L.F;
     a.sfA = sdy;
     a.kt_a = L.H / 128;
@@ -575,10 +625,12 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
   }));
   // B5: down wgrad over the padded token layout
   MOE_TRY(run("mx_quant_aw_tokens", s, fl, [&] {
-    return launch_quant_cols_tokens(b.aw, L.mt_max, L.F, awt, sawt, b.offsets, b.mtile, L.E, s);
+    return launch_quant_cols_tokens(b.aw, L.mt_max, L.F, awt, sawt, b.offsets, b.counts, b.mtile,
+                                    L.E, s);
   }));
   MOE_TRY(run("mx_quant_dy_tokens", s, fl, [&] {
-    return launch_quant_cols_tokens(b.dyp, L.mt_max, L.H, dyt, sdyt, b.offsets, b.mtile, L.E, s);
+    return launch_quant_cols_tokens(b.dyp, L.mt_max, L.H, dyt, sdyt, b.offsets, b.counts, b.mtile,
+                                    L.E, s);
   }));
   {
     GemmArgs a = base_args(st, fl);
@@ -591,6 +643,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     a.n_tiles = L.H / 128;
     a.num_groups = L.E;
     a.offsets = b.offsets;
+    a.counts = b.counts;
     a.mtile_off = b.mtile;
     a.group_order = b.order;
     a.out0 = b.dW_down;
@@ -601,9 +654,6 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     MOE_TRY(run("down_wgrad_mx", s, fl, [&] { return launch_down_wgrad_mx(a, grid, s); }));
   }
   // B6 + B7: gate/up dgrad, then the un-permute
-  MOE_TRY(run("mx_quant_dh", s, fl, [&] {
-    return launch_quant_rows_permuted(b.dh, L.P, 2 * L.F, dhq, sdh, b.offsets, b.mtile, L.E, s);
-  }));
   MOE_TRY(run("mx_quant_w_gate_f", s, fl, [&] {
     return launch_quant_rows_dense(b.W_gate, static_cast<int64_t>(L.E) * L.H, L.F, wg, swg, s);
   }));
@@ -612,7 +662,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
   }));
   {
     GemmArgs a = base_args(st, fl);
-    if (!make_map_u8(&a.mapA, dhq, 2ull * L.F, L.P, 2ull * L.F) ||
+    if (!make_map_u8(&a.mapA, dhq, 2ull * L.F, L.Pa, 2ull * L.F) ||
         !make_map_u8(&a.mapB0, wg, L.F, static_cast<uint64_t>(L.E) * L.H, L.F) ||
         !make_map_u8(&a.mapB1, wu, L.F, static_cast<uint64_t>(L.E) * L.H, L.F))
       return MOE_ERR_CUDA;
@@ -623,6 +673,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     a.num_groups = L.E;
     a.b_group_rows = L.H;
     a.offsets = b.offsets;
+    a.counts = b.counts;
     a.mtile_off = b.mtile;
     a.in1 = b.row_slot;
     a.out0 = b.scratch;
@@ -640,10 +691,12 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
   }));
   // B8: gate/up wgrad over the padded token layout
   MOE_TRY(run("mx_quant_x_tokens", s, fl, [&] {
-    return launch_quant_cols_tokens(b.xperm, L.mt_max, L.H, xt, sxt, b.offsets, b.mtile, L.E, s);
+    return launch_quant_cols_tokens(b.xperm, L.mt_max, L.H, xt, sxt, b.offsets, b.counts,
+                                    b.mtile, L.E, s);
   }));
   MOE_TRY(run("mx_quant_dh_tokens", s, fl, [&] {
-    return launch_quant_cols_tokens(b.dh, L.mt_max, 2 * L.F, dht, sdht, b.offsets, b.mtile, L.E, s);
+    return launch_quant_cols_tokens(b.dh, L.mt_max, 2 * L.F, dht, sdht, b.offsets, b.counts,
+                                    b.mtile, L.E, s);
   }));
   {
     GemmArgs a = base_args(st, fl);
@@ -657,6 +710,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     a.n_tiles = 2 * L.F / 128;
     a.num_groups = L.E;
     a.offsets = b.offsets;
+    a.counts = b.counts;
     a.mtile_off = b.mtile;
     a.group_order = b.order;
     a.out0 = b.dW_gate;
@@ -719,7 +773,8 @@ moe_status_t moe_route(const moe_config_t* cfg, const moe_bf16_t* x, const moe_b
   RouteBufs b{x, W_r, logit_bias, logits, topk_idx, topk_w, counts, offsets, perm_token,
               slot_row, at<int>(ws, L.r_row_slot), at<float>(ws, L.r_w_row),
               at<int>(ws, L.r_mtile), at<int>(ws, L.r_order), at<uint16_t>(ws, L.r_wrt),
-              at<int>(ws, L.f_hist), at<int>(ws, L.f_base), st};
+              at<int>(ws, L.f_hist), at<int>(ws, L.f_base), st, at<int>(ws, L.r_poff),
+              at<int>(ws, L.r_mtile2), at<int>(ws, L.r_slotpad)};
   return run_routing(*cfg, L, b, d.sms, s);
 }
 
@@ -742,33 +797,40 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
 
   int* idx = at<int>(ctx, L.c_idx);
   int* offsets = at<int>(ctx, L.c_offsets);
+  int* counts = at<int>(ctx, L.c_counts);
+  int* poff = at<int>(ctx, L.c_poff);
   int* slot = at<int>(ctx, L.c_slot);
+  int* slot_pad = at<int>(ctx, L.c_slotpad);
   int* row_slot = at<int>(ctx, L.c_row_slot);
   float* w_row = at<float>(ctx, L.c_w_row);
   int* mtile = at<int>(ctx, L.c_mtile);
+  int* mtile2 = at<int>(ctx, L.c_mtile2);
   uint16_t* xperm = at<uint16_t>(ctx, L.c_xperm);
   uint16_t* h = at<uint16_t>(ctx, L.c_h);
   uint16_t* act = at<uint16_t>(ws, L.f_a);
   uint16_t* scratch = at<uint16_t>(ws, L.f_scratch);
 
-  RouteBufs b{x, W_r, logit_bias, nullptr, idx, at<float>(ctx, L.c_w),
-              at<int>(ctx, L.c_counts), offsets, at<int>(ctx, L.c_perm), slot, row_slot,
-              w_row, mtile, at<int>(ctx, L.c_order), at<uint16_t>(ctx, L.c_wrt),
-              at<int>(ws, L.f_hist), at<int>(ws, L.f_base), st};
+  RouteBufs b{x, W_r, logit_bias, nullptr, idx, at<float>(ctx, L.c_w), counts, offsets,
+              at<int>(ctx, L.c_perm), slot, row_slot, w_row, mtile, at<int>(ctx, L.c_order),
+              at<uint16_t>(ctx, L.c_wrt), at<int>(ws, L.f_hist), at<int>(ws, L.f_base), st,
+              poff, mtile2, slot_pad};
   MOE_TRY(run_routing(*cfg, L, b, d.sms, s));
 
-  // F6: dispatch x to the expert-major rows
+  // F6: dispatch x to the padded expert-major rows (segment tails zeroed: they
+  // are K rows of the gate/up weight gradient)
   MOE_TRY(run("gather_x", s, fl,
-              [&] { return launch_gather_rows(x, slot, xperm, L.T, L.H, L.k, s); }));
+              [&] { return launch_gather_rows(x, slot_pad, xperm, L.T, L.H, L.k, s); }));
+  MOE_TRY(run("zero_pad_rows_x", s, fl,
+              [&] { return launch_zero_pad_rows(xperm, poff, counts, L.E, L.H, s); }));
 
   if (cfg->precision == MOE_MXFP8) {
-    MOE_TRY(forward_gemms_mx(L, d.sms, s, fl, st, xperm, W_gate, W_up, W_down, offsets, mtile,
-                             w_row, row_slot, act, h, scratch, ws));
+    MOE_TRY(forward_gemms_mx(L, d.sms, s, fl, st, xperm, W_gate, W_up, W_down, poff, counts,
+                             mtile, w_row, row_slot, act, h, scratch, ws));
   } else {
     // F7 + F8: gate/up GEMM with SwiGLU
     {
       GemmArgs a = base_args(st, fl);
-      if (!make_map(&a.mapA, xperm, L.H, L.P, 2ull * L.H, 64, 128) ||
+      if (!make_map(&a.mapA, xperm, L.H, L.Pa, 2ull * L.H, 64, 128) ||
           !make_map(&a.mapB0, W_gate, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 64) ||
           !make_map(&a.mapB1, W_up, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 64))
         return MOE_ERR_CUDA;
@@ -777,8 +839,10 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
       a.n_tiles = L.F / 128;
       a.num_groups = L.E;
       a.b_group_rows = L.H;
-      a.offsets = offsets;
+      a.offsets = poff;
+      a.counts = counts;
       a.mtile_off = mtile;
+      a.mtile2_off = mtile2;
       a.out0 = act;
       a.out1 = h;
       a.ld0 = L.F;
@@ -786,13 +850,18 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
         a.flags = 2u;
         a.wait_limit_ns = kTestWaitNs;
       }
-      const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
-      MOE_TRY(run("gate_up_gemm_swiglu", s, fl, [&] { return launch_gate_up_fwd(a, grid, s); }));
+      if (L.pair_gu_fwd) {
+        const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, d.sms);
+        MOE_TRY(run("gate_up_gemm_swiglu", s, fl, [&] { return launch_gate_up_fwd_pair(a, grid, s); }));
+      } else {
+        const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
+        MOE_TRY(run("gate_up_gemm_swiglu", s, fl, [&] { return launch_gate_up_fwd(a, grid, s); }));
+      }
     }
     // F9 + F10: down GEMM with the weighted scatter, then the k-way combine
     {
       GemmArgs a = base_args(st, fl);
-      if (!make_map(&a.mapA, act, L.F, L.P, 2ull * L.F, 64, 128) ||
+      if (!make_map(&a.mapA, act, L.F, L.Pa, 2ull * L.F, 64, 128) ||
           !make_map(&a.mapB0, W_down, L.H, static_cast<uint64_t>(L.E) * L.F, 2ull * L.H, 64, 64))
         return MOE_ERR_CUDA;
       a.mapB1 = a.mapB0;
@@ -801,14 +870,21 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
       a.n_tiles = L.H / 256;
       a.num_groups = L.E;
       a.b_group_rows = L.F;
-      a.offsets = offsets;
+      a.offsets = poff;
+      a.counts = counts;
       a.mtile_off = mtile;
+      a.mtile2_off = mtile2;
       a.in0 = w_row;
       a.in1 = row_slot;
       a.out0 = scratch;
       a.ld0 = L.H;
-      const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
-      MOE_TRY(run("down_gemm_scatter", s, fl, [&] { return launch_down_fwd(a, grid, s); }));
+      if (L.pair_down_fwd) {
+        const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, d.sms);
+        MOE_TRY(run("down_gemm_scatter", s, fl, [&] { return launch_down_fwd_pair(a, grid, s); }));
+      } else {
+        const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
+        MOE_TRY(run("down_gemm_scatter", s, fl, [&] { return launch_down_fwd(a, grid, s); }));
+      }
     }
   }
   MOE_TRY(run("combine", s, fl, [&] { return launch_combine(scratch, y, L.T, L.H, L.k, s); }));
@@ -837,11 +913,13 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
 
   const int* idx = at<int>(ctx, L.c_idx);
   const float* w = at<float>(ctx, L.c_w);
-  const int* offsets = at<int>(ctx, L.c_offsets);
-  const int* slot = at<int>(ctx, L.c_slot);
+  const int* counts = at<int>(ctx, L.c_counts);
+  const int* poff = at<int>(ctx, L.c_poff);
+  const int* slot_pad = at<int>(ctx, L.c_slotpad);
   const int* row_slot = at<int>(ctx, L.c_row_slot);
   const float* w_row = at<float>(ctx, L.c_w_row);
   const int* mtile = at<int>(ctx, L.c_mtile);
+  const int* mtile2 = at<int>(ctx, L.c_mtile2);
   const int* order = at<int>(ctx, L.c_order);
   const uint16_t* wrt = at<uint16_t>(ctx, L.c_wrt);
   const uint16_t* xperm = at<uint16_t>(ctx, L.c_xperm);
@@ -856,12 +934,15 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
   float* wrp = at<float>(ws, L.b_wrp);
   (void)W_r;
 
-  // B1: dispatch dY to the expert-major rows
+  // B1: dispatch dY to the padded expert-major rows (segment tails zeroed:
+  // they are K rows of the down weight gradient)
   MOE_TRY(run("gather_dy", s, fl,
-              [&] { return launch_gather_rows(dY, slot, dyp, L.T, L.H, L.k, s); }));
+              [&] { return launch_gather_rows(dY, slot_pad, dyp, L.T, L.H, L.k, s); }));
+  MOE_TRY(run("zero_pad_rows_dy", s, fl,
+              [&] { return launch_zero_pad_rows(dyp, poff, counts, L.E, L.H, s); }));
 
   if (cfg->precision != MOE_BF16) {
-    const BwdBufs bb{W_gate, W_up, W_down, dyp, xperm, h, offsets, mtile, order, slot,
+    const BwdBufs bb{W_gate, W_up, W_down, dyp, xperm, h, poff, counts, mtile, order, slot_pad,
                      row_slot, w_row, w, idx, wrt, dh, aw, dwp, dl, dlt, scratch, dx,
                      dW_gate, dW_up, dW_down, ws};
     MOE_TRY(backward_expert_gemms_mx(L, d.sms, s, fl, st, bb));
@@ -869,9 +950,9 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
     // B2-B4: down dgrad with the SwiGLU backward and router-weight partials
     {
       GemmArgs a = base_args(st, fl);
-      if (!make_map(&a.mapA, dyp, L.H, L.P, 2ull * L.H, 64, 128) ||
+      if (!make_map(&a.mapA, dyp, L.H, L.Pa, 2ull * L.H, 64, 128) ||
           !make_map(&a.mapB0, W_down, L.H, static_cast<uint64_t>(L.E) * L.F, 2ull * L.H, 64,
-                    L.dgrad_bn))
+                    L.pair_down_dgrad ? 128 : L.dgrad_bn))
         return MOE_ERR_CUDA;
       a.mapB1 = a.mapB0;
       a.K = L.H;
@@ -879,8 +960,10 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
       a.n_tiles = L.F / L.dgrad_bn;
       a.num_groups = L.E;
       a.b_group_rows = L.F;
-      a.offsets = offsets;
+      a.offsets = poff;
+      a.counts = counts;
       a.mtile_off = mtile;
+      a.mtile2_off = mtile2;
       a.in0 = h;
       a.in1 = w_row;
       a.out0 = dh;
@@ -891,40 +974,54 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
         a.flags = 2u;
         a.wait_limit_ns = kTestWaitNs;
       }
-      const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
-      MOE_TRY(run("down_dgrad_swiglu_bwd", s, fl,
-                  [&] { return launch_down_dgrad(L.dgrad_bn, a, grid, s); }));
+      if (L.pair_down_dgrad) {
+        const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, d.sms);
+        MOE_TRY(run("down_dgrad_swiglu_bwd", s, fl,
+                    [&] { return launch_down_dgrad_pair(a, grid, s); }));
+      } else {
+        const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
+        MOE_TRY(run("down_dgrad_swiglu_bwd", s, fl,
+                    [&] { return launch_down_dgrad(L.dgrad_bn, a, grid, s); }));
+      }
     }
     // B9: router softmax / top-k backward
     if (cudaMemsetAsync(dlt, 0, 2ull * L.E * L.T_pad, s) != cudaSuccess) return MOE_ERR_CUDA;
     MOE_TRY(run("router_bwd", s, fl, [&] {
-      return launch_router_bwd(dwp, L.nparts, slot, w, idx, L.T, L.k, dl, dlt, L.T_pad, s);
+      return launch_router_bwd(dwp, L.nparts, slot_pad, w, idx, L.T, L.k, dl, dlt, L.T_pad, s);
     }));
-    // B5: down wgrad over ragged K
+    // B5: down wgrad over the padded token segments
     {
       GemmArgs a = base_args(st, fl);
-      if (!make_map(&a.mapA, aw, L.F, L.P, 2ull * L.F, 64, 64) ||
-          !make_map(&a.mapB0, dyp, L.H, L.P, 2ull * L.H, 64, 64))
+      if (!make_map(&a.mapA, aw, L.F, L.Pa, 2ull * L.F, 64, 64) ||
+          !make_map(&a.mapB0, dyp, L.H, L.Pa, 2ull * L.H, 64, 64))
         return MOE_ERR_CUDA;
       a.mapB1 = a.mapB0;
       a.M = L.F;
       a.N = L.H;
-      a.m_tiles = L.F / 128;
+      a.m_tiles = L.F / (L.pair_down_wgrad ? 256 : 128);
       a.n_tiles = L.H / 256;
       a.num_groups = L.E;
-      a.offsets = offsets;
+      a.offsets = poff;
+      a.counts = counts;
       a.group_order = order;
       a.out0 = dW_down;
       a.ld0 = L.H;
-      const int grid = grid_for(static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles, d.sms);
-      MOE_TRY(run("down_wgrad", s, fl, [&] { return launch_down_wgrad(a, grid, s); }));
+      const int64_t tiles = static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles;
+      if (L.pair_down_wgrad) {
+        const int grid = grid_for_pairs(tiles, d.sms);
+        MOE_TRY(run("down_wgrad", s, fl, [&] { return launch_down_wgrad_pair(a, grid, s); }));
+      } else {
+        const int grid = grid_for(tiles, d.sms);
+        MOE_TRY(run("down_wgrad", s, fl, [&] { return launch_down_wgrad(a, grid, s); }));
+      }
     }
     // B6 + B7: gate/up dgrad with the scatter, then the un-permute (+ router dgrad)
     {
       GemmArgs a = base_args(st, fl);
-      if (!make_map(&a.mapA, dh, 2ull * L.F, L.P, 4ull * L.F, 64, 128) ||
-          !make_map(&a.mapB0, W_gate, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 256) ||
-          !make_map(&a.mapB1, W_up, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 256))
+      const uint32_t brows = L.pair_gu_dgrad ? 128 : 256;
+      if (!make_map(&a.mapA, dh, 2ull * L.F, L.Pa, 4ull * L.F, 64, 128) ||
+          !make_map(&a.mapB0, W_gate, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, brows) ||
+          !make_map(&a.mapB1, W_up, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, brows))
         return MOE_ERR_CUDA;
       a.K = 2 * L.F;
       a.k_half = L.F;
@@ -932,36 +1029,50 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
       a.n_tiles = L.H / 256;
       a.num_groups = L.E;
       a.b_group_rows = L.H;
-      a.offsets = offsets;
+      a.offsets = poff;
+      a.counts = counts;
       a.mtile_off = mtile;
+      a.mtile2_off = mtile2;
       a.in1 = row_slot;
       a.out0 = scratch;
       a.ld0 = L.H;
-      const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
-      MOE_TRY(run("gate_up_dgrad_scatter", s, fl, [&] { return launch_gate_up_dgrad(a, grid, s); }));
+      if (L.pair_gu_dgrad) {
+        const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, d.sms);
+        MOE_TRY(run("gate_up_dgrad_scatter", s, fl, [&] { return launch_gate_up_dgrad_pair(a, grid, s); }));
+      } else {
+        const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
+        MOE_TRY(run("gate_up_dgrad_scatter", s, fl, [&] { return launch_gate_up_dgrad(a, grid, s); }));
+      }
     }
     MOE_TRY(run("unpermute_dx", s, fl, [&] {
       return launch_unpermute(scratch, dl, idx, wrt, dx, L.T, L.H, L.k, s);
     }));
-    // B8: gate/up wgrad over ragged K
+    // B8: gate/up wgrad over the padded token segments
     {
       GemmArgs a = base_args(st, fl);
-      if (!make_map(&a.mapA, xperm, L.H, L.P, 2ull * L.H, 64, 64) ||
-          !make_map(&a.mapB0, dh, 2ull * L.F, L.P, 4ull * L.F, 64, 64))
+      if (!make_map(&a.mapA, xperm, L.H, L.Pa, 2ull * L.H, 64, 64) ||
+          !make_map(&a.mapB0, dh, 2ull * L.F, L.Pa, 4ull * L.F, 64, 64))
         return MOE_ERR_CUDA;
       a.mapB1 = a.mapB0;
       a.M = L.H;
       a.N = 2 * L.F;
-      a.m_tiles = L.H / 128;
+      a.m_tiles = L.H / (L.pair_gu_wgrad ? 256 : 128);
       a.n_tiles = (2 * L.F) / 256;
       a.num_groups = L.E;
-      a.offsets = offsets;
+      a.offsets = poff;
+      a.counts = counts;
       a.group_order = order;
       a.out0 = dW_gate;
       a.out1 = dW_up;
       a.ld0 = L.F;
-      const int grid = grid_for(static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles, d.sms);
-      MOE_TRY(run("gate_up_wgrad", s, fl, [&] { return launch_gate_up_wgrad(a, grid, s); }));
+      const int64_t tiles = static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles;
+      if (L.pair_gu_wgrad) {
+        const int grid = grid_for_pairs(tiles, d.sms);
+        MOE_TRY(run("gate_up_wgrad", s, fl, [&] { return launch_gate_up_wgrad_pair(a, grid, s); }));
+      } else {
+        const int grid = grid_for(tiles, d.sms);
+        MOE_TRY(run("gate_up_wgrad", s, fl, [&] { return launch_gate_up_wgrad(a, grid, s); }));
+      }
     }
   }
   // B10: router weight gradient dW_r = x^T dl (split-K, then reduce + transpose)
@@ -1157,7 +1268,7 @@ moe_status_t noalloc_scratch_address(void** out) {
 // bases, W_r^T, the row -> (token, slot) map, row weights, m-tile prefix and
 // expert order.
 struct RouteScratch {
-  size_t status, hist, base, wrt, row_slot, w_row, mtile, order, total;
+  size_t status, hist, base, wrt, row_slot, w_row, mtile, order, poff, mtile2, slot_pad, total;
 };
 
 RouteScratch route_scratch_layout(const Layout& L) {
@@ -1168,10 +1279,13 @@ RouteScratch route_scratch_layout(const Layout& L) {
   r.hist = c.take(sizeof(int) * L.ntiles * E);
   r.base = c.take(sizeof(int) * L.ntiles * E);
   r.wrt = c.take(2 * E * H);
-  r.row_slot = c.take(sizeof(int) * P);
-  r.w_row = c.take(sizeof(float) * P);
+  r.row_slot = c.take(sizeof(int) * static_cast<size_t>(L.Pa));
+  r.w_row = c.take(sizeof(float) * static_cast<size_t>(L.Pa));
   r.mtile = c.take(sizeof(int) * (E + 1));
   r.order = c.take(sizeof(int) * E);
+  r.poff = c.take(sizeof(int) * (E + 1));
+  r.mtile2 = c.take(sizeof(int) * (E + 1));
+  r.slot_pad = c.take(sizeof(int) * P);
   r.total = c.off;
   return r;
 }
@@ -1204,7 +1318,8 @@ extern "C" moe_status_t moe_route_noalloc(const moe_config_t* cfg, const moe_bf1
   RouteBufs b{x, W_r, logit_bias, logits, topk_idx, topk_w, counts, offsets, perm_token,
               slot_row, at<int>(base, R.row_slot), at<float>(base, R.w_row),
               at<int>(base, R.mtile), at<int>(base, R.order), at<uint16_t>(base, R.wrt),
-              at<int>(base, R.hist), at<int>(base, R.base), st};
+              at<int>(base, R.hist), at<int>(base, R.base), st, at<int>(base, R.poff),
+              at<int>(base, R.mtile2), at<int>(base, R.slot_pad)};
   MOE_TRY(run_routing(*cfg, L, b, d.sms, s));
   if (device_status != nullptr &&
       cudaMemcpyAsync(device_status, &st->code, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) !=

@@ -31,16 +31,23 @@ __global__ void transpose_bf16_kernel(const uint16_t* __restrict__ in, uint16_t*
 
 // One block of 256 threads (thread = expert).  From the per-tile histograms
 // hist[tiles, E] it writes counts[E], offsets[E+1] (exclusive prefix sum),
-// block_base[tiles, E] (first row of each tile's tokens inside each expert's
-// segment), mtile_off[E+1] (prefix of ceil(count / 128), the grouped-GEMM
-// m-tiles) and group_order[E] (experts by descending count, ties by id).
+// poff[E+1] (the same over counts rounded up to 64: the internal permuted
+// layout gives every expert a 64-row aligned segment whose tail rows are
+// zero), block_base[tiles, E] (first unpadded row of each tile's tokens inside
+// each expert's segment), mtile_off[E+1] / mtile2_off[E+1] (prefixes of
+// ceil(count / 128) and ceil(count / 256): the grouped-GEMM m-tiles of one CTA
+// and of a CTA pair) and group_order[E] (experts by descending count, ties by
+// id).
 __global__ void scan_kernel(const int* __restrict__ hist, int ntiles, int E,
                             int* __restrict__ counts, int* __restrict__ offsets,
-                            int* __restrict__ block_base, int* __restrict__ mtile_off,
+                            int* __restrict__ poff, int* __restrict__ block_base,
+                            int* __restrict__ mtile_off, int* __restrict__ mtile2_off,
                             int* __restrict__ group_order) {
   __shared__ int s_cnt[256];
   __shared__ int s_off[257];
+  __shared__ int s_poff[257];
   __shared__ int s_mt[257];
+  __shared__ int s_mt2[257];
   const int e = threadIdx.x;
   int run = 0;
   if (e < E) {
@@ -53,21 +60,29 @@ __global__ void scan_kernel(const int* __restrict__ hist, int ntiles, int E,
   s_cnt[e] = (e < E) ? run : 0;
   __syncthreads();
   if (threadIdx.x == 0) {
-    int acc = 0, acc_mt = 0;
+    int acc = 0, acc_p = 0, acc_mt = 0, acc_mt2 = 0;
     for (int i = 0; i < E; ++i) {
       s_off[i] = acc;
+      s_poff[i] = acc_p;
       s_mt[i] = acc_mt;
+      s_mt2[i] = acc_mt2;
       acc += s_cnt[i];
+      acc_p += (s_cnt[i] + 63) / 64 * 64;
       acc_mt += (s_cnt[i] + 127) / 128;
+      acc_mt2 += (s_cnt[i] + 255) / 256;
     }
     s_off[E] = acc;
+    s_poff[E] = acc_p;
     s_mt[E] = acc_mt;
+    s_mt2[E] = acc_mt2;
   }
   __syncthreads();
   if (e < E) {
     counts[e] = run;
     offsets[e] = s_off[e];
+    poff[e] = s_poff[e];
     mtile_off[e] = s_mt[e];
+    mtile2_off[e] = s_mt2[e];
     for (int b = 0; b < ntiles; ++b) block_base[static_cast<int64_t>(b) * E + e] += s_off[e];
     int rank = 0;
     for (int i = 0; i < E; ++i) rank += (s_cnt[i] > run) || (s_cnt[i] == run && i < e);
@@ -75,7 +90,9 @@ __global__ void scan_kernel(const int* __restrict__ hist, int ntiles, int E,
   }
   if (e == 0) {
     offsets[E] = s_off[E];
+    poff[E] = s_poff[E];
     mtile_off[E] = s_mt[E];
+    mtile2_off[E] = s_mt2[E];
   }
 }
 
@@ -85,10 +102,13 @@ __global__ void scan_kernel(const int* __restrict__ hist, int ntiles, int E,
 // expert e goes to row block_base[tile, e] + (number of earlier tokens of the
 // tile routed to e); per-warp lane masks give that count without atomics on
 // global memory, so rows are expert-major with ascending token inside an
-// expert.
+// expert.  The same row shifted to the expert's padded segment (slot_pad) is
+// the row the kernels use internally.
 __global__ void permute_kernel(const int* __restrict__ idx, const float* __restrict__ w,
-                               const int* __restrict__ block_base, int64_t T, int k, int E,
-                               int* __restrict__ perm_token, int* __restrict__ slot_row,
+                               const int* __restrict__ block_base,
+                               const int* __restrict__ offsets, const int* __restrict__ poff,
+                               int64_t T, int k, int E, int* __restrict__ perm_token,
+                               int* __restrict__ slot_row, int* __restrict__ slot_pad,
                                int* __restrict__ row_slot, float* __restrict__ w_row) {
   __shared__ unsigned mask[4][256];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -106,10 +126,12 @@ __global__ void permute_kernel(const int* __restrict__ idx, const float* __restr
     int before = __popc(mask[warp][e] & lt);
     for (int q = 0; q < warp; ++q) before += __popc(mask[q][e]);
     const int r = block_base[static_cast<int64_t>(blockIdx.x) * E + e] + before;
+    const int pr = r - offsets[e] + poff[e];     // row of the padded internal layout
     perm_token[r] = static_cast<int>(t);
     slot_row[t * k + j] = r;
-    row_slot[r] = static_cast<int>(t * k + j);
-    w_row[r] = w[t * k + j];
+    slot_pad[t * k + j] = pr;
+    row_slot[pr] = static_cast<int>(t * k + j);
+    w_row[pr] = w[t * k + j];
   }
 }
 
@@ -133,6 +155,21 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ src, const int* 
 #pragma unroll
     for (int j = 0; j < 16; ++j)
       if (j < k) st_global_v4(dst + rows[j] + c * 8, v.x, v.y, v.z, v.w);
+  }
+}
+
+// Zeroes the tail rows [poff[e] + counts[e], poff[e+1]) of every expert's
+// padded segment of a [rows, H] bf16 matrix (one block per expert).
+__global__ void zero_pad_rows_kernel(uint16_t* __restrict__ m, const int* __restrict__ poff,
+                                     const int* __restrict__ counts, int H) {
+  const int e = blockIdx.x;
+  const int64_t r0 = static_cast<int64_t>(poff[e]) + counts[e];
+  const int64_t r1 = poff[e + 1];
+  const int cpr = H >> 3;
+  for (int64_t i = threadIdx.x; i < (r1 - r0) * cpr; i += blockDim.x) {
+    const int64_t row = r0 + i / cpr;
+    const int c = static_cast<int>(i % cpr) * 8;
+    st_global_v4(m + row * H + c, 0u, 0u, 0u, 0u);
   }
 }
 
@@ -258,17 +295,26 @@ cudaError_t launch_transpose_bf16(const uint16_t* in, uint16_t* out, int rows, i
 }
 
 cudaError_t launch_scan(const int* hist, int ntiles, int E, int* counts, int* offsets,
-                        int* block_base, int* mtile_off, int* group_order, cudaStream_t s) {
-  scan_kernel<<<1, 256, 0, s>>>(hist, ntiles, E, counts, offsets, block_base, mtile_off,
-                                group_order);
+                        int* poff, int* block_base, int* mtile_off, int* mtile2_off,
+                        int* group_order, cudaStream_t s) {
+  scan_kernel<<<1, 256, 0, s>>>(hist, ntiles, E, counts, offsets, poff, block_base, mtile_off,
+                                mtile2_off, group_order);
   return cudaGetLastError();
 }
 
-cudaError_t launch_permute(const int* idx, const float* w, const int* block_base, int64_t T,
-                           int k, int E, int* perm_token, int* slot_row, int* row_slot,
+cudaError_t launch_permute(const int* idx, const float* w, const int* block_base,
+                           const int* offsets, const int* poff, int64_t T, int k, int E,
+                           int* perm_token, int* slot_row, int* slot_pad, int* row_slot,
                            float* w_row, cudaStream_t s) {
-  permute_kernel<<<blocks_for(T, 128), 128, 0, s>>>(idx, w, block_base, T, k, E, perm_token,
-                                                    slot_row, row_slot, w_row);
+  permute_kernel<<<blocks_for(T, 128), 128, 0, s>>>(idx, w, block_base, offsets, poff, T, k, E,
+                                                    perm_token, slot_row, slot_pad, row_slot,
+                                                    w_row);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_pad_rows(uint16_t* m, const int* poff, const int* counts, int E, int H,
+                                 cudaStream_t s) {
+  zero_pad_rows_kernel<<<E, 256, 0, s>>>(m, poff, counts, H);
   return cudaGetLastError();
 }
 

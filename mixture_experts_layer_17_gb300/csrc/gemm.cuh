@@ -44,13 +44,16 @@ struct GemmArgs {
   int kb_per_split;    // split-K: k-blocks per chunk
   int b_group_rows;    // rows of one expert in B's 2-D tensor map
   int k_half;          // gate/up dgrad: K index where B switches from W_gate to W_up
-  const int* offsets;  // [E + 1] row offsets of the permuted layout
+  const int* offsets;  // [E + 1] padded segment starts of the internal permuted layout
+  const int* counts;   // [E] valid rows of every segment
   const int* mtile_off;     // [E + 1] prefix of ceil(count / 128)
+  const int* mtile2_off;    // [E + 1] prefix of ceil(count / 256) (CTA-pair tiles)
   const int* group_order;   // grouped-K: experts in processing order
   void* out0;
   void* out1;
   void* out2;
   void* out3;
+  void* out4;
   const void* in0;
   const void* in1;
   const void* in2;
@@ -74,6 +77,7 @@ struct TileInfo {
   int m0;       // first output row (grouped-M: row of the permuted layout)
   int n0;       // first output column
   int rows;     // valid output rows in the tile
+  int rows_pad; // rows of the tile inside the expert's padded segment (>= rows)
   int kb0;      // first k-block
   int num_kb;   // k-blocks
   int k_last;   // valid K rows in the last k-block (grouped-K)
@@ -83,9 +87,10 @@ struct TileInfo {
 
 // ------------------------------------------------------------ schedules
 
-// Grouped-M: rows of expert e are [offsets[e], offsets[e+1]); its m-tiles are
-// numbered from mtile_off[e].  Tiles are ordered (expert, n-tile, m-tile) so
-// that CTAs running at the same time share the expert's weight panel in L2.
+// Grouped-M: expert e's segment starts at the padded offset offsets[e] and
+// holds counts[e] rows followed by zero rows up to offsets[e+1]; its m-tiles
+// are numbered from mtile_off[e].  Tiles are ordered (expert, n-tile, m-tile)
+// so that CTAs running at the same time share the expert's weight panel in L2.
 MOE_DEV int grouped_m_num_tiles(const GemmArgs& a) {
   return __ldg(a.mtile_off + a.num_groups) * a.n_tiles;
 }
@@ -104,12 +109,12 @@ MOE_DEV TileInfo grouped_m_tile(const GemmArgs& a, int t, int BN) {
   const int nt = local / mt_e;
   const int mt = local - nt * mt_e;
   const int r0 = __ldg(a.offsets + e);
-  const int r1 = __ldg(a.offsets + e + 1);
   TileInfo ti;
   ti.e = e;
   ti.m0 = r0 + mt * kBM;
   ti.n0 = nt * BN;
-  ti.rows = min(kBM, r1 - ti.m0);
+  ti.rows = min(kBM, r0 + __ldg(a.counts + e) - ti.m0);
+  ti.rows_pad = min(kBM, __ldg(a.offsets + e + 1) - ti.m0);
   ti.kb0 = 0;
   ti.num_kb = (a.K + kBK - 1) / kBK;
   ti.k_last = kBK;
@@ -119,7 +124,8 @@ MOE_DEV TileInfo grouped_m_tile(const GemmArgs& a, int t, int BN) {
 }
 
 // Grouped-K (weight gradients): every expert owns m_tiles x n_tiles output
-// tiles; its K range is its token rows [offsets[e], offsets[e+1]).
+// tiles; its K range is its padded segment [offsets[e], offsets[e+1]), whole
+// 64-row blocks whose rows past counts[e] are zero.
 MOE_DEV int grouped_k_num_tiles(const GemmArgs& a) {
   return a.num_groups * a.m_tiles * a.n_tiles;
 }
@@ -132,17 +138,59 @@ MOE_DEV TileInfo grouped_k_tile(const GemmArgs& a, int t, int BN) {
   const int nt = local - mt * a.n_tiles;
   const int e = a.group_order != nullptr ? __ldg(a.group_order + gi) : gi;
   const int r0 = __ldg(a.offsets + e);
-  const int cnt = __ldg(a.offsets + e + 1) - r0;
   TileInfo ti;
   ti.e = e;
   ti.m0 = mt * kBM;
   ti.n0 = nt * BN;
   ti.rows = min(kBM, a.M - ti.m0);
+  ti.rows_pad = ti.rows;
   ti.kb0 = 0;
-  ti.num_kb = (cnt + kBK - 1) / kBK;
-  ti.k_last = cnt - (ti.num_kb - 1) * kBK;
+  ti.num_kb = (__ldg(a.offsets + e + 1) - r0) / kBK;
+  ti.k_last = kBK;
   ti.krow0 = r0;
   ti.mt = mt;
+  return ti;
+}
+
+// CTA-pair variants: 256-row tiles.  Grouped-M pair tiles of expert e are
+// numbered from mtile2_off[e]; grouped-K uses m_tiles = M / 256.
+MOE_DEV int grouped_m_num_tiles_pair(const GemmArgs& a) {
+  return __ldg(a.mtile2_off + a.num_groups) * a.n_tiles;
+}
+
+MOE_DEV TileInfo grouped_m_tile_pair(const GemmArgs& a, int t, int BN) {
+  const int q = t / a.n_tiles;
+  int lo = 0, hi = a.num_groups - 1;   // largest e with mtile2_off[e] <= q
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(a.mtile2_off + mid) <= q) lo = mid; else hi = mid - 1;
+  }
+  const int e = lo;
+  const int mbase = __ldg(a.mtile2_off + e);
+  const int mt_e = __ldg(a.mtile2_off + e + 1) - mbase;
+  const int local = t - mbase * a.n_tiles;
+  const int nt = local / mt_e;
+  const int mt = local - nt * mt_e;
+  const int r0 = __ldg(a.offsets + e);
+  TileInfo ti;
+  ti.e = e;
+  ti.m0 = r0 + mt * 2 * kBM;
+  ti.n0 = nt * BN;
+  ti.rows = min(2 * kBM, r0 + __ldg(a.counts + e) - ti.m0);
+  ti.rows_pad = min(2 * kBM, __ldg(a.offsets + e + 1) - ti.m0);
+  ti.kb0 = 0;
+  ti.num_kb = (a.K + kBK - 1) / kBK;
+  ti.k_last = kBK;
+  ti.krow0 = 0;
+  ti.mt = mt;
+  return ti;
+}
+
+MOE_DEV TileInfo grouped_k_tile_pair(const GemmArgs& a, int t, int BN) {
+  TileInfo ti = grouped_k_tile(a, t, BN);
+  ti.m0 = ti.mt * 2 * kBM;
+  ti.rows = min(2 * kBM, a.M - ti.m0);
+  ti.rows_pad = ti.rows;
   return ti;
 }
 
@@ -158,6 +206,7 @@ MOE_DEV TileInfo dense_tile(const GemmArgs& a, int t, int BN) {
   ti.m0 = mt * kBM;
   ti.n0 = nt * BN;
   ti.rows = min(kBM, a.M - ti.m0);
+  ti.rows_pad = ti.rows;
   ti.kb0 = 0;
   ti.num_kb = (a.K + kBK - 1) / kBK;
   ti.k_last = kBK;
@@ -182,6 +231,7 @@ MOE_DEV TileInfo split_k_tile(const GemmArgs& a, int t, int BN) {
   ti.m0 = mt * kBM;
   ti.n0 = nt * BN;
   ti.rows = min(kBM, a.M - ti.m0);
+  ti.rows_pad = ti.rows;
   ti.kb0 = ks * a.kb_per_split;
   ti.num_kb = max(0, min(total_kb, ti.kb0 + a.kb_per_split) - ti.kb0);
   ti.k_last = kBK;
@@ -198,11 +248,19 @@ struct IsMX : std::false_type {};
 template <class P>
 struct IsMX<P, std::void_t<decltype(P::kMX)>> : std::integral_constant<bool, P::kMX> {};
 
+// Problems with `static constexpr bool kPair = true` run as CTA pairs: a
+// cluster of two CTAs computes a 256-row tile with M = 256 tcgen05.mma of
+// cta_group::2; each CTA stages its own 128 rows of A and half of B.
+template <class P, class = void>
+struct IsPair : std::false_type {};
+template <class P>
+struct IsPair<P, std::void_t<decltype(P::kPair)>> : std::integral_constant<bool, P::kPair> {};
+
 // Stage geometry.  bf16: a stage holds K = 64 (128 bytes per row).  MXFP8: a
 // stage holds K = 128 E4M3 (128 bytes per row) plus one 512-byte scale atom
 // for A and BN/128 for B; accumulators use TMEM columns [0, 2*BN) and the
 // stage's scales are copied to columns 256 + 8*stage (A) and +4 (B).
-template <class P, bool MX = IsMX<P>::value>
+template <class P, bool MX = IsMX<P>::value, bool PAIR = IsPair<P>::value>
 struct StageCfg {
   static constexpr int BN = P::BN;
   static constexpr uint32_t kABytes = kBM * kBK * 2;
@@ -212,8 +270,21 @@ struct StageCfg {
   static constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
 };
 
+// CTA pair, bf16: per CTA a stage holds its 128 rows of A and BN/2 rows of B
+// (32 KB for BN = 256), so six stages fit.
 template <class P>
-struct StageCfg<P, true> {
+struct StageCfg<P, false, true> {
+  static constexpr int BN = P::BN;
+  static_assert(BN == 256, "CTA-pair tiles are 256 x 256");
+  static constexpr uint32_t kABytes = kBM * kBK * 2;
+  static constexpr uint32_t kBBytes = (BN / 2) * kBK * 2;
+  static constexpr uint32_t kSFBytes = 0;
+  static constexpr int kStages = 6;
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+template <class P>
+struct StageCfg<P, true, false> {
   static constexpr int BN = P::BN;
   static_assert(BN == 128, "MXFP8 tiles are 128 x 128");
   static constexpr uint32_t kABytes = kBM * 128;
@@ -240,8 +311,9 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
   constexpr uint32_t kA = C::kABytes;
   constexpr uint32_t kB = C::kBBytes;
   constexpr uint32_t kSF = C::kSFBytes;
+  constexpr bool kPair = IsPair<P>::value;
   constexpr uint32_t kIdesc = kMX ? make_idesc_mxf8(kBM, BN, P::kAMN, P::kBMN)
-                                  : make_idesc_bf16(kBM, BN, P::kAMN, P::kBMN);
+                                  : make_idesc_bf16(kPair ? 2 * kBM : kBM, BN, P::kAMN, P::kBMN);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -262,6 +334,10 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // CTA pairs: rank in the cluster (0 issues the MMAs) and the pair's tiles
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const int t_first = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int t_step = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -270,7 +346,7 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull_bar + i, 1);
-      mbar_init(tempty_bar + i, 4 * P::kEpiGroups);
+      mbar_init(tempty_bar + i, (kPair ? 2 : 1) * 4 * P::kEpiGroups);
     }
     mbar_init(drain_bar, 1);
     mbar_init(never_bar, 1);
@@ -279,11 +355,15 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(tmem_holder, C::kTmemCols);
+    if constexpr (kPair)
+      tmem_alloc_pair(tmem_holder, C::kTmemCols);
+    else
+      tmem_alloc(tmem_holder, C::kTmemCols);
   }
   P::init_extra(args, extra);
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync();   // the peer's barriers are initialised
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int num_tiles = P::num_tiles(args);
@@ -299,7 +379,7 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
       uint32_t phase = 0;
       uint32_t issued_mask = 0, parity_mask = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int t = t_first; t < num_tiles && ok; t += t_step) {
         const TileInfo ti = P::tile(args, t);
         for (int kb = 0; kb < ti.num_kb; ++kb) {
           if (!mbar_wait_bounded(empty_bar + stage, phase ^ 1u, abort_flag, limit)) {
@@ -308,12 +388,19 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar + stage, kA + kB + kSF);
-          if constexpr (kMX)
+          if constexpr (kPair) {
+            // both halves complete on the leader's full barrier
+            if (rank == 0) mbar_arrive_expect_tx(full_bar + stage, 2 * (kA + kB));
+            P::load_pair(args, ti, kb, static_cast<int>(rank), sA + stage * kA, sB + stage * kB,
+                         map_to_rank(full_bar + stage, 0));
+          } else if constexpr (kMX) {
+            mbar_arrive_expect_tx(full_bar + stage, kA + kB + kSF);
             P::load_mx(args, ti, kb, sA + stage * kA, sB + stage * kB, sSF + stage * kSF,
                        full_bar + stage);
-          else
+          } else {
+            mbar_arrive_expect_tx(full_bar + stage, kA + kB);
             P::load(args, ti, kb, sA + stage * kA, sB + stage * kB, full_bar + stage);
+          }
           issued_mask |= 1u << stage;
           parity_mask = (parity_mask & ~(1u << stage)) | (phase << stage);
           if (++stage == S) {
@@ -323,23 +410,30 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
         }
       }
       if (!ok) {
-        // let every load already in flight land before the CTA exits
-        for (int s = 0; s < S; ++s) {
-          if (issued_mask & (1u << s)) {
-            mbar_wait_bounded(full_bar + s, (parity_mask >> s) & 1u, zero_flag, 100000000ull);
+        // let every load already in flight land before the CTA exits (a
+        // pair's second CTA cannot observe its loads: it waits 200 us)
+        if (!kPair || rank == 0) {
+          for (int s = 0; s < S; ++s) {
+            if (issued_mask & (1u << s)) {
+              mbar_wait_bounded(full_bar + s, (parity_mask >> s) & 1u, zero_flag, 100000000ull);
+            }
+          }
+        } else {
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < 200000ull) {
           }
         }
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
+  } else if (warp == 1 && (!kPair || rank == 0)) {
+    // ------------------------------------------------ MMA issuer (pair: leader only)
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
     bool committed_any = false;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+    for (int t = t_first; t < num_tiles && ok; t += t_step) {
       const TileInfo ti = P::tile(args, t);
       if (ti.num_kb == 0) continue;
       if (!mbar_wait_bounded(tempty_bar + acc, acc_phase ^ 1u, abort_flag, limit)) {
@@ -357,32 +451,12 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
           ok = false;
           break;
         }
-        // grouped-K tail: the last k-block holds k_last valid K rows; only
-        // ceil(k_last / 16) MMAs are issued and A's rows [k_last, next multiple
-        // of 16) - the next expert's tokens - are cleared.  B's rows there hold
-        // finite values of the next expert (or TMA zero fill), so the zero A
-        // rows remove their contribution.
-        int n_mma = kBK / 16;
-        if (P::kTailZero && kb == ti.num_kb - 1 && ti.k_last < kBK) {
-          n_mma = (ti.k_last + 15) >> 4;
-          const uint32_t k16 = static_cast<uint32_t>(n_mma) * 16u;
-          const uint32_t nbytes = (k16 - static_cast<uint32_t>(ti.k_last)) * 128u;
-          const uint32_t off = static_cast<uint32_t>(ti.k_last) * 128u;
-          for (int c = 0; c < static_cast<int>(kA / kChunkBytes); ++c) {
-            uint8_t* base = sA + stage * kA + c * kChunkBytes;
-            for (uint32_t b = lane * 16u; b < nbytes; b += 32u * 16u) {
-              *reinterpret_cast<uint4*>(base + off + b) = make_uint4(0, 0, 0, 0);
-            }
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
         if constexpr (kMX) {
           if (lane == 0) {
             tc_fence_after();
             // scales of this stage -> TMEM (4-column aligned slots), then four
             // K = 32 block-scaled MMAs selecting the K-block with sf_id
-            const uint32_t sf_t = tmem_base + StageCfg<P, true>::kSFCol0 + 8u * stage;
+            const uint32_t sf_t = tmem_base + StageCfg<P, true, false>::kSFCol0 + 8u * stage;
             sf_copy_to_tmem(sf_t, sSF + stage * kSF);
             sf_copy_to_tmem(sf_t + 4, sSF + stage * kSF + 512);
             const uint32_t a_base = smem_u32(sA + stage * kA);
@@ -408,16 +482,21 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
             const uint32_t b_base = smem_u32(sB + stage * kB);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
-              if (k >= n_mma) break;
               const uint64_t adesc =
                   P::kAMN ? make_smem_desc(a_base + k * 2048, kChunkBytes, 1024)
                           : make_smem_desc(a_base + k * 32, 16, 1024);
               const uint64_t bdesc =
                   P::kBMN ? make_smem_desc(b_base + k * 2048, kChunkBytes, 1024)
                           : make_smem_desc(b_base + k * 32, 16, 1024);
-              mma_bf16(d_tmem, adesc, bdesc, kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
+              if constexpr (kPair)
+                mma_bf16_pair(d_tmem, adesc, bdesc, kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
+              else
+                mma_bf16(d_tmem, adesc, bdesc, kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
             }
-            mma_commit(empty_bar + stage);
+            if constexpr (kPair)
+              mma_commit_pair(empty_bar + stage, 0x3);   // frees the stage in both CTAs
+            else
+              mma_commit(empty_bar + stage);
             committed_any = true;
           }
         }
@@ -429,8 +508,13 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
       }
       if (!ok) break;
       if (lane == 0) {
-        const bool inject = (args.flags & 2u) != 0 && t == static_cast<int>(blockIdx.x);
-        if (!inject) mma_commit(tfull_bar + acc);
+        const bool inject = (args.flags & 2u) != 0 && t == t_first;
+        if (!inject) {
+          if constexpr (kPair)
+            mma_commit_pair(tfull_bar + acc, 0x3);
+          else
+            mma_commit(tfull_bar + acc);
+        }
       }
       __syncwarp();
       if (++acc == 2) {
@@ -440,11 +524,14 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
     }
     // wait until every MMA this thread issued has completed
     if (lane == 0 && committed_any) {
-      mma_commit(drain_bar);
+      if constexpr (kPair)
+        mma_commit_pair(drain_bar, 0x1);
+      else
+        mma_commit(drain_bar);
       mbar_wait_bounded(drain_bar, 0, zero_flag, 100000000ull);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 2) {
     // ------------------------------------------------ epilogue (warps 2..)
     const int quarter = warp & 3;            // TMEM lane quarter of this warp
     const int group = (warp - 2) >> 2;       // column group of this warp
@@ -453,8 +540,14 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
     int acc = 0;
     uint32_t acc_phase = 0;
     bool first = true;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-      const TileInfo ti = P::tile(args, t);
+    for (int t = t_first; t < num_tiles; t += t_step) {
+      TileInfo ti = P::tile(args, t);
+      if constexpr (kPair) {
+        // this CTA owns rows [128 * rank, 128 * rank + 128) of the pair's tile
+        ti.m0 += 128 * static_cast<int>(rank);
+        ti.rows = max(0, min(kBM, ti.rows - 128 * static_cast<int>(rank)));
+        ti.rows_pad = max(0, min(kBM, ti.rows_pad - 128 * static_cast<int>(rank)));
+      }
       if (ti.num_kb == 0) {
         P::epilogue_empty(args, ti, r, group, extra);
         continue;
@@ -478,7 +571,12 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
                   extra);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar + acc);
+      if (lane == 0) {
+        if (kPair && rank != 0)
+          mbar_arrive_remote(map_to_rank(tempty_bar + acc, 0));
+        else
+          mbar_arrive(tempty_bar + acc);
+      }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -488,9 +586,13 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync();   // the peer is done with this CTA's smem and TMEM
   tc_fence_after();
   if (warp == 0) {
-    tmem_dealloc(tmem_base, C::kTmemCols);
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, C::kTmemCols);
+    else
+      tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
 

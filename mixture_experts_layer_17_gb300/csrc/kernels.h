@@ -19,6 +19,14 @@ cudaError_t launch_gate_up_wgrad(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_router_wgrad(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_dense(bool a_mn, bool b_mn, const GemmArgs& a, int grid, cudaStream_t s);
 
+// CTA-pair GEMMs (gemm_pair.cu): grid must be even
+cudaError_t launch_gate_up_fwd_pair(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_down_fwd_pair(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_down_dgrad_pair(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_gate_up_dgrad_pair(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_down_wgrad_pair(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_gate_up_wgrad_pair(const GemmArgs& a, int grid, cudaStream_t s);
+
 // MXFP8 GEMMs (gemm_mx.cu)
 cudaError_t launch_gate_up_fwd_mx(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_down_fwd_mx(const GemmArgs& a, int grid, cudaStream_t s);
@@ -39,17 +47,21 @@ cudaError_t launch_quant_cols_weights(const uint16_t* src, int E, int R, int C, 
 cudaError_t launch_quant_cols_gate_up(const uint16_t* W_gate, const uint16_t* W_up, int E, int H,
                                       int F, uint8_t* dst, uint8_t* sf, cudaStream_t s);
 cudaError_t launch_quant_cols_tokens(const uint16_t* src, int64_t max_ktiles, int C, uint8_t* dst,
-                                     uint8_t* sf, const int* offsets, const int* mtile_off, int E,
-                                     cudaStream_t s);
+                                     uint8_t* sf, const int* poff, const int* counts,
+                                     const int* mtile_off, int E, cudaStream_t s);
 
 // memory-bound kernels (elementwise.cu)
 cudaError_t launch_transpose_bf16(const uint16_t* in, uint16_t* out, int rows, int cols,
                                   cudaStream_t s);
 cudaError_t launch_scan(const int* hist, int ntiles, int E, int* counts, int* offsets,
-                        int* block_base, int* mtile_off, int* group_order, cudaStream_t s);
-cudaError_t launch_permute(const int* idx, const float* w, const int* block_base, int64_t T,
-                           int k, int E, int* perm_token, int* slot_row, int* row_slot,
+                        int* poff, int* block_base, int* mtile_off, int* mtile2_off,
+                        int* group_order, cudaStream_t s);
+cudaError_t launch_permute(const int* idx, const float* w, const int* block_base,
+                           const int* offsets, const int* poff, int64_t T, int k, int E,
+                           int* perm_token, int* slot_row, int* slot_pad, int* row_slot,
                            float* w_row, cudaStream_t s);
+cudaError_t launch_zero_pad_rows(uint16_t* m, const int* poff, const int* counts, int E, int H,
+                                 cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t* src, const int* slot_row, uint16_t* dst,
                                int64_t T, int H, int k, cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* scratch, uint16_t* y, int64_t T, int H, int k,
@@ -80,8 +92,27 @@ cudaError_t launch_gemm(const GemmArgs& a, int grid, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured |= bit;
   }
-  gemm_kernel<P><<<grid, gemm_threads<P>(), smem, s>>>(a);
-  return cudaGetLastError();
+  if constexpr (IsPair<P>::value) {
+    // clusters of two CTAs (grid is even)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(gemm_threads<P>());
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gemm_kernel<P>, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  } else {
+    gemm_kernel<P><<<grid, gemm_threads<P>(), smem, s>>>(a);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace moe

@@ -15,9 +15,10 @@ namespace {
 // --------------------------------------------------------------------------
 // Along the contiguous dimension (K-major operand [R, C], K = C).
 //   kRowsDense:    atom group of row = row / 128, r = row % 128 (weights).
-//   kRowsPermuted: rows of the expert-major permuted layout; the atom group is
-//                  the row's grouped-GEMM m-tile, mtile_off[e] + (row -
-//                  offsets[e]) / 128, and r its row inside that tile.
+//   kRowsPermuted: rows of the padded expert-major layout (offsets = padded
+//                  segment starts); the atom group is the row's grouped-GEMM
+//                  m-tile, mtile_off[e] + (row - offsets[e]) / 128, and r its
+//                  row inside that tile.
 // Atom index = group * (C / 128) + k / 128.  One warp per row.
 // --------------------------------------------------------------------------
 enum RowMode { kRowsDense = 0, kRowsPermuted = 1 };
@@ -36,6 +37,7 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, int64_t R, i
     group = row >> 7;
     r = static_cast<int>(row & 127);
   } else {
+    if (row >= __ldg(offsets + E)) return;   // rows past the last padded segment
     int lo = 0, hi = E - 1;     // largest e with offsets[e] <= row
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -79,9 +81,11 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, int64_t R, i
 //   kColsGateUp:   as kColsWeights over R = H rows, but the output [E, H, 2F]
 //                  interleaves W_gate and W_up in 64-column halves of every
 //                  128-column tile (gate columns 64j.., then up columns 64j..).
-//   kColsTokens:   the expert-major token rows, each expert's segment padded
-//                  to whole 128-row tiles (tile g of expert e is output rows
-//                  128*(mtile_off[e] + g) ..); rows past the segment are zero.
+//   kColsTokens:   the expert-major token rows (segments starting at the
+//                  padded offsets, counts[e] valid rows), each expert's
+//                  segment padded to whole 128-row tiles (tile g of expert e
+//                  is output rows 128*(mtile_off[e] + g) ..); rows past the
+//                  segment are zero.
 // Atom index = (k-tile) * (C_out / 128) + column tile for the token layout,
 // (expert * (C_out / 128) + column tile) * (R / 128) + k-tile for weights.
 // --------------------------------------------------------------------------
@@ -92,6 +96,7 @@ __global__ void __launch_bounds__(64) quant_cols_kernel(const uint16_t* __restri
                                   const uint16_t* __restrict__ src1, int R, int C_in,
                                   uint8_t* __restrict__ dst, uint8_t* __restrict__ sf,
                                   const int* __restrict__ offsets,
+                                  const int* __restrict__ counts,
                                   const int* __restrict__ mtile_off, int E) {
   // 64 threads: thread = (32-row block rb in 0..3, group of 8 columns cg in 0..15);
   // each reads 32 rows x 16 bytes, keeps 8 running maxima, writes 32 x 8 bytes.
@@ -114,7 +119,7 @@ __global__ void __launch_bounds__(64) quant_cols_kernel(const uint16_t* __restri
     }
     const int g = kg - __ldg(mtile_off + lo);
     src_row0 = static_cast<int64_t>(__ldg(offsets + lo)) + 128 * g;
-    valid = min(128, static_cast<int>(__ldg(offsets + lo + 1) - src_row0));
+    valid = min(128, __ldg(counts + lo) - 128 * g);
     dst_row0 = 128ll * kg;
     atom = static_cast<int64_t>(kg) * (C_out >> 7) + ct;
     src_col = ct * 128 + cg * 8;
@@ -197,7 +202,7 @@ cudaError_t launch_quant_cols_weights(const uint16_t* src, int E, int R, int C, 
                                       uint8_t* sf, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(E * (R / 128)), static_cast<unsigned>(C / 128));
   quant_cols_kernel<kColsWeights><<<grid, 64, 0, s>>>(src, nullptr, R, C, dst, sf, nullptr,
-                                                       nullptr, E);
+                                                      nullptr, nullptr, E);
   return cudaGetLastError();
 }
 
@@ -205,16 +210,16 @@ cudaError_t launch_quant_cols_gate_up(const uint16_t* W_gate, const uint16_t* W_
                                       int F, uint8_t* dst, uint8_t* sf, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(E * (H / 128)), static_cast<unsigned>(2 * F / 128));
   quant_cols_kernel<kColsGateUp><<<grid, 64, 0, s>>>(W_gate, W_up, H, F, dst, sf, nullptr,
-                                                      nullptr, E);
+                                                     nullptr, nullptr, E);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_cols_tokens(const uint16_t* src, int64_t max_ktiles, int C, uint8_t* dst,
-                                     uint8_t* sf, const int* offsets, const int* mtile_off, int E,
-                                     cudaStream_t s) {
+                                     uint8_t* sf, const int* poff, const int* counts,
+                                     const int* mtile_off, int E, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(max_ktiles), static_cast<unsigned>(C / 128));
-  quant_cols_kernel<kColsTokens><<<grid, 64, 0, s>>>(src, nullptr, 0, C, dst, sf, offsets,
-                                                      mtile_off, E);
+  quant_cols_kernel<kColsTokens><<<grid, 64, 0, s>>>(src, nullptr, 0, C, dst, sf, poff, counts,
+                                                     mtile_off, E);
   return cudaGetLastError();
 }
 

@@ -26,7 +26,6 @@ struct RouterProblem {
   static constexpr int BN = BN_;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
-  static constexpr bool kTailZero = false;
   static constexpr size_t kExtraSmem = 256 * sizeof(int);
   static constexpr int kEpiGroups = 1;      // a thread needs its whole row for the top-k
   static constexpr int kMaxK = 16;
@@ -141,7 +140,6 @@ struct GateUpFwdProblem {
   static constexpr int BN = 256;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = true;
-  static constexpr bool kTailZero = false;
   static constexpr size_t kExtraSmem = 0;
   static constexpr int kEpiGroups = 2;
 
@@ -198,7 +196,6 @@ struct DownFwdProblem {
   static constexpr int BN = 256;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = true;
-  static constexpr bool kTailZero = false;
   static constexpr size_t kExtraSmem = 0;
   static constexpr int kEpiGroups = 2;
 

@@ -25,7 +25,6 @@ struct DownDgradProblem {
   static constexpr int BN = BN_;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
-  static constexpr bool kTailZero = false;
   static constexpr size_t kExtraSmem = 0;
   static constexpr int kEpiGroups = 2;
 
@@ -46,7 +45,10 @@ struct DownDgradProblem {
                                int group, uint8_t*) {
     constexpr int kHalf = BN / 2;
     const bool valid = r < ti.rows;
-    const int64_t row = static_cast<int64_t>(ti.m0) + (valid ? r : 0);
+    // rows past the expert's tokens but inside its padded segment: dh and w*a
+    // are weight-gradient operands there, so they must read as zero
+    const bool pad = !valid && r < ti.rows_pad;
+    const int64_t row = static_cast<int64_t>(ti.m0) + ((valid || pad) ? r : 0);
     const int F = a.ld0;
     const int c0 = group * kHalf;
     const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(a.in0) + row * 2 * F + ti.n0;
@@ -96,6 +98,13 @@ struct DownDgradProblem {
         store_bf16x16(dh + c, dhg);
         store_bf16x16(dh + F + c, dhu);
         store_bf16x16(aw + c, awv);
+      } else if (pad) {
+        st_global_v4(dh + c, 0u, 0u, 0u, 0u);
+        st_global_v4(dh + c + 8, 0u, 0u, 0u, 0u);
+        st_global_v4(dh + F + c, 0u, 0u, 0u, 0u);
+        st_global_v4(dh + F + c + 8, 0u, 0u, 0u, 0u);
+        st_global_v4(aw + c, 0u, 0u, 0u, 0u);
+        st_global_v4(aw + c + 8, 0u, 0u, 0u, 0u);
       }
     }
     // one router-weight partial per (row, n-tile, column half)
@@ -117,7 +126,6 @@ struct GateUpDgradProblem {
   static constexpr int BN = 256;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
-  static constexpr bool kTailZero = false;
   static constexpr size_t kExtraSmem = 0;
   static constexpr int kEpiGroups = 2;
 
@@ -179,7 +187,6 @@ struct DownWgradProblem {
   static constexpr int BN = 256;
   static constexpr bool kAMN = true;
   static constexpr bool kBMN = true;
-  static constexpr bool kTailZero = true;
   static constexpr size_t kExtraSmem = 0;
   static constexpr int kEpiGroups = 2;
 
@@ -221,7 +228,6 @@ struct GateUpWgradProblem {
   static constexpr int BN = 256;
   static constexpr bool kAMN = true;
   static constexpr bool kBMN = true;
-  static constexpr bool kTailZero = true;
   static constexpr size_t kExtraSmem = 0;
   static constexpr int kEpiGroups = 2;
 
@@ -276,7 +282,6 @@ struct RouterWgradProblem {
   static constexpr int BN = 256;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = true;
-  static constexpr bool kTailZero = false;
   static constexpr size_t kExtraSmem = 0;
   static constexpr int kEpiGroups = 2;
 
@@ -331,7 +336,6 @@ struct DenseProblem {
   static constexpr int BN = 256;
   static constexpr bool kAMN = A_MN;
   static constexpr bool kBMN = B_MN;
-  static constexpr bool kTailZero = false;
   static constexpr size_t kExtraSmem = 0;
   static constexpr int kEpiGroups = 2;
 

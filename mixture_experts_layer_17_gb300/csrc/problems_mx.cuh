@@ -16,6 +16,34 @@ namespace moe {
 
 MOE_DEV const uint8_t* sf_atom(const uint8_t* base, int64_t index) { return base + index * 512; }
 
+// Quantises one 32-element MX block held by this thread (fp32 values) to E4M3
+// at dst (32 bytes) and writes its E8M0 scale byte at *scale.
+MOE_DEV void mx_block_store(const float (&v)[32], uint8_t* dst, uint8_t* scale) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int X = mx_exponent(amax);
+  const float inv = ldexpf(1.0f, -X);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w[i] = to_e4m3x4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], inv);
+  st_global_v4(dst, w[0], w[1], w[2], w[3]);
+  st_global_v4(dst + 16, w[4], w[5], w[6], w[7]);
+  *scale = static_cast<uint8_t>(X + 127);
+}
+
+MOE_DEV void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  float a[16], b[16];
+  tmem_ld16(taddr, a);
+  tmem_ld16(taddr + 16, b);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v[i] = a[i];
+    v[16 + i] = b[i];
+  }
+}
+
 // grouped-M tile with 128-element (fp8) K stages
 MOE_DEV TileInfo grouped_m_tile_mx(const GemmArgs& a, int t, int nstep) {
   TileInfo ti = grouped_m_tile(a, t, nstep);
@@ -38,6 +66,7 @@ MOE_DEV TileInfo grouped_k_tile_mx(const GemmArgs& a, int t, int BN) {
   ti.m0 = mt * kBM;
   ti.n0 = nt * BN;
   ti.rows = min(kBM, a.M - ti.m0);
+  ti.rows_pad = ti.rows;
   ti.kb0 = k0;
   ti.num_kb = __ldg(a.mtile_off + e + 1) - k0;
   ti.k_last = 128;
@@ -55,7 +84,6 @@ struct GateUpFwdMXProblem {
   static constexpr int BN = 128;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = true;
-  static constexpr bool kTailZero = false;
   static constexpr bool kMX = true;
   static constexpr size_t kExtraSmem = 0;
   static constexpr int kEpiGroups = 2;
@@ -73,30 +101,39 @@ struct GateUpFwdMXProblem {
     bulk_load(sSF + 512, sf_atom(a.sfB0, (static_cast<int64_t>(ti.e) * a.n_tiles + nt) * a.kt_b + kb), 512, bar);
   }
   MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
+  // out0 = a as E4M3 [Pa, F] (quantised here from fp32, one MX block of 32
+  // columns per thread), out1 = h bf16 [Pa, 2F], out2 = scale atoms of a
+  // (((mtile_off[e] + m-tile) * F/128 + f/128) * 512).
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
                                int group, uint8_t*) {
     const bool valid = r < ti.rows;
     const int64_t row = static_cast<int64_t>(ti.m0) + r;
     const int F = a.ld0;
     const int f0 = ti.n0 + 32 * group;
-    __nv_bfloat16* act = static_cast<__nv_bfloat16*>(a.out0) + row * F + f0;
+    float g[32], u[32];
+    tmem_ld32(taddr + 32 * group, g);
+    tmem_ld32(taddr + 64 + 32 * group, u);
+    if (!valid) return;
     __nv_bfloat16* hg = static_cast<__nv_bfloat16*>(a.out1) + row * 2 * F + f0;
-    __nv_bfloat16* hu = hg + F;
-#pragma unroll 1
-    for (int c = 0; c < 32; c += 16) {
-      float g[16], u[16];
-      tmem_ld16(taddr + 32 * group + c, g);
-      tmem_ld16(taddr + 64 + 32 * group + c, u);
-      tmem_ld_wait();
-      if (valid) {
-        float v[16];
+    float g16[16], u16[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = g[i] * sigmoidf_fast(g[i]) * u[i];
-        store_bf16x16(act + c, v);
-        store_bf16x16(hg + c, g);
-        store_bf16x16(hu + c, u);
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        g16[i] = g[16 * half + i];
+        u16[i] = u[16 * half + i];
       }
+      store_bf16x16(hg + 16 * half, g16);
+      store_bf16x16(hg + F + 16 * half, u16);
     }
+    float act[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) act[i] = g[i] * sigmoidf_fast(g[i]) * u[i];
+    uint8_t* aq = static_cast<uint8_t*>(a.out0) + row * F + f0;
+    uint8_t* sf = static_cast<uint8_t*>(a.out2) +
+                  ((static_cast<int64_t>(__ldg(a.mtile_off + ti.e)) + ti.mt) * (F / 128) + f0 / 128) * 512 +
+                  sf_atom_offset(r, (f0 >> 5) & 3);
+    mx_block_store(act, aq, sf);
   }
 };
 
@@ -106,7 +143,6 @@ struct DownFwdMXProblem {
   static constexpr int BN = 128;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = true;
-  static constexpr bool kTailZero = false;
   static constexpr bool kMX = true;
   static constexpr size_t kExtraSmem = 0;
   static constexpr int kEpiGroups = 2;
@@ -153,6 +189,69 @@ struct DownFwdMXProblem {
 // ([E*F, H], K-major); the SwiGLU-backward epilogue of DownDgradProblem<128>.
 struct DownDgradMXProblem : DownDgradProblem<128> {
   static constexpr bool kMX = true;
+  // As DownDgradProblem<128> (dh, w*a in bf16 for the weight gradients, the
+  // router-weight partials), plus dh quantised to E4M3 along F straight from
+  // fp32 for the gate/up dgrad: out3 = dh E4M3 [Pa, 2F], out4 = its scale
+  // atoms (((mtile_off[e] + m-tile) * 2F/128 + column/128) * 512).
+  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
+                               int group, uint8_t*) {
+    const bool valid = r < ti.rows;
+    const bool pad = !valid && r < ti.rows_pad;
+    const int64_t row = static_cast<int64_t>(ti.m0) + ((valid || pad) ? r : 0);
+    const int F = a.ld0;
+    const int c0 = group * 64;
+    const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(a.in0) + row * 2 * F + ti.n0;
+    __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(a.out0) + row * 2 * F + ti.n0;
+    __nv_bfloat16* aw = static_cast<__nv_bfloat16*>(a.out1) + row * F + ti.n0;
+    uint8_t* dhq = static_cast<uint8_t*>(a.out3) + row * 2 * F;
+    const int64_t atom_row = (static_cast<int64_t>(__ldg(a.mtile_off + ti.e)) + ti.mt) * (2 * F / 128);
+    uint8_t* sfq = static_cast<uint8_t*>(a.out4);
+    const float w = valid ? __ldg(static_cast<const float*>(a.in1) + row) : 0.f;
+    float dw = 0.f;
+#pragma unroll 1
+    for (int c = c0; c < c0 + 64; c += 32) {
+      float g[32];
+      tmem_ld32(taddr + c, g);
+      if (valid) {
+        float hg[32], hu[32], dhg[32], dhu[32], awv[32];
+        load_bf16x16(h + c, *reinterpret_cast<float(*)[16]>(hg));
+        load_bf16x16(h + c + 16, *reinterpret_cast<float(*)[16]>(hg + 16));
+        load_bf16x16(h + F + c, *reinterpret_cast<float(*)[16]>(hu));
+        load_bf16x16(h + F + c + 16, *reinterpret_cast<float(*)[16]>(hu + 16));
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float s = sigmoidf_fast(hg[i]);
+          const float silu = hg[i] * s;
+          const float act = silu * hu[i];
+          dw = fmaf(g[i], act, dw);
+          const float da = w * g[i];
+          dhg[i] = da * hu[i] * s * (1.0f + hg[i] * (1.0f - s));
+          dhu[i] = da * silu;
+          awv[i] = w * act;
+        }
+        store_bf16x16(dh + c, *reinterpret_cast<float(*)[16]>(dhg));
+        store_bf16x16(dh + c + 16, *reinterpret_cast<float(*)[16]>(dhg + 16));
+        store_bf16x16(dh + F + c, *reinterpret_cast<float(*)[16]>(dhu));
+        store_bf16x16(dh + F + c + 16, *reinterpret_cast<float(*)[16]>(dhu + 16));
+        store_bf16x16(aw + c, *reinterpret_cast<float(*)[16]>(awv));
+        store_bf16x16(aw + c + 16, *reinterpret_cast<float(*)[16]>(awv + 16));
+        const int cg = ti.n0 + c;           // gate column; up column = F + cg
+        mx_block_store(dhg, dhq + cg, sfq + (atom_row + cg / 128) * 512 + sf_atom_offset(r, (cg >> 5) & 3));
+        mx_block_store(dhu, dhq + F + cg,
+                       sfq + (atom_row + (F + cg) / 128) * 512 + sf_atom_offset(r, ((F + cg) >> 5) & 3));
+      } else if (pad) {
+#pragma unroll
+        for (int q = 0; q < 32; q += 8) {
+          st_global_v4(dh + c + q, 0u, 0u, 0u, 0u);
+          st_global_v4(dh + F + c + q, 0u, 0u, 0u, 0u);
+          st_global_v4(aw + c + q, 0u, 0u, 0u, 0u);
+        }
+      }
+    }
+    if (valid)
+      static_cast<float*>(a.out2)[row * (a.n_tiles * kEpiGroups) + (ti.n0 / BN) * kEpiGroups +
+                                  group] = dw;
+  }
   MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile_mx(a, t, 128); }
   MOE_DEV static void load_mx(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
                               uint8_t* sB, uint8_t* sSF, uint64_t* bar) {
@@ -171,7 +270,6 @@ struct GateUpDgradMXProblem {
   static constexpr int BN = 128;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
-  static constexpr bool kTailZero = false;
   static constexpr bool kMX = true;
   static constexpr size_t kExtraSmem = 0;
   static constexpr int kEpiGroups = 2;
@@ -224,7 +322,6 @@ struct WgradMXProblem {
   static constexpr int BN = 128;
   static constexpr bool kAMN = true;
   static constexpr bool kBMN = true;
-  static constexpr bool kTailZero = false;
   static constexpr bool kMX = true;
   static constexpr size_t kExtraSmem = 0;
   static constexpr int kEpiGroups = 2;
@@ -279,7 +376,6 @@ struct DenseMXProblem {
   static constexpr int BN = 128;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
-  static constexpr bool kTailZero = false;
   static constexpr bool kMX = true;
   static constexpr size_t kExtraSmem = 0;
   static constexpr int kEpiGroups = 2;

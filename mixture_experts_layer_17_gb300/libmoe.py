@@ -20,6 +20,8 @@ MOE_BF16, MOE_MXFP8, MOE_FP8_BWD = 0, 1, 2
 PRECISIONS = {"bf16": MOE_BF16, "mxfp8": MOE_MXFP8, "fp8_bwd": MOE_FP8_BWD}
 MOE_FLAG_SYNC_CHECK = 0x1
 MOE_FLAG_TEST_TIMEOUT = 0x2
+MOE_FLAG_CTA_PAIRS_OFF = 0x4
+MOE_FLAG_CTA_PAIRS_ON = 0x8
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
           3: "MOE_ERR_WORKSPACE_TOO_SMALL", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT",

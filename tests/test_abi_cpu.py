@@ -69,6 +69,8 @@ def test_null_and_flag_validation(lib):
     assert lib.moe_workspace_size(None, None, None, None) == 1
     cfg = libmoe.make_config(128, 256, 128, 8, 2, flags=0x100)
     assert lib.moe_workspace_size(ctypes.byref(cfg), None, None, None) == 1
+    cfg = libmoe.make_config(128, 256, 128, 8, 2, flags=0x4 | 0x8)   # pairs off and on
+    assert lib.moe_workspace_size(ctypes.byref(cfg), None, None, None) == 1
     cfg = libmoe.make_config(128, 256, 128, 8, 2)
     cfg.precision = 7
     assert lib.moe_workspace_size(ctypes.byref(cfg), None, None, None) == 1

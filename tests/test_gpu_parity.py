@@ -65,16 +65,30 @@ SWEEP = [
 ]
 
 
+# expert GEMMs on single-CTA 128-row tiles, or on CTA-pair 256-row tiles
+# (cta_group::2) wherever the shape allows
+PAIR_MODES = {"single": 0x4, "pairs": 0x8}
+
+
+@pytest.mark.parametrize("mode", sorted(PAIR_MODES))
 @pytest.mark.parametrize("T,H,F,E,k,seed", SWEEP)
-def test_shape_sweep(T, H, F, E, k, seed):
+def test_shape_sweep(T, H, F, E, k, seed, mode):
     sh = si.custom_shape(T, H, F, E, k, seed=seed)
     inp = si.make_inputs(sh, "cuda")
-    ref = _full_compare(sh, inp, run_layer(sh, inp))
+    out = run_layer(sh, inp, flags=PAIR_MODES[mode])
+    ref = _full_compare(sh, inp, out)
     if k == 1:
         # a single selected expert has w = 1 and no router gradient at all
-        out_dWr = run_layer(sh, inp)["dW_r"]
-        assert np.all(out_dWr == 0.0)
+        assert np.all(out["dW_r"] == 0.0)
         assert np.all(ref["dW_r"] == 0.0)
+
+
+@pytest.mark.parametrize("mode", sorted(PAIR_MODES))
+def test_pair_tiles_with_large_experts(mode):
+    # several 256-row tiles per expert, ragged last tiles and padded tails
+    sh = si.custom_shape(1500, 512, 512, 6, 2, seed=16)
+    inp = si.make_inputs(sh, "cuda")
+    _full_compare(sh, inp, run_layer(sh, inp, flags=PAIR_MODES[mode]))
 
 
 def test_zero_router_ties_go_to_lower_ids():
@@ -87,14 +101,15 @@ def test_zero_router_ties_go_to_lower_ids():
     _full_compare(sh, inp, out)
 
 
-def test_experts_without_tokens():
+@pytest.mark.parametrize("mode", sorted(PAIR_MODES))
+def test_experts_without_tokens(mode):
     sh = si.custom_shape(256, 256, 256, 12, 2, seed=22)
     inp = si.make_inputs(sh, "cuda")
     bias = torch.zeros(12, device="cuda")
     bias[3] = -30.0
     bias[7] = -30.0
     inp["logit_bias"] = bias
-    out = run_layer(sh, inp)
+    out = run_layer(sh, inp, flags=PAIR_MODES[mode])
     assert out["counts"][3] == 0 and out["counts"][7] == 0
     _full_compare(sh, inp, out)
 
