@@ -84,6 +84,65 @@ def stored_traffic(kernel: str, workload: str):
     return rec["bytes_per_launch"]
 
 
+# ncu kernel name (template argument) -> the label the library's profiler uses
+NCU_LABELS = [
+    ("WgradMXProblem<true>", "gate_up_wgrad_mx"), ("WgradMXProblem<false>", "down_wgrad_mx"),
+    ("GateUpFwdMXProblem", "gate_up_gemm_swiglu_mx"), ("DownFwdMXProblem", "down_gemm_scatter_mx"),
+    ("DownDgradMXProblem", "down_dgrad_swiglu_bwd_mx"),
+    ("GateUpDgradMXProblem", "gate_up_dgrad_scatter_mx"),
+    ("GateUpWgradProblem", "gate_up_wgrad"), ("DownWgradProblem", "down_wgrad"),
+    ("GateUpFwdPairProblem", "gate_up_gemm_swiglu"), ("GateUpFwdProblem", "gate_up_gemm_swiglu"),
+    ("DownFwdPairProblem", "down_gemm_scatter"), ("DownFwdProblem", "down_gemm_scatter"),
+    ("DownDgradPairProblem", "down_dgrad_swiglu_bwd"), ("DownDgradProblem", "down_dgrad_swiglu_bwd"),
+    ("GateUpDgradPairProblem", "gate_up_dgrad_scatter"),
+    ("GateUpDgradProblem", "gate_up_dgrad_scatter"),
+    ("RouterWgradProblem", "router_wgrad"), ("RouterProblem", "router_gemm_topk"),
+    ("combine_kernel", "combine"), ("unpermute_kernel", "unpermute_dx"),
+]
+_BYTE_UNITS = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "MB": 1e6,
+               "GB": 1e9}
+
+
+def record_traffic(csv_path: str, workload: str, command: str, path: str = None) -> dict:
+    """Fold an ncu CSV (metrics dram__bytes_read.sum and dram__bytes_write.sum,
+    one row per launch and metric) into profiles/dram_traffic.json: bytes per
+    launch for each library kernel of ``workload``, stamped with the hash of
+    the kernel sources they were taken on."""
+    import csv
+    rows = []
+    with open(csv_path) as fh:
+        lines = [ln for ln in fh if ln.startswith('"')]
+    for rec in csv.DictReader(lines):
+        rows.append(rec)
+    per_launch = {}
+    for rec in rows:
+        metric = rec.get("Metric Name", "")
+        if metric not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        label = next((lab for pat, lab in NCU_LABELS if pat in rec["Kernel Name"]), None)
+        if label is None:
+            continue
+        val = float(rec["Metric Value"].replace(",", "")) * _BYTE_UNITS.get(rec["Metric Unit"], 1)
+        key = (label, rec["ID"])
+        per_launch[key] = per_launch.get(key, 0.0) + val
+    table = {}
+    path = path or os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            table = json.load(fh)
+    labels = sorted({lab for lab, _ in per_launch})
+    h = csrc_hash()
+    for lab in labels:
+        vals = [v for (l2, _), v in per_launch.items() if l2 == lab]
+        table[f"{lab}@{workload}"] = {"bytes_per_launch": sum(vals) / len(vals),
+                                      "launches": len(vals), "csrc_hash": h,
+                                      "command": command}
+    with open(path, "w") as fh:
+        json.dump(table, fh, indent=1, sort_keys=True)
+        fh.write("\n")
+    return {lab: table[f"{lab}@{workload}"]["bytes_per_launch"] for lab in labels}
+
+
 def layer_flops(sh):
     fwd = 6 * sh.P * sh.H * sh.F + 2 * sh.T * sh.H * sh.E
     bwd = 12 * sh.P * sh.H * sh.F + 4 * sh.T * sh.H * sh.E
@@ -429,7 +488,14 @@ def main():
                     help="T,H,F,E,top_k: a custom shape (profiling aid) instead of --workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
+    ap.add_argument("--record-traffic", default=None, metavar="NCU_CSV",
+                    help="store per-launch DRAM bytes from an ncu CSV for --workload and exit")
+    ap.add_argument("--traffic-command", default="",
+                    help="the ncu command line the CSV came from (stored beside the figures)")
     args = ap.parse_args()
+    if args.record_traffic:
+        print(json.dumps(record_traffic(args.record_traffic, args.workload, args.traffic_command)))
+        return
     args.warmup = max(args.warmup, 3)
     if args.shape:
         T, H, F, E, k = (int(v) for v in args.shape.split(","))

@@ -3,6 +3,7 @@ exports every entry point include/moe.h declares, status strings, and argument
 validation (which runs before any CUDA call)."""
 
 import ctypes
+import json
 import os
 import re
 
@@ -80,3 +81,29 @@ def test_null_and_flag_validation(lib):
     assert lib.moe_route(ctypes.byref(cfg), *([None] * 10), 0, None) == 1
     assert lib.moe_backward(ctypes.byref(cfg), *([None] * 13), 0, None) == 1
     assert lib.moe_gemm_bf16(128, 100, 64, None, 1, None, 1, None, None, 0, None) == 2
+
+
+def test_bench_records_ncu_traffic(tmp_path):
+    """bench.py folds an ncu metrics CSV into per-launch DRAM bytes per kernel
+    label, stamped with the kernel-source hash that stored_traffic checks."""
+    import bench
+    head = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",'
+            '"Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit",'
+            '"Metric Value"\n')
+    body = []
+    for lid, kern, rd, wr in [
+            (0, "void moe::gemm_kernel<moe::GateUpFwdPairProblem>(moe::GemmArgs)", "1,000", "500"),
+            (1, "void moe::gemm_kernel<moe::GateUpFwdProblem>(moe::GemmArgs)", "3,000", "500"),
+            (2, "void moe::gemm_kernel<moe::WgradPairProblem<moe::GateUpWgradProblem>>(moe::GemmArgs)",
+             "2", "1"),
+            (3, "void at::native::vectorized_elementwise_kernel<...>", "7", "7")]:
+        for m, v, u in (("dram__bytes_read.sum", rd, "Kbyte"), ("dram__bytes_write.sum", wr, "byte")):
+            body.append(f'"{lid}","1","python","h","{kern}","1","7","(320, 1, 1)","(152, 1, 1)",'
+                        f'"0","10.3","Command line profiler metrics","{m}","{u}","{v}"\n')
+    csv_path = tmp_path / "t.csv"
+    csv_path.write_text("==PROF== Connected\n" + head + "".join(body))
+    out = tmp_path / "traffic.json"
+    got = bench.record_traffic(str(csv_path), "w", "ncu ...", path=str(out))
+    assert got == {"gate_up_gemm_swiglu": (1e6 + 500 + 3e6 + 500) / 2, "gate_up_wgrad": 2001.0}
+    stored = json.loads(out.read_text())
+    assert stored["gate_up_wgrad@w"]["csrc_hash"] == bench.csrc_hash()
