@@ -52,8 +52,9 @@ class MoeShape:
         return self.T * self.top_k
 
 
-# The five workloads.  Seeds: 0 for the tiny layer (as specified), 1, 2 and 3 for
-# the 30B, skewed 30B and 235B shapes; the MXFP8 workloads reuse the 235B seed.
+# The workloads.  Seeds: 0 for the tiny layer (as specified), 1, 2 and 3 for the
+# 30B, skewed 30B and 235B shapes; the MXFP8 workloads reuse the 235B seed, and
+# the skewed MXFP8 one adds the Zipf bias to it.
 WORKLOADS: Dict[str, MoeShape] = {
     "tiny": MoeShape("tiny", T=128, H=256, F=128, E=8, top_k=2, seed=0, keep_fp32=True),
     "qwen3_30b": MoeShape("qwen3_30b", T=4096, H=2048, F=768, E=128, top_k=8, seed=1),
@@ -64,6 +65,9 @@ WORKLOADS: Dict[str, MoeShape] = {
                                  seed=3, precision="mxfp8"),
     "qwen3_235b_fp8_bwd": MoeShape("qwen3_235b_fp8_bwd", T=16384, H=4096, F=1536, E=128,
                                    top_k=8, seed=3, precision="fp8_bwd"),
+    # the MXFP8 layer once more with the skewed routing of the 30B-skew workload
+    "qwen3_235b_mxfp8_skew": MoeShape("qwen3_235b_mxfp8_skew", T=16384, H=4096, F=1536, E=128,
+                                      top_k=8, seed=3, skew=True, precision="mxfp8"),
 }
 
 ZIPF_S = 1.1

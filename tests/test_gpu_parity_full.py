@@ -52,7 +52,8 @@ def _report_and_check(name, errs, prec, bad):
 
 
 @pytest.mark.parametrize("name", ["qwen3_30b", "qwen3_30b_skew", "qwen3_235b",
-                                  "qwen3_235b_mxfp8", "qwen3_235b_fp8_bwd"])
+                                  "qwen3_235b_mxfp8", "qwen3_235b_fp8_bwd",
+                                  "qwen3_235b_mxfp8_skew"])
 def test_full_size_sampled(name):
     from mixture_experts_layer_17_gb300 import MoeLayer
     sh = si.shape(name)
