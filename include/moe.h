@@ -83,6 +83,20 @@ typedef enum {
                                          when experts average >= 512 rows, pairs
                                          run the gate/up dgrad, the down forward
                                          and the two expert weight gradients      */
+#define MOE_FLAG_RECOMPUTE      0x10u /* activation checkpointing (full activation
+                                         checkpointing is the training setting of
+                                         the end-to-end runs in "Os Números..." on
+                                         bitsgeniais.com.br): ctx keeps only the
+                                         routing and permutation; the permuted
+                                         input x_perm and the pre-activations h
+                                         live in the forward workspace instead,
+                                         and moe_backward dispatches x again and
+                                         recomputes h with the gate/up GEMM (in
+                                         the forward's precision) before the
+                                         backward GEMMs.  ctx_bytes shrinks by
+                                         (T*top_k + 64*E) * (H + 2F) * 2 bytes;
+                                         forward and backward must both be given
+                                         the flag                                 */
 
 typedef struct {
   int64_t T;           /* tokens                                   */
@@ -92,6 +106,18 @@ typedef struct {
   int32_t top_k;       /* experts per token                        */
   int32_t precision;   /* moe_precision_t                          */
   uint32_t flags;      /* MOE_FLAG_*                               */
+  int32_t max_sms;     /* SM budget: 0 = every SM of the device;
+                          else the persistent kernels launch at most
+                          this many CTAs (one per SM), leaving the
+                          other SMs to work on other streams.  The
+                          counterpart of reserving SMs for
+                          communication ("Detalhes Técnicos
+                          Rápidos" on bitsgeniais.com.br).  CTA
+                          pairs need at least 2; below that every
+                          GEMM runs single-CTA tiles.  Results are
+                          the same for every budget except dW_r,
+                          whose split-K depth follows the budget
+                          (summation order only).  Must be >= 0. */
 } moe_config_t;
 
 /* Bytes of device memory each call needs from the caller:
@@ -143,6 +169,24 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
                           moe_bf16_t* dx, moe_bf16_t* dW_r, moe_bf16_t* dW_gate,
                           moe_bf16_t* dW_up, moe_bf16_t* dW_down, void* ws, size_t ws_bytes,
                           moe_stream_t stream);
+
+/* moe_backward for gradient accumulation over micro-batches (the end-to-end
+ * runs of "Os Números..." on bitsgeniais.com.br train on micro-batches of
+ * 16,384-token sequences): the weight gradients are ADDED into caller-owned
+ * fp32 buffers, gW_r [H,E] += dW_r, gW_gate / gW_up [E,H,F] += dW_gate /
+ * dW_up, gW_down [E,F,H] += dW_down, straight from the fp32 accumulators
+ * (no bf16 rounding of the increment).  dx is written in bf16 as in
+ * moe_backward.  An expert that received no token leaves its slices of the
+ * buffers unchanged.  The buffers must be 16-byte aligned, hold finite
+ * values, and not overlap each other or any input.  Same ctx, cfg, ws and
+ * error behaviour as moe_backward. */
+moe_status_t moe_backward_accumulate(const moe_config_t* cfg, const moe_bf16_t* x,
+                                     const moe_bf16_t* W_r, const moe_bf16_t* W_gate,
+                                     const moe_bf16_t* W_up, const moe_bf16_t* W_down,
+                                     const void* ctx, const moe_bf16_t* dY, moe_bf16_t* dx,
+                                     float* gW_r, float* gW_gate, float* gW_up,
+                                     float* gW_down, void* ws, size_t ws_bytes,
+                                     moe_stream_t stream);
 
 /* Dense bf16 GEMM on the same tcgen05 engine: D[M,N] = sum_k A(m,k) B(n,k),
  * fp32 accumulation, D written as fp32 row-major [M, N] (ldd = N).

@@ -14,8 +14,8 @@ from typing import Dict, Optional
 import torch
 
 from . import libmoe
-from .libmoe import (MoeConfig, MoeError, make_config, moe_backward, moe_forward,  # noqa: F401
-                     moe_gemm_bf16, moe_get_device_status, moe_launch_count,
+from .libmoe import (MoeConfig, MoeError, make_config, moe_backward,  # noqa: F401
+                     moe_backward_accumulate, moe_forward, moe_gemm_bf16, moe_get_device_status, moe_launch_count,
                      moe_profile_enable, moe_profile_read, moe_route, moe_status_string,
                      moe_workspace_size)
 
@@ -28,8 +28,8 @@ class MoeLayer:
     """
 
     def __init__(self, T: int, H: int, F: int, E: int, top_k: int, precision: str = "bf16",
-                 flags: int = 0, device="cuda"):
-        self.cfg = make_config(T, H, F, E, top_k, precision, flags)
+                 flags: int = 0, device="cuda", max_sms: int = 0):
+        self.cfg = make_config(T, H, F, E, top_k, precision, flags, max_sms)
         self.T, self.H, self.F, self.E, self.top_k = T, H, F, E, top_k
         self.device = torch.device(device)
         f, c, b = moe_workspace_size(self.cfg)
@@ -72,6 +72,17 @@ class MoeLayer:
                      grads["dW_r"], grads["dW_gate"], grads["dW_up"], grads["dW_down"],
                      self.bwd_ws, stream)
         return grads
+
+    def backward_accumulate(self, x, W_r, W_gate, W_up, W_down, dY, acc: Dict[str, torch.Tensor],
+                            dx: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """Adds the weight gradients into the fp32 tensors acc["dW_r"],
+        acc["dW_gate"], acc["dW_up"], acc["dW_down"]; returns dx (bf16)."""
+        if dx is None:
+            dx = torch.empty_like(x)
+        moe_backward_accumulate(self.cfg, x, W_r, W_gate, W_up, W_down, self.ctx, dY, dx,
+                                acc["dW_r"], acc["dW_gate"], acc["dW_up"], acc["dW_down"],
+                                self.bwd_ws, stream)
+        return dx
 
     def device_status(self, which: str = "fwd", stream=None) -> int:
         ws = self.fwd_ws if which == "fwd" else self.bwd_ws

@@ -194,6 +194,11 @@ struct Layout {
       c_order, c_wrt, c_xperm, c_h, c_poff, c_mtile2, c_slotpad, c_total;
   // backward workspace
   size_t b_status, b_dyp, b_dh, b_aw, b_dwp, b_dl, b_dlt, b_scratch, b_wrp, b_total;
+  // MOE_FLAG_RECOMPUTE: x_perm and h live in the forward workspace, and the
+  // backward re-dispatches x and recomputes h into its own workspace
+  bool recompute;
+  size_t f_xperm, f_h, b_xperm, b_h;
+  size_t bq_rx, bs_rx, bq_ra, bs_ra, bq_rwgu, bs_rwgu;   // MXFP8 recompute operands
   // MXFP8 buffers (E4M3 data + scale atoms); present only when the precision uses them
   int64_t mt_max;    // upper bound of the 128-row m-tiles (= K-tiles of the padded token layout)
   size_t fq_x, fs_x, fq_a, fs_a, fq_wgu, fs_wgu, fq_wd, fs_wd;
@@ -202,7 +207,7 @@ struct Layout {
 };
 
 Layout make_layout(const moe_config_t& c, int sms) {
-  Layout L;
+  Layout L{};
   L.T = c.T;
   L.H = c.H;
   L.F = c.F;
@@ -223,13 +228,15 @@ Layout make_layout(const moe_config_t& c, int sms) {
   const bool bf = c.precision != MOE_MXFP8;        // bf16 forward GEMMs
   const bool bb = c.precision == MOE_BF16;         // bf16 backward GEMMs
   const bool big = L.P >= 512ll * L.E;             // experts average >= 512 rows
-  const bool pp = !pairs_off && (pairs_on || big);
-  L.pair_gu_fwd = bf && !pairs_off && pairs_on;
+  const bool can_pair = sms >= 2;                    // an SM budget of 1 runs single CTAs
+  const bool pp = can_pair && !pairs_off && (pairs_on || big);
+  L.pair_gu_fwd = bf && can_pair && !pairs_off && pairs_on;
   L.pair_down_fwd = bf && pp;
-  L.pair_down_dgrad = bb && !pairs_off && pairs_on && (L.F % 256 == 0);
+  L.pair_down_dgrad = bb && can_pair && !pairs_off && pairs_on && (L.F % 256 == 0);
   L.pair_gu_dgrad = bb && pp;
   L.pair_down_wgrad = bb && pp && (L.F % 256 == 0);
   L.pair_gu_wgrad = bb && pp;
+  L.recompute = (c.flags & MOE_FLAG_RECOMPUTE) != 0;
   L.ntiles = static_cast<int>((L.T + kBM - 1) / kBM);
   L.router_bn = next_pow2_at_least16(L.E);
   L.dgrad_bn = (L.F % 256 == 0) ? 256 : 128;
@@ -260,6 +267,10 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.r_slotpad = f.take(sizeof(int) * P);
   L.f_a = f.take(2 * Pa * F);
   L.f_scratch = f.take(2 * P * H);
+  if (L.recompute) {
+    L.f_xperm = f.take(2 * Pa * H);
+    L.f_h = f.take(2 * Pa * 2 * F);
+  }
   L.mt_max = (L.P + kBM - 1) / kBM + L.E;
   const size_t mt = static_cast<size_t>(L.mt_max);
   if (c.precision == MOE_MXFP8) {
@@ -286,8 +297,10 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.c_mtile = x.take(sizeof(int) * (E + 1));
   L.c_order = x.take(sizeof(int) * E);
   L.c_wrt = x.take(2 * E * H);
-  L.c_xperm = x.take(2 * Pa * H);
-  L.c_h = x.take(2 * Pa * 2 * F);
+  if (!L.recompute) {
+    L.c_xperm = x.take(2 * Pa * H);
+    L.c_h = x.take(2 * Pa * 2 * F);
+  }
   L.c_poff = x.take(sizeof(int) * (E + 1));
   L.c_mtile2 = x.take(sizeof(int) * (E + 1));
   L.c_slotpad = x.take(sizeof(int) * P);
@@ -303,6 +316,18 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.b_dlt = b.take(2 * E * static_cast<size_t>(L.T_pad));
   L.b_scratch = b.take(2 * P * H);
   L.b_wrp = b.take(sizeof(float) * L.wr_split * E * H);
+  if (L.recompute) {
+    L.b_xperm = b.take(2 * Pa * H);
+    L.b_h = b.take(2 * Pa * 2 * F);
+    if (c.precision == MOE_MXFP8) {
+      L.bq_rx = b.take(Pa * H);
+      L.bs_rx = b.take(mt * (H / 128) * 512);
+      L.bq_ra = b.take(Pa * F);
+      L.bs_ra = b.take(mt * (F / 128) * 512);
+      L.bq_rwgu = b.take(E * H * 2 * F);
+      L.bs_rwgu = b.take(E * (2 * F / 128) * (H / 128) * 512);
+    }
+  }
   if (c.precision != MOE_BF16) {
     const size_t Pp = 128 * mt;   // padded token rows
     L.bq_dy = b.take(Pa * H);
@@ -332,8 +357,9 @@ Layout make_layout(const moe_config_t& c, int sms) {
 moe_status_t validate(const moe_config_t* c) {
   if (c == nullptr) return MOE_ERR_INVALID_ARG;
   if (c->flags & ~(MOE_FLAG_SYNC_CHECK | MOE_FLAG_TEST_TIMEOUT | MOE_FLAG_CTA_PAIRS_OFF |
-                   MOE_FLAG_CTA_PAIRS_ON))
+                   MOE_FLAG_CTA_PAIRS_ON | MOE_FLAG_RECOMPUTE))
     return MOE_ERR_INVALID_ARG;
+  if (c->max_sms < 0) return MOE_ERR_INVALID_ARG;
   if ((c->flags & MOE_FLAG_CTA_PAIRS_OFF) && (c->flags & MOE_FLAG_CTA_PAIRS_ON))
     return MOE_ERR_INVALID_ARG;
   if (c->precision < MOE_BF16 || c->precision > MOE_FP8_BWD) return MOE_ERR_INVALID_ARG;
@@ -366,6 +392,11 @@ GemmArgs base_args(DeviceStatus* st, uint32_t flags) {
 int grid_for(int64_t tiles, int sms) {
   if (tiles < 1) return 1;
   return static_cast<int>(tiles < sms ? tiles : sms);
+}
+
+// SMs the persistent kernels of a call may use (moe_config_t.max_sms)
+int sm_budget(int device_sms, const moe_config_t& c) {
+  return (c.max_sms > 0 && c.max_sms < device_sms) ? c.max_sms : device_sms;
 }
 
 }  // namespace
@@ -451,60 +482,111 @@ bool all_aligned16(std::initializer_list<const void*> ps) {
 
 // ---------------------------------------------------------------- MXFP8 passes
 
-// F7 + F8 and F9 in MXFP8: quantise the gate/up operands (x_perm along H;
-// W_gate / W_up along H, interleaved per 128 columns), the block-scaled
-// gate/up GEMM with SwiGLU whose epilogue quantises a along F from fp32,
-// quantise W_down along F, then the block-scaled down GEMM with the weighted
-// scatter.
+// F7 + F8 in bf16: the gate/up GEMM with the SwiGLU epilogue, writing a and
+// the pre-activations h.  `recompute` names the launch of the backward's
+// recomputation (MOE_FLAG_RECOMPUTE).
+moe_status_t gate_up_fwd_bf16(const Layout& L, int sms, cudaStream_t s, uint32_t fl,
+                              DeviceStatus* st, const uint16_t* xperm, const uint16_t* W_gate,
+                              const uint16_t* W_up, const int* poff, const int* counts,
+                              const int* mtile, const int* mtile2, uint16_t* act, uint16_t* h,
+                              bool recompute) {
+  GemmArgs a = base_args(st, fl);
+  if (!make_map(&a.mapA, xperm, L.H, L.Pa, 2ull * L.H, 64, 128) ||
+      !make_map(&a.mapB0, W_gate, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 64) ||
+      !make_map(&a.mapB1, W_up, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 64))
+    return MOE_ERR_CUDA;
+  a.K = L.H;
+  a.N = 2 * L.F;
+  a.n_tiles = L.F / 128;
+  a.num_groups = L.E;
+  a.b_group_rows = L.H;
+  a.offsets = poff;
+  a.counts = counts;
+  a.mtile_off = mtile;
+  a.mtile2_off = mtile2;
+  a.out0 = act;
+  a.out1 = h;
+  a.ld0 = L.F;
+  if (fl & MOE_FLAG_TEST_TIMEOUT) {
+    a.flags = kGemmInjectWait;
+    a.wait_limit_ns = kTestWaitNs;
+  }
+  const char* label = recompute ? "recompute_gate_up_gemm_swiglu" : "gate_up_gemm_swiglu";
+  if (L.pair_gu_fwd) {
+    const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, sms);
+    return run(label, s, fl, [&] { return launch_gate_up_fwd_pair(a, grid, s); });
+  }
+  const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, sms);
+  return run(label, s, fl, [&] { return launch_gate_up_fwd(a, grid, s); });
+}
+
+// E4M3 operands and scale atoms of the MXFP8 gate/up GEMM
+struct MxGateUpBufs {
+  uint8_t *xq, *sx, *aq, *sa, *wgu, *swgu;
+};
+
+// F7 + F8 in MXFP8: quantise x_perm along H and W_gate / W_up along H
+// (interleaved per 128 columns), then the block-scaled gate/up GEMM with
+// SwiGLU whose epilogue writes h and quantises a along F from fp32.
+moe_status_t gate_up_fwd_mx(const Layout& L, int sms, cudaStream_t s, uint32_t fl,
+                            DeviceStatus* st, const uint16_t* xperm, const uint16_t* W_gate,
+                            const uint16_t* W_up, const int* offsets, const int* counts,
+                            const int* mtile, uint16_t* h, const MxGateUpBufs& q,
+                            bool recompute) {
+  MOE_TRY(run(recompute ? "recompute_mx_quant_x" : "mx_quant_x", s, fl, [&] {
+    return launch_quant_rows_permuted(xperm, L.Pa, L.H, q.xq, q.sx, offsets, mtile, L.E, s);
+  }));
+  MOE_TRY(run(recompute ? "recompute_mx_quant_w_gate_up" : "mx_quant_w_gate_up", s, fl, [&] {
+    return launch_quant_cols_gate_up(W_gate, W_up, L.E, L.H, L.F, q.wgu, q.swgu, s);
+  }));
+  GemmArgs a = base_args(st, fl);
+  if (!make_map_u8(&a.mapA, q.xq, L.H, L.Pa, L.H) ||
+      !make_map_u8(&a.mapB0, q.wgu, 2ull * L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F))
+    return MOE_ERR_CUDA;
+  a.mapB1 = a.mapB0;
+  a.K = L.H;
+  a.N = 2 * L.F;
+  a.n_tiles = 2 * L.F / 128;
+  a.num_groups = L.E;
+  a.b_group_rows = L.H;
+  a.offsets = offsets;
+  a.counts = counts;
+  a.mtile_off = mtile;
+  a.out0 = q.aq;    // a quantised to E4M3 in the epilogue
+  a.out1 = h;
+  a.out2 = q.sa;    // its scale atoms
+  a.ld0 = L.F;
+  a.sfA = q.sx;
+  a.kt_a = L.H / 128;
+  a.sfB0 = q.swgu;
+  a.kt_b = L.H / 128;
+  if (fl & MOE_FLAG_TEST_TIMEOUT) {
+    a.flags = kGemmInjectWait;
+    a.wait_limit_ns = kTestWaitNs;
+  }
+  const int grid = grid_for(((L.P + kBM - 1) / kBM + L.E) * a.n_tiles, sms);
+  return run(recompute ? "recompute_gate_up_gemm_swiglu_mx" : "gate_up_gemm_swiglu_mx", s, fl,
+             [&] { return launch_gate_up_fwd_mx(a, grid, s); });
+}
+
+// F7 + F8 and F9 in MXFP8: the gate/up part above, then W_down quantised
+// along F and the block-scaled down GEMM with the weighted scatter.
 moe_status_t forward_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t fl,
                               DeviceStatus* st, const uint16_t* xperm, const uint16_t* W_gate,
                               const uint16_t* W_up, const uint16_t* W_down, const int* offsets,
                               const int* counts, const int* mtile, const float* w_row,
                               const int* row_slot,
                               uint16_t* act, uint16_t* h, uint16_t* scratch, void* ws) {
-  uint8_t* xq = at<uint8_t>(ws, L.fq_x);
-  uint8_t* sx = at<uint8_t>(ws, L.fs_x);
-  uint8_t* aq = at<uint8_t>(ws, L.fq_a);
-  uint8_t* sa = at<uint8_t>(ws, L.fs_a);
-  uint8_t* wgu = at<uint8_t>(ws, L.fq_wgu);
-  uint8_t* swgu = at<uint8_t>(ws, L.fs_wgu);
+  (void)act;
+  const MxGateUpBufs q{at<uint8_t>(ws, L.fq_x), at<uint8_t>(ws, L.fs_x), at<uint8_t>(ws, L.fq_a),
+                       at<uint8_t>(ws, L.fs_a), at<uint8_t>(ws, L.fq_wgu),
+                       at<uint8_t>(ws, L.fs_wgu)};
+  uint8_t* aq = q.aq;
+  uint8_t* sa = q.sa;
   uint8_t* wd = at<uint8_t>(ws, L.fq_wd);
   uint8_t* swd = at<uint8_t>(ws, L.fs_wd);
-  MOE_TRY(run("mx_quant_x", s, fl, [&] {
-    return launch_quant_rows_permuted(xperm, L.Pa, L.H, xq, sx, offsets, mtile, L.E, s);
-  }));
-  MOE_TRY(run("mx_quant_w_gate_up", s, fl, [&] {
-    return launch_quant_cols_gate_up(W_gate, W_up, L.E, L.H, L.F, wgu, swgu, s);
-  }));
-  {
-    GemmArgs a = base_args(st, fl);
-    if (!make_map_u8(&a.mapA, xq, L.H, L.Pa, L.H) ||
-        !make_map_u8(&a.mapB0, wgu, 2ull * L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F))
-      return MOE_ERR_CUDA;
-    a.mapB1 = a.mapB0;
-    a.K = L.H;
-    a.N = 2 * L.F;
-    a.n_tiles = 2 * L.F / 128;
-    a.num_groups = L.E;
-    a.b_group_rows = L.H;
-    a.offsets = offsets;
-    a.counts = counts;
-    a.mtile_off = mtile;
-    a.out0 = aq;    // a quantised to E4M3 in the epilogue
-    a.out1 = h;
-    a.out2 = sa;    // its scale atoms
-    a.ld0 = L.F;
-    a.sfA = sx;
-    a.kt_a = L.H / 128;
-    a.sfB0 = swgu;
-    a.kt_b = L.H / 128;
-    if (fl & MOE_FLAG_TEST_TIMEOUT) {
-      a.flags = 2u;
-      a.wait_limit_ns = kTestWaitNs;
-    }
-    const int grid = grid_for(((L.P + kBM - 1) / kBM + L.E) * a.n_tiles, sms);
-    MOE_TRY(run("gate_up_gemm_swiglu_mx", s, fl, [&] { return launch_gate_up_fwd_mx(a, grid, s); }));
-  }
+  MOE_TRY(gate_up_fwd_mx(L, sms, s, fl, st, xperm, W_gate, W_up, offsets, counts, mtile, h, q,
+                         false));
   MOE_TRY(run("mx_quant_w_down_f", s, fl, [&] {
     return launch_quant_cols_weights(W_down, L.E, L.F, L.H, wd, swd, s);
   }));
@@ -545,8 +627,10 @@ struct BwdBufs {
   const uint16_t* wrt;
   uint16_t *dh, *aw;
   float *dwp, *dl;
-  uint16_t *dlt, *scratch, *dx, *dW_gate, *dW_up, *dW_down;
+  uint16_t *dlt, *scratch, *dx;
+  void *dW_gate, *dW_up, *dW_down;   // bf16, or fp32 accumulation buffers
   void* ws;
+  uint32_t wflags;                   // kGemmAccumF32 or 0, for the weight gradients
 };
 
 // B2-B9 in MXFP8 (precision mxfp8 and fp8_bwd): every expert GEMM of the
@@ -612,7 +696,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     a.sfB0 = swdh;
     a.kt_b = L.H / 128;
     if (fl & MOE_FLAG_TEST_TIMEOUT) {
-      a.flags = 2u;
+      a.flags = kGemmInjectWait;
       a.wait_limit_ns = kTestWaitNs;
     }
     const int grid = grid_for(mtiles * a.n_tiles, sms);
@@ -634,6 +718,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
   }));
   {
     GemmArgs a = base_args(st, fl);
+    a.flags = b.wflags;
     if (!make_map_u8(&a.mapA, awt, L.F, Pp, L.F) || !make_map_u8(&a.mapB0, dyt, L.H, Pp, L.H))
       return MOE_ERR_CUDA;
     a.mapB1 = a.mapB0;
@@ -700,6 +785,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
   }));
   {
     GemmArgs a = base_args(st, fl);
+    a.flags = b.wflags;
     if (!make_map_u8(&a.mapA, xt, L.H, Pp, L.H) ||
         !make_map_u8(&a.mapB0, dht, 2ull * L.F, Pp, 2ull * L.F))
       return MOE_ERR_CUDA;
@@ -747,7 +833,8 @@ moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* fwd_ws, size_t*
   MOE_TRY(validate(cfg));
   DevInfo d;
   MOE_TRY(current_device(&d));
-  const Layout L = make_layout(*cfg, d.sms);
+  const int sms = sm_budget(d.sms, *cfg);
+  const Layout L = make_layout(*cfg, sms);
   if (fwd_ws) *fwd_ws = L.f_total;
   if (ctx_bytes) *ctx_bytes = L.c_total;
   if (bwd_ws) *bwd_ws = L.b_total;
@@ -765,7 +852,8 @@ moe_status_t moe_route(const moe_config_t* cfg, const moe_bf16_t* x, const moe_b
     return MOE_ERR_INVALID_ARG;
   DevInfo d;
   MOE_TRY(current_device(&d));
-  const Layout L = make_layout(*cfg, d.sms);
+  const int sms = sm_budget(d.sms, *cfg);
+  const Layout L = make_layout(*cfg, sms);
   if (ws_bytes < L.f_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   DeviceStatus* st = at<DeviceStatus>(ws, L.f_status);
@@ -775,7 +863,7 @@ moe_status_t moe_route(const moe_config_t* cfg, const moe_bf16_t* x, const moe_b
               at<int>(ws, L.r_mtile), at<int>(ws, L.r_order), at<uint16_t>(ws, L.r_wrt),
               at<int>(ws, L.f_hist), at<int>(ws, L.f_base), st, at<int>(ws, L.r_poff),
               at<int>(ws, L.r_mtile2), at<int>(ws, L.r_slotpad)};
-  return run_routing(*cfg, L, b, d.sms, s);
+  return run_routing(*cfg, L, b, sms, s);
 }
 
 moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe_bf16_t* W_r,
@@ -788,7 +876,8 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
     return MOE_ERR_INVALID_ARG;
   DevInfo d;
   MOE_TRY(current_device(&d));
-  const Layout L = make_layout(*cfg, d.sms);
+  const int sms = sm_budget(d.sms, *cfg);
+  const Layout L = make_layout(*cfg, sms);
   if (ws_bytes < L.f_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const uint32_t fl = cfg->flags;
@@ -805,8 +894,9 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
   float* w_row = at<float>(ctx, L.c_w_row);
   int* mtile = at<int>(ctx, L.c_mtile);
   int* mtile2 = at<int>(ctx, L.c_mtile2);
-  uint16_t* xperm = at<uint16_t>(ctx, L.c_xperm);
-  uint16_t* h = at<uint16_t>(ctx, L.c_h);
+  // x_perm and h: kept in ctx for the backward, or (recompute) in the workspace
+  uint16_t* xperm = L.recompute ? at<uint16_t>(ws, L.f_xperm) : at<uint16_t>(ctx, L.c_xperm);
+  uint16_t* h = L.recompute ? at<uint16_t>(ws, L.f_h) : at<uint16_t>(ctx, L.c_h);
   uint16_t* act = at<uint16_t>(ws, L.f_a);
   uint16_t* scratch = at<uint16_t>(ws, L.f_scratch);
 
@@ -814,7 +904,7 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
               at<int>(ctx, L.c_perm), slot, row_slot, w_row, mtile, at<int>(ctx, L.c_order),
               at<uint16_t>(ctx, L.c_wrt), at<int>(ws, L.f_hist), at<int>(ws, L.f_base), st,
               poff, mtile2, slot_pad};
-  MOE_TRY(run_routing(*cfg, L, b, d.sms, s));
+  MOE_TRY(run_routing(*cfg, L, b, sms, s));
 
   // F6: dispatch x to the padded expert-major rows (segment tails zeroed: they
   // are K rows of the gate/up weight gradient)
@@ -824,40 +914,12 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
               [&] { return launch_zero_pad_rows(xperm, poff, counts, L.E, L.H, s); }));
 
   if (cfg->precision == MOE_MXFP8) {
-    MOE_TRY(forward_gemms_mx(L, d.sms, s, fl, st, xperm, W_gate, W_up, W_down, poff, counts,
+    MOE_TRY(forward_gemms_mx(L, sms, s, fl, st, xperm, W_gate, W_up, W_down, poff, counts,
                              mtile, w_row, row_slot, act, h, scratch, ws));
   } else {
     // F7 + F8: gate/up GEMM with SwiGLU
-    {
-      GemmArgs a = base_args(st, fl);
-      if (!make_map(&a.mapA, xperm, L.H, L.Pa, 2ull * L.H, 64, 128) ||
-          !make_map(&a.mapB0, W_gate, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 64) ||
-          !make_map(&a.mapB1, W_up, L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F, 64, 64))
-        return MOE_ERR_CUDA;
-      a.K = L.H;
-      a.N = 2 * L.F;
-      a.n_tiles = L.F / 128;
-      a.num_groups = L.E;
-      a.b_group_rows = L.H;
-      a.offsets = poff;
-      a.counts = counts;
-      a.mtile_off = mtile;
-      a.mtile2_off = mtile2;
-      a.out0 = act;
-      a.out1 = h;
-      a.ld0 = L.F;
-      if (fl & MOE_FLAG_TEST_TIMEOUT) {
-        a.flags = 2u;
-        a.wait_limit_ns = kTestWaitNs;
-      }
-      if (L.pair_gu_fwd) {
-        const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, d.sms);
-        MOE_TRY(run("gate_up_gemm_swiglu", s, fl, [&] { return launch_gate_up_fwd_pair(a, grid, s); }));
-      } else {
-        const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
-        MOE_TRY(run("gate_up_gemm_swiglu", s, fl, [&] { return launch_gate_up_fwd(a, grid, s); }));
-      }
-    }
+    MOE_TRY(gate_up_fwd_bf16(L, sms, s, fl, st, xperm, W_gate, W_up, poff, counts, mtile, mtile2,
+                             act, h, false));
     // F9 + F10: down GEMM with the weighted scatter, then the k-way combine
     {
       GemmArgs a = base_args(st, fl);
@@ -879,10 +941,10 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
       a.out0 = scratch;
       a.ld0 = L.H;
       if (L.pair_down_fwd) {
-        const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, d.sms);
+        const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, sms);
         MOE_TRY(run("down_gemm_scatter", s, fl, [&] { return launch_down_fwd_pair(a, grid, s); }));
       } else {
-        const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
+        const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, sms);
         MOE_TRY(run("down_gemm_scatter", s, fl, [&] { return launch_down_fwd(a, grid, s); }));
       }
     }
@@ -891,19 +953,22 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
   return MOE_OK;
 }
 
-moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const moe_bf16_t* W_r,
-                          const moe_bf16_t* W_gate, const moe_bf16_t* W_up,
-                          const moe_bf16_t* W_down, const void* ctx_in, const moe_bf16_t* dY,
-                          moe_bf16_t* dx, moe_bf16_t* dW_r, moe_bf16_t* dW_gate,
-                          moe_bf16_t* dW_up, moe_bf16_t* dW_down, void* ws, size_t ws_bytes,
-                          moe_stream_t stream) {
+// moe_backward and moe_backward_accumulate: the weight gradients are bf16
+// outputs, or (accum) fp32 buffers the gradients are added into.
+static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
+                                  const moe_bf16_t* W_r, const moe_bf16_t* W_gate,
+                                  const moe_bf16_t* W_up, const moe_bf16_t* W_down,
+                                  const void* ctx_in, const moe_bf16_t* dY, moe_bf16_t* dx,
+                                  void* dW_r, void* dW_gate, void* dW_up, void* dW_down,
+                                  bool accum, void* ws, size_t ws_bytes, moe_stream_t stream) {
   MOE_TRY(validate(cfg));
   if (!all_aligned16({x, W_r, W_gate, W_up, W_down, dY, dx, dW_r, dW_gate, dW_up, dW_down}) ||
       ctx_in == nullptr || ws == nullptr || !aligned(ctx_in, 256) || !aligned(ws, 256))
     return MOE_ERR_INVALID_ARG;
   DevInfo d;
   MOE_TRY(current_device(&d));
-  const Layout L = make_layout(*cfg, d.sms);
+  const int sms = sm_budget(d.sms, *cfg);
+  const Layout L = make_layout(*cfg, sms);
   if (ws_bytes < L.b_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const uint32_t fl = cfg->flags;
@@ -922,8 +987,8 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
   const int* mtile2 = at<int>(ctx, L.c_mtile2);
   const int* order = at<int>(ctx, L.c_order);
   const uint16_t* wrt = at<uint16_t>(ctx, L.c_wrt);
-  const uint16_t* xperm = at<uint16_t>(ctx, L.c_xperm);
-  const uint16_t* h = at<uint16_t>(ctx, L.c_h);
+  const uint16_t* xperm = L.recompute ? at<uint16_t>(ws, L.b_xperm) : at<uint16_t>(ctx, L.c_xperm);
+  const uint16_t* h = L.recompute ? at<uint16_t>(ws, L.b_h) : at<uint16_t>(ctx, L.c_h);
   uint16_t* dyp = at<uint16_t>(ws, L.b_dyp);
   uint16_t* dh = at<uint16_t>(ws, L.b_dh);
   uint16_t* aw = at<uint16_t>(ws, L.b_aw);
@@ -933,6 +998,28 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
   uint16_t* scratch = at<uint16_t>(ws, L.b_scratch);
   float* wrp = at<float>(ws, L.b_wrp);
   (void)W_r;
+  const uint32_t wflags = accum ? kGemmAccumF32 : 0u;   // weight-gradient epilogues
+
+  if (L.recompute) {
+    // activation checkpointing: dispatch x again and recompute h (and a, which
+    // lands in aw and is overwritten by the down dgrad) in the forward's precision
+    uint16_t* xp = at<uint16_t>(ws, L.b_xperm);
+    uint16_t* hh = at<uint16_t>(ws, L.b_h);
+    MOE_TRY(run("recompute_gather_x", s, fl,
+                [&] { return launch_gather_rows(x, slot_pad, xp, L.T, L.H, L.k, s); }));
+    MOE_TRY(run("recompute_zero_pad_rows_x", s, fl,
+                [&] { return launch_zero_pad_rows(xp, poff, counts, L.E, L.H, s); }));
+    if (cfg->precision == MOE_MXFP8) {
+      const MxGateUpBufs q{at<uint8_t>(ws, L.bq_rx), at<uint8_t>(ws, L.bs_rx),
+                           at<uint8_t>(ws, L.bq_ra), at<uint8_t>(ws, L.bs_ra),
+                           at<uint8_t>(ws, L.bq_rwgu), at<uint8_t>(ws, L.bs_rwgu)};
+      MOE_TRY(gate_up_fwd_mx(L, sms, s, fl, st, xp, W_gate, W_up, poff, counts, mtile, hh, q,
+                             true));
+    } else {
+      MOE_TRY(gate_up_fwd_bf16(L, sms, s, fl, st, xp, W_gate, W_up, poff, counts, mtile, mtile2,
+                               at<uint16_t>(ws, L.b_aw), hh, true));
+    }
+  }
 
   // B1: dispatch dY to the padded expert-major rows (segment tails zeroed:
   // they are K rows of the down weight gradient)
@@ -944,8 +1031,8 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
   if (cfg->precision != MOE_BF16) {
     const BwdBufs bb{W_gate, W_up, W_down, dyp, xperm, h, poff, counts, mtile, order, slot_pad,
                      row_slot, w_row, w, idx, wrt, dh, aw, dwp, dl, dlt, scratch, dx,
-                     dW_gate, dW_up, dW_down, ws};
-    MOE_TRY(backward_expert_gemms_mx(L, d.sms, s, fl, st, bb));
+                     dW_gate, dW_up, dW_down, ws, wflags};
+    MOE_TRY(backward_expert_gemms_mx(L, sms, s, fl, st, bb));
   } else {
     // B2-B4: down dgrad with the SwiGLU backward and router-weight partials
     {
@@ -971,15 +1058,15 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
       a.out2 = dwp;
       a.ld0 = L.F;
       if (fl & MOE_FLAG_TEST_TIMEOUT) {
-        a.flags = 2u;
+        a.flags = kGemmInjectWait;
         a.wait_limit_ns = kTestWaitNs;
       }
       if (L.pair_down_dgrad) {
-        const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, d.sms);
+        const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, sms);
         MOE_TRY(run("down_dgrad_swiglu_bwd", s, fl,
                     [&] { return launch_down_dgrad_pair(a, grid, s); }));
       } else {
-        const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
+        const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, sms);
         MOE_TRY(run("down_dgrad_swiglu_bwd", s, fl,
                     [&] { return launch_down_dgrad(L.dgrad_bn, a, grid, s); }));
       }
@@ -992,6 +1079,7 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
     // B5: down wgrad over the padded token segments
     {
       GemmArgs a = base_args(st, fl);
+      a.flags = wflags;
       if (!make_map(&a.mapA, aw, L.F, L.Pa, 2ull * L.F, 64, 64) ||
           !make_map(&a.mapB0, dyp, L.H, L.Pa, 2ull * L.H, 64, 64))
         return MOE_ERR_CUDA;
@@ -1008,10 +1096,10 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
       a.ld0 = L.H;
       const int64_t tiles = static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles;
       if (L.pair_down_wgrad) {
-        const int grid = grid_for_pairs(tiles, d.sms);
+        const int grid = grid_for_pairs(tiles, sms);
         MOE_TRY(run("down_wgrad", s, fl, [&] { return launch_down_wgrad_pair(a, grid, s); }));
       } else {
-        const int grid = grid_for(tiles, d.sms);
+        const int grid = grid_for(tiles, sms);
         MOE_TRY(run("down_wgrad", s, fl, [&] { return launch_down_wgrad(a, grid, s); }));
       }
     }
@@ -1037,10 +1125,10 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
       a.out0 = scratch;
       a.ld0 = L.H;
       if (L.pair_gu_dgrad) {
-        const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, d.sms);
+        const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, sms);
         MOE_TRY(run("gate_up_dgrad_scatter", s, fl, [&] { return launch_gate_up_dgrad_pair(a, grid, s); }));
       } else {
-        const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, d.sms);
+        const int grid = grid_for(grouped_m_tile_bound(L) * a.n_tiles, sms);
         MOE_TRY(run("gate_up_dgrad_scatter", s, fl, [&] { return launch_gate_up_dgrad(a, grid, s); }));
       }
     }
@@ -1050,6 +1138,7 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
     // B8: gate/up wgrad over the padded token segments
     {
       GemmArgs a = base_args(st, fl);
+      a.flags = wflags;
       if (!make_map(&a.mapA, xperm, L.H, L.Pa, 2ull * L.H, 64, 64) ||
           !make_map(&a.mapB0, dh, 2ull * L.F, L.Pa, 4ull * L.F, 64, 64))
         return MOE_ERR_CUDA;
@@ -1067,10 +1156,10 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
       a.ld0 = L.F;
       const int64_t tiles = static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles;
       if (L.pair_gu_wgrad) {
-        const int grid = grid_for_pairs(tiles, d.sms);
+        const int grid = grid_for_pairs(tiles, sms);
         MOE_TRY(run("gate_up_wgrad", s, fl, [&] { return launch_gate_up_wgrad_pair(a, grid, s); }));
       } else {
-        const int grid = grid_for(tiles, d.sms);
+        const int grid = grid_for(tiles, sms);
         MOE_TRY(run("gate_up_wgrad", s, fl, [&] { return launch_gate_up_wgrad(a, grid, s); }));
       }
     }
@@ -1092,12 +1181,33 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
     a.out0 = wrp;
     a.ld0 = L.H;
     const int grid =
-        grid_for(static_cast<int64_t>(L.wr_split) * L.wr_mtiles * L.wr_ntiles, d.sms);
+        grid_for(static_cast<int64_t>(L.wr_split) * L.wr_mtiles * L.wr_ntiles, sms);
     MOE_TRY(run("router_wgrad", s, fl, [&] { return launch_router_wgrad(a, grid, s); }));
   }
   MOE_TRY(run("router_wgrad_reduce", s, fl,
-              [&] { return launch_wr_reduce(wrp, L.wr_split, L.E, L.H, dW_r, s); }));
+              [&] { return launch_wr_reduce(wrp, L.wr_split, L.E, L.H, dW_r, accum, s); }));
   return MOE_OK;
+}
+
+moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const moe_bf16_t* W_r,
+                          const moe_bf16_t* W_gate, const moe_bf16_t* W_up,
+                          const moe_bf16_t* W_down, const void* ctx, const moe_bf16_t* dY,
+                          moe_bf16_t* dx, moe_bf16_t* dW_r, moe_bf16_t* dW_gate,
+                          moe_bf16_t* dW_up, moe_bf16_t* dW_down, void* ws, size_t ws_bytes,
+                          moe_stream_t stream) {
+  return backward_impl(cfg, x, W_r, W_gate, W_up, W_down, ctx, dY, dx, dW_r, dW_gate, dW_up,
+                       dW_down, false, ws, ws_bytes, stream);
+}
+
+moe_status_t moe_backward_accumulate(const moe_config_t* cfg, const moe_bf16_t* x,
+                                     const moe_bf16_t* W_r, const moe_bf16_t* W_gate,
+                                     const moe_bf16_t* W_up, const moe_bf16_t* W_down,
+                                     const void* ctx, const moe_bf16_t* dY, moe_bf16_t* dx,
+                                     float* gW_r, float* gW_gate, float* gW_up,
+                                     float* gW_down, void* ws, size_t ws_bytes,
+                                     moe_stream_t stream) {
+  return backward_impl(cfg, x, W_r, W_gate, W_up, W_down, ctx, dY, dx, gW_r, gW_gate, gW_up,
+                       gW_down, true, ws, ws_bytes, stream);
 }
 
 moe_status_t moe_gemm_bf16(int64_t M, int64_t N, int64_t K, const moe_bf16_t* A, int a_kmajor,
@@ -1305,7 +1415,8 @@ extern "C" moe_status_t moe_route_noalloc(const moe_config_t* cfg, const moe_bf1
     return MOE_ERR_INVALID_ARG;
   DevInfo d;
   MOE_TRY(current_device(&d));
-  const Layout L = make_layout(*cfg, d.sms);
+  const int sms = sm_budget(d.sms, *cfg);
+  const Layout L = make_layout(*cfg, sms);
   const RouteScratch R = route_scratch_layout(L);
   if (R.total > static_cast<size_t>(MOE_NOALLOC_SCRATCH_BYTES)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   void* base = nullptr;
@@ -1320,7 +1431,7 @@ extern "C" moe_status_t moe_route_noalloc(const moe_config_t* cfg, const moe_bf1
               at<int>(base, R.mtile), at<int>(base, R.order), at<uint16_t>(base, R.wrt),
               at<int>(base, R.hist), at<int>(base, R.base), st, at<int>(base, R.poff),
               at<int>(base, R.mtile2), at<int>(base, R.slot_pad)};
-  MOE_TRY(run_routing(*cfg, L, b, d.sms, s));
+  MOE_TRY(run_routing(*cfg, L, b, sms, s));
   if (device_status != nullptr &&
       cudaMemcpyAsync(device_status, &st->code, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) !=
           cudaSuccess)

@@ -277,6 +277,38 @@ MOE_DEV void load_bf16x16(const void* p, float (&v)[16]) {
 
 MOE_DEV float sigmoidf_fast(float z) { return 1.0f / (1.0f + __expf(-z)); }
 
+// p[i] += v[i] for 16 fp32 values at p (16-byte aligned); loads issued first
+MOE_DEV void accum_f32x16(void* p, const float (&v)[16]) {
+  char* q = static_cast<char*>(p);
+  uint4 o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[i] = ld_global_v4(q + 16 * i);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    st_global_v4(q + 16 * i, __float_as_uint(__uint_as_float(o[i].x) + v[4 * i]),
+                 __float_as_uint(__uint_as_float(o[i].y) + v[4 * i + 1]),
+                 __float_as_uint(__uint_as_float(o[i].z) + v[4 * i + 2]),
+                 __float_as_uint(__uint_as_float(o[i].w) + v[4 * i + 3]));
+}
+
+// A 16-column chunk of a weight gradient at element idx of base: stored as
+// bf16, or (accumulate mode) added into an fp32 buffer.
+MOE_DEV void wgrad_store16(void* base, int64_t idx, bool accum, const float (&v)[16]) {
+  if (accum)
+    accum_f32x16(static_cast<float*>(base) + idx, v);
+  else
+    store_bf16x16(static_cast<__nv_bfloat16*>(base) + idx, v);
+}
+
+// The same chunk of an expert that received no token: bf16 zeros, or nothing
+// to add in accumulate mode.
+MOE_DEV void wgrad_zero16(void* base, int64_t idx, bool accum) {
+  if (accum) return;
+  __nv_bfloat16* p = static_cast<__nv_bfloat16*>(base) + idx;
+  st_global_v4(p, 0u, 0u, 0u, 0u);
+  st_global_v4(p + 8, 0u, 0u, 0u, 0u);
+}
+
 }  // namespace moe
 
 // ---------------------------------------------------------------- MXFP8

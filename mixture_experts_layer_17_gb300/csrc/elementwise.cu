@@ -262,8 +262,11 @@ __global__ void unpermute_kernel(const uint16_t* __restrict__ scratch, const flo
 // ---------------------------------------------------------------- B10: dW_r
 
 // dW_r[h, e] = sum over splits of part[s, e, h] (fp32), written as bf16 [H, E].
+// dW_r[h, e] = sum over splits of part[split, e, h]: bf16 output, or (kAccum)
+// added into an fp32 [H, E] buffer
+template <bool kAccum>
 __global__ void wr_reduce_kernel(const float* __restrict__ part, int S, int E, int H,
-                                 uint16_t* __restrict__ dWr) {
+                                 void* __restrict__ out) {
   __shared__ float tile[32][33];
   const int h0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
@@ -277,8 +280,13 @@ __global__ void wr_reduce_kernel(const float* __restrict__ part, int S, int E, i
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
     const int h = h0 + i, e = e0 + threadIdx.x;
     if (h < H && e < E) {
-      __nv_bfloat16 b = __float2bfloat16_rn(tile[threadIdx.x][i]);
-      dWr[static_cast<int64_t>(h) * E + e] = *reinterpret_cast<uint16_t*>(&b);
+      const int64_t o = static_cast<int64_t>(h) * E + e;
+      if (kAccum) {
+        static_cast<float*>(out)[o] += tile[threadIdx.x][i];
+      } else {
+        __nv_bfloat16 b = __float2bfloat16_rn(tile[threadIdx.x][i]);
+        static_cast<uint16_t*>(out)[o] = *reinterpret_cast<uint16_t*>(&b);
+      }
     }
   }
 }
@@ -346,10 +354,13 @@ cudaError_t launch_unpermute(const uint16_t* scratch, const float* dl, const int
   return cudaGetLastError();
 }
 
-cudaError_t launch_wr_reduce(const float* part, int S, int E, int H, uint16_t* dWr,
+cudaError_t launch_wr_reduce(const float* part, int S, int E, int H, void* dWr, bool accum_f32,
                              cudaStream_t s) {
   dim3 grid(blocks_for(H, 32), blocks_for(E, 32));
-  wr_reduce_kernel<<<grid, dim3(32, 8), 0, s>>>(part, S, E, H, dWr);
+  if (accum_f32)
+    wr_reduce_kernel<true><<<grid, dim3(32, 8), 0, s>>>(part, S, E, H, dWr);
+  else
+    wr_reduce_kernel<false><<<grid, dim3(32, 8), 0, s>>>(part, S, E, H, dWr);
   return cudaGetLastError();
 }
 

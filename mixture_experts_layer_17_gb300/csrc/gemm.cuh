@@ -69,8 +69,11 @@ struct GemmArgs {
   int kt_b;             // MXFP8: K-tiles (of 128) per atom row of B
   DeviceStatus* status;
   uint64_t wait_limit_ns;
-  uint32_t flags;      // bit 1: inject a wait that nothing signals (timeout test)
+  uint32_t flags;      // kGemmInjectWait, kGemmAccumF32
 };
+
+constexpr uint32_t kGemmInjectWait = 2u;   // wait on a barrier nothing signals (timeout test)
+constexpr uint32_t kGemmAccumF32 = 4u;     // weight gradients: out += acc in fp32
 
 struct TileInfo {
   int e;        // expert (group), -1 for dense problems
@@ -508,7 +511,7 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
       }
       if (!ok) break;
       if (lane == 0) {
-        const bool inject = (args.flags & 2u) != 0 && t == t_first;
+        const bool inject = (args.flags & kGemmInjectWait) != 0 && t == t_first;
         if (!inject) {
           if constexpr (kPair)
             mma_commit_pair(tfull_bar + acc, 0x3);
@@ -552,7 +555,7 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
         P::epilogue_empty(args, ti, r, group, extra);
         continue;
       }
-      if (first && (args.flags & 2u) != 0) {
+      if (first && (args.flags & kGemmInjectWait) != 0) {
         // test hook: a wait on a barrier that nothing signals
         if (!mbar_wait_bounded(never_bar, 0, abort_flag, limit)) {
           record_timeout(args.status, kWaitInjected);

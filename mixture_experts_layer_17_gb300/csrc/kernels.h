@@ -72,7 +72,7 @@ cudaError_t launch_router_bwd(const float* dw_part, int nparts, const int* slot_
 cudaError_t launch_unpermute(const uint16_t* scratch, const float* dl, const int* idx,
                              const uint16_t* WrT, uint16_t* dx, int64_t T, int H, int k,
                              cudaStream_t s);
-cudaError_t launch_wr_reduce(const float* part, int S, int E, int H, uint16_t* dWr,
+cudaError_t launch_wr_reduce(const float* part, int S, int E, int H, void* dWr, bool accum_f32,
                              cudaStream_t s);
 
 // Launches gemm_kernel<P>, raising the dynamic shared-memory limit once per

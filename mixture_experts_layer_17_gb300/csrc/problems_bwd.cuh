@@ -162,21 +162,6 @@ struct GateUpDgradProblem {
   }
 };
 
-// Stores columns [c0, c1) of a fp32 accumulator row as bf16 (weight gradients).
-MOE_DEV void store_tile_bf16(uint32_t taddr, bool valid, __nv_bfloat16* dst, int c0, int c1) {
-#pragma unroll 1
-  for (int c = c0; c < c1; c += 16) {
-    float v[16];
-    tmem_ld16(taddr + c, v);
-    tmem_ld_wait();
-    if (valid) store_bf16x16(dst + c, v);
-  }
-}
-
-MOE_DEV void zero_row_bf16(__nv_bfloat16* dst, int n) {
-  for (int c = 0; c < n; c += 8) st_global_v4(dst + c, 0u, 0u, 0u, 0u);
-}
-
 // ------------------------------------------------------------------------
 // B5: down wgrad dW_down[e] = (w·a)_e^T · dY_perm_e, K = tokens of expert e.
 //   mapA  = aw [P, F] MN-major, box {64, 64}      (M = F)
@@ -201,19 +186,28 @@ struct DownWgradProblem {
 #pragma unroll
     for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * kChunkBytes, &a.mapB0, ti.n0 + 64 * c, krow, bar);
   }
-  MOE_DEV static __nv_bfloat16* out_row(const GemmArgs& a, const TileInfo& ti, int r) {
-    return static_cast<__nv_bfloat16*>(a.out0) +
-           (static_cast<int64_t>(ti.e) * a.M + ti.m0 + r) * a.ld0 + ti.n0;
+  MOE_DEV static int64_t out_idx(const GemmArgs& a, const TileInfo& ti, int r) {
+    return (static_cast<int64_t>(ti.e) * a.M + ti.m0 + r) * a.ld0 + ti.n0;
   }
   MOE_DEV static void epilogue_empty(const GemmArgs& a, const TileInfo& ti, int r, int group,
                                      uint8_t*) {
-    if (r < ti.rows) zero_row_bf16(out_row(a, ti, r) + group * (BN / 2), BN / 2);
+    if (r >= ti.rows) return;
+    const bool acc = (a.flags & kGemmAccumF32) != 0;
+    for (int c = group * (BN / 2); c < (group + 1) * (BN / 2); c += 16)
+      wgrad_zero16(a.out0, out_idx(a, ti, r) + c, acc);
   }
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
                                int group, uint8_t*) {
     const bool valid = r < ti.rows;
-    store_tile_bf16(taddr, valid, valid ? out_row(a, ti, r) : nullptr, group * (BN / 2),
-                    (group + 1) * (BN / 2));
+    const bool acc = (a.flags & kGemmAccumF32) != 0;
+    const int64_t row = valid ? out_idx(a, ti, r) : 0;
+#pragma unroll 1
+    for (int c = group * (BN / 2); c < (group + 1) * (BN / 2); c += 16) {
+      float v[16];
+      tmem_ld16(taddr + c, v);
+      tmem_ld_wait();
+      if (valid) wgrad_store16(a.out0, row + c, acc, v);
+    }
   }
 };
 
@@ -242,31 +236,40 @@ struct GateUpWgradProblem {
 #pragma unroll
     for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * kChunkBytes, &a.mapB0, ti.n0 + 64 * c, krow, bar);
   }
-  // 16-column chunk starting at global column gc of the [gate | up] range
-  MOE_DEV static __nv_bfloat16* out_ptr(const GemmArgs& a, const TileInfo& ti, int r, int gc) {
+  // (buffer, element index) of the 16-column chunk at global column gc of the
+  // [gate | up] range (F is a multiple of 128, so no chunk straddles the two)
+  MOE_DEV static void out_loc(const GemmArgs& a, const TileInfo& ti, int r, int gc, void*& base,
+                              int64_t& idx) {
     const int F = a.ld0;
-    __nv_bfloat16* base = static_cast<__nv_bfloat16*>(gc < F ? a.out0 : a.out1);
-    const int col = gc < F ? gc : gc - F;
-    return base + (static_cast<int64_t>(ti.e) * a.M + ti.m0 + r) * F + col;
+    base = gc < F ? a.out0 : a.out1;
+    idx = (static_cast<int64_t>(ti.e) * a.M + ti.m0 + r) * F + (gc < F ? gc : gc - F);
   }
   MOE_DEV static void epilogue_empty(const GemmArgs& a, const TileInfo& ti, int r, int group,
                                      uint8_t*) {
     if (r >= ti.rows) return;
+    const bool acc = (a.flags & kGemmAccumF32) != 0;
     for (int c = group * (BN / 2); c < (group + 1) * (BN / 2); c += 16) {
-      __nv_bfloat16* p = out_ptr(a, ti, r, ti.n0 + c);
-      st_global_v4(p, 0u, 0u, 0u, 0u);
-      st_global_v4(p + 8, 0u, 0u, 0u, 0u);
+      void* base;
+      int64_t idx;
+      out_loc(a, ti, r, ti.n0 + c, base, idx);
+      wgrad_zero16(base, idx, acc);
     }
   }
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
                                int group, uint8_t*) {
     const bool valid = r < ti.rows;
+    const bool acc = (a.flags & kGemmAccumF32) != 0;
 #pragma unroll 1
     for (int c = group * (BN / 2); c < (group + 1) * (BN / 2); c += 16) {
       float v[16];
       tmem_ld16(taddr + c, v);
       tmem_ld_wait();
-      if (valid) store_bf16x16(out_ptr(a, ti, r, ti.n0 + c), v);
+      if (valid) {
+        void* base;
+        int64_t idx;
+        out_loc(a, ti, r, ti.n0 + c, base, idx);
+        wgrad_store16(base, idx, acc, v);
+      }
     }
   }
 };

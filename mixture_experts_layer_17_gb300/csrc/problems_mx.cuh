@@ -338,34 +338,43 @@ struct WgradMXProblem {
     bulk_load(sSF, sf_atom(a.sfA, static_cast<int64_t>(kt) * a.m_tiles + ti.mt), 512, bar);
     bulk_load(sSF + 512, sf_atom(a.sfB0, static_cast<int64_t>(kt) * a.n_tiles + ti.n0 / BN), 512, bar);
   }
-  MOE_DEV static __nv_bfloat16* out_ptr(const GemmArgs& a, const TileInfo& ti, int r, int gc) {
+  MOE_DEV static void out_loc(const GemmArgs& a, const TileInfo& ti, int r, int gc, void*& base,
+                              int64_t& idx) {
     if (kGateUp) {
       const int F = a.ld0;
-      __nv_bfloat16* base = static_cast<__nv_bfloat16*>(gc < F ? a.out0 : a.out1);
-      const int col = gc < F ? gc : gc - F;
-      return base + (static_cast<int64_t>(ti.e) * a.M + ti.m0 + r) * F + col;
+      base = gc < F ? a.out0 : a.out1;
+      idx = (static_cast<int64_t>(ti.e) * a.M + ti.m0 + r) * F + (gc < F ? gc : gc - F);
+    } else {
+      base = a.out0;
+      idx = (static_cast<int64_t>(ti.e) * a.M + ti.m0 + r) * a.ld0 + gc;
     }
-    return static_cast<__nv_bfloat16*>(a.out0) +
-           (static_cast<int64_t>(ti.e) * a.M + ti.m0 + r) * a.ld0 + gc;
   }
   MOE_DEV static void epilogue_empty(const GemmArgs& a, const TileInfo& ti, int r, int group,
                                      uint8_t*) {
     if (r >= ti.rows) return;
+    const bool acc = (a.flags & kGemmAccumF32) != 0;
     for (int c = group * 64; c < group * 64 + 64; c += 16) {
-      __nv_bfloat16* p = out_ptr(a, ti, r, ti.n0 + c);
-      st_global_v4(p, 0u, 0u, 0u, 0u);
-      st_global_v4(p + 8, 0u, 0u, 0u, 0u);
+      void* base;
+      int64_t idx;
+      out_loc(a, ti, r, ti.n0 + c, base, idx);
+      wgrad_zero16(base, idx, acc);
     }
   }
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
                                int group, uint8_t*) {
     const bool valid = r < ti.rows;
+    const bool acc = (a.flags & kGemmAccumF32) != 0;
 #pragma unroll 1
     for (int c = group * 64; c < group * 64 + 64; c += 16) {
       float v[16];
       tmem_ld16(taddr + c, v);
       tmem_ld_wait();
-      if (valid) store_bf16x16(out_ptr(a, ti, r, ti.n0 + c), v);
+      if (valid) {
+        void* base;
+        int64_t idx;
+        out_loc(a, ti, r, ti.n0 + c, base, idx);
+        wgrad_store16(base, idx, acc, v);
+      }
     }
   }
 };

@@ -22,6 +22,7 @@ MOE_FLAG_SYNC_CHECK = 0x1
 MOE_FLAG_TEST_TIMEOUT = 0x2
 MOE_FLAG_CTA_PAIRS_OFF = 0x4
 MOE_FLAG_CTA_PAIRS_ON = 0x8
+MOE_FLAG_RECOMPUTE = 0x10
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
           3: "MOE_ERR_WORKSPACE_TOO_SMALL", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT",
@@ -30,13 +31,14 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
 # every symbol include/moe.h declares
 EXPORTED = ("moe_workspace_size", "moe_route", "moe_forward", "moe_backward", "moe_gemm_bf16",
             "moe_get_device_status", "moe_status_string", "moe_profile_enable",
-            "moe_profile_read", "moe_launch_count", "moe_route_noalloc", "moe_gemm_mxfp8")
+            "moe_profile_read", "moe_launch_count", "moe_route_noalloc", "moe_gemm_mxfp8",
+            "moe_backward_accumulate")
 
 
 class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int32), ("F", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("top_k", ctypes.c_int32), ("precision", ctypes.c_int32),
-                ("flags", ctypes.c_uint32)]
+                ("flags", ctypes.c_uint32), ("max_sms", ctypes.c_int32)]
 
 
 class MoeError(RuntimeError):
@@ -64,6 +66,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_route": [cfgp] + [_vp] * 10 + [_sz, _vp],
         "moe_forward": [cfgp] + [_vp] * 9 + [_sz, _vp],
         "moe_backward": [cfgp] + [_vp] * 13 + [_sz, _vp],
+        "moe_backward_accumulate": [cfgp] + [_vp] * 13 + [_sz, _vp],
         "moe_gemm_bf16": [_i64, _i64, _i64, _vp, _i32, _vp, _i32, _vp, _vp, _sz, _vp],
         "moe_get_device_status": [_vp, _vp],
         "moe_status_string": [_i32],
@@ -108,9 +111,9 @@ def _check(code: int, where: str) -> None:
 
 
 def make_config(T: int, H: int, F: int, E: int, top_k: int, precision="bf16",
-                flags: int = 0) -> MoeConfig:
+                flags: int = 0, max_sms: int = 0) -> MoeConfig:
     prec = PRECISIONS[precision] if isinstance(precision, str) else int(precision)
-    return MoeConfig(T, H, F, E, top_k, prec, flags)
+    return MoeConfig(T, H, F, E, top_k, prec, flags, max_sms)
 
 
 def moe_workspace_size(cfg: MoeConfig) -> Tuple[int, int, int]:
@@ -160,6 +163,16 @@ def moe_backward(cfg: MoeConfig, x, W_r, W_gate, W_up, W_down, ctx, dY, dx, dW_r
                                _ptr(dx, bf), _ptr(dW_r, bf), _ptr(dW_gate, bf), _ptr(dW_up, bf),
                                _ptr(dW_down, bf), _ptr(ws), ws.numel() * ws.element_size(),
                                _stream(stream)), "moe_backward")
+
+
+def moe_backward_accumulate(cfg: MoeConfig, x, W_r, W_gate, W_up, W_down, ctx, dY, dx, gW_r,
+                            gW_gate, gW_up, gW_down, ws, stream=None) -> None:
+    bf, f32 = torch.bfloat16, torch.float32
+    _check(load().moe_backward_accumulate(
+        ctypes.byref(cfg), _ptr(x, bf), _ptr(W_r, bf), _ptr(W_gate, bf), _ptr(W_up, bf),
+        _ptr(W_down, bf), _ptr(ctx), _ptr(dY, bf), _ptr(dx, bf), _ptr(gW_r, f32),
+        _ptr(gW_gate, f32), _ptr(gW_up, f32), _ptr(gW_down, f32), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)), "moe_backward_accumulate")
 
 
 def moe_gemm_bf16(A, a_kmajor: bool, B, b_kmajor: bool, D, ws, stream=None) -> None:

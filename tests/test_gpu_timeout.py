@@ -1,7 +1,10 @@
 """Failure detection without a GPU fault: with MOE_FLAG_TEST_TIMEOUT the first
 grouped GEMM of a call waits on a barrier that nothing signals, with a 20 ms
 limit.  The kernel must give up, record MOE_ERR_TIMEOUT in the workspace
-status word, free its tensor memory and return, leaving the context usable."""
+status word, free its tensor memory and return, leaving the context usable.
+Run on the single-CTA bf16 kernels, on CTA pairs (where each CTA of a pair
+gives up on its own and both still meet at the closing cluster barrier) and on
+the MXFP8 kernels."""
 
 import numpy as np
 import pytest
@@ -14,12 +17,16 @@ from oracle import moe_oracle as mo
 pytestmark = pytest.mark.gpu
 
 
-def test_bounded_wait_times_out_and_context_survives():
+@pytest.mark.parametrize("precision,extra", [("bf16", 0), ("bf16", "pairs"), ("mxfp8", 0)])
+def test_bounded_wait_times_out_and_context_survives(precision, extra):
     from mixture_experts_layer_17_gb300 import MoeLayer, libmoe
     sh = si.custom_shape(384, 256, 256, 8, 2, seed=31)
     inp = si.make_inputs(sh, "cuda")
     args = (inp["x"], inp["W_r"], inp["W_gate"], inp["W_up"], inp["W_down"])
-    bad = MoeLayer(sh.T, sh.H, sh.F, sh.E, sh.top_k, flags=libmoe.MOE_FLAG_TEST_TIMEOUT)
+    flags = libmoe.MOE_FLAG_TEST_TIMEOUT
+    if extra == "pairs":
+        flags |= libmoe.MOE_FLAG_CTA_PAIRS_ON
+    bad = MoeLayer(sh.T, sh.H, sh.F, sh.E, sh.top_k, precision, flags=flags)
     bad.forward(*args)
     torch.cuda.synchronize()
     assert bad.device_status("fwd") == 5          # MOE_ERR_TIMEOUT
