@@ -319,16 +319,28 @@ def run_ours(args, sh, world, rank, local):
     import dataclasses
     shr = dataclasses.replace(shr, seed=shr.seed + 1000 * rank) if rank else shr
     inp = si.make_inputs(shr, dev)
-    layer = MoeLayer(sh.T, sh.H, sh.F, sh.E, sh.top_k, sh.precision, flags=args.flags, device=dev)
+    layer = MoeLayer(sh.T, sh.H, sh.F, sh.E, sh.top_k, sh.precision, flags=args.flags, device=dev,
+                     max_sms=args.max_sms)
     grads = {"dx": torch.empty_like(inp["x"]), "dW_r": torch.empty_like(inp["W_r"]),
              "dW_gate": torch.empty_like(inp["W_gate"]), "dW_up": torch.empty_like(inp["W_up"]),
              "dW_down": torch.empty_like(inp["W_down"])}
     y = torch.empty_like(inp["x"])
     W = (inp["W_r"], inp["W_gate"], inp["W_up"], inp["W_down"])
+    acc = None
+    if args.accumulate:
+        # fp32 gradient accumulation buffers (micro-batch training)
+        acc = {k: torch.zeros(inp[k[1:]].shape, dtype=torch.float32, device=dev)
+               for k in ("dW_r", "dW_gate", "dW_up", "dW_down")}
+
+    def backward(x, dY):
+        if acc is None:
+            layer.backward(x, W[0], W[1], W[2], W[3], dY, grads=grads)
+        else:
+            layer.backward_accumulate(x, W[0], W[1], W[2], W[3], dY, acc, dx=grads["dx"])
 
     def step(x, dY):
         layer.forward(x, W[0], W[1], W[2], W[3], inp["logit_bias"], y=y)
-        layer.backward(x, W[0], W[1], W[2], W[3], dY, grads=grads)
+        backward(x, dY)
 
     for _ in range(args.warmup):
         step(inp["x"], inp["dY"])
@@ -354,7 +366,7 @@ def run_ours(args, sh, world, rank, local):
         ev[i][0].record(stream)
         layer.forward(inp["x"], W[0], W[1], W[2], W[3], inp["logit_bias"], y=y)
         ev[i][1].record(stream)
-        layer.backward(inp["x"], W[0], W[1], W[2], W[3], inp["dY"], grads=grads)
+        backward(inp["x"], inp["dY"])
         ev[i][2].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -386,7 +398,7 @@ def run_ours(args, sh, world, rank, local):
         x_dev.copy_(hx, non_blocking=True)
         dY_dev.copy_(hdY, non_blocking=True)
         layer.forward(x_dev, W[0], W[1], W[2], W[3], inp["logit_bias"], y=y)
-        layer.backward(x_dev, W[0], W[1], W[2], W[3], dY_dev, grads=grads)
+        backward(x_dev, dY_dev)
         hy.copy_(y, non_blocking=True)
         hdx.copy_(grads["dx"], non_blocking=True)
     e1.record(stream)
@@ -444,6 +456,8 @@ def run_ours(args, sh, world, rank, local):
         "config": {"workload": sh.name, "T": sh.T, "H": sh.H, "F": sh.F, "E": sh.E,
                    "top_k": sh.top_k, "precision": sh.precision,
                    "parallelism": "replicas" if world > 1 else "single",
+                   "flags": args.flags, "max_sms": args.max_sms,
+                   "grad_accumulate_fp32": bool(args.accumulate),
                    "l2": "inputs larger than L2 (no flush): weights and activations exceed 129 MB"},
         "tflops": world * (fwd_fl + bwd_fl) / (ms_per_step * 1e-3) / 1e12,
         "fwd_ms": fwd_ms,
@@ -507,6 +521,11 @@ def main():
                     help="moe_config_t flags (e.g. 0x4: single-CTA tiles only; 0x8: CTA pairs)")
     ap.add_argument("--shape", default=None,
                     help="T,H,F,E,top_k: a custom shape (profiling aid) instead of --workload")
+    ap.add_argument("--precision", default="bf16", choices=["bf16", "mxfp8", "fp8_bwd"],
+                    help="precision of a --shape layer")
+    ap.add_argument("--accumulate", action="store_true",
+                    help="backward adds the weight gradients into fp32 buffers")
+    ap.add_argument("--max-sms", type=int, default=0, help="SM budget (0: every SM)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
     ap.add_argument("--record-traffic", default=None, metavar="NCU_CSV",
@@ -520,7 +539,8 @@ def main():
     args.warmup = max(args.warmup, 3)
     if args.shape:
         T, H, F, E, k = (int(v) for v in args.shape.split(","))
-        sh = si.custom_shape(T, H, F, E, k, seed=5, name=f"custom_{T}x{H}x{F}x{E}x{k}")
+        sh = si.custom_shape(T, H, F, E, k, seed=5, precision=args.precision,
+                             name=f"custom_{T}x{H}x{F}x{E}x{k}_{args.precision}")
     else:
         sh = si.shape(args.workload)
     world, rank, local = dist_setup(args)

@@ -91,25 +91,26 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, int64_t R, i
 // --------------------------------------------------------------------------
 enum ColMode { kColsWeights = 0, kColsGateUp = 1, kColsTokens = 2 };
 
+constexpr int kColThreads = 256;
+
 template <int MODE>
-__global__ void __launch_bounds__(64) quant_cols_kernel(const uint16_t* __restrict__ src0,
-                                  const uint16_t* __restrict__ src1, int R, int C_in,
-                                  uint8_t* __restrict__ dst, uint8_t* __restrict__ sf,
-                                  const int* __restrict__ offsets,
-                                  const int* __restrict__ counts,
-                                  const int* __restrict__ mtile_off, int E) {
-  // 64 threads: thread = (32-row block rb in 0..3, group of 8 columns cg in 0..15);
-  // each reads 32 rows x 16 bytes, keeps 8 running maxima, writes 32 x 8 bytes.
+__global__ void __launch_bounds__(kColThreads) quant_cols_kernel(
+    const uint16_t* __restrict__ src0, const uint16_t* __restrict__ src1, int R, int C_in,
+    uint8_t* __restrict__ dst, uint8_t* __restrict__ sf, const int* __restrict__ offsets,
+    const int* __restrict__ counts, const int* __restrict__ mtile_off, int E) {
+  // One pass: the 128-row x 128-column bf16 tile is read once into shared
+  // memory (coalesced 16-byte loads), each thread turns two (column, 32-row
+  // block) units into a scale and 32 E4M3 bytes, and the E4M3 tile leaves
+  // through shared memory as coalesced 16-byte row stores.
+  __shared__ __align__(16) uint16_t tile[128][128];
+  __shared__ __align__(16) uint8_t qtile[128][128];
   const int kg = blockIdx.x;           // K-tile (global)
   const int ct = blockIdx.y;           // 128-column tile of the output
-  const int cg = threadIdx.x & 15;
-  const int rb = threadIdx.x >> 4;
+  const int tid = threadIdx.x;
   const int C_out = (MODE == kColsGateUp) ? 2 * C_in : C_in;
   int64_t src_row0, dst_row0;
   int valid;                           // valid rows of this K-tile
   int64_t atom;
-  const uint16_t* src = src0;
-  int src_col;
   if (MODE == kColsTokens) {
     if (kg >= __ldg(mtile_off + E)) return;   // the grid is sized for the worst case
     int lo = 0, hi = E - 1;            // largest e with mtile_off[e] <= kg
@@ -122,7 +123,6 @@ __global__ void __launch_bounds__(64) quant_cols_kernel(const uint16_t* __restri
     valid = min(128, __ldg(counts + lo) - 128 * g);
     dst_row0 = 128ll * kg;
     atom = static_cast<int64_t>(kg) * (C_out >> 7) + ct;
-    src_col = ct * 128 + cg * 8;
   } else {
     const int kt_per = R >> 7;
     const int e = kg / kt_per;
@@ -131,53 +131,59 @@ __global__ void __launch_bounds__(64) quant_cols_kernel(const uint16_t* __restri
     dst_row0 = src_row0;
     valid = 128;
     atom = (static_cast<int64_t>(e) * (C_out >> 7) + ct) * kt_per + kt;
-    if (MODE == kColsGateUp) {
-      src = (cg < 8) ? src0 : src1;    // output columns 0..63 gate, 64..127 up
-      src_col = ct * 64 + (cg & 7) * 8;
-    } else {
-      src_col = ct * 128 + cg * 8;
-    }
   }
-  const int out_col = ct * 128 + cg * 8;
-  // pass 1: column maxima of the 32-row block; pass 2 re-reads the same
-  // 512 bytes per thread (cache-resident) and converts
-  float amax[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  const uint16_t* base = src + src_row0 * C_in + src_col;
-#pragma unroll 8
-  for (int i = 0; i < 32; ++i) {
-    const int rr = rb * 32 + i;
-    if (rr < valid) {
-      const uint4 u = ld_global_v4(base + static_cast<int64_t>(rr) * C_in);
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  // load: 16 threads per row, 16 bytes (8 columns) each; rows >= valid are zero
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float lo, hi;
-        unpack_bf16x2(w[q], lo, hi);
-        amax[2 * q] = fmaxf(amax[2 * q], fabsf(lo));
-        amax[2 * q + 1] = fmaxf(amax[2 * q + 1], fabsf(hi));
-      }
-    }
-  }
-  float inv[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int X = mx_exponent(amax[j]);
-    inv[j] = ldexpf(1.0f, -X);
-    sf[atom * 512 + sf_atom_offset(cg * 8 + j, rb)] = static_cast<uint8_t>(X + 127);
-  }
-#pragma unroll 8
-  for (int i = 0; i < 32; ++i) {
-    const int rr = rb * 32 + i;
+  for (int i = 0; i < 8; ++i) {
+    const int chunk = tid + kColThreads * i;   // 0 .. 2047
+    const int row = chunk >> 4;
+    const int c8 = (chunk & 15) * 8;           // output column of the chunk
     uint4 u = make_uint4(0, 0, 0, 0);
-    if (rr < valid) u = ld_global_v4(base + static_cast<int64_t>(rr) * C_in);
-    float v[8];
-    unpack_bf16x2(u.x, v[0], v[1]);
-    unpack_bf16x2(u.y, v[2], v[3]);
-    unpack_bf16x2(u.z, v[4], v[5]);
-    unpack_bf16x2(u.w, v[6], v[7]);
-    const uint32_t lo = to_e4m3x4(v[0] * inv[0], v[1] * inv[1], v[2] * inv[2], v[3] * inv[3], 1.0f);
-    const uint32_t hi = to_e4m3x4(v[4] * inv[4], v[5] * inv[5], v[6] * inv[6], v[7] * inv[7], 1.0f);
-    *reinterpret_cast<uint2*>(dst + (dst_row0 + rb * 32 + i) * C_out + out_col) = make_uint2(lo, hi);
+    if (row < valid) {
+      const uint16_t* src = src0;
+      int col = ct * 128 + c8;
+      if (MODE == kColsGateUp) {               // output columns 0..63 gate, 64..127 up
+        src = c8 < 64 ? src0 : src1;
+        col = ct * 64 + (c8 & 63);
+      }
+      u = ld_global_nc_v4(src + (src_row0 + row) * C_in + col);
+    }
+    *reinterpret_cast<uint4*>(&tile[row][c8]) = u;
+  }
+  __syncthreads();
+  // convert: unit = (column c, 32-row block kb)
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int c = tid & 127;
+    const int kb = (tid >> 7) + 2 * i;
+    float v[32];
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      v[j] = __uint_as_float(static_cast<uint32_t>(tile[kb * 32 + j][c]) << 16);
+      amax = fmaxf(amax, fabsf(v[j]));
+    }
+    const int X = mx_exponent(amax);
+    const float inv = ldexpf(1.0f, -X);
+    sf[atom * 512 + sf_atom_offset(c, kb)] = static_cast<uint8_t>(X + 127);
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      const uint32_t q = to_e4m3x4(v[j], v[j + 1], v[j + 2], v[j + 3], inv);
+      qtile[kb * 32 + j][c] = static_cast<uint8_t>(q);
+      qtile[kb * 32 + j + 1][c] = static_cast<uint8_t>(q >> 8);
+      qtile[kb * 32 + j + 2][c] = static_cast<uint8_t>(q >> 16);
+      qtile[kb * 32 + j + 3][c] = static_cast<uint8_t>(q >> 24);
+    }
+  }
+  __syncthreads();
+  // store: 8 threads per 128-byte output row
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int chunk = tid + kColThreads * i;   // 0 .. 1023
+    const int row = chunk >> 3;
+    const int c16 = (chunk & 7) * 16;
+    const uint4 q = *reinterpret_cast<const uint4*>(&qtile[row][c16]);
+    st_global_v4(dst + (dst_row0 + row) * C_out + ct * 128 + c16, q.x, q.y, q.z, q.w);
   }
 }
 
@@ -201,7 +207,7 @@ cudaError_t launch_quant_rows_permuted(const uint16_t* src, int64_t P, int C, ui
 cudaError_t launch_quant_cols_weights(const uint16_t* src, int E, int R, int C, uint8_t* dst,
                                       uint8_t* sf, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(E * (R / 128)), static_cast<unsigned>(C / 128));
-  quant_cols_kernel<kColsWeights><<<grid, 64, 0, s>>>(src, nullptr, R, C, dst, sf, nullptr,
+  quant_cols_kernel<kColsWeights><<<grid, kColThreads, 0, s>>>(src, nullptr, R, C, dst, sf, nullptr,
                                                       nullptr, nullptr, E);
   return cudaGetLastError();
 }
@@ -209,7 +215,7 @@ cudaError_t launch_quant_cols_weights(const uint16_t* src, int E, int R, int C, 
 cudaError_t launch_quant_cols_gate_up(const uint16_t* W_gate, const uint16_t* W_up, int E, int H,
                                       int F, uint8_t* dst, uint8_t* sf, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(E * (H / 128)), static_cast<unsigned>(2 * F / 128));
-  quant_cols_kernel<kColsGateUp><<<grid, 64, 0, s>>>(W_gate, W_up, H, F, dst, sf, nullptr,
+  quant_cols_kernel<kColsGateUp><<<grid, kColThreads, 0, s>>>(W_gate, W_up, H, F, dst, sf, nullptr,
                                                      nullptr, nullptr, E);
   return cudaGetLastError();
 }
@@ -218,7 +224,7 @@ cudaError_t launch_quant_cols_tokens(const uint16_t* src, int64_t max_ktiles, in
                                      uint8_t* sf, const int* poff, const int* counts,
                                      const int* mtile_off, int E, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(max_ktiles), static_cast<unsigned>(C / 128));
-  quant_cols_kernel<kColsTokens><<<grid, 64, 0, s>>>(src, nullptr, 0, C, dst, sf, poff, counts,
+  quant_cols_kernel<kColsTokens><<<grid, kColThreads, 0, s>>>(src, nullptr, 0, C, dst, sf, poff, counts,
                                                      mtile_off, E);
   return cudaGetLastError();
 }
