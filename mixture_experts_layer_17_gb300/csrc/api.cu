@@ -546,7 +546,7 @@ moe_status_t gate_up_fwd_mx(const Layout& L, int sms, cudaStream_t s, uint32_t f
   a.mapB1 = a.mapB0;
   a.K = L.H;
   a.N = 2 * L.F;
-  a.n_tiles = 2 * L.F / 128;
+  a.n_tiles = 2 * L.F / 256;   // 128 x 256 tiles
   a.num_groups = L.E;
   a.b_group_rows = L.H;
   a.offsets = offsets;
@@ -598,7 +598,7 @@ moe_status_t forward_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t
     a.mapB1 = a.mapB0;
     a.K = L.F;
     a.N = L.H;
-    a.n_tiles = L.H / 128;
+    a.n_tiles = L.H / 256;   // 128 x 256 tiles
     a.num_groups = L.E;
     a.b_group_rows = L.F;
     a.offsets = offsets;
@@ -725,7 +725,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     a.M = L.F;
     a.N = L.H;
     a.m_tiles = L.F / 128;
-    a.n_tiles = L.H / 128;
+    a.n_tiles = L.H / 256;   // 128 x 256 tiles
     a.num_groups = L.E;
     a.offsets = b.offsets;
     a.counts = b.counts;
@@ -754,7 +754,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     a.K = 2 * L.F;
     a.k_half = L.F;
     a.N = L.H;
-    a.n_tiles = L.H / 128;
+    a.n_tiles = L.H / 256;   // 128 x 256 tiles
     a.num_groups = L.E;
     a.b_group_rows = L.H;
     a.offsets = b.offsets;
@@ -793,7 +793,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     a.M = L.H;
     a.N = 2 * L.F;
     a.m_tiles = L.H / 128;
-    a.n_tiles = 2 * L.F / 128;
+    a.n_tiles = 2 * L.F / 256;   // 128 x 256 tiles
     a.num_groups = L.E;
     a.offsets = b.offsets;
     a.counts = b.counts;
@@ -1283,13 +1283,19 @@ moe_status_t moe_gemm_mxfp8(int64_t M, int64_t N, int64_t K, const moe_bf16_t* A
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
   a.K = static_cast<int>(K);
-  a.n_tiles = static_cast<int>(nt);
   a.out0 = D;
   a.ld0 = static_cast<int>(N);
   a.sfA = sa;
   a.kt_a = static_cast<int>(kt);
   a.sfB0 = sb;
   a.kt_b = static_cast<int>(kt);
+  if (N % 256 == 0) {   // 128 x 256 tiles
+    a.n_tiles = static_cast<int>(N / 256);
+    const int64_t tiles = static_cast<int64_t>(mt) * a.n_tiles;
+    return run("dense_gemm_mx", s, 0,
+               [&] { return launch_dense_mx256(a, grid_for(tiles, d.sms), s); });
+  }
+  a.n_tiles = static_cast<int>(nt);
   const int64_t tiles = static_cast<int64_t>(mt * nt);
   return run("dense_gemm_mx", s, 0, [&] { return launch_dense_mx(a, grid_for(tiles, d.sms), s); });
 }

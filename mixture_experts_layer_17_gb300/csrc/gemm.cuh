@@ -259,10 +259,22 @@ struct IsPair : std::false_type {};
 template <class P>
 struct IsPair<P, std::void_t<decltype(P::kPair)>> : std::integral_constant<bool, P::kPair> {};
 
+// Problems that define `struct Frag` free their TMEM accumulator early: the
+// epilogue copies its fragment to registers (P::epilogue_load), releases the
+// accumulator to the MMA warp, then computes and stores from registers
+// (P::epilogue_store).
+template <class P, class = void>
+struct HasFrag : std::false_type {};
+template <class P>
+struct HasFrag<P, std::void_t<typename P::Frag>> : std::true_type {};
+
 // Stage geometry.  bf16: a stage holds K = 64 (128 bytes per row).  MXFP8: a
 // stage holds K = 128 E4M3 (128 bytes per row) plus one 512-byte scale atom
-// for A and BN/128 for B; accumulators use TMEM columns [0, 2*BN) and the
-// stage's scales are copied to columns 256 + 8*stage (A) and +4 (B).
+// for A and BN/128 for B.  128-wide MXFP8 tiles double-buffer the accumulator
+// (TMEM columns [0, 256)) and copy the stage's scales to columns 256 +
+// 8*stage (A) and +4 (B); 256-wide tiles have one accumulator (columns
+// [0, 256), released early by the epilogue) and scales at 256 + 16*stage
+// (A), +4 (B rows 0..127) and +8 (B rows 128..255).  kAccBufs: accumulators.
 template <class P, bool MX = IsMX<P>::value, bool PAIR = IsPair<P>::value>
 struct StageCfg {
   static constexpr int BN = P::BN;
@@ -271,6 +283,7 @@ struct StageCfg {
   static constexpr uint32_t kSFBytes = 0;
   static constexpr int kStages = (BN >= 256) ? 4 : (BN >= 128 ? 6 : 8);
   static constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
+  static constexpr int kAccBufs = 2;
 };
 
 // CTA pair, bf16: per CTA a stage holds its 128 rows of A and BN/2 rows of B
@@ -284,18 +297,22 @@ struct StageCfg<P, false, true> {
   static constexpr uint32_t kSFBytes = 0;
   static constexpr int kStages = 6;
   static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kAccBufs = 2;
 };
 
 template <class P>
 struct StageCfg<P, true, false> {
   static constexpr int BN = P::BN;
-  static_assert(BN == 128, "MXFP8 tiles are 128 x 128");
+  static_assert(BN == 128 || BN == 256, "MXFP8 tiles are 128 x 128 or 128 x 256");
+  static_assert(BN == 128 || HasFrag<P>::value, "256-wide MXFP8 tiles release TMEM early");
   static constexpr uint32_t kABytes = kBM * 128;
   static constexpr uint32_t kBBytes = BN * 128;
   static constexpr uint32_t kSFBytes = 512 + (BN / 128) * 512;
-  static constexpr int kStages = 6;
+  static constexpr int kStages = BN == 256 ? 4 : 6;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSFCol0 = 256;
+  static constexpr uint32_t kSFStride = BN == 256 ? 16 : 8;   // TMEM columns per stage
+  static constexpr int kAccBufs = BN == 256 ? 1 : 2;
 };
 
 template <class P>
@@ -459,9 +476,10 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
             tc_fence_after();
             // scales of this stage -> TMEM (4-column aligned slots), then four
             // K = 32 block-scaled MMAs selecting the K-block with sf_id
-            const uint32_t sf_t = tmem_base + StageCfg<P, true, false>::kSFCol0 + 8u * stage;
+            const uint32_t sf_t = tmem_base + C::kSFCol0 + C::kSFStride * stage;
             sf_copy_to_tmem(sf_t, sSF + stage * kSF);
             sf_copy_to_tmem(sf_t + 4, sSF + stage * kSF + 512);
+            if constexpr (BN == 256) sf_copy_to_tmem(sf_t + 8, sSF + stage * kSF + 1024);
             const uint32_t a_base = smem_u32(sA + stage * kA);
             const uint32_t b_base = smem_u32(sB + stage * kB);
 #pragma unroll
@@ -520,7 +538,7 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
         }
       }
       __syncwarp();
-      if (++acc == 2) {
+      if (++acc == C::kAccBufs) {
         acc = 0;
         acc_phase ^= 1u;
       }
@@ -570,17 +588,28 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
         break;
       }
       tc_fence_after();
-      P::epilogue(args, ti, tmem_base + lane_off + static_cast<uint32_t>(acc * BN), r, group,
-                  extra);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (kPair && rank != 0)
-          mbar_arrive_remote(map_to_rank(tempty_bar + acc, 0));
-        else
-          mbar_arrive(tempty_bar + acc);
+      const uint32_t taddr = tmem_base + lane_off + static_cast<uint32_t>(acc * BN);
+      if constexpr (HasFrag<P>::value) {
+        // early release: fragment -> registers, accumulator back to the MMA
+        // warp, then the element-wise work and the stores
+        typename P::Frag f;
+        P::epilogue_load(args, ti, taddr, r, group, f);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar + acc);
+        P::epilogue_store(args, ti, r, group, f, extra);
+      } else {
+        P::epilogue(args, ti, taddr, r, group, extra);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (kPair && rank != 0)
+            mbar_arrive_remote(map_to_rank(tempty_bar + acc, 0));
+          else
+            mbar_arrive(tempty_bar + acc);
+        }
       }
-      if (++acc == 2) {
+      if (++acc == C::kAccBufs) {
         acc = 0;
         acc_phase ^= 1u;
       }

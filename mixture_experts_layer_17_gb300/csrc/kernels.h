@@ -35,6 +35,7 @@ cudaError_t launch_gate_up_dgrad_mx(const GemmArgs& a, int grid, cudaStream_t s)
 cudaError_t launch_down_wgrad_mx(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_gate_up_wgrad_mx(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_dense_mx(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_dense_mx256(const GemmArgs& a, int grid, cudaStream_t s);
 
 // MXFP8 quantisers (mx_quant.cu): E4M3 data + 512-byte scale atoms
 cudaError_t launch_quant_rows_dense(const uint16_t* src, int64_t R, int C, uint8_t* dst,

@@ -44,6 +44,25 @@ MOE_DEV void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   }
 }
 
+// Copies 8 x 16 TMEM columns starting at taddr into v (one wait for all).
+MOE_DEV void tmem_ld128(uint32_t taddr, float (&v)[128]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) tmem_ld16(taddr + 16 * i, *reinterpret_cast<float(*)[16]>(v + 16 * i));
+  tmem_ld_wait();
+}
+
+// B operand of a 256-wide MXFP8 tile: two 128-row TMA boxes (K-major: rows
+// n0 and n0 + 128 at sB and sB + 16 KB; MN-major: columns n0 and n0 + 128,
+// the second chunk at the descriptor's LBO of 16 KB).
+MOE_DEV void load_b256_kmajor(const CUtensorMap* map, int k0, int row0, uint8_t* sB, uint64_t* bar) {
+  tma_load_2d(sB, map, k0, row0, bar);
+  tma_load_2d(sB + 16384, map, k0, row0 + 128, bar);
+}
+MOE_DEV void load_b256_mnmajor(const CUtensorMap* map, int col0, int krow, uint8_t* sB, uint64_t* bar) {
+  tma_load_2d(sB, map, col0, krow, bar);
+  tma_load_2d(sB + 16384, map, col0 + 128, krow, bar);
+}
+
 // grouped-M tile with 128-element (fp8) K stages
 MOE_DEV TileInfo grouped_m_tile_mx(const GemmArgs& a, int t, int nstep) {
   TileInfo ti = grouped_m_tile(a, t, nstep);
@@ -77,75 +96,78 @@ MOE_DEV TileInfo grouped_k_tile_mx(const GemmArgs& a, int t, int BN) {
 
 // ------------------------------------------------------------------------
 // F7 + F8 in MXFP8: A = x_perm E4M3 [P, H]; B = W_gate|W_up quantised along H
-// and interleaved per 128-column tile as [64 gate | 64 up] ([E*H, 2F], MN-major).
-// Tile = 128 rows x (64 gate + 64 up) columns; outputs as GateUpFwdProblem.
+// and interleaved per 128-column block as [64 gate | 64 up] ([E*H, 2F],
+// MN-major).  Tile = 128 rows x 256 B columns = two interleaved blocks, i.e.
+// 128 F columns; epilogue group g owns block g (64 gate + 64 up columns).
+// Outputs: out0 = a as E4M3 [Pa, F] (quantised here from fp32), out1 = h bf16
+// [Pa, 2F], out2 = scale atoms of a (((mtile_off[e] + m-tile) * F/128 +
+// f/128) * 512).
 // ------------------------------------------------------------------------
 struct GateUpFwdMXProblem {
-  static constexpr int BN = 128;
+  static constexpr int BN = 256;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = true;
   static constexpr bool kMX = true;
   static constexpr size_t kExtraSmem = 0;
   static constexpr int kEpiGroups = 2;
+  struct Frag {
+    float v[128];   // [0, 64): gate, [64, 128): up
+  };
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
-  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile_mx(a, t, 64); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile_mx(a, t, 128); }
   MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
   MOE_DEV static void load_mx(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
                               uint8_t* sB, uint8_t* sSF, uint64_t* bar) {
     const int k0 = kb * 128;
-    const int nt = ti.n0 / 64;
+    const int nb = ti.n0 / 64;                // first interleaved 128-column block
     tma_load_2d(sA, &a.mapA, k0, ti.m0, bar);
-    tma_load_2d(sB, &a.mapB0, nt * 128, ti.e * a.b_group_rows + k0, bar);
+    load_b256_mnmajor(&a.mapB0, nb * 128, ti.e * a.b_group_rows + k0, sB, bar);
     bulk_load(sSF, sf_atom(a.sfA, (static_cast<int64_t>(__ldg(a.mtile_off + ti.e)) + ti.mt) * a.kt_a + kb), 512, bar);
-    bulk_load(sSF + 512, sf_atom(a.sfB0, (static_cast<int64_t>(ti.e) * a.n_tiles + nt) * a.kt_b + kb), 512, bar);
+    const int64_t wrow = static_cast<int64_t>(ti.e) * (2 * a.n_tiles) + nb;
+    bulk_load(sSF + 512, sf_atom(a.sfB0, wrow * a.kt_b + kb), 512, bar);
+    bulk_load(sSF + 1024, sf_atom(a.sfB0, (wrow + 1) * a.kt_b + kb), 512, bar);
   }
   MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
-  // out0 = a as E4M3 [Pa, F] (quantised here from fp32, one MX block of 32
-  // columns per thread), out1 = h bf16 [Pa, 2F], out2 = scale atoms of a
-  // (((mtile_off[e] + m-tile) * F/128 + f/128) * 512).
-  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               int group, uint8_t*) {
-    const bool valid = r < ti.rows;
+  MOE_DEV static void epilogue_load(const GemmArgs&, const TileInfo&, uint32_t taddr, int,
+                                    int group, Frag& f) {
+    tmem_ld128(taddr + 128 * group, f.v);
+  }
+  MOE_DEV static void epilogue_store(const GemmArgs& a, const TileInfo& ti, int r, int group,
+                                     Frag& f, uint8_t*) {
+    if (r >= ti.rows) return;
     const int64_t row = static_cast<int64_t>(ti.m0) + r;
     const int F = a.ld0;
-    const int f0 = ti.n0 + 32 * group;
-    float g[32], u[32];
-    tmem_ld32(taddr + 32 * group, g);
-    tmem_ld32(taddr + 64 + 32 * group, u);
-    if (!valid) return;
+    const int f0 = ti.n0 + 64 * group;        // first F column of this group
     __nv_bfloat16* hg = static_cast<__nv_bfloat16*>(a.out1) + row * 2 * F + f0;
-    float g16[16], u16[16];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        g16[i] = g[16 * half + i];
-        u16[i] = u[16 * half + i];
-      }
-      store_bf16x16(hg + 16 * half, g16);
-      store_bf16x16(hg + F + 16 * half, u16);
+    for (int i = 0; i < 64; i += 16) {
+      store_bf16x16(hg + i, *reinterpret_cast<const float(*)[16]>(f.v + i));
+      store_bf16x16(hg + F + i, *reinterpret_cast<const float(*)[16]>(f.v + 64 + i));
     }
-    float act[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) act[i] = g[i] * sigmoidf_fast(g[i]) * u[i];
+    for (int i = 0; i < 64; ++i) f.v[i] = f.v[i] * sigmoidf_fast(f.v[i]) * f.v[64 + i];
     uint8_t* aq = static_cast<uint8_t*>(a.out0) + row * F + f0;
     uint8_t* sf = static_cast<uint8_t*>(a.out2) +
-                  ((static_cast<int64_t>(__ldg(a.mtile_off + ti.e)) + ti.mt) * (F / 128) + f0 / 128) * 512 +
-                  sf_atom_offset(r, (f0 >> 5) & 3);
-    mx_block_store(act, aq, sf);
+                  ((static_cast<int64_t>(__ldg(a.mtile_off + ti.e)) + ti.mt) * (F / 128) + f0 / 128) * 512;
+    mx_block_store(*reinterpret_cast<const float(*)[32]>(f.v), aq, sf + sf_atom_offset(r, (f0 >> 5) & 3));
+    mx_block_store(*reinterpret_cast<const float(*)[32]>(f.v + 32), aq + 32,
+                   sf + sf_atom_offset(r, ((f0 >> 5) & 3) + 1));
   }
 };
 
 // F9 + F10 in MXFP8: A = a E4M3 [P, F]; B = W_down quantised along F
-// ([E*F, H], MN-major); weighted scatter epilogue.
+// ([E*F, H], MN-major); 128 x 256 tiles, weighted scatter epilogue.
 struct DownFwdMXProblem {
-  static constexpr int BN = 128;
+  static constexpr int BN = 256;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = true;
   static constexpr bool kMX = true;
   static constexpr size_t kExtraSmem = 0;
   static constexpr int kEpiGroups = 2;
+  struct Frag {
+    float v[128];
+  };
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
   MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile_mx(a, t, BN); }
@@ -153,35 +175,30 @@ struct DownFwdMXProblem {
   MOE_DEV static void load_mx(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
                               uint8_t* sB, uint8_t* sSF, uint64_t* bar) {
     const int k0 = kb * 128;
-    const int nt = ti.n0 / BN;
     tma_load_2d(sA, &a.mapA, k0, ti.m0, bar);
-    tma_load_2d(sB, &a.mapB0, ti.n0, ti.e * a.b_group_rows + k0, bar);
+    load_b256_mnmajor(&a.mapB0, ti.n0, ti.e * a.b_group_rows + k0, sB, bar);
     bulk_load(sSF, sf_atom(a.sfA, (static_cast<int64_t>(__ldg(a.mtile_off + ti.e)) + ti.mt) * a.kt_a + kb), 512, bar);
-    bulk_load(sSF + 512, sf_atom(a.sfB0, (static_cast<int64_t>(ti.e) * a.n_tiles + nt) * a.kt_b + kb), 512, bar);
+    const int64_t wrow = static_cast<int64_t>(ti.e) * (2 * a.n_tiles) + ti.n0 / 128;
+    bulk_load(sSF + 512, sf_atom(a.sfB0, wrow * a.kt_b + kb), 512, bar);
+    bulk_load(sSF + 1024, sf_atom(a.sfB0, (wrow + 1) * a.kt_b + kb), 512, bar);
   }
   MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
-  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               int group, uint8_t*) {
-    const bool valid = r < ti.rows;
+  MOE_DEV static void epilogue_load(const GemmArgs&, const TileInfo&, uint32_t taddr, int,
+                                    int group, Frag& f) {
+    tmem_ld128(taddr + 128 * group, f.v);
+  }
+  MOE_DEV static void epilogue_store(const GemmArgs& a, const TileInfo& ti, int r, int group,
+                                     Frag& f, uint8_t*) {
+    if (r >= ti.rows) return;
     const int64_t row = static_cast<int64_t>(ti.m0) + r;
-    float w = 0.f;
-    __nv_bfloat16* dst = nullptr;
-    if (valid) {
-      w = __ldg(static_cast<const float*>(a.in0) + row);
-      const int slot = __ldg(static_cast<const int*>(a.in1) + row);
-      dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 + ti.n0;
-    }
-#pragma unroll 1
-    for (int c = group * 64; c < group * 64 + 64; c += 16) {
-      float v[16];
-      tmem_ld16(taddr + c, v);
-      tmem_ld_wait();
-      if (valid) {
+    const float w = __ldg(static_cast<const float*>(a.in0) + row);
+    const int slot = __ldg(static_cast<const int*>(a.in1) + row);
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 +
+                         ti.n0 + 128 * group;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] *= w;
-        store_bf16x16(dst + c, v);
-      }
-    }
+    for (int i = 0; i < 128; ++i) f.v[i] *= w;
+#pragma unroll
+    for (int i = 0; i < 128; i += 16) store_bf16x16(dst + i, *reinterpret_cast<const float(*)[16]>(f.v + i));
   }
 };
 
@@ -265,14 +282,18 @@ struct DownDgradMXProblem : DownDgradProblem<128> {
 };
 
 // B6 in MXFP8: A = dh E4M3 [P, 2F] (each half quantised along F); B = W_gate
-// then W_up quantised along F ([E*H, F], K-major); scatter epilogue.
+// then W_up quantised along F ([E*H, F], K-major); 128 x 256 tiles, scatter
+// epilogue.
 struct GateUpDgradMXProblem {
-  static constexpr int BN = 128;
+  static constexpr int BN = 256;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
   static constexpr bool kMX = true;
   static constexpr size_t kExtraSmem = 0;
   static constexpr int kEpiGroups = 2;
+  struct Frag {
+    float v[128];
+  };
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
   MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile_mx(a, t, BN); }
@@ -280,51 +301,50 @@ struct GateUpDgradMXProblem {
   MOE_DEV static void load_mx(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
                               uint8_t* sB, uint8_t* sSF, uint64_t* bar) {
     const int k0 = kb * 128;
-    const int nt = ti.n0 / BN;
     const int brow = ti.e * a.b_group_rows + ti.n0;
     tma_load_2d(sA, &a.mapA, k0, ti.m0, bar);
     bulk_load(sSF, sf_atom(a.sfA, (static_cast<int64_t>(__ldg(a.mtile_off + ti.e)) + ti.mt) * a.kt_a + kb), 512, bar);
-    const int64_t wrow = static_cast<int64_t>(ti.e) * a.n_tiles + nt;
-    if (k0 < a.k_half) {
-      tma_load_2d(sB, &a.mapB0, k0, brow, bar);
-      bulk_load(sSF + 512, sf_atom(a.sfB0, wrow * a.kt_b + kb), 512, bar);
-    } else {
-      tma_load_2d(sB, &a.mapB1, k0 - a.k_half, brow, bar);
-      bulk_load(sSF + 512, sf_atom(a.sfB1, wrow * a.kt_b + kb - a.kt_b), 512, bar);
-    }
+    const int64_t wrow = static_cast<int64_t>(ti.e) * (2 * a.n_tiles) + ti.n0 / 128;
+    const bool up = k0 >= a.k_half;
+    const uint8_t* sfb = up ? a.sfB1 : a.sfB0;
+    const int kbw = up ? kb - a.kt_b : kb;
+    load_b256_kmajor(up ? &a.mapB1 : &a.mapB0, up ? k0 - a.k_half : k0, brow, sB, bar);
+    bulk_load(sSF + 512, sf_atom(sfb, wrow * a.kt_b + kbw), 512, bar);
+    bulk_load(sSF + 1024, sf_atom(sfb, (wrow + 1) * a.kt_b + kbw), 512, bar);
   }
   MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
-  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               int group, uint8_t*) {
-    const bool valid = r < ti.rows;
+  MOE_DEV static void epilogue_load(const GemmArgs&, const TileInfo&, uint32_t taddr, int,
+                                    int group, Frag& f) {
+    tmem_ld128(taddr + 128 * group, f.v);
+  }
+  MOE_DEV static void epilogue_store(const GemmArgs& a, const TileInfo& ti, int r, int group,
+                                     Frag& f, uint8_t*) {
+    if (r >= ti.rows) return;
     const int64_t row = static_cast<int64_t>(ti.m0) + r;
-    __nv_bfloat16* dst = nullptr;
-    if (valid) {
-      const int slot = __ldg(static_cast<const int*>(a.in1) + row);
-      dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 + ti.n0;
-    }
-#pragma unroll 1
-    for (int c = group * 64; c < group * 64 + 64; c += 16) {
-      float v[16];
-      tmem_ld16(taddr + c, v);
-      tmem_ld_wait();
-      if (valid) store_bf16x16(dst + c, v);
-    }
+    const int slot = __ldg(static_cast<const int*>(a.in1) + row);
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 +
+                         ti.n0 + 128 * group;
+#pragma unroll
+    for (int i = 0; i < 128; i += 16) store_bf16x16(dst + i, *reinterpret_cast<const float(*)[16]>(f.v + i));
   }
 };
 
 // Weight gradients in MXFP8 over the padded token layout (both operands
-// MN-major, quantised along tokens per expert segment).
+// MN-major, quantised along tokens per expert segment); 128 x 256 tiles.
 //   Down:    A = w*a [P_pad, F] (M = F), B = dY_perm [P_pad, H] (N = H) -> dW_down [E, F, H]
 //   Gate/up: A = x_perm [P_pad, H] (M = H), B = dh [P_pad, 2F] (N = 2F) -> dW_gate, dW_up
+// B's two 128-column atoms of a k-tile are adjacent: one 1 KB scale copy.
 template <bool kGateUp>
 struct WgradMXProblem {
-  static constexpr int BN = 128;
+  static constexpr int BN = 256;
   static constexpr bool kAMN = true;
   static constexpr bool kBMN = true;
   static constexpr bool kMX = true;
   static constexpr size_t kExtraSmem = 0;
   static constexpr int kEpiGroups = 2;
+  struct Frag {
+    float v[128];
+  };
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_k_num_tiles(a); }
   MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_k_tile_mx(a, t, BN); }
@@ -334,10 +354,12 @@ struct WgradMXProblem {
     const int kt = ti.kb0 + kb;
     const int krow = 128 * kt;
     tma_load_2d(sA, &a.mapA, ti.m0, krow, bar);
-    tma_load_2d(sB, &a.mapB0, ti.n0, krow, bar);
+    load_b256_mnmajor(&a.mapB0, ti.n0, krow, sB, bar);
     bulk_load(sSF, sf_atom(a.sfA, static_cast<int64_t>(kt) * a.m_tiles + ti.mt), 512, bar);
-    bulk_load(sSF + 512, sf_atom(a.sfB0, static_cast<int64_t>(kt) * a.n_tiles + ti.n0 / BN), 512, bar);
+    bulk_load(sSF + 512, sf_atom(a.sfB0, static_cast<int64_t>(kt) * (2 * a.n_tiles) + ti.n0 / 128),
+              1024, bar);
   }
+  // (buffer, element index) of column gc of output row r
   MOE_DEV static void out_loc(const GemmArgs& a, const TileInfo& ti, int r, int gc, void*& base,
                               int64_t& idx) {
     if (kGateUp) {
@@ -353,29 +375,25 @@ struct WgradMXProblem {
                                      uint8_t*) {
     if (r >= ti.rows) return;
     const bool acc = (a.flags & kGemmAccumF32) != 0;
-    for (int c = group * 64; c < group * 64 + 64; c += 16) {
-      void* base;
-      int64_t idx;
-      out_loc(a, ti, r, ti.n0 + c, base, idx);
-      wgrad_zero16(base, idx, acc);
-    }
+    void* base;
+    int64_t idx;
+    out_loc(a, ti, r, ti.n0 + 128 * group, base, idx);   // 128 columns never straddle F
+    for (int c = 0; c < 128; c += 16) wgrad_zero16(base, idx + c, acc);
   }
-  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               int group, uint8_t*) {
-    const bool valid = r < ti.rows;
+  MOE_DEV static void epilogue_load(const GemmArgs&, const TileInfo&, uint32_t taddr, int,
+                                    int group, Frag& f) {
+    tmem_ld128(taddr + 128 * group, f.v);
+  }
+  MOE_DEV static void epilogue_store(const GemmArgs& a, const TileInfo& ti, int r, int group,
+                                     Frag& f, uint8_t*) {
+    if (r >= ti.rows) return;
     const bool acc = (a.flags & kGemmAccumF32) != 0;
-#pragma unroll 1
-    for (int c = group * 64; c < group * 64 + 64; c += 16) {
-      float v[16];
-      tmem_ld16(taddr + c, v);
-      tmem_ld_wait();
-      if (valid) {
-        void* base;
-        int64_t idx;
-        out_loc(a, ti, r, ti.n0 + c, base, idx);
-        wgrad_store16(base, idx, acc, v);
-      }
-    }
+    void* base;
+    int64_t idx;
+    out_loc(a, ti, r, ti.n0 + 128 * group, base, idx);
+#pragma unroll
+    for (int c = 0; c < 128; c += 16)
+      wgrad_store16(base, idx + c, acc, *reinterpret_cast<const float(*)[16]>(f.v + c));
   }
 };
 
@@ -420,6 +438,53 @@ struct DenseMXProblem {
                        __float_as_uint(v[i + 2]), __float_as_uint(v[i + 3]));
       }
     }
+  }
+};
+
+// Dense MXFP8 GEMM with 128 x 256 tiles (N a multiple of 256): as
+// DenseMXProblem, B atoms (n-tile of 128 rows) * kt + k-tile, two per stage;
+// one accumulator, released as soon as the epilogue holds its fragment.
+struct DenseMX256Problem {
+  static constexpr int BN = 256;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = false;
+  static constexpr bool kMX = true;
+  static constexpr size_t kExtraSmem = 0;
+  static constexpr int kEpiGroups = 2;
+  struct Frag {
+    float v[128];
+  };
+
+  MOE_DEV static int num_tiles(const GemmArgs& a) { return dense_num_tiles(a); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) {
+    TileInfo ti = dense_tile(a, t, BN);
+    ti.num_kb = (a.K + 127) / 128;
+    return ti;
+  }
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
+  MOE_DEV static void load_mx(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
+                              uint8_t* sB, uint8_t* sSF, uint64_t* bar) {
+    tma_load_2d(sA, &a.mapA, kb * 128, ti.m0, bar);
+    load_b256_kmajor(&a.mapB0, kb * 128, ti.n0, sB, bar);
+    const int64_t nt = ti.n0 / 128;
+    bulk_load(sSF, sf_atom(a.sfA, static_cast<int64_t>(ti.mt) * a.kt_a + kb), 512, bar);
+    bulk_load(sSF + 512, sf_atom(a.sfB0, nt * a.kt_b + kb), 512, bar);
+    bulk_load(sSF + 1024, sf_atom(a.sfB0, (nt + 1) * a.kt_b + kb), 512, bar);
+  }
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
+  MOE_DEV static void epilogue_load(const GemmArgs&, const TileInfo&, uint32_t taddr, int,
+                                    int group, Frag& f) {
+    tmem_ld128(taddr + 128 * group, f.v);
+  }
+  MOE_DEV static void epilogue_store(const GemmArgs& a, const TileInfo& ti, int r, int group,
+                                     const Frag& f, uint8_t*) {
+    if (r >= ti.rows) return;
+    float* p = static_cast<float*>(a.out0) + (static_cast<int64_t>(ti.m0) + r) * a.ld0 + ti.n0 +
+               128 * group;
+#pragma unroll
+    for (int i = 0; i < 128; i += 4)
+      st_global_v4(p + i, __float_as_uint(f.v[i]), __float_as_uint(f.v[i + 1]),
+                   __float_as_uint(f.v[i + 2]), __float_as_uint(f.v[i + 3]));
   }
 };
 
