@@ -240,8 +240,9 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.ntiles = static_cast<int>((L.T + kBM - 1) / kBM);
   L.router_bn = next_pow2_at_least16(L.E);
   L.dgrad_bn = (L.F % 256 == 0) ? 256 : 128;
-  // one router-weight partial per n-tile and epilogue column half (MXFP8 tiles are 128 wide)
-  L.nparts = (c.precision == MOE_BF16 ? L.F / L.dgrad_bn : L.F / 128) * 2;
+  // one router-weight partial per n-tile and epilogue column half (the bf16
+  // and MXFP8 down dgrads both use 256-wide tiles when F allows)
+  L.nparts = (L.F / L.dgrad_bn) * 2;
   L.wr_mtiles = (L.E + kBM - 1) / kBM;
   L.wr_ntiles = L.H / 256;
   const int total_kb = static_cast<int>((L.T + kBK - 1) / kBK);
@@ -332,10 +333,10 @@ Layout make_layout(const moe_config_t& c, int sms) {
     const size_t Pp = 128 * mt;   // padded token rows
     L.bq_dy = b.take(Pa * H);
     L.bs_dy = b.take(mt * (H / 128) * 512);
-    L.bq_wdh = b.take(E * F * H);
-    L.bs_wdh = b.take(E * (F / 128) * (H / 128) * 512);
     L.bq_dh = b.take(Pa * 2 * F);
     L.bs_dh = b.take(mt * (2 * F / 128) * 512);
+    L.bq_wdh = b.take(E * F * H);
+    L.bs_wdh = b.take(E * (F / 128) * (H / 128) * 512);
     L.bq_wg = b.take(E * H * F);
     L.bs_wg = b.take(E * (H / 128) * (F / 128) * 512);
     L.bq_wu = b.take(E * H * F);
@@ -523,6 +524,7 @@ moe_status_t gate_up_fwd_bf16(const Layout& L, int sms, cudaStream_t s, uint32_t
 // E4M3 operands and scale atoms of the MXFP8 gate/up GEMM
 struct MxGateUpBufs {
   uint8_t *xq, *sx, *aq, *sa, *wgu, *swgu;
+  bool x_ready = false;   // xq / sx already written by the fused gather
 };
 
 // F7 + F8 in MXFP8: quantise x_perm along H and W_gate / W_up along H
@@ -533,9 +535,11 @@ moe_status_t gate_up_fwd_mx(const Layout& L, int sms, cudaStream_t s, uint32_t f
                             const uint16_t* W_up, const int* offsets, const int* counts,
                             const int* mtile, uint16_t* h, const MxGateUpBufs& q,
                             bool recompute) {
-  MOE_TRY(run(recompute ? "recompute_mx_quant_x" : "mx_quant_x", s, fl, [&] {
-    return launch_quant_rows_permuted(xperm, L.Pa, L.H, q.xq, q.sx, offsets, mtile, L.E, s);
-  }));
+  if (!q.x_ready) {
+    MOE_TRY(run(recompute ? "recompute_mx_quant_x" : "mx_quant_x", s, fl, [&] {
+      return launch_quant_rows_permuted(xperm, L.Pa, L.H, q.xq, q.sx, offsets, mtile, L.E, s);
+    }));
+  }
   MOE_TRY(run(recompute ? "recompute_mx_quant_w_gate_up" : "mx_quant_w_gate_up", s, fl, [&] {
     return launch_quant_cols_gate_up(W_gate, W_up, L.E, L.H, L.F, q.wgu, q.swgu, s);
   }));
@@ -578,9 +582,9 @@ moe_status_t forward_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t
                               const int* row_slot,
                               uint16_t* act, uint16_t* h, uint16_t* scratch, void* ws) {
   (void)act;
-  const MxGateUpBufs q{at<uint8_t>(ws, L.fq_x), at<uint8_t>(ws, L.fs_x), at<uint8_t>(ws, L.fq_a),
-                       at<uint8_t>(ws, L.fs_a), at<uint8_t>(ws, L.fq_wgu),
-                       at<uint8_t>(ws, L.fs_wgu)};
+  MxGateUpBufs q{at<uint8_t>(ws, L.fq_x), at<uint8_t>(ws, L.fs_x), at<uint8_t>(ws, L.fq_a),
+                 at<uint8_t>(ws, L.fs_a), at<uint8_t>(ws, L.fq_wgu), at<uint8_t>(ws, L.fs_wgu)};
+  q.x_ready = true;   // moe_forward's gather quantised x_perm along H
   uint8_t* aq = q.aq;
   uint8_t* sa = q.sa;
   uint8_t* wd = at<uint8_t>(ws, L.fq_wd);
@@ -662,10 +666,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
   const uint64_t Pp = 128ull * static_cast<uint64_t>(L.mt_max);
   const int64_t mtiles = (L.P + kBM - 1) / kBM + L.E;
 
-  // B2-B4: down dgrad
-  MOE_TRY(run("mx_quant_dy", s, fl, [&] {
-    return launch_quant_rows_permuted(b.dyp, L.Pa, L.H, dyq, sdy, b.offsets, b.mtile, L.E, s);
-  }));
+  // B2-B4: down dgrad (dY_perm was quantised along H by the fused gather)
   MOE_TRY(run("mx_quant_w_down_h", s, fl, [&] {
     return launch_quant_rows_dense(b.W_down, static_cast<int64_t>(L.E) * L.F, L.H, wdh, swdh, s);
   }));
@@ -677,7 +678,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     a.mapB1 = a.mapB0;
     a.K = L.H;
     a.N = L.F;
-    a.n_tiles = L.F / 128;
+    a.n_tiles = L.F / L.dgrad_bn;
     a.num_groups = L.E;
     a.b_group_rows = L.F;
     a.offsets = b.offsets;
@@ -700,7 +701,8 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
       a.wait_limit_ns = kTestWaitNs;
     }
     const int grid = grid_for(mtiles * a.n_tiles, sms);
-    MOE_TRY(run("down_dgrad_swiglu_bwd_mx", s, fl, [&] { return launch_down_dgrad_mx(a, grid, s); }));
+    MOE_TRY(run("down_dgrad_swiglu_bwd_mx", s, fl,
+                [&] { return launch_down_dgrad_mx(L.dgrad_bn, a, grid, s); }));
   }
   // B9: router softmax / top-k backward
   if (cudaMemsetAsync(b.dlt, 0, 2ull * L.E * L.T_pad, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -908,8 +910,15 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
 
   // F6: dispatch x to the padded expert-major rows (segment tails zeroed: they
   // are K rows of the gate/up weight gradient)
-  MOE_TRY(run("gather_x", s, fl,
-              [&] { return launch_gather_rows(x, slot_pad, xperm, L.T, L.H, L.k, s); }));
+  if (cfg->precision == MOE_MXFP8) {   // bf16 rows plus their E4M3 copy along H
+    MOE_TRY(run("gather_x_mx", s, fl, [&] {
+      return launch_gather_rows_mx(x, slot_pad, idx, poff, mtile, xperm, at<uint8_t>(ws, L.fq_x),
+                                   at<uint8_t>(ws, L.fs_x), L.T, L.H, L.k, s);
+    }));
+  } else {
+    MOE_TRY(run("gather_x", s, fl,
+                [&] { return launch_gather_rows(x, slot_pad, xperm, L.T, L.H, L.k, s); }));
+  }
   MOE_TRY(run("zero_pad_rows_x", s, fl,
               [&] { return launch_zero_pad_rows(xperm, poff, counts, L.E, L.H, s); }));
 
@@ -1005,14 +1014,22 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
     // lands in aw and is overwritten by the down dgrad) in the forward's precision
     uint16_t* xp = at<uint16_t>(ws, L.b_xperm);
     uint16_t* hh = at<uint16_t>(ws, L.b_h);
-    MOE_TRY(run("recompute_gather_x", s, fl,
-                [&] { return launch_gather_rows(x, slot_pad, xp, L.T, L.H, L.k, s); }));
+    if (cfg->precision == MOE_MXFP8) {
+      MOE_TRY(run("recompute_gather_x_mx", s, fl, [&] {
+        return launch_gather_rows_mx(x, slot_pad, idx, poff, mtile, xp, at<uint8_t>(ws, L.bq_rx),
+                                     at<uint8_t>(ws, L.bs_rx), L.T, L.H, L.k, s);
+      }));
+    } else {
+      MOE_TRY(run("recompute_gather_x", s, fl,
+                  [&] { return launch_gather_rows(x, slot_pad, xp, L.T, L.H, L.k, s); }));
+    }
     MOE_TRY(run("recompute_zero_pad_rows_x", s, fl,
                 [&] { return launch_zero_pad_rows(xp, poff, counts, L.E, L.H, s); }));
     if (cfg->precision == MOE_MXFP8) {
-      const MxGateUpBufs q{at<uint8_t>(ws, L.bq_rx), at<uint8_t>(ws, L.bs_rx),
-                           at<uint8_t>(ws, L.bq_ra), at<uint8_t>(ws, L.bs_ra),
-                           at<uint8_t>(ws, L.bq_rwgu), at<uint8_t>(ws, L.bs_rwgu)};
+      MxGateUpBufs q{at<uint8_t>(ws, L.bq_rx), at<uint8_t>(ws, L.bs_rx),
+                     at<uint8_t>(ws, L.bq_ra), at<uint8_t>(ws, L.bs_ra),
+                     at<uint8_t>(ws, L.bq_rwgu), at<uint8_t>(ws, L.bs_rwgu)};
+      q.x_ready = true;
       MOE_TRY(gate_up_fwd_mx(L, sms, s, fl, st, xp, W_gate, W_up, poff, counts, mtile, hh, q,
                              true));
     } else {
@@ -1023,8 +1040,15 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
 
   // B1: dispatch dY to the padded expert-major rows (segment tails zeroed:
   // they are K rows of the down weight gradient)
-  MOE_TRY(run("gather_dy", s, fl,
-              [&] { return launch_gather_rows(dY, slot_pad, dyp, L.T, L.H, L.k, s); }));
+  if (cfg->precision != MOE_BF16) {   // bf16 rows plus their E4M3 copy along H
+    MOE_TRY(run("gather_dy_mx", s, fl, [&] {
+      return launch_gather_rows_mx(dY, slot_pad, idx, poff, mtile, dyp, at<uint8_t>(ws, L.bq_dy),
+                                   at<uint8_t>(ws, L.bs_dy), L.T, L.H, L.k, s);
+    }));
+  } else {
+    MOE_TRY(run("gather_dy", s, fl,
+                [&] { return launch_gather_rows(dY, slot_pad, dyp, L.T, L.H, L.k, s); }));
+  }
   MOE_TRY(run("zero_pad_rows_dy", s, fl,
               [&] { return launch_zero_pad_rows(dyp, poff, counts, L.E, L.H, s); }));
 

@@ -273,7 +273,8 @@ struct HasFrag<P, std::void_t<typename P::Frag>> : std::true_type {};
 // for A and BN/128 for B.  128-wide MXFP8 tiles double-buffer the accumulator
 // (TMEM columns [0, 256)) and copy the stage's scales to columns 256 +
 // 8*stage (A) and +4 (B); 256-wide tiles have one accumulator (columns
-// [0, 256), released early by the epilogue) and scales at 256 + 16*stage
+// [0, 256), released early by epilogues with a Frag, else after the
+// epilogue) and scales at 256 + 16*stage
 // (A), +4 (B rows 0..127) and +8 (B rows 128..255).  kAccBufs: accumulators.
 template <class P, bool MX = IsMX<P>::value, bool PAIR = IsPair<P>::value>
 struct StageCfg {
@@ -304,7 +305,6 @@ template <class P>
 struct StageCfg<P, true, false> {
   static constexpr int BN = P::BN;
   static_assert(BN == 128 || BN == 256, "MXFP8 tiles are 128 x 128 or 128 x 256");
-  static_assert(BN == 128 || HasFrag<P>::value, "256-wide MXFP8 tiles release TMEM early");
   static constexpr uint32_t kABytes = kBM * 128;
   static constexpr uint32_t kBBytes = BN * 128;
   static constexpr uint32_t kSFBytes = 512 + (BN / 128) * 512;

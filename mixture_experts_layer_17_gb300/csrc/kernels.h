@@ -30,7 +30,7 @@ cudaError_t launch_gate_up_wgrad_pair(const GemmArgs& a, int grid, cudaStream_t 
 // MXFP8 GEMMs (gemm_mx.cu)
 cudaError_t launch_gate_up_fwd_mx(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_down_fwd_mx(const GemmArgs& a, int grid, cudaStream_t s);
-cudaError_t launch_down_dgrad_mx(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_down_dgrad_mx(int bn, const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_gate_up_dgrad_mx(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_down_wgrad_mx(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_gate_up_wgrad_mx(const GemmArgs& a, int grid, cudaStream_t s);
@@ -65,6 +65,12 @@ cudaError_t launch_zero_pad_rows(uint16_t* m, const int* poff, const int* counts
                                  cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t* src, const int* slot_row, uint16_t* dst,
                                int64_t T, int H, int k, cudaStream_t s);
+// launch_gather_rows plus the MXFP8 copy of every row along H (padded rows,
+// scale atoms of the expert m-tiles); idx = the slot's expert
+cudaError_t launch_gather_rows_mx(const uint16_t* src, const int* slot_row, const int* idx,
+                                  const int* poff, const int* mtile_off, uint16_t* dst,
+                                  uint8_t* dstq, uint8_t* sf, int64_t T, int H, int k,
+                                  cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* scratch, uint16_t* y, int64_t T, int H, int k,
                            cudaStream_t s);
 cudaError_t launch_router_bwd(const float* dw_part, int nparts, const int* slot_row,

@@ -203,20 +203,48 @@ struct DownFwdMXProblem {
 };
 
 // B2-B4 in MXFP8: A = dY_perm E4M3 [P, H]; B = W_down quantised along H
-// ([E*F, H], K-major); the SwiGLU-backward epilogue of DownDgradProblem<128>.
-struct DownDgradMXProblem : DownDgradProblem<128> {
+// ([E*F, H], K-major); the SwiGLU-backward epilogue of DownDgradProblem: dh
+// and w*a in bf16 for the weight gradients, the router-weight partials, and
+// dh quantised to E4M3 along F straight from fp32 for the gate/up dgrad:
+// out3 = dh E4M3 [Pa, 2F], out4 = its scale atoms (((mtile_off[e] +
+// m-tile) * 2F/128 + column/128) * 512).  BN = 256 (F a multiple of 256) runs
+// one accumulator and a serial epilogue (too many live values for an early
+// release), BN = 128 double-buffers.
+template <int BN_>
+struct DownDgradMXProblem {
+  static constexpr int BN = BN_;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = false;
   static constexpr bool kMX = true;
-  // As DownDgradProblem<128> (dh, w*a in bf16 for the weight gradients, the
-  // router-weight partials), plus dh quantised to E4M3 along F straight from
-  // fp32 for the gate/up dgrad: out3 = dh E4M3 [Pa, 2F], out4 = its scale
-  // atoms (((mtile_off[e] + m-tile) * 2F/128 + column/128) * 512).
+  static constexpr size_t kExtraSmem = 0;
+  static constexpr int kEpiGroups = 2;
+
+  MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile_mx(a, t, BN); }
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
+  MOE_DEV static void load_mx(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
+                              uint8_t* sB, uint8_t* sSF, uint64_t* bar) {
+    const int k0 = kb * 128;
+    const int brow = ti.e * a.b_group_rows + ti.n0;
+    tma_load_2d(sA, &a.mapA, k0, ti.m0, bar);
+    if constexpr (BN == 256)
+      load_b256_kmajor(&a.mapB0, k0, brow, sB, bar);
+    else
+      tma_load_2d(sB, &a.mapB0, k0, brow, bar);
+    bulk_load(sSF, sf_atom(a.sfA, (static_cast<int64_t>(__ldg(a.mtile_off + ti.e)) + ti.mt) * a.kt_a + kb), 512, bar);
+    const int64_t wrow = static_cast<int64_t>(ti.e) * (a.b_group_rows / 128) + ti.n0 / 128;
+    bulk_load(sSF + 512, sf_atom(a.sfB0, wrow * a.kt_b + kb), 512, bar);
+    if constexpr (BN == 256) bulk_load(sSF + 1024, sf_atom(a.sfB0, (wrow + 1) * a.kt_b + kb), 512, bar);
+  }
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
                                int group, uint8_t*) {
+    constexpr int kHalf = BN / 2;
     const bool valid = r < ti.rows;
     const bool pad = !valid && r < ti.rows_pad;
     const int64_t row = static_cast<int64_t>(ti.m0) + ((valid || pad) ? r : 0);
     const int F = a.ld0;
-    const int c0 = group * 64;
+    const int c0 = group * kHalf;
     const __nv_bfloat16* h = static_cast<const __nv_bfloat16*>(a.in0) + row * 2 * F + ti.n0;
     __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(a.out0) + row * 2 * F + ti.n0;
     __nv_bfloat16* aw = static_cast<__nv_bfloat16*>(a.out1) + row * F + ti.n0;
@@ -226,7 +254,7 @@ struct DownDgradMXProblem : DownDgradProblem<128> {
     const float w = valid ? __ldg(static_cast<const float*>(a.in1) + row) : 0.f;
     float dw = 0.f;
 #pragma unroll 1
-    for (int c = c0; c < c0 + 64; c += 32) {
+    for (int c = c0; c < c0 + kHalf; c += 32) {
       float g[32];
       tmem_ld32(taddr + c, g);
       if (valid) {
@@ -268,16 +296,6 @@ struct DownDgradMXProblem : DownDgradProblem<128> {
     if (valid)
       static_cast<float*>(a.out2)[row * (a.n_tiles * kEpiGroups) + (ti.n0 / BN) * kEpiGroups +
                                   group] = dw;
-  }
-  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile_mx(a, t, 128); }
-  MOE_DEV static void load_mx(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
-                              uint8_t* sB, uint8_t* sSF, uint64_t* bar) {
-    const int k0 = kb * 128;
-    const int nt = ti.n0 / 128;
-    tma_load_2d(sA, &a.mapA, k0, ti.m0, bar);
-    tma_load_2d(sB, &a.mapB0, k0, ti.e * a.b_group_rows + ti.n0, bar);
-    bulk_load(sSF, sf_atom(a.sfA, (static_cast<int64_t>(__ldg(a.mtile_off + ti.e)) + ti.mt) * a.kt_a + kb), 512, bar);
-    bulk_load(sSF + 512, sf_atom(a.sfB0, (static_cast<int64_t>(ti.e) * a.n_tiles + nt) * a.kt_b + kb), 512, bar);
   }
 };
 
