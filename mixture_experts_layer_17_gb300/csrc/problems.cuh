@@ -13,6 +13,82 @@ namespace moe {
 MOE_DEV void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // ------------------------------------------------------------------------
+// Coalesced row stores.  An epilogue thread owns one output row, so a direct
+// store instruction of a warp touches 32 rows (32 cache lines).  Instead each
+// epilogue warp stages 32 rows x 128 bytes in its own 4 KB of shared memory
+// (16-byte chunks XOR-swizzled by row: neither the row-wise writes nor the
+// line-wise reads conflict on banks), then writes 4 whole 128-byte lines per
+// store instruction, every row to the destination its owner thread names
+// (nullptr: the row is skipped).  Every lane of the warp takes part.
+// ------------------------------------------------------------------------
+constexpr int kStageWarpBytes = 4096;
+constexpr size_t kStageSmem = 8 * kStageWarpBytes;   // two epilogue warpgroups of 4 warps
+
+MOE_DEV uint8_t* stage_of(uint8_t* extra, int r, int group) {
+  return extra + (group * 4 + (r >> 5)) * kStageWarpBytes;
+}
+MOE_DEV int stage_off(int row, int chunk) { return row * 128 + ((chunk ^ (row & 7)) << 4); }
+
+// 16 fp32 values as bf16 into 32-byte piece q (0..3) of this lane's staged row
+MOE_DEV void stage_bf16x16(uint8_t* st, int lane, int q, const float (&v)[16]) {
+  uint32_t u[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) u[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+  *reinterpret_cast<uint4*>(st + stage_off(lane, 2 * q)) = make_uint4(u[0], u[1], u[2], u[3]);
+  *reinterpret_cast<uint4*>(st + stage_off(lane, 2 * q + 1)) = make_uint4(u[4], u[5], u[6], u[7]);
+}
+
+// 16 fp32 values into 64-byte piece q (0..1) of this lane's staged row
+MOE_DEV void stage_f32x16(uint8_t* st, int lane, int q, const float (&v)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    *reinterpret_cast<uint4*>(st + stage_off(lane, 4 * q + i)) =
+        make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                   __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
+}
+
+// Writes the warp's 32 staged rows: row i (lane i's) to lane i's dst.
+MOE_DEV void stage_flush(const uint8_t* st, int lane, void* dst) {
+  __syncwarp();
+  const unsigned long long d = reinterpret_cast<unsigned long long>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = 4 * i + (lane >> 3), chunk = lane & 7;
+    const unsigned long long p = __shfl_sync(0xffffffffu, d, row);
+    const uint4 v = *reinterpret_cast<const uint4*>(st + stage_off(row, chunk));
+    if (p != 0ull) st_global_v4(reinterpret_cast<char*>(p) + 16 * chunk, v.x, v.y, v.z, v.w);
+  }
+  __syncwarp();
+}
+
+// As stage_flush for fp32 rows, adding them to what dst holds (dst += staged);
+// the eight loads of the old values are issued before any of them is used.
+MOE_DEV void stage_flush_add_f32(const uint8_t* st, int lane, float* dst) {
+  __syncwarp();
+  const unsigned long long d = reinterpret_cast<unsigned long long>(dst);
+  const int chunk = lane & 7;
+  unsigned long long p[8];
+  uint4 o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    p[i] = __shfl_sync(0xffffffffu, d, 4 * i + (lane >> 3));
+    o[i] = p[i] != 0ull ? ld_global_v4(reinterpret_cast<char*>(p[i]) + 16 * chunk)
+                        : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (p[i] == 0ull) continue;
+    const uint4 v = *reinterpret_cast<const uint4*>(st + stage_off(4 * i + (lane >> 3), chunk));
+    st_global_v4(reinterpret_cast<char*>(p[i]) + 16 * chunk,
+                 __float_as_uint(__uint_as_float(o[i].x) + __uint_as_float(v.x)),
+                 __float_as_uint(__uint_as_float(o[i].y) + __uint_as_float(v.y)),
+                 __float_as_uint(__uint_as_float(o[i].z) + __uint_as_float(v.z)),
+                 __float_as_uint(__uint_as_float(o[i].w) + __uint_as_float(v.w)));
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------------
 // F1 + F2 (+ histogram): router logits x·W_r (+ logit_bias), top-k selection
 // with ties to the lower expert id, softmax weights renormalised over the
 // selected experts, and the expert histogram of this 128-token tile.
@@ -140,7 +216,7 @@ struct GateUpFwdProblem {
   static constexpr int BN = 256;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = true;
-  static constexpr size_t kExtraSmem = 0;
+  static constexpr size_t kExtraSmem = kStageSmem;
   static constexpr int kEpiGroups = 2;
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
@@ -157,29 +233,46 @@ struct GateUpFwdProblem {
     tma_load_2d(sB + 3 * kChunkBytes, &a.mapB1, ti.n0 + 64, brow, bar);
   }
   MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
+  // Three sweeps over the group's 64 gate and 64 up accumulator columns, one
+  // per output (h_gate, h_up, a), each leaving through the warp's stage.
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               int group, uint8_t*) {
+                               int group, uint8_t* extra) {
     const bool valid = r < ti.rows;
+    const int lane = r & 31;
+    uint8_t* st = stage_of(extra, r, group);
     const int64_t row = static_cast<int64_t>(ti.m0) + r;
     const int F = a.ld0;
-    __nv_bfloat16* act = static_cast<__nv_bfloat16*>(a.out0) + row * F + ti.n0;
-    __nv_bfloat16* hg = static_cast<__nv_bfloat16*>(a.out1) + row * 2 * F + ti.n0;
-    __nv_bfloat16* hu = hg + F;
+    const int cb = group * 64;
+    __nv_bfloat16* act = valid ? static_cast<__nv_bfloat16*>(a.out0) + row * F + ti.n0 + cb : nullptr;
+    __nv_bfloat16* hg = valid ? static_cast<__nv_bfloat16*>(a.out1) + row * 2 * F + ti.n0 + cb : nullptr;
+    __nv_bfloat16* hu = valid ? hg + F : nullptr;
 #pragma unroll 1
-    for (int c = group * 64; c < group * 64 + 64; c += 16) {
-      float g[16], u[16];
-      tmem_ld16(taddr + c, g);
-      tmem_ld16(taddr + 128 + c, u);
+    for (int q = 0; q < 4; ++q) {
+      float g[16];
+      tmem_ld16(taddr + cb + 16 * q, g);
       tmem_ld_wait();
-      if (valid) {
-        float v[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = g[i] * sigmoidf_fast(g[i]) * u[i];
-        store_bf16x16(act + c, v);
-        store_bf16x16(hg + c, g);
-        store_bf16x16(hu + c, u);
-      }
+      stage_bf16x16(st, lane, q, g);
     }
+    stage_flush(st, lane, hg);
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      float u[16];
+      tmem_ld16(taddr + 128 + cb + 16 * q, u);
+      tmem_ld_wait();
+      stage_bf16x16(st, lane, q, u);
+    }
+    stage_flush(st, lane, hu);
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      float g[16], u[16];
+      tmem_ld16(taddr + cb + 16 * q, g);
+      tmem_ld16(taddr + 128 + cb + 16 * q, u);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) g[i] = g[i] * sigmoidf_fast(g[i]) * u[i];
+      stage_bf16x16(st, lane, q, g);
+    }
+    stage_flush(st, lane, act);
   }
 };
 
@@ -196,7 +289,7 @@ struct DownFwdProblem {
   static constexpr int BN = 256;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = true;
-  static constexpr size_t kExtraSmem = 0;
+  static constexpr size_t kExtraSmem = kStageSmem;
   static constexpr int kEpiGroups = 2;
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
@@ -212,8 +305,10 @@ struct DownFwdProblem {
   }
   MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               int group, uint8_t*) {
+                               int group, uint8_t* extra) {
     const bool valid = r < ti.rows;
+    const int lane = r & 31;
+    uint8_t* st = stage_of(extra, r, group);
     const int64_t row = static_cast<int64_t>(ti.m0) + r;
     float w = 0.f;
     __nv_bfloat16* dst = nullptr;
@@ -223,15 +318,17 @@ struct DownFwdProblem {
       dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 + ti.n0;
     }
 #pragma unroll 1
-    for (int c = group * (BN / 2); c < (group + 1) * (BN / 2); c += 16) {
-      float v[16];
-      tmem_ld16(taddr + c, v);
-      tmem_ld_wait();
-      if (valid) {
+    for (int c0 = group * (BN / 2); c0 < (group + 1) * (BN / 2); c0 += 64) {
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        float v[16];
+        tmem_ld16(taddr + c0 + 16 * q, v);
+        tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 16; ++i) v[i] *= w;
-        store_bf16x16(dst + c, v);
+        stage_bf16x16(st, lane, q, v);
       }
+      stage_flush(st, lane, valid ? dst + c0 : nullptr);
     }
   }
 };

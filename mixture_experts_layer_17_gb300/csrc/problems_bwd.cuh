@@ -126,7 +126,7 @@ struct GateUpDgradProblem {
   static constexpr int BN = 256;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
-  static constexpr size_t kExtraSmem = 0;
+  static constexpr size_t kExtraSmem = kStageSmem;
   static constexpr int kEpiGroups = 2;
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
@@ -144,8 +144,10 @@ struct GateUpDgradProblem {
   }
   MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               int group, uint8_t*) {
+                               int group, uint8_t* extra) {
     const bool valid = r < ti.rows;
+    const int lane = r & 31;
+    uint8_t* st = stage_of(extra, r, group);
     const int64_t row = static_cast<int64_t>(ti.m0) + r;
     __nv_bfloat16* dst = nullptr;
     if (valid) {
@@ -153,11 +155,15 @@ struct GateUpDgradProblem {
       dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 + ti.n0;
     }
 #pragma unroll 1
-    for (int c = group * (BN / 2); c < (group + 1) * (BN / 2); c += 16) {
-      float v[16];
-      tmem_ld16(taddr + c, v);
-      tmem_ld_wait();
-      if (valid) store_bf16x16(dst + c, v);
+    for (int c0 = group * (BN / 2); c0 < (group + 1) * (BN / 2); c0 += 64) {
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        float v[16];
+        tmem_ld16(taddr + c0 + 16 * q, v);
+        tmem_ld_wait();
+        stage_bf16x16(st, lane, q, v);
+      }
+      stage_flush(st, lane, valid ? dst + c0 : nullptr);
     }
   }
 };
@@ -172,7 +178,7 @@ struct DownWgradProblem {
   static constexpr int BN = 256;
   static constexpr bool kAMN = true;
   static constexpr bool kBMN = true;
-  static constexpr size_t kExtraSmem = 0;
+  static constexpr size_t kExtraSmem = kStageSmem;
   static constexpr int kEpiGroups = 2;
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_k_num_tiles(a); }
@@ -197,16 +203,29 @@ struct DownWgradProblem {
       wgrad_zero16(a.out0, out_idx(a, ti, r) + c, acc);
   }
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               int group, uint8_t*) {
+                               int group, uint8_t* extra) {
     const bool valid = r < ti.rows;
     const bool acc = (a.flags & kGemmAccumF32) != 0;
-    const int64_t row = valid ? out_idx(a, ti, r) : 0;
+    const int lane = r & 31;
+    uint8_t* st = stage_of(extra, r, group);
+    const int64_t idx = valid ? out_idx(a, ti, r) : 0;
+    const int step = acc ? 32 : 64;           // columns per 128-byte staged row
 #pragma unroll 1
-    for (int c = group * (BN / 2); c < (group + 1) * (BN / 2); c += 16) {
-      float v[16];
-      tmem_ld16(taddr + c, v);
-      tmem_ld_wait();
-      if (valid) wgrad_store16(a.out0, row + c, acc, v);
+    for (int c0 = group * (BN / 2); c0 < (group + 1) * (BN / 2); c0 += step) {
+#pragma unroll 1
+      for (int q = 0; q < step / 16; ++q) {
+        float v[16];
+        tmem_ld16(taddr + c0 + 16 * q, v);
+        tmem_ld_wait();
+        if (acc)
+          stage_f32x16(st, lane, q, v);
+        else
+          stage_bf16x16(st, lane, q, v);
+      }
+      if (acc)
+        stage_flush_add_f32(st, lane, valid ? static_cast<float*>(a.out0) + idx + c0 : nullptr);
+      else
+        stage_flush(st, lane, valid ? static_cast<__nv_bfloat16*>(a.out0) + idx + c0 : nullptr);
     }
   }
 };
@@ -222,7 +241,7 @@ struct GateUpWgradProblem {
   static constexpr int BN = 256;
   static constexpr bool kAMN = true;
   static constexpr bool kBMN = true;
-  static constexpr size_t kExtraSmem = 0;
+  static constexpr size_t kExtraSmem = kStageSmem;
   static constexpr int kEpiGroups = 2;
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_k_num_tiles(a); }
@@ -256,20 +275,31 @@ struct GateUpWgradProblem {
     }
   }
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               int group, uint8_t*) {
+                               int group, uint8_t* extra) {
     const bool valid = r < ti.rows;
     const bool acc = (a.flags & kGemmAccumF32) != 0;
+    const int lane = r & 31;
+    uint8_t* st = stage_of(extra, r, group);
+    const int step = acc ? 32 : 64;           // columns per 128-byte staged row
 #pragma unroll 1
-    for (int c = group * (BN / 2); c < (group + 1) * (BN / 2); c += 16) {
-      float v[16];
-      tmem_ld16(taddr + c, v);
-      tmem_ld_wait();
-      if (valid) {
-        void* base;
-        int64_t idx;
-        out_loc(a, ti, r, ti.n0 + c, base, idx);
-        wgrad_store16(base, idx, acc, v);
+    for (int c0 = group * (BN / 2); c0 < (group + 1) * (BN / 2); c0 += step) {
+#pragma unroll 1
+      for (int q = 0; q < step / 16; ++q) {
+        float v[16];
+        tmem_ld16(taddr + c0 + 16 * q, v);
+        tmem_ld_wait();
+        if (acc)
+          stage_f32x16(st, lane, q, v);
+        else
+          stage_bf16x16(st, lane, q, v);
       }
+      void* base;
+      int64_t idx;
+      out_loc(a, ti, r, ti.n0 + c0, base, idx);   // 64 columns never straddle the gate / up split
+      if (acc)
+        stage_flush_add_f32(st, lane, valid ? static_cast<float*>(base) + idx : nullptr);
+      else
+        stage_flush(st, lane, valid ? static_cast<__nv_bfloat16*>(base) + idx : nullptr);
     }
   }
 };
