@@ -297,13 +297,16 @@ def blas_threads() -> int:
 def cpu_baseline(sh, inp, budget_s: float = 20.0):
     """Oracle throughput on a bounded sample of the same workload."""
     inp_cpu = host_copy_for_oracle(inp)
+    # grow the sample until one timing takes about budget_s / 2 (the cost is
+    # not linear in small samples: every touched expert's weights are widened)
     n = 8
     dt = oracle_sample_time(sh, inp_cpu, n)
-    # grow the sample to about budget_s / 2 of work, then time it once more
-    target = int(n * max(1.0, (budget_s / 2) / max(dt, 1e-3)))
-    n2 = max(n, min(sh.T, target))
-    if n2 > n:
-        n, dt = n2, oracle_sample_time(sh, inp_cpu, n2)
+    for _ in range(4):
+        if dt >= 0.35 * budget_s or n >= sh.T:
+            break
+        grow = min(8.0, (0.5 * budget_s) / max(dt, 1e-3))
+        n = min(sh.T, max(n + 1, int(n * grow)))
+        dt = oracle_sample_time(sh, inp_cpu, n)
     return {"value": n / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
             "sample": f"first {n} of {sh.T} tokens of {sh.name}: route + fwd + full bwd in "
                       f"numpy fp64 ({dt:.1f} s)"}
