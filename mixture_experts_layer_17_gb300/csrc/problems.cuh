@@ -61,6 +61,63 @@ MOE_DEV void stage_flush(const uint8_t* st, int lane, void* dst) {
   __syncwarp();
 }
 
+// Half-size stage for kernels with less shared memory to spare (MXFP8): 32
+// rows x 64 bytes per warp, chunk j of row r at r * 64 + 16 * (j ^ ((r >> 1) & 3))
+// (a quarter-warp's eight rows x one chunk, or two rows x four chunks, hit
+// eight distinct bank groups); a store instruction writes 8 half-lines.
+constexpr int kStage64WarpBytes = 2048;
+constexpr size_t kStage64Smem = 8 * kStage64WarpBytes;
+
+MOE_DEV uint8_t* stage64_of(uint8_t* extra, int r, int group) {
+  return extra + (group * 4 + (r >> 5)) * kStage64WarpBytes;
+}
+MOE_DEV int stage64_off(int row, int chunk) { return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4); }
+
+// 16 fp32 values as bf16 into 32-byte piece q (0..1) of this lane's staged row
+MOE_DEV void stage64_bf16x16(uint8_t* st, int lane, int q, const float* v) {
+  uint32_t u[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) u[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+  *reinterpret_cast<uint4*>(st + stage64_off(lane, 2 * q)) = make_uint4(u[0], u[1], u[2], u[3]);
+  *reinterpret_cast<uint4*>(st + stage64_off(lane, 2 * q + 1)) = make_uint4(u[4], u[5], u[6], u[7]);
+}
+
+// 16 fp32 values into this lane's staged row (all four chunks)
+MOE_DEV void stage64_f32x16(uint8_t* st, int lane, const float* v) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    *reinterpret_cast<uint4*>(st + stage64_off(lane, i)) =
+        make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                   __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3]));
+}
+
+// Writes the warp's 32 staged 64-byte rows (fp32 rows added to dst when add)
+MOE_DEV void stage64_flush(const uint8_t* st, int lane, void* dst, bool add) {
+  __syncwarp();
+  const unsigned long long d = reinterpret_cast<unsigned long long>(dst);
+  const int chunk = lane & 3;
+  unsigned long long p[4];
+  uint4 o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    p[i] = __shfl_sync(0xffffffffu, d, 8 * i + (lane >> 2));
+    o[i] = (add && p[i] != 0ull) ? ld_global_v4(reinterpret_cast<char*>(p[i]) + 16 * chunk)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (p[i] == 0ull) continue;
+    uint4 v = *reinterpret_cast<const uint4*>(st + stage64_off(8 * i + (lane >> 2), chunk));
+    if (add)
+      v = make_uint4(__float_as_uint(__uint_as_float(o[i].x) + __uint_as_float(v.x)),
+                     __float_as_uint(__uint_as_float(o[i].y) + __uint_as_float(v.y)),
+                     __float_as_uint(__uint_as_float(o[i].z) + __uint_as_float(v.z)),
+                     __float_as_uint(__uint_as_float(o[i].w) + __uint_as_float(v.w)));
+    st_global_v4(reinterpret_cast<char*>(p[i]) + 16 * chunk, v.x, v.y, v.z, v.w);
+  }
+  __syncwarp();
+}
+
 // As stage_flush for fp32 rows, adding them to what dst holds (dst += staged);
 // the eight loads of the old values are issued before any of them is used.
 MOE_DEV void stage_flush_add_f32(const uint8_t* st, int lane, float* dst) {

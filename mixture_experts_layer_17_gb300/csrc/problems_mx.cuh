@@ -108,7 +108,7 @@ struct GateUpFwdMXProblem {
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = true;
   static constexpr bool kMX = true;
-  static constexpr size_t kExtraSmem = 0;
+  static constexpr size_t kExtraSmem = kStage64Smem;
   static constexpr int kEpiGroups = 2;
   struct Frag {
     float v[128];   // [0, 64): gate, [64, 128): up
@@ -134,27 +134,45 @@ struct GateUpFwdMXProblem {
     tmem_ld128(taddr + 128 * group, f.v);
   }
   MOE_DEV static void epilogue_store(const GemmArgs& a, const TileInfo& ti, int r, int group,
-                                     Frag& f, uint8_t*) {
-    if (r >= ti.rows) return;
+                                     Frag& f, uint8_t* extra) {
+    const bool valid = r < ti.rows;
     const int64_t row = static_cast<int64_t>(ti.m0) + r;
+    const int lane = r & 31;
+    uint8_t* st = stage64_of(extra, r, group);
     const int F = a.ld0;
     const int f0 = ti.n0 + 64 * group;        // first F column of this group
     __nv_bfloat16* hg = static_cast<__nv_bfloat16*>(a.out1) + row * 2 * F + f0;
+    // h_gate then h_up, 32 columns (64 bytes) per staged row
 #pragma unroll
-    for (int i = 0; i < 64; i += 16) {
-      store_bf16x16(hg + i, *reinterpret_cast<const float(*)[16]>(f.v + i));
-      store_bf16x16(hg + F + i, *reinterpret_cast<const float(*)[16]>(f.v + 64 + i));
+    for (int c = 0; c < 128; c += 32) {
+      stage64_bf16x16(st, lane, 0, f.v + c);
+      stage64_bf16x16(st, lane, 1, f.v + c + 16);
+      stage64_flush(st, lane, valid ? hg + (c < 64 ? c : F + c - 64) : nullptr, false);
     }
 #pragma unroll
     for (int i = 0; i < 64; ++i) f.v[i] = f.v[i] * sigmoidf_fast(f.v[i]) * f.v[64 + i];
-    uint8_t* aq = static_cast<uint8_t*>(a.out0) + row * F + f0;
+    // a: two MX blocks of 32 columns -> 64 E4M3 bytes (staged) and two scale bytes
     uint8_t* sf = static_cast<uint8_t*>(a.out2) +
                   ((static_cast<int64_t>(__ldg(a.mtile_off + ti.e)) + ti.mt) * (F / 128) + f0 / 128) * 512;
-    mx_block_store(*reinterpret_cast<const float(*)[32]>(f.v), aq, sf + sf_atom_offset(r, (f0 >> 5) & 3));
-    mx_block_store(*reinterpret_cast<const float(*)[32]>(f.v + 32), aq + 32,
-                   sf + sf_atom_offset(r, ((f0 >> 5) & 3) + 1));
+#pragma unroll
+    for (int blk2 = 0; blk2 < 2; ++blk2) {
+      const float* v = f.v + 32 * blk2;
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      const int X = mx_exponent(amax);
+      const float inv = ldexpf(1.0f, -X);
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = to_e4m3x4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], inv);
+      *reinterpret_cast<uint4*>(st + stage64_off(lane, 2 * blk2)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(st + stage64_off(lane, 2 * blk2 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+      if (valid) sf[sf_atom_offset(r, ((f0 >> 5) & 3) + blk2)] = static_cast<uint8_t>(X + 127);
+    }
+    stage64_flush(st, lane, valid ? static_cast<uint8_t*>(a.out0) + row * F + f0 : nullptr, false);
   }
 };
+
 
 // F9 + F10 in MXFP8: A = a E4M3 [P, F]; B = W_down quantised along F
 // ([E*F, H], MN-major); 128 x 256 tiles, weighted scatter epilogue.
@@ -163,7 +181,7 @@ struct DownFwdMXProblem {
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = true;
   static constexpr bool kMX = true;
-  static constexpr size_t kExtraSmem = 0;
+  static constexpr size_t kExtraSmem = kStage64Smem;
   static constexpr int kEpiGroups = 2;
   struct Frag {
     float v[128];
@@ -188,19 +206,30 @@ struct DownFwdMXProblem {
     tmem_ld128(taddr + 128 * group, f.v);
   }
   MOE_DEV static void epilogue_store(const GemmArgs& a, const TileInfo& ti, int r, int group,
-                                     Frag& f, uint8_t*) {
-    if (r >= ti.rows) return;
+                                     Frag& f, uint8_t* extra) {
+    const bool valid = r < ti.rows;
     const int64_t row = static_cast<int64_t>(ti.m0) + r;
-    const float w = __ldg(static_cast<const float*>(a.in0) + row);
-    const int slot = __ldg(static_cast<const int*>(a.in1) + row);
-    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 +
-                         ti.n0 + 128 * group;
+    const int lane = r & 31;
+    uint8_t* st = stage64_of(extra, r, group);
+    float w = 0.f;
+    __nv_bfloat16* dst = nullptr;
+    if (valid) {
+      w = __ldg(static_cast<const float*>(a.in0) + row);
+      const int slot = __ldg(static_cast<const int*>(a.in1) + row);
+      dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 + ti.n0 +
+            128 * group;
+    }
 #pragma unroll
     for (int i = 0; i < 128; ++i) f.v[i] *= w;
 #pragma unroll
-    for (int i = 0; i < 128; i += 16) store_bf16x16(dst + i, *reinterpret_cast<const float(*)[16]>(f.v + i));
+    for (int c = 0; c < 128; c += 32) {
+      stage64_bf16x16(st, lane, 0, f.v + c);
+      stage64_bf16x16(st, lane, 1, f.v + c + 16);
+      stage64_flush(st, lane, valid ? dst + c : nullptr, false);
+    }
   }
 };
+
 
 // B2-B4 in MXFP8: A = dY_perm E4M3 [P, H]; B = W_down quantised along H
 // ([E*F, H], K-major); the SwiGLU-backward epilogue of DownDgradProblem: dh
@@ -299,6 +328,7 @@ struct DownDgradMXProblem {
   }
 };
 
+
 // B6 in MXFP8: A = dh E4M3 [P, 2F] (each half quantised along F); B = W_gate
 // then W_up quantised along F ([E*H, F], K-major); 128 x 256 tiles, scatter
 // epilogue.
@@ -307,7 +337,7 @@ struct GateUpDgradMXProblem {
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
   static constexpr bool kMX = true;
-  static constexpr size_t kExtraSmem = 0;
+  static constexpr size_t kExtraSmem = kStage64Smem;
   static constexpr int kEpiGroups = 2;
   struct Frag {
     float v[128];
@@ -336,16 +366,26 @@ struct GateUpDgradMXProblem {
     tmem_ld128(taddr + 128 * group, f.v);
   }
   MOE_DEV static void epilogue_store(const GemmArgs& a, const TileInfo& ti, int r, int group,
-                                     Frag& f, uint8_t*) {
-    if (r >= ti.rows) return;
+                                     Frag& f, uint8_t* extra) {
+    const bool valid = r < ti.rows;
     const int64_t row = static_cast<int64_t>(ti.m0) + r;
-    const int slot = __ldg(static_cast<const int*>(a.in1) + row);
-    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 +
-                         ti.n0 + 128 * group;
+    const int lane = r & 31;
+    uint8_t* st = stage64_of(extra, r, group);
+    __nv_bfloat16* dst = nullptr;
+    if (valid) {
+      const int slot = __ldg(static_cast<const int*>(a.in1) + row);
+      dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 + ti.n0 +
+            128 * group;
+    }
 #pragma unroll
-    for (int i = 0; i < 128; i += 16) store_bf16x16(dst + i, *reinterpret_cast<const float(*)[16]>(f.v + i));
+    for (int c = 0; c < 128; c += 32) {
+      stage64_bf16x16(st, lane, 0, f.v + c);
+      stage64_bf16x16(st, lane, 1, f.v + c + 16);
+      stage64_flush(st, lane, valid ? dst + c : nullptr, false);
+    }
   }
 };
+
 
 // Weight gradients in MXFP8 over the padded token layout (both operands
 // MN-major, quantised along tokens per expert segment); 128 x 256 tiles.
@@ -358,7 +398,7 @@ struct WgradMXProblem {
   static constexpr bool kAMN = true;
   static constexpr bool kBMN = true;
   static constexpr bool kMX = true;
-  static constexpr size_t kExtraSmem = 0;
+  static constexpr size_t kExtraSmem = kStage64Smem;
   static constexpr int kEpiGroups = 2;
   struct Frag {
     float v[128];
@@ -403,17 +443,33 @@ struct WgradMXProblem {
     tmem_ld128(taddr + 128 * group, f.v);
   }
   MOE_DEV static void epilogue_store(const GemmArgs& a, const TileInfo& ti, int r, int group,
-                                     Frag& f, uint8_t*) {
-    if (r >= ti.rows) return;
+                                     Frag& f, uint8_t* extra) {
+    const bool valid = r < ti.rows;
     const bool acc = (a.flags & kGemmAccumF32) != 0;
+    const int lane = r & 31;
+    uint8_t* st = stage64_of(extra, r, group);
     void* base;
     int64_t idx;
-    out_loc(a, ti, r, ti.n0 + 128 * group, base, idx);
+    out_loc(a, ti, r, ti.n0 + 128 * group, base, idx);   // 128 columns never straddle F
+    if (acc) {
+      float* dst = static_cast<float*>(base) + idx;
 #pragma unroll
-    for (int c = 0; c < 128; c += 16)
-      wgrad_store16(base, idx + c, acc, *reinterpret_cast<const float(*)[16]>(f.v + c));
+      for (int c = 0; c < 128; c += 16) {
+        stage64_f32x16(st, lane, f.v + c);
+        stage64_flush(st, lane, valid ? dst + c : nullptr, true);
+      }
+    } else {
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(base) + idx;
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) {
+        stage64_bf16x16(st, lane, 0, f.v + c);
+        stage64_bf16x16(st, lane, 1, f.v + c + 16);
+        stage64_flush(st, lane, valid ? dst + c : nullptr, false);
+      }
+    }
   }
 };
+
 
 // Dense MXFP8 GEMM for moe_gemm_mxfp8: A [M, K] and B [N, K] E4M3 (K-major),
 // atoms (m-tile * kt + k-tile) and (n-tile * kt + k-tile); D fp32 [M, N].
