@@ -71,6 +71,7 @@ MX_SHAPES = [
     (300, 256, 256, 8, 2, 51),      # ragged tiles, few experts
     (517, 512, 384, 16, 4, 52),     # F = 3 x 128, several tiles per expert
     (200, 256, 128, 4, 1, 53),      # top-1
+    (1, 256, 256, 4, 2, 55),        # a single token
 ]
 
 

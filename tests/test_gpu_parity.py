@@ -40,6 +40,8 @@ def _full_compare(sh, inp, out):
     print(sh, {k: f"{v:.2e}" for k, v in errs.items()})
     for name, e in errs.items():
         if name == "dW_r" and sh.top_k == 1:
+            # top-1: w = 1 exactly, so dl = w (dw - w dw) = 0 and dW_r is exactly zero
+            assert np.all(out["dW_r"] == 0.0)
             continue
         assert e <= BF16_TOL, (name, e)
     # experts without tokens get exactly-zero weight gradients
@@ -62,6 +64,8 @@ SWEEP = [
     (64, 256, 128, 4, 4, 13),       # top_k = E: dense softmax mixture
     (517, 768, 256, 32, 8, 14),     # several tiles per expert, ragged tails
     (129, 256, 512, 256, 16, 15),   # E = 256, top-16: router N = 256
+    (1, 256, 128, 8, 2, 16),        # a single token: two rows in two experts
+    (100, 256, 128, 1, 1, 17),      # one expert, top-1: a plain SwiGLU FFN, w = 1, dW_r = 0
 ]
 
 
