@@ -118,6 +118,12 @@ typedef struct {
                           the same for every budget except dW_r,
                           whose split-K depth follows the budget
                           (summation order only).  Must be >= 0. */
+  const void* prepared_weights; /* MXFP8 and FP8_BWD: NULL, or a buffer
+                          written by moe_prepare_weights for these
+                          weights; the MXFP8 GEMMs then read it
+                          instead of quantising W_gate, W_up and
+                          W_down in every call.  Ignored for BF16.
+                          256-byte aligned. */
 } moe_config_t;
 
 /* Bytes of device memory each call needs from the caller:
@@ -169,6 +175,21 @@ moe_status_t moe_backward(const moe_config_t* cfg, const moe_bf16_t* x, const mo
                           moe_bf16_t* dx, moe_bf16_t* dW_r, moe_bf16_t* dW_gate,
                           moe_bf16_t* dW_up, moe_bf16_t* dW_down, void* ws, size_t ws_bytes,
                           moe_stream_t stream);
+
+/* MXFP8 weight preparation ("Supporto di precisione" on roccomilluzzo.it
+ * names MXFP8 training; the weights change once per optimizer step, however
+ * many micro-batches share them).  Quantises W_gate, W_up and W_down (bf16,
+ * the layouts above) into wq, in every orientation the MXFP8 GEMMs read:
+ * W_gate / W_up along H (forward) and along F (backward), W_down along F
+ * (forward) and along H (backward); E4M3 elements with E8M0 scale atoms, the
+ * same bytes the calls would compute themselves.  Point
+ * cfg->prepared_weights at wq for the forward and backward calls that use
+ * these weights; prepare again after the weights change.  cfg->precision
+ * must be MOE_MXFP8 or MOE_FP8_BWD.  *bytes receives the size wq needs. */
+moe_status_t moe_prepared_weights_size(const moe_config_t* cfg, size_t* bytes);
+moe_status_t moe_prepare_weights(const moe_config_t* cfg, const moe_bf16_t* W_gate,
+                                 const moe_bf16_t* W_up, const moe_bf16_t* W_down, void* wq,
+                                 size_t wq_bytes, moe_stream_t stream);
 
 /* moe_backward for gradient accumulation over micro-batches (the end-to-end
  * runs of "Os Números..." on bitsgeniais.com.br train on micro-batches of

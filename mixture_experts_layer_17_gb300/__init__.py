@@ -73,6 +73,20 @@ class MoeLayer:
                      self.bwd_ws, stream)
         return grads
 
+    def prepare_weights(self, W_gate, W_up, W_down, stream=None) -> torch.Tensor:
+        """MXFP8 / FP8_BWD: quantise the expert weights once (every orientation
+        the GEMMs read) and let the following forward and backward calls use
+        them; call again whenever the weights change.  Returns the buffer."""
+        n = libmoe.moe_prepared_weights_size(self.cfg)
+        self.wq = torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
+        libmoe.moe_prepare_weights(self.cfg, W_gate, W_up, W_down, self.wq, stream)
+        self.cfg.prepared_weights = self.wq.data_ptr()
+        return self.wq
+
+    def drop_prepared_weights(self) -> None:
+        self.cfg.prepared_weights = None
+        self.wq = None
+
     def backward_accumulate(self, x, W_r, W_gate, W_up, W_down, dY, acc: Dict[str, torch.Tensor],
                             dx: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
         """Adds the weight gradients into the fp32 tensors acc["dW_r"],

@@ -204,6 +204,9 @@ struct Layout {
   size_t fq_x, fs_x, fq_a, fs_a, fq_wgu, fs_wgu, fq_wd, fs_wd;
   size_t bq_dy, bs_dy, bq_wdh, bs_wdh, bq_dh, bs_dh, bq_wg, bs_wg, bq_wu, bs_wu;
   size_t bq_awt, bs_awt, bq_dyt, bs_dyt, bq_xt, bs_xt, bq_dht, bs_dht;
+  // prepared MXFP8 weights (moe_prepare_weights): every orientation the GEMMs read
+  bool prepared;
+  size_t q_gu_h, qs_gu_h, q_d_f, qs_d_f, q_g_f, qs_g_f, q_u_f, qs_u_f, q_d_h, qs_d_h, q_total;
 };
 
 Layout make_layout(const moe_config_t& c, int sms) {
@@ -237,6 +240,7 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.pair_down_wgrad = bb && pp && (L.F % 256 == 0);
   L.pair_gu_wgrad = bb && pp;
   L.recompute = (c.flags & MOE_FLAG_RECOMPUTE) != 0;
+  L.prepared = c.precision != MOE_BF16 && c.prepared_weights != nullptr;
   L.ntiles = static_cast<int>((L.T + kBM - 1) / kBM);
   L.router_bn = next_pow2_at_least16(L.E);
   L.dgrad_bn = (L.F % 256 == 0) ? 256 : 128;
@@ -279,10 +283,12 @@ Layout make_layout(const moe_config_t& c, int sms) {
     L.fs_x = f.take(mt * (H / 128) * 512);
     L.fq_a = f.take(Pa * F);
     L.fs_a = f.take(mt * (F / 128) * 512);
-    L.fq_wgu = f.take(E * H * 2 * F);
-    L.fs_wgu = f.take(E * (2 * F / 128) * (H / 128) * 512);
-    L.fq_wd = f.take(E * F * H);
-    L.fs_wd = f.take(E * (H / 128) * (F / 128) * 512);
+    if (!L.prepared) {
+      L.fq_wgu = f.take(E * H * 2 * F);
+      L.fs_wgu = f.take(E * (2 * F / 128) * (H / 128) * 512);
+      L.fq_wd = f.take(E * F * H);
+      L.fs_wd = f.take(E * (H / 128) * (F / 128) * 512);
+    }
   }
   L.f_total = f.off;
 
@@ -325,8 +331,10 @@ Layout make_layout(const moe_config_t& c, int sms) {
       L.bs_rx = b.take(mt * (H / 128) * 512);
       L.bq_ra = b.take(Pa * F);
       L.bs_ra = b.take(mt * (F / 128) * 512);
-      L.bq_rwgu = b.take(E * H * 2 * F);
-      L.bs_rwgu = b.take(E * (2 * F / 128) * (H / 128) * 512);
+      if (!L.prepared) {
+        L.bq_rwgu = b.take(E * H * 2 * F);
+        L.bs_rwgu = b.take(E * (2 * F / 128) * (H / 128) * 512);
+      }
     }
   }
   if (c.precision != MOE_BF16) {
@@ -335,12 +343,14 @@ Layout make_layout(const moe_config_t& c, int sms) {
     L.bs_dy = b.take(mt * (H / 128) * 512);
     L.bq_dh = b.take(Pa * 2 * F);
     L.bs_dh = b.take(mt * (2 * F / 128) * 512);
-    L.bq_wdh = b.take(E * F * H);
-    L.bs_wdh = b.take(E * (F / 128) * (H / 128) * 512);
-    L.bq_wg = b.take(E * H * F);
-    L.bs_wg = b.take(E * (H / 128) * (F / 128) * 512);
-    L.bq_wu = b.take(E * H * F);
-    L.bs_wu = b.take(E * (H / 128) * (F / 128) * 512);
+    if (!L.prepared) {
+      L.bq_wdh = b.take(E * F * H);
+      L.bs_wdh = b.take(E * (F / 128) * (H / 128) * 512);
+      L.bq_wg = b.take(E * H * F);
+      L.bs_wg = b.take(E * (H / 128) * (F / 128) * 512);
+      L.bq_wu = b.take(E * H * F);
+      L.bs_wu = b.take(E * (H / 128) * (F / 128) * 512);
+    }
     L.bq_awt = b.take(Pp * F);
     L.bs_awt = b.take(mt * (F / 128) * 512);
     L.bq_dyt = b.take(Pp * H);
@@ -351,6 +361,19 @@ Layout make_layout(const moe_config_t& c, int sms) {
     L.bs_dht = b.take(mt * (2 * F / 128) * 512);
   }
   L.b_total = b.off;
+
+  Carver q;   // moe_prepare_weights buffer
+  L.q_gu_h = q.take(E * H * 2 * F);
+  L.qs_gu_h = q.take(E * (2 * F / 128) * (H / 128) * 512);
+  L.q_d_f = q.take(E * F * H);
+  L.qs_d_f = q.take(E * (H / 128) * (F / 128) * 512);
+  L.q_g_f = q.take(E * H * F);
+  L.qs_g_f = q.take(E * (H / 128) * (F / 128) * 512);
+  L.q_u_f = q.take(E * H * F);
+  L.qs_u_f = q.take(E * (H / 128) * (F / 128) * 512);
+  L.q_d_h = q.take(E * F * H);
+  L.qs_d_h = q.take(E * (F / 128) * (H / 128) * 512);
+  L.q_total = q.off;
   (void)T;
   return L;
 }
@@ -361,6 +384,9 @@ moe_status_t validate(const moe_config_t* c) {
                    MOE_FLAG_CTA_PAIRS_ON | MOE_FLAG_RECOMPUTE))
     return MOE_ERR_INVALID_ARG;
   if (c->max_sms < 0) return MOE_ERR_INVALID_ARG;
+  if (c->prepared_weights != nullptr &&
+      (reinterpret_cast<uintptr_t>(c->prepared_weights) & 255u) != 0)
+    return MOE_ERR_INVALID_ARG;
   if ((c->flags & MOE_FLAG_CTA_PAIRS_OFF) && (c->flags & MOE_FLAG_CTA_PAIRS_ON))
     return MOE_ERR_INVALID_ARG;
   if (c->precision < MOE_BF16 || c->precision > MOE_FP8_BWD) return MOE_ERR_INVALID_ARG;
@@ -525,6 +551,7 @@ moe_status_t gate_up_fwd_bf16(const Layout& L, int sms, cudaStream_t s, uint32_t
 struct MxGateUpBufs {
   uint8_t *xq, *sx, *aq, *sa, *wgu, *swgu;
   bool x_ready = false;   // xq / sx already written by the fused gather
+  bool w_ready = false;   // wgu / swgu prepared by moe_prepare_weights
 };
 
 // F7 + F8 in MXFP8: quantise x_perm along H and W_gate / W_up along H
@@ -540,9 +567,11 @@ moe_status_t gate_up_fwd_mx(const Layout& L, int sms, cudaStream_t s, uint32_t f
       return launch_quant_rows_permuted(xperm, L.Pa, L.H, q.xq, q.sx, offsets, mtile, L.E, s);
     }));
   }
-  MOE_TRY(run(recompute ? "recompute_mx_quant_w_gate_up" : "mx_quant_w_gate_up", s, fl, [&] {
-    return launch_quant_cols_gate_up(W_gate, W_up, L.E, L.H, L.F, q.wgu, q.swgu, s);
-  }));
+  if (!q.w_ready) {
+    MOE_TRY(run(recompute ? "recompute_mx_quant_w_gate_up" : "mx_quant_w_gate_up", s, fl, [&] {
+      return launch_quant_cols_gate_up(W_gate, W_up, L.E, L.H, L.F, q.wgu, q.swgu, s);
+    }));
+  }
   GemmArgs a = base_args(st, fl);
   if (!make_map_u8(&a.mapA, q.xq, L.H, L.Pa, L.H) ||
       !make_map_u8(&a.mapB0, q.wgu, 2ull * L.F, static_cast<uint64_t>(L.E) * L.H, 2ull * L.F))
@@ -580,20 +609,31 @@ moe_status_t forward_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t
                               const uint16_t* W_up, const uint16_t* W_down, const int* offsets,
                               const int* counts, const int* mtile, const float* w_row,
                               const int* row_slot,
-                              uint16_t* act, uint16_t* h, uint16_t* scratch, void* ws) {
+                              uint16_t* act, uint16_t* h, uint16_t* scratch, void* ws,
+                              void* wq) {
   (void)act;
   MxGateUpBufs q{at<uint8_t>(ws, L.fq_x), at<uint8_t>(ws, L.fs_x), at<uint8_t>(ws, L.fq_a),
-                 at<uint8_t>(ws, L.fs_a), at<uint8_t>(ws, L.fq_wgu), at<uint8_t>(ws, L.fs_wgu)};
+                 at<uint8_t>(ws, L.fs_a), nullptr, nullptr};
   q.x_ready = true;   // moe_forward's gather quantised x_perm along H
+  if (wq != nullptr) {
+    q.wgu = at<uint8_t>(wq, L.q_gu_h);
+    q.swgu = at<uint8_t>(wq, L.qs_gu_h);
+    q.w_ready = true;
+  } else {
+    q.wgu = at<uint8_t>(ws, L.fq_wgu);
+    q.swgu = at<uint8_t>(ws, L.fs_wgu);
+  }
   uint8_t* aq = q.aq;
   uint8_t* sa = q.sa;
-  uint8_t* wd = at<uint8_t>(ws, L.fq_wd);
-  uint8_t* swd = at<uint8_t>(ws, L.fs_wd);
+  uint8_t* wd = wq != nullptr ? at<uint8_t>(wq, L.q_d_f) : at<uint8_t>(ws, L.fq_wd);
+  uint8_t* swd = wq != nullptr ? at<uint8_t>(wq, L.qs_d_f) : at<uint8_t>(ws, L.fs_wd);
   MOE_TRY(gate_up_fwd_mx(L, sms, s, fl, st, xperm, W_gate, W_up, offsets, counts, mtile, h, q,
                          false));
-  MOE_TRY(run("mx_quant_w_down_f", s, fl, [&] {
-    return launch_quant_cols_weights(W_down, L.E, L.F, L.H, wd, swd, s);
-  }));
+  if (wq == nullptr) {
+    MOE_TRY(run("mx_quant_w_down_f", s, fl, [&] {
+      return launch_quant_cols_weights(W_down, L.E, L.F, L.H, wd, swd, s);
+    }));
+  }
   {
     GemmArgs a = base_args(st, fl);
     if (!make_map_u8(&a.mapA, aq, L.F, L.Pa, L.F) ||
@@ -635,6 +675,7 @@ struct BwdBufs {
   void *dW_gate, *dW_up, *dW_down;   // bf16, or fp32 accumulation buffers
   void* ws;
   uint32_t wflags;                   // kGemmAccumF32 or 0, for the weight gradients
+  void* wq;                          // prepared MXFP8 weights, or nullptr
 };
 
 // B2-B9 in MXFP8 (precision mxfp8 and fp8_bwd): every expert GEMM of the
@@ -647,14 +688,15 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
   void* ws = b.ws;
   uint8_t* dyq = at<uint8_t>(ws, L.bq_dy);
   uint8_t* sdy = at<uint8_t>(ws, L.bs_dy);
-  uint8_t* wdh = at<uint8_t>(ws, L.bq_wdh);
-  uint8_t* swdh = at<uint8_t>(ws, L.bs_wdh);
+  const bool prep = b.wq != nullptr;
+  uint8_t* wdh = prep ? at<uint8_t>(b.wq, L.q_d_h) : at<uint8_t>(ws, L.bq_wdh);
+  uint8_t* swdh = prep ? at<uint8_t>(b.wq, L.qs_d_h) : at<uint8_t>(ws, L.bs_wdh);
   uint8_t* dhq = at<uint8_t>(ws, L.bq_dh);
   uint8_t* sdh = at<uint8_t>(ws, L.bs_dh);
-  uint8_t* wg = at<uint8_t>(ws, L.bq_wg);
-  uint8_t* swg = at<uint8_t>(ws, L.bs_wg);
-  uint8_t* wu = at<uint8_t>(ws, L.bq_wu);
-  uint8_t* swu = at<uint8_t>(ws, L.bs_wu);
+  uint8_t* wg = prep ? at<uint8_t>(b.wq, L.q_g_f) : at<uint8_t>(ws, L.bq_wg);
+  uint8_t* swg = prep ? at<uint8_t>(b.wq, L.qs_g_f) : at<uint8_t>(ws, L.bs_wg);
+  uint8_t* wu = prep ? at<uint8_t>(b.wq, L.q_u_f) : at<uint8_t>(ws, L.bq_wu);
+  uint8_t* swu = prep ? at<uint8_t>(b.wq, L.qs_u_f) : at<uint8_t>(ws, L.bs_wu);
   uint8_t* awt = at<uint8_t>(ws, L.bq_awt);
   uint8_t* sawt = at<uint8_t>(ws, L.bs_awt);
   uint8_t* dyt = at<uint8_t>(ws, L.bq_dyt);
@@ -667,9 +709,11 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
   const int64_t mtiles = (L.P + kBM - 1) / kBM + L.E;
 
   // B2-B4: down dgrad (dY_perm was quantised along H by the fused gather)
-  MOE_TRY(run("mx_quant_w_down_h", s, fl, [&] {
-    return launch_quant_rows_dense(b.W_down, static_cast<int64_t>(L.E) * L.F, L.H, wdh, swdh, s);
-  }));
+  if (!prep) {
+    MOE_TRY(run("mx_quant_w_down_h", s, fl, [&] {
+      return launch_quant_rows_dense(b.W_down, static_cast<int64_t>(L.E) * L.F, L.H, wdh, swdh, s);
+    }));
+  }
   {
     GemmArgs a = base_args(st, fl);
     if (!make_map_u8(&a.mapA, dyq, L.H, L.Pa, L.H) ||
@@ -741,12 +785,14 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     MOE_TRY(run("down_wgrad_mx", s, fl, [&] { return launch_down_wgrad_mx(a, grid, s); }));
   }
   // B6 + B7: gate/up dgrad, then the un-permute
-  MOE_TRY(run("mx_quant_w_gate_f", s, fl, [&] {
-    return launch_quant_rows_dense(b.W_gate, static_cast<int64_t>(L.E) * L.H, L.F, wg, swg, s);
-  }));
-  MOE_TRY(run("mx_quant_w_up_f", s, fl, [&] {
-    return launch_quant_rows_dense(b.W_up, static_cast<int64_t>(L.E) * L.H, L.F, wu, swu, s);
-  }));
+  if (!prep) {
+    MOE_TRY(run("mx_quant_w_gate_f", s, fl, [&] {
+      return launch_quant_rows_dense(b.W_gate, static_cast<int64_t>(L.E) * L.H, L.F, wg, swg, s);
+    }));
+    MOE_TRY(run("mx_quant_w_up_f", s, fl, [&] {
+      return launch_quant_rows_dense(b.W_up, static_cast<int64_t>(L.E) * L.H, L.F, wu, swu, s);
+    }));
+  }
   {
     GemmArgs a = base_args(st, fl);
     if (!make_map_u8(&a.mapA, dhq, 2ull * L.F, L.Pa, 2ull * L.F) ||
@@ -843,6 +889,50 @@ moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* fwd_ws, size_t*
   return MOE_OK;
 }
 
+moe_status_t moe_prepared_weights_size(const moe_config_t* cfg, size_t* bytes) {
+  MOE_TRY(validate(cfg));
+  if (bytes == nullptr || cfg->precision == MOE_BF16) return MOE_ERR_INVALID_ARG;
+  DevInfo d;
+  MOE_TRY(current_device(&d));
+  *bytes = make_layout(*cfg, sm_budget(d.sms, *cfg)).q_total;
+  return MOE_OK;
+}
+
+moe_status_t moe_prepare_weights(const moe_config_t* cfg, const moe_bf16_t* W_gate,
+                                 const moe_bf16_t* W_up, const moe_bf16_t* W_down, void* wq,
+                                 size_t wq_bytes, moe_stream_t stream) {
+  MOE_TRY(validate(cfg));
+  if (cfg->precision == MOE_BF16 || !all_aligned16({W_gate, W_up, W_down}) || wq == nullptr ||
+      !aligned(wq, 256))
+    return MOE_ERR_INVALID_ARG;
+  DevInfo d;
+  MOE_TRY(current_device(&d));
+  const Layout L = make_layout(*cfg, sm_budget(d.sms, *cfg));
+  if (wq_bytes < L.q_total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const uint32_t fl = cfg->flags;
+  MOE_TRY(run("prepare_w_gate_up_h", s, fl, [&] {
+    return launch_quant_cols_gate_up(W_gate, W_up, L.E, L.H, L.F, at<uint8_t>(wq, L.q_gu_h),
+                                     at<uint8_t>(wq, L.qs_gu_h), s);
+  }));
+  MOE_TRY(run("prepare_w_down_f", s, fl, [&] {
+    return launch_quant_cols_weights(W_down, L.E, L.F, L.H, at<uint8_t>(wq, L.q_d_f),
+                                     at<uint8_t>(wq, L.qs_d_f), s);
+  }));
+  MOE_TRY(run("prepare_w_gate_f", s, fl, [&] {
+    return launch_quant_rows_dense(W_gate, static_cast<int64_t>(L.E) * L.H, L.F,
+                                   at<uint8_t>(wq, L.q_g_f), at<uint8_t>(wq, L.qs_g_f), s);
+  }));
+  MOE_TRY(run("prepare_w_up_f", s, fl, [&] {
+    return launch_quant_rows_dense(W_up, static_cast<int64_t>(L.E) * L.H, L.F,
+                                   at<uint8_t>(wq, L.q_u_f), at<uint8_t>(wq, L.qs_u_f), s);
+  }));
+  return run("prepare_w_down_h", s, fl, [&] {
+    return launch_quant_rows_dense(W_down, static_cast<int64_t>(L.E) * L.F, L.H,
+                                   at<uint8_t>(wq, L.q_d_h), at<uint8_t>(wq, L.qs_d_h), s);
+  });
+}
+
 moe_status_t moe_route(const moe_config_t* cfg, const moe_bf16_t* x, const moe_bf16_t* W_r,
                        const float* logit_bias, float* logits, int32_t* topk_idx, float* topk_w,
                        int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* slot_row,
@@ -924,7 +1014,8 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
 
   if (cfg->precision == MOE_MXFP8) {
     MOE_TRY(forward_gemms_mx(L, sms, s, fl, st, xperm, W_gate, W_up, W_down, poff, counts,
-                             mtile, w_row, row_slot, act, h, scratch, ws));
+                             mtile, w_row, row_slot, act, h, scratch, ws,
+                             const_cast<void*>(cfg->prepared_weights)));
   } else {
     // F7 + F8: gate/up GEMM with SwiGLU
     MOE_TRY(gate_up_fwd_bf16(L, sms, s, fl, st, xperm, W_gate, W_up, poff, counts, mtile, mtile2,
@@ -1030,6 +1121,12 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
                      at<uint8_t>(ws, L.bq_ra), at<uint8_t>(ws, L.bs_ra),
                      at<uint8_t>(ws, L.bq_rwgu), at<uint8_t>(ws, L.bs_rwgu)};
       q.x_ready = true;
+      if (L.prepared) {
+        void* wq = const_cast<void*>(cfg->prepared_weights);
+        q.wgu = at<uint8_t>(wq, L.q_gu_h);
+        q.swgu = at<uint8_t>(wq, L.qs_gu_h);
+        q.w_ready = true;
+      }
       MOE_TRY(gate_up_fwd_mx(L, sms, s, fl, st, xp, W_gate, W_up, poff, counts, mtile, hh, q,
                              true));
     } else {
@@ -1055,7 +1152,8 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
   if (cfg->precision != MOE_BF16) {
     const BwdBufs bb{W_gate, W_up, W_down, dyp, xperm, h, poff, counts, mtile, order, slot_pad,
                      row_slot, w_row, w, idx, wrt, dh, aw, dwp, dl, dlt, scratch, dx,
-                     dW_gate, dW_up, dW_down, ws, wflags};
+                     dW_gate, dW_up, dW_down, ws, wflags,
+                     L.prepared ? const_cast<void*>(cfg->prepared_weights) : nullptr};
     MOE_TRY(backward_expert_gemms_mx(L, sms, s, fl, st, bb));
   } else {
     // B2-B4: down dgrad with the SwiGLU backward and router-weight partials

@@ -32,13 +32,14 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
 EXPORTED = ("moe_workspace_size", "moe_route", "moe_forward", "moe_backward", "moe_gemm_bf16",
             "moe_get_device_status", "moe_status_string", "moe_profile_enable",
             "moe_profile_read", "moe_launch_count", "moe_route_noalloc", "moe_gemm_mxfp8",
-            "moe_backward_accumulate")
+            "moe_backward_accumulate", "moe_prepared_weights_size", "moe_prepare_weights")
 
 
 class MoeConfig(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int32), ("F", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("top_k", ctypes.c_int32), ("precision", ctypes.c_int32),
-                ("flags", ctypes.c_uint32), ("max_sms", ctypes.c_int32)]
+                ("flags", ctypes.c_uint32), ("max_sms", ctypes.c_int32),
+                ("prepared_weights", ctypes.c_void_p)]
 
 
 class MoeError(RuntimeError):
@@ -67,6 +68,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_forward": [cfgp] + [_vp] * 9 + [_sz, _vp],
         "moe_backward": [cfgp] + [_vp] * 13 + [_sz, _vp],
         "moe_backward_accumulate": [cfgp] + [_vp] * 13 + [_sz, _vp],
+        "moe_prepared_weights_size": [cfgp, ctypes.POINTER(_sz)],
+        "moe_prepare_weights": [cfgp, _vp, _vp, _vp, _vp, _sz, _vp],
         "moe_gemm_bf16": [_i64, _i64, _i64, _vp, _i32, _vp, _i32, _vp, _vp, _sz, _vp],
         "moe_get_device_status": [_vp, _vp],
         "moe_status_string": [_i32],
@@ -173,6 +176,20 @@ def moe_backward_accumulate(cfg: MoeConfig, x, W_r, W_gate, W_up, W_down, ctx, d
         _ptr(W_down, bf), _ptr(ctx), _ptr(dY, bf), _ptr(dx, bf), _ptr(gW_r, f32),
         _ptr(gW_gate, f32), _ptr(gW_up, f32), _ptr(gW_down, f32), _ptr(ws),
         ws.numel() * ws.element_size(), _stream(stream)), "moe_backward_accumulate")
+
+
+def moe_prepared_weights_size(cfg: MoeConfig) -> int:
+    n = _sz()
+    _check(load().moe_prepared_weights_size(ctypes.byref(cfg), ctypes.byref(n)),
+           "moe_prepared_weights_size")
+    return n.value
+
+
+def moe_prepare_weights(cfg: MoeConfig, W_gate, W_up, W_down, wq, stream=None) -> None:
+    bf = torch.bfloat16
+    _check(load().moe_prepare_weights(ctypes.byref(cfg), _ptr(W_gate, bf), _ptr(W_up, bf),
+                                      _ptr(W_down, bf), _ptr(wq), wq.numel() * wq.element_size(),
+                                      _stream(stream)), "moe_prepare_weights")
 
 
 def moe_gemm_bf16(A, a_kmajor: bool, B, b_kmajor: bool, D, ws, stream=None) -> None:

@@ -81,6 +81,13 @@ def test_null_and_flag_validation(lib):
     assert lib.moe_route(ctypes.byref(cfg), *([None] * 10), 0, None) == 1
     assert lib.moe_backward(ctypes.byref(cfg), *([None] * 13), 0, None) == 1
     assert lib.moe_backward_accumulate(ctypes.byref(cfg), *([None] * 13), 0, None) == 1
+    # weight preparation: bf16 has nothing to prepare; null buffers are rejected
+    assert lib.moe_prepared_weights_size(ctypes.byref(cfg), None) == 1
+    assert lib.moe_prepare_weights(ctypes.byref(cfg), None, None, None, None, 0, None) == 1
+    cfg_mx = libmoe.make_config(128, 256, 128, 8, 2, "mxfp8")
+    assert lib.moe_prepare_weights(ctypes.byref(cfg_mx), None, None, None, None, 0, None) == 1
+    cfg_mx.prepared_weights = 0x1000 + 16              # not 256-byte aligned
+    assert lib.moe_workspace_size(ctypes.byref(cfg_mx), None, None, None) == 1
     assert lib.moe_gemm_bf16(128, 100, 64, None, 1, None, 1, None, None, 0, None) == 2
 
 
@@ -88,7 +95,7 @@ def test_config_extensions_validation(lib):
     """max_sms must be >= 0; the recompute flag and an SM budget are accepted
     (validation passes and the call reaches the device query)."""
     from mixture_experts_layer_17_gb300 import libmoe
-    assert ctypes.sizeof(libmoe.MoeConfig) == 40
+    assert ctypes.sizeof(libmoe.MoeConfig) == 48
     cfg = libmoe.make_config(128, 256, 128, 8, 2, max_sms=-1)
     assert lib.moe_workspace_size(ctypes.byref(cfg), None, None, None) == 1
     for flags, max_sms in ((libmoe.MOE_FLAG_RECOMPUTE, 0), (0, 1), (libmoe.MOE_FLAG_RECOMPUTE, 16)):

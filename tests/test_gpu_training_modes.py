@@ -144,3 +144,27 @@ def test_sm_budget_mxfp8_and_recompute_together():
     for key in ("dx", "dW_gate", "dW_up", "dW_down"):
         assert torch.equal(g0[key], g1[key]), key
     assert np.isfinite(f64(g1["dW_r"])).all()
+
+
+@pytest.mark.parametrize("precision,extra", [("mxfp8", 0), ("fp8_bwd", 0), ("mxfp8", "recompute")])
+def test_prepared_weights_are_bit_identical(precision, extra):
+    """moe_prepare_weights writes the bytes the calls would quantise
+    themselves, and the calls read them instead of the bf16 weights."""
+    from mixture_experts_layer_17_gb300 import MoeLayer, libmoe
+    fl = libmoe.MOE_FLAG_RECOMPUTE if extra == "recompute" else 0
+    sh, inp = _inputs((517, 512, 384, 16, 4, 66), precision)
+    plain = MoeLayer(sh.T, sh.H, sh.F, sh.E, sh.top_k, precision, flags=fl)
+    prep = MoeLayer(sh.T, sh.H, sh.F, sh.E, sh.top_k, precision, flags=fl)
+    prep.prepare_weights(inp["W_gate"], inp["W_up"], inp["W_down"])
+    y0, g0 = _run(plain, inp)
+    y1, g1 = _run(prep, inp)
+    assert torch.equal(y0, y1)
+    for key in GRAD_KEYS:
+        assert torch.equal(g0[key], g1[key]), key
+    if precision == "mxfp8":
+        # weights prepared from 2 * W_down: doubling moves only the MX scale
+        # exponents, so the layer output doubles exactly
+        prep.prepare_weights(inp["W_gate"], inp["W_up"], 2 * inp["W_down"])
+        y2 = prep.forward(*_weights(inp), inp["logit_bias"])
+        torch.cuda.synchronize()
+        assert torch.equal(y2, 2 * y0)
