@@ -81,8 +81,7 @@ typedef enum {
 #define MOE_FLAG_CTA_PAIRS_ON   0x8u  /* use CTA-pair 256-row tiles (cta_group::2)
                                          wherever the shape allows; by default,
                                          when experts average >= 512 rows, pairs
-                                         run the gate/up dgrad, the down forward
-                                         and the two expert weight gradients      */
+                                         run every expert GEMM but the down dgrad */
 #define MOE_FLAG_RECOMPUTE      0x10u /* activation checkpointing (full activation
                                          checkpointing is the training setting of
                                          the end-to-end runs in "Os Números..." on

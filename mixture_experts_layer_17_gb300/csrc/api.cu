@@ -222,10 +222,11 @@ Layout make_layout(const moe_config_t& c, int sms) {
   // CTA pairs (256-row tiles, cta_group::2): each CTA stages half of B, so six
   // stages fit and the operand-latency lookahead grows by half; a pair tile
   // of a grouped-M GEMM wastes more rows at the end of each expert.  Measured
-  // on the 235B shape (1024 rows per expert), pairs win for the gate/up dgrad,
-  // the down forward and both weight gradients, and lose for the gate/up
-  // forward and the down dgrad; with ~256 rows per expert they lose
-  // everywhere.  MOE_FLAG_CTA_PAIRS_ON / _OFF override the choice.
+  // on the 235B shape (1024 rows per expert), pairs win for the gate/up
+  // forward and dgrad, the down forward and both weight gradients (the gate/up
+  // forward by 4.5% once its epilogue stores went through shared memory), and
+  // lose for the down dgrad, whose epilogue dominates; with ~256 rows per
+  // expert they lose everywhere.  MOE_FLAG_CTA_PAIRS_ON / _OFF override.
   const bool pairs_on = (c.flags & MOE_FLAG_CTA_PAIRS_ON) != 0;
   const bool pairs_off = (c.flags & MOE_FLAG_CTA_PAIRS_OFF) != 0;
   const bool bf = c.precision != MOE_MXFP8;        // bf16 forward GEMMs
@@ -233,7 +234,7 @@ Layout make_layout(const moe_config_t& c, int sms) {
   const bool big = L.P >= 512ll * L.E;             // experts average >= 512 rows
   const bool can_pair = sms >= 2;                    // an SM budget of 1 runs single CTAs
   const bool pp = can_pair && !pairs_off && (pairs_on || big);
-  L.pair_gu_fwd = bf && can_pair && !pairs_off && pairs_on;
+  L.pair_gu_fwd = bf && pp;
   L.pair_down_fwd = bf && pp;
   L.pair_down_dgrad = bb && can_pair && !pairs_off && pairs_on && (L.F % 256 == 0);
   L.pair_gu_dgrad = bb && pp;
