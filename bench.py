@@ -455,6 +455,30 @@ def run_ours(args, sh, world, rank, local):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
 
+    # ---- the same step captured once into a CUDA graph and replayed (the C ABI
+    # only enqueues work on the caller's stream, so a whole step captures)
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step(inp["x"], inp["dY"])
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(inp["x"], inp["dY"])
+    graph.replay()
+    torch.cuda.synchronize()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    g0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = max_over_ranks(g0.elapsed_time(g1), world) / args.steps
+    assert layer.device_status("fwd") == 0 and layer.device_status("bwd") == 0
+
     fwd_fl, bwd_fl = layer_flops(sh)
     flops = gemm_flops_all(sh)
     byts = kernel_bytes(sh)
@@ -523,6 +547,8 @@ def run_ours(args, sh, world, rank, local):
         "e2e": {"value": world * sh.T / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * hx.numel() * 2, "d2h_bytes_per_step": 2 * hx.numel() * 2,
                 "copies": "pinned host memory, side stream, double-buffered across steps"},
+        "graph": {"ms_per_step": graph_ms, "value": world * sh.T / (graph_ms * 1e-3),
+                  "unit": "tokens/s", "note": "one fwd+bwd step captured in a CUDA graph, replayed"},
         "gpu_launches": launches,
         "roofline": roof,
         "kernels": per_kernel,
