@@ -222,10 +222,9 @@ Layout make_layout(const moe_config_t& c, int sms) {
   // CTA pairs (256-row tiles, cta_group::2): each CTA stages half of B, so six
   // stages fit and the operand-latency lookahead grows by half; a pair tile
   // of a grouped-M GEMM wastes more rows at the end of each expert.  Measured
-  // on the 235B shape (1024 rows per expert), pairs win for the gate/up
-  // forward and dgrad, the down forward and both weight gradients (the gate/up
-  // forward by 4.5% once its epilogue stores went through shared memory), and
-  // lose for the down dgrad, whose epilogue dominates; with ~256 rows per
+  // on the 235B shape (1024 rows per expert), pairs win for every expert GEMM
+  // once the epilogue stores go through shared memory (the down dgrad's, at
+  // five stages, by 12%; the gate/up forward's by 4.5%); with ~256 rows per
   // expert they lose everywhere.  MOE_FLAG_CTA_PAIRS_ON / _OFF override.
   const bool pairs_on = (c.flags & MOE_FLAG_CTA_PAIRS_ON) != 0;
   const bool pairs_off = (c.flags & MOE_FLAG_CTA_PAIRS_OFF) != 0;
@@ -236,7 +235,7 @@ Layout make_layout(const moe_config_t& c, int sms) {
   const bool pp = can_pair && !pairs_off && (pairs_on || big);
   L.pair_gu_fwd = bf && pp;
   L.pair_down_fwd = bf && pp;
-  L.pair_down_dgrad = bb && can_pair && !pairs_off && pairs_on && (L.F % 256 == 0);
+  L.pair_down_dgrad = bb && pp && (L.F % 256 == 0);
   L.pair_gu_dgrad = bb && pp;
   L.pair_down_wgrad = bb && pp && (L.F % 256 == 0);
   L.pair_gu_wgrad = bb && pp;

@@ -282,7 +282,11 @@ struct StageCfg {
   static constexpr uint32_t kABytes = kBM * kBK * 2;
   static constexpr uint32_t kBBytes = BN * kBK * 2;
   static constexpr uint32_t kSFBytes = 0;
-  static constexpr int kStages = (BN >= 256) ? 4 : (BN >= 128 ? 6 : 8);
+  // as many stages as the problem's own shared memory leaves room for
+  static constexpr int kFit =
+      static_cast<int>((232448 - 1024 - 256 - P::kExtraSmem) / (kABytes + kBBytes));
+  static constexpr int kWant = (BN >= 256) ? 4 : (BN >= 128 ? 6 : 8);
+  static constexpr int kStages = kWant < kFit ? kWant : kFit;
   static constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
   static constexpr int kAccBufs = 2;
 };
@@ -296,7 +300,9 @@ struct StageCfg<P, false, true> {
   static constexpr uint32_t kABytes = kBM * kBK * 2;
   static constexpr uint32_t kBBytes = (BN / 2) * kBK * 2;
   static constexpr uint32_t kSFBytes = 0;
-  static constexpr int kStages = 6;
+  static constexpr int kFit =
+      static_cast<int>((232448 - 1024 - 256 - P::kExtraSmem) / (kABytes + kBBytes));
+  static constexpr int kStages = 6 < kFit ? 6 : kFit;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kAccBufs = 2;
 };

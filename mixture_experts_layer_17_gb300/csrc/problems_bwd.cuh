@@ -20,12 +20,15 @@ namespace moe {
 //   out2 = dw_part f32 [P, 2 * n_tiles] (one partial per n-tile and column half)
 //   ld0 = F;  K = H;  n_tiles = F / BN;  b_group_rows = F
 // ------------------------------------------------------------------------
-template <int BN_>
+template <int BN_, bool kStaged = false>
 struct DownDgradProblem {
   static constexpr int BN = BN_;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
-  static constexpr size_t kExtraSmem = 0;
+  // kStaged: dh_gate, dh_up and w*a leave through three 2 KB stages per
+  // epilogue warp as whole half-lines (the CTA-pair version, which has the
+  // shared memory for them at five stages)
+  static constexpr size_t kExtraSmem = kStaged ? 8 * 3 * kStage64WarpBytes : 0;
   static constexpr int kEpiGroups = 2;
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
@@ -42,12 +45,14 @@ struct DownDgradProblem {
   // for chunk c + 16 are issued before chunk c is computed, so their latency
   // overlaps the arithmetic and stores of chunk c.
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               int group, uint8_t*) {
+                               int group, uint8_t* extra) {
     constexpr int kHalf = BN / 2;
     const bool valid = r < ti.rows;
     // rows past the expert's tokens but inside its padded segment: dh and w*a
     // are weight-gradient operands there, so they must read as zero
     const bool pad = !valid && r < ti.rows_pad;
+    const int lane = r & 31;
+    uint8_t* st = kStaged ? extra + (group * 4 + (r >> 5)) * 3 * kStage64WarpBytes : nullptr;
     const int64_t row = static_cast<int64_t>(ti.m0) + ((valid || pad) ? r : 0);
     const int F = a.ld0;
     const int c0 = group * kHalf;
@@ -95,9 +100,24 @@ struct DownDgradProblem {
           dhu[i] = da * silu;
           awv[i] = w * act;
         }
-        store_bf16x16(dh + c, dhg);
-        store_bf16x16(dh + F + c, dhu);
-        store_bf16x16(aw + c, awv);
+        if constexpr (kStaged) {
+          const int q = ((c - c0) >> 4) & 1;
+          stage64_bf16x16(st, lane, q, dhg);
+          stage64_bf16x16(st + kStage64WarpBytes, lane, q, dhu);
+          stage64_bf16x16(st + 2 * kStage64WarpBytes, lane, q, awv);
+        } else {
+          store_bf16x16(dh + c, dhg);
+          store_bf16x16(dh + F + c, dhu);
+          store_bf16x16(aw + c, awv);
+        }
+      } else if (kStaged) {
+        // zeros for the padded rows (and for rows nobody writes)
+        const int q = ((c - c0) >> 4) & 1;
+        const float z[16] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f,
+                             0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        stage64_bf16x16(st, lane, q, z);
+        stage64_bf16x16(st + kStage64WarpBytes, lane, q, z);
+        stage64_bf16x16(st + 2 * kStage64WarpBytes, lane, q, z);
       } else if (pad) {
         st_global_v4(dh + c, 0u, 0u, 0u, 0u);
         st_global_v4(dh + c + 8, 0u, 0u, 0u, 0u);
@@ -105,6 +125,15 @@ struct DownDgradProblem {
         st_global_v4(dh + F + c + 8, 0u, 0u, 0u, 0u);
         st_global_v4(aw + c, 0u, 0u, 0u, 0u);
         st_global_v4(aw + c + 8, 0u, 0u, 0u, 0u);
+      }
+      if constexpr (kStaged) {
+        if (((c - c0) >> 4) & 1) {             // 32 columns staged: flush the three outputs
+          const int c32 = c - 16;
+          const bool w_row = valid || pad;
+          stage64_flush(st, lane, w_row ? dh + c32 : nullptr, false);
+          stage64_flush(st + kStage64WarpBytes, lane, w_row ? dh + F + c32 : nullptr, false);
+          stage64_flush(st + 2 * kStage64WarpBytes, lane, w_row ? aw + c32 : nullptr, false);
+        }
       }
     }
     // one router-weight partial per (row, n-tile, column half)

@@ -42,7 +42,7 @@ struct DownFwdPairProblem : DownFwdProblem {
 };
 
 // B2-B4: B K-major (box {64, 128}), N-rows 128*rank ...
-struct DownDgradPairProblem : DownDgradProblem<256> {
+struct DownDgradPairProblem : DownDgradProblem<256, true> {
   static constexpr bool kPair = true;
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles_pair(a); }
   MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile_pair(a, t, BN); }
