@@ -183,7 +183,8 @@ struct Layout {
   int H, F, E, k;
   int ntiles;        // router tiles of 128 tokens
   int router_bn;     // N of the router GEMM (power of two >= E, >= 16)
-  int dgrad_bn;      // N tile of the down dgrad (256 if F % 256 == 0, else 128)
+  int dgrad_bn;      // N tile of the bf16 down dgrad (256 if F % 256 == 0, else 128)
+  int mx_dgrad_bn;   // N tile of the MXFP8 down dgrad (128: double-buffered, staged outputs)
   int nparts;        // dw partials per row = 2 * F / dgrad_bn
   int wr_split, wr_kbps, wr_mtiles, wr_ntiles;
   // forward / route workspace
@@ -244,9 +245,10 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.ntiles = static_cast<int>((L.T + kBM - 1) / kBM);
   L.router_bn = next_pow2_at_least16(L.E);
   L.dgrad_bn = (L.F % 256 == 0) ? 256 : 128;
+  L.mx_dgrad_bn = 128;
   // one router-weight partial per n-tile and epilogue column half (the bf16
   // and MXFP8 down dgrads both use 256-wide tiles when F allows)
-  L.nparts = (L.F / L.dgrad_bn) * 2;
+  L.nparts = (L.F / (bb ? L.dgrad_bn : L.mx_dgrad_bn)) * 2;
   L.wr_mtiles = (L.E + kBM - 1) / kBM;
   L.wr_ntiles = L.H / 256;
   const int total_kb = static_cast<int>((L.T + kBK - 1) / kBK);
@@ -722,7 +724,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     a.mapB1 = a.mapB0;
     a.K = L.H;
     a.N = L.F;
-    a.n_tiles = L.F / L.dgrad_bn;
+    a.n_tiles = L.F / L.mx_dgrad_bn;
     a.num_groups = L.E;
     a.b_group_rows = L.F;
     a.offsets = b.offsets;
@@ -746,7 +748,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     }
     const int grid = grid_for(mtiles * a.n_tiles, sms);
     MOE_TRY(run("down_dgrad_swiglu_bwd_mx", s, fl,
-                [&] { return launch_down_dgrad_mx(L.dgrad_bn, a, grid, s); }));
+                [&] { return launch_down_dgrad_mx(a, grid, s); }));
   }
   // B9: router softmax / top-k backward
   if (cudaMemsetAsync(b.dlt, 0, 2ull * L.E * L.T_pad, s) != cudaSuccess) return MOE_ERR_CUDA;

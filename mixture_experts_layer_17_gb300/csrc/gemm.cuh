@@ -314,7 +314,10 @@ struct StageCfg<P, true, false> {
   static constexpr uint32_t kABytes = kBM * 128;
   static constexpr uint32_t kBBytes = BN * 128;
   static constexpr uint32_t kSFBytes = 512 + (BN / 128) * 512;
-  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kFit =
+      static_cast<int>((232448 - 1024 - 256 - P::kExtraSmem) / (kABytes + kBBytes + kSFBytes));
+  static constexpr int kWant = BN == 256 ? 4 : 6;
+  static constexpr int kStages = kWant < kFit ? kWant : kFit;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSFCol0 = 256;
   static constexpr uint32_t kSFStride = BN == 256 ? 16 : 8;   // TMEM columns per stage

@@ -10,9 +10,8 @@ cudaError_t launch_gate_up_fwd_mx(const GemmArgs& a, int grid, cudaStream_t s) {
 cudaError_t launch_down_fwd_mx(const GemmArgs& a, int grid, cudaStream_t s) {
   return launch_gemm<DownFwdMXProblem>(a, grid, s);
 }
-cudaError_t launch_down_dgrad_mx(int bn, const GemmArgs& a, int grid, cudaStream_t s) {
-  if (bn == 256) return launch_gemm<DownDgradMXProblem<256>>(a, grid, s);
-  return launch_gemm<DownDgradMXProblem<128>>(a, grid, s);
+cudaError_t launch_down_dgrad_mx(const GemmArgs& a, int grid, cudaStream_t s) {
+  return launch_gemm<DownDgradMXProblem<128, true>>(a, grid, s);
 }
 cudaError_t launch_gate_up_dgrad_mx(const GemmArgs& a, int grid, cudaStream_t s) {
   return launch_gemm<GateUpDgradMXProblem>(a, grid, s);

@@ -30,7 +30,7 @@ cudaError_t launch_gate_up_wgrad_pair(const GemmArgs& a, int grid, cudaStream_t 
 // MXFP8 GEMMs (gemm_mx.cu)
 cudaError_t launch_gate_up_fwd_mx(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_down_fwd_mx(const GemmArgs& a, int grid, cudaStream_t s);
-cudaError_t launch_down_dgrad_mx(int bn, const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_down_dgrad_mx(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_gate_up_dgrad_mx(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_down_wgrad_mx(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_gate_up_wgrad_mx(const GemmArgs& a, int grid, cudaStream_t s);

@@ -236,16 +236,19 @@ struct DownFwdMXProblem {
 // and w*a in bf16 for the weight gradients, the router-weight partials, and
 // dh quantised to E4M3 along F straight from fp32 for the gate/up dgrad:
 // out3 = dh E4M3 [Pa, 2F], out4 = its scale atoms (((mtile_off[e] +
-// m-tile) * 2F/128 + column/128) * 512).  BN = 256 (F a multiple of 256) runs
-// one accumulator and a serial epilogue (too many live values for an early
-// release), BN = 128 double-buffers.
-template <int BN_>
+// m-tile) * 2F/128 + column/128) * 512).  The layer runs BN = 128 with a
+// double-buffered accumulator and kStaged (dh_gate, dh_up and w*a through
+// three 2 KB shared-memory stages per warp, five stages): the epilogue is
+// heavy and overlaps the next tile's MMAs that way (a 256-wide tile with one
+// accumulator, whose epilogue runs serially, measured slower).
+template <int BN_, bool kStaged = false>
 struct DownDgradMXProblem {
   static constexpr int BN = BN_;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
   static constexpr bool kMX = true;
-  static constexpr size_t kExtraSmem = 0;
+  // kStaged: dh_gate, dh_up and w*a leave through three 2 KB stages per warp
+  static constexpr size_t kExtraSmem = kStaged ? 8 * 3 * kStage64WarpBytes : 0;
   static constexpr int kEpiGroups = 2;
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
@@ -267,10 +270,12 @@ struct DownDgradMXProblem {
   }
   MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               int group, uint8_t*) {
+                               int group, uint8_t* extra) {
     constexpr int kHalf = BN / 2;
     const bool valid = r < ti.rows;
     const bool pad = !valid && r < ti.rows_pad;
+    const int lane = r & 31;
+    uint8_t* st = kStaged ? extra + (group * 4 + (r >> 5)) * 3 * kStage64WarpBytes : nullptr;
     const int64_t row = static_cast<int64_t>(ti.m0) + ((valid || pad) ? r : 0);
     const int F = a.ld0;
     const int c0 = group * kHalf;
@@ -303,16 +308,33 @@ struct DownDgradMXProblem {
           dhu[i] = da * silu;
           awv[i] = w * act;
         }
-        store_bf16x16(dh + c, *reinterpret_cast<float(*)[16]>(dhg));
-        store_bf16x16(dh + c + 16, *reinterpret_cast<float(*)[16]>(dhg + 16));
-        store_bf16x16(dh + F + c, *reinterpret_cast<float(*)[16]>(dhu));
-        store_bf16x16(dh + F + c + 16, *reinterpret_cast<float(*)[16]>(dhu + 16));
-        store_bf16x16(aw + c, *reinterpret_cast<float(*)[16]>(awv));
-        store_bf16x16(aw + c + 16, *reinterpret_cast<float(*)[16]>(awv + 16));
+        if constexpr (kStaged) {
+          stage64_bf16x16(st, lane, 0, dhg);
+          stage64_bf16x16(st, lane, 1, dhg + 16);
+          stage64_bf16x16(st + kStage64WarpBytes, lane, 0, dhu);
+          stage64_bf16x16(st + kStage64WarpBytes, lane, 1, dhu + 16);
+          stage64_bf16x16(st + 2 * kStage64WarpBytes, lane, 0, awv);
+          stage64_bf16x16(st + 2 * kStage64WarpBytes, lane, 1, awv + 16);
+        } else {
+          store_bf16x16(dh + c, *reinterpret_cast<float(*)[16]>(dhg));
+          store_bf16x16(dh + c + 16, *reinterpret_cast<float(*)[16]>(dhg + 16));
+          store_bf16x16(dh + F + c, *reinterpret_cast<float(*)[16]>(dhu));
+          store_bf16x16(dh + F + c + 16, *reinterpret_cast<float(*)[16]>(dhu + 16));
+          store_bf16x16(aw + c, *reinterpret_cast<float(*)[16]>(awv));
+          store_bf16x16(aw + c + 16, *reinterpret_cast<float(*)[16]>(awv + 16));
+        }
         const int cg = ti.n0 + c;           // gate column; up column = F + cg
         mx_block_store(dhg, dhq + cg, sfq + (atom_row + cg / 128) * 512 + sf_atom_offset(r, (cg >> 5) & 3));
         mx_block_store(dhu, dhq + F + cg,
                        sfq + (atom_row + (F + cg) / 128) * 512 + sf_atom_offset(r, ((F + cg) >> 5) & 3));
+      } else if (kStaged) {
+        const float z[16] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f,
+                             0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int o = 0; o < 3; ++o) {
+          stage64_bf16x16(st + o * kStage64WarpBytes, lane, 0, z);
+          stage64_bf16x16(st + o * kStage64WarpBytes, lane, 1, z);
+        }
       } else if (pad) {
 #pragma unroll
         for (int q = 0; q < 32; q += 8) {
@@ -320,6 +342,12 @@ struct DownDgradMXProblem {
           st_global_v4(dh + F + c + q, 0u, 0u, 0u, 0u);
           st_global_v4(aw + c + q, 0u, 0u, 0u, 0u);
         }
+      }
+      if constexpr (kStaged) {
+        const bool w_row = valid || pad;
+        stage64_flush(st, lane, w_row ? dh + c : nullptr, false);
+        stage64_flush(st + kStage64WarpBytes, lane, w_row ? dh + F + c : nullptr, false);
+        stage64_flush(st + 2 * kStage64WarpBytes, lane, w_row ? aw + c : nullptr, false);
       }
     }
     if (valid)
