@@ -5,15 +5,23 @@
 
 namespace moe {
 
-cudaError_t launch_router_fwd(int bn, const GemmArgs& a, int grid, cudaStream_t s) {
+template <int kSlots>
+cudaError_t launch_router_slots(int bn, const GemmArgs& a, int grid, cudaStream_t s) {
   switch (bn) {
-    case 16: return launch_gemm<RouterProblem<16>>(a, grid, s);
-    case 32: return launch_gemm<RouterProblem<32>>(a, grid, s);
-    case 64: return launch_gemm<RouterProblem<64>>(a, grid, s);
-    case 128: return launch_gemm<RouterProblem<128>>(a, grid, s);
-    case 256: return launch_gemm<RouterProblem<256>>(a, grid, s);
+    case 16: return launch_gemm<RouterProblem<16, kSlots>>(a, grid, s);
+    case 32: return launch_gemm<RouterProblem<32, kSlots>>(a, grid, s);
+    case 64: return launch_gemm<RouterProblem<64, kSlots>>(a, grid, s);
+    case 128: return launch_gemm<RouterProblem<128, kSlots>>(a, grid, s);
+    case 256: return launch_gemm<RouterProblem<256, kSlots>>(a, grid, s);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_router_fwd(int bn, const GemmArgs& a, int grid, cudaStream_t s) {
+  // the top-k list holds 8 entries when top_k <= 8 (the inner loop of the
+  // epilogue runs over all of them for every logit)
+  return a.top_k <= 8 ? launch_router_slots<8>(bn, a, grid, s)
+                      : launch_router_slots<16>(bn, a, grid, s);
 }
 
 cudaError_t launch_gate_up_fwd(const GemmArgs& a, int grid, cudaStream_t s) {

@@ -10,7 +10,9 @@
 
 namespace moe {
 
-MOE_DEV void epi_bar_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// named barrier 1 over the epilogue warps (nthreads: 128 per warpgroup)
+template <int kThreads = 128>
+MOE_DEV void epi_bar_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
 
 // ------------------------------------------------------------------------
 // Coalesced row stores.  An epilogue thread owns one output row, so a direct
@@ -154,14 +156,20 @@ MOE_DEV void stage_flush_add_f32(const uint8_t* st, int lane, float* dst) {
 //   in0 = logit_bias f32 [E] or null;  out0 = logits f32 [T, E] or null
 //   out1 = topk_idx i32 [T, k];  out2 = topk_w f32 [T, k];  out3 = hist i32 [tiles, E]
 // ------------------------------------------------------------------------
-template <int BN_>
+template <int BN_, int kSlots = 16>
 struct RouterProblem {
   static constexpr int BN = BN_;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
-  static constexpr size_t kExtraSmem = 256 * sizeof(int);
-  static constexpr int kEpiGroups = 1;      // a thread needs its whole row for the top-k
-  static constexpr int kMaxK = 16;
+  // four warpgroups each keep the sorted top-k list of a quarter of the
+  // experts (narrow routers: one); the lists meet in shared memory
+  static constexpr int kEpiGroups = BN >= 64 ? 4 : 1;
+  static constexpr int kCols = BN / kEpiGroups;
+  // length of the per-token sorted lists: every logit is inserted through all
+  // of it, so it is sized at compile time (8 when top_k <= 8, else 16)
+  static constexpr int kMaxK = kSlots;
+  static constexpr size_t kListBytes = kEpiGroups > 1 ? size_t(128) * kEpiGroups * kMaxK * 8 : 0;
+  static constexpr size_t kExtraSmem = 256 * sizeof(int) + kListBytes;
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return dense_num_tiles(a); }
   MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return dense_tile(a, t, BN); }
@@ -176,9 +184,28 @@ struct RouterProblem {
   }
   MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
 
+  // (cv, ci) into the list ordered by (-logit, expert id)
+  MOE_DEV static void insert(float (&topv)[kMaxK], int (&topi)[kMaxK], int k, float cv, int ci) {
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s) {
+      if (s < k) {
+        const bool better = (cv > topv[s]) || (cv == topv[s] && ci < topi[s]);
+        if (better) {
+          const float tv = topv[s];
+          const int tt = topi[s];
+          topv[s] = cv;
+          topi[s] = ci;
+          cv = tv;
+          ci = tt;
+        }
+      }
+    }
+  }
+
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
-                               int, uint8_t* extra) {
+                               int group, uint8_t* extra) {
     int* hist = reinterpret_cast<int*>(extra);
+    float2* lists = reinterpret_cast<float2*>(extra + 256 * sizeof(int));   // [row][group][slot]
     const int E = a.E;
     const int k = a.top_k;
     const bool valid = r < ti.rows;
@@ -193,7 +220,7 @@ struct RouterProblem {
       topi[i] = 0x7fffffff;
     }
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
+    for (int c = group * kCols; c < (group + 1) * kCols; c += 16) {
       float v[16];
       tmem_ld16(taddr + c, v);
       tmem_ld_wait();
@@ -204,23 +231,7 @@ struct RouterProblem {
           float l = v[i];
           if (bias != nullptr) l += __ldg(bias + e);
           v[i] = l;
-          // insert (l, e) into the list ordered by (-logit, id)
-          float cv = l;
-          int ci = e;
-#pragma unroll
-          for (int s = 0; s < kMaxK; ++s) {
-            if (s < k) {
-              const bool better = (cv > topv[s]) || (cv == topv[s] && ci < topi[s]);
-              if (better) {
-                const float tv = topv[s];
-                const int tt = topi[s];
-                topv[s] = cv;
-                topi[s] = ci;
-                cv = tv;
-                ci = tt;
-              }
-            }
-          }
+          insert(topv, topi, k, l, e);
         }
       }
       if (valid && logits != nullptr) {
@@ -230,7 +241,28 @@ struct RouterProblem {
           if (c + i < E) dst[i] = v[i];
       }
     }
-    if (valid) {
+    if constexpr (kEpiGroups > 1) {
+      // merge: every group leaves its list, group 0 folds the others into its own
+      float2* mine = lists + (static_cast<size_t>(r) * kEpiGroups + group) * kMaxK;
+      if (group != 0) {
+#pragma unroll
+        for (int i = 0; i < kMaxK; ++i)
+          if (i < k) mine[i] = make_float2(topv[i], __int_as_float(topi[i]));
+      }
+      epi_bar_sync<128 * kEpiGroups>();
+      if (group == 0) {
+#pragma unroll 1
+        for (int g = 1; g < kEpiGroups; ++g) {
+          const float2* other = lists + (static_cast<size_t>(r) * kEpiGroups + g) * kMaxK;
+#pragma unroll 1
+          for (int i = 0; i < k; ++i) {
+            const float2 o = other[i];
+            insert(topv, topi, k, o.x, __float_as_int(o.y));
+          }
+        }
+      }
+    }
+    if (group == 0 && valid) {
       const float m = topv[0];
       float ex[kMaxK];
       float sum = 0.f;
@@ -251,15 +283,16 @@ struct RouterProblem {
         }
       }
     }
-    epi_bar_sync();
+    epi_bar_sync<128 * kEpiGroups>();
     int* hist_out = static_cast<int*>(a.out3) + static_cast<int64_t>(ti.mt) * E;
-    for (int e = r; e < E; e += 128) {
+    for (int e = group * 128 + r; e < E; e += 128 * kEpiGroups) {
       hist_out[e] = hist[e];
       hist[e] = 0;
     }
-    epi_bar_sync();
+    epi_bar_sync<128 * kEpiGroups>();
   }
 };
+
 
 // ------------------------------------------------------------------------
 // F7 + F8: expert gate/up GEMM with the SwiGLU epilogue.
