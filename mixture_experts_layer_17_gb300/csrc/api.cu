@@ -193,6 +193,7 @@ struct Layout {
   // context
   size_t c_idx, c_w, c_counts, c_offsets, c_perm, c_slot, c_row_slot, c_w_row, c_mtile,
       c_order, c_wrt, c_xperm, c_h, c_poff, c_mtile2, c_slotpad, c_total;
+  size_t c_xt, c_sxt;   // mxfp8: x along the tokens (E4M3, atoms) instead of x_perm
   // backward workspace
   size_t b_status, b_dyp, b_dh, b_aw, b_dwp, b_dl, b_dlt, b_scratch, b_wrp, b_total;
   // MOE_FLAG_RECOMPUTE: x_perm and h live in the forward workspace, and the
@@ -307,7 +308,12 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.c_order = x.take(sizeof(int) * E);
   L.c_wrt = x.take(2 * E * H);
   if (!L.recompute) {
-    L.c_xperm = x.take(2 * Pa * H);
+    if (c.precision == MOE_MXFP8) {   // what the gate/up wgrad reads of x
+      L.c_xt = x.take(128 * mt * H);
+      L.c_sxt = x.take(mt * (H / 128) * 512);
+    } else {
+      L.c_xperm = x.take(2 * Pa * H);
+    }
     L.c_h = x.take(2 * Pa * 2 * F);
   }
   L.c_poff = x.take(sizeof(int) * (E + 1));
@@ -678,6 +684,7 @@ struct BwdBufs {
   void* ws;
   uint32_t wflags;                   // kGemmAccumF32 or 0, for the weight gradients
   void* wq;                          // prepared MXFP8 weights, or nullptr
+  const uint8_t *xt, *sxt;           // x along the tokens already in E4M3, or nullptr
 };
 
 // B2-B9 in MXFP8 (precision mxfp8 and fp8_bwd): every expert GEMM of the
@@ -703,14 +710,15 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
   uint8_t* sawt = at<uint8_t>(ws, L.bs_awt);
   uint8_t* dyt = at<uint8_t>(ws, L.bq_dyt);
   uint8_t* sdyt = at<uint8_t>(ws, L.bs_dyt);
-  uint8_t* xt = at<uint8_t>(ws, L.bq_xt);
-  uint8_t* sxt = at<uint8_t>(ws, L.bs_xt);
+  const bool x_ready = b.xt != nullptr;
+  uint8_t* xt = x_ready ? const_cast<uint8_t*>(b.xt) : at<uint8_t>(ws, L.bq_xt);
+  uint8_t* sxt = x_ready ? const_cast<uint8_t*>(b.sxt) : at<uint8_t>(ws, L.bs_xt);
   uint8_t* dht = at<uint8_t>(ws, L.bq_dht);
   uint8_t* sdht = at<uint8_t>(ws, L.bs_dht);
   const uint64_t Pp = 128ull * static_cast<uint64_t>(L.mt_max);
   const int64_t mtiles = (L.P + kBM - 1) / kBM + L.E;
 
-  // B2-B4: down dgrad (dY_perm was quantised along H by the fused gather)
+  // B2-B4: down dgrad (dY was dispatched straight into its E4M3 copies)
   if (!prep) {
     MOE_TRY(run("mx_quant_w_down_h", s, fl, [&] {
       return launch_quant_rows_dense(b.W_down, static_cast<int64_t>(L.E) * L.F, L.H, wdh, swdh, s);
@@ -760,10 +768,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     return launch_quant_cols_tokens(b.aw, L.mt_max, L.F, awt, sawt, b.offsets, b.counts, b.mtile,
                                     L.E, s);
   }));
-  MOE_TRY(run("mx_quant_dy_tokens", s, fl, [&] {
-    return launch_quant_cols_tokens(b.dyp, L.mt_max, L.H, dyt, sdyt, b.offsets, b.counts, b.mtile,
-                                    L.E, s);
-  }));
+  // (dY along the tokens came from the dispatch)
   {
     GemmArgs a = base_args(st, fl);
     a.flags = b.wflags;
@@ -825,10 +830,12 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     return launch_unpermute(b.scratch, b.dl, b.idx, b.wrt, b.dx, L.T, L.H, L.k, s);
   }));
   // B8: gate/up wgrad over the padded token layout
-  MOE_TRY(run("mx_quant_x_tokens", s, fl, [&] {
-    return launch_quant_cols_tokens(b.xperm, L.mt_max, L.H, xt, sxt, b.offsets, b.counts,
-                                    b.mtile, L.E, s);
-  }));
+  if (!x_ready) {
+    MOE_TRY(run("mx_quant_x_tokens", s, fl, [&] {
+      return launch_quant_cols_tokens(b.xperm, L.mt_max, L.H, xt, sxt, b.offsets, b.counts,
+                                      b.mtile, L.E, s);
+    }));
+  }
   MOE_TRY(run("mx_quant_dh_tokens", s, fl, [&] {
     return launch_quant_cols_tokens(b.dh, L.mt_max, 2 * L.F, dht, sdht, b.offsets, b.counts,
                                     b.mtile, L.E, s);
@@ -1002,17 +1009,23 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
 
   // F6: dispatch x to the padded expert-major rows (segment tails zeroed: they
   // are K rows of the gate/up weight gradient)
-  if (cfg->precision == MOE_MXFP8) {   // bf16 rows plus their E4M3 copy along H
-    MOE_TRY(run("gather_x_mx", s, fl, [&] {
-      return launch_gather_rows_mx(x, slot_pad, idx, poff, mtile, xperm, at<uint8_t>(ws, L.fq_x),
-                                   at<uint8_t>(ws, L.fs_x), L.T, L.H, L.k, s);
+  if (cfg->precision == MOE_MXFP8) {
+    // x dispatched straight into its E4M3 copies: along H for the gate/up GEMM,
+    // along the tokens (kept in ctx) for the backward's gate/up wgrad
+    xperm = nullptr;
+    MOE_TRY(run("dispatch_x_mx", s, fl, [&] {
+      return launch_dispatch_quant(x, at<int>(ctx, L.c_perm), offsets, poff, counts, mtile,
+                                   L.mt_max, L.E, L.H,
+                                   L.recompute ? nullptr : at<uint8_t>(ctx, L.c_xt),
+                                   L.recompute ? nullptr : at<uint8_t>(ctx, L.c_sxt),
+                                   at<uint8_t>(ws, L.fq_x), at<uint8_t>(ws, L.fs_x), s);
     }));
   } else {
     MOE_TRY(run("gather_x", s, fl,
                 [&] { return launch_gather_rows(x, slot_pad, xperm, L.T, L.H, L.k, s); }));
+    MOE_TRY(run("zero_pad_rows_x", s, fl,
+                [&] { return launch_zero_pad_rows(xperm, poff, counts, L.E, L.H, s); }));
   }
-  MOE_TRY(run("zero_pad_rows_x", s, fl,
-              [&] { return launch_zero_pad_rows(xperm, poff, counts, L.E, L.H, s); }));
 
   if (cfg->precision == MOE_MXFP8) {
     MOE_TRY(forward_gemms_mx(L, sms, s, fl, st, xperm, W_gate, W_up, W_down, poff, counts,
@@ -1091,6 +1104,14 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
   const uint16_t* wrt = at<uint16_t>(ctx, L.c_wrt);
   const uint16_t* xperm = L.recompute ? at<uint16_t>(ws, L.b_xperm) : at<uint16_t>(ctx, L.c_xperm);
   const uint16_t* h = L.recompute ? at<uint16_t>(ws, L.b_h) : at<uint16_t>(ctx, L.c_h);
+  // mxfp8: x along the tokens comes from the forward's dispatch (ctx) or from
+  // the recompute dispatch below (ws); fp8_bwd quantises it from x_perm
+  const uint8_t* x_tok = nullptr;
+  const uint8_t* x_tok_sf = nullptr;
+  if (cfg->precision == MOE_MXFP8) {
+    x_tok = L.recompute ? at<uint8_t>(ws, L.bq_xt) : at<uint8_t>(ctx, L.c_xt);
+    x_tok_sf = L.recompute ? at<uint8_t>(ws, L.bs_xt) : at<uint8_t>(ctx, L.c_sxt);
+  }
   uint16_t* dyp = at<uint16_t>(ws, L.b_dyp);
   uint16_t* dh = at<uint16_t>(ws, L.b_dh);
   uint16_t* aw = at<uint16_t>(ws, L.b_aw);
@@ -1108,16 +1129,18 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
     uint16_t* xp = at<uint16_t>(ws, L.b_xperm);
     uint16_t* hh = at<uint16_t>(ws, L.b_h);
     if (cfg->precision == MOE_MXFP8) {
-      MOE_TRY(run("recompute_gather_x_mx", s, fl, [&] {
-        return launch_gather_rows_mx(x, slot_pad, idx, poff, mtile, xp, at<uint8_t>(ws, L.bq_rx),
-                                     at<uint8_t>(ws, L.bs_rx), L.T, L.H, L.k, s);
+      MOE_TRY(run("recompute_dispatch_x_mx", s, fl, [&] {
+        return launch_dispatch_quant(x, at<int>(ctx, L.c_perm), at<int>(ctx, L.c_offsets), poff,
+                                     counts, mtile, L.mt_max, L.E, L.H, at<uint8_t>(ws, L.bq_xt),
+                                     at<uint8_t>(ws, L.bs_xt), at<uint8_t>(ws, L.bq_rx),
+                                     at<uint8_t>(ws, L.bs_rx), s);
       }));
     } else {
       MOE_TRY(run("recompute_gather_x", s, fl,
                   [&] { return launch_gather_rows(x, slot_pad, xp, L.T, L.H, L.k, s); }));
+      MOE_TRY(run("recompute_zero_pad_rows_x", s, fl,
+                  [&] { return launch_zero_pad_rows(xp, poff, counts, L.E, L.H, s); }));
     }
-    MOE_TRY(run("recompute_zero_pad_rows_x", s, fl,
-                [&] { return launch_zero_pad_rows(xp, poff, counts, L.E, L.H, s); }));
     if (cfg->precision == MOE_MXFP8) {
       MxGateUpBufs q{at<uint8_t>(ws, L.bq_rx), at<uint8_t>(ws, L.bs_rx),
                      at<uint8_t>(ws, L.bq_ra), at<uint8_t>(ws, L.bs_ra),
@@ -1139,23 +1162,28 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
 
   // B1: dispatch dY to the padded expert-major rows (segment tails zeroed:
   // they are K rows of the down weight gradient)
-  if (cfg->precision != MOE_BF16) {   // bf16 rows plus their E4M3 copy along H
-    MOE_TRY(run("gather_dy_mx", s, fl, [&] {
-      return launch_gather_rows_mx(dY, slot_pad, idx, poff, mtile, dyp, at<uint8_t>(ws, L.bq_dy),
-                                   at<uint8_t>(ws, L.bs_dy), L.T, L.H, L.k, s);
+  if (cfg->precision != MOE_BF16) {
+    // MXFP8: dY dispatched straight into its two E4M3 copies (along H for the
+    // down dgrad, along the tokens for the down wgrad); no bf16 dY_perm
+    MOE_TRY(run("dispatch_dy_mx", s, fl, [&] {
+      return launch_dispatch_quant(dY, at<int>(ctx, L.c_perm), at<int>(ctx, L.c_offsets), poff,
+                                   counts, mtile, L.mt_max, L.E, L.H, at<uint8_t>(ws, L.bq_dyt),
+                                   at<uint8_t>(ws, L.bs_dyt), at<uint8_t>(ws, L.bq_dy),
+                                   at<uint8_t>(ws, L.bs_dy), s);
     }));
   } else {
     MOE_TRY(run("gather_dy", s, fl,
                 [&] { return launch_gather_rows(dY, slot_pad, dyp, L.T, L.H, L.k, s); }));
+    MOE_TRY(run("zero_pad_rows_dy", s, fl,
+                [&] { return launch_zero_pad_rows(dyp, poff, counts, L.E, L.H, s); }));
   }
-  MOE_TRY(run("zero_pad_rows_dy", s, fl,
-              [&] { return launch_zero_pad_rows(dyp, poff, counts, L.E, L.H, s); }));
 
   if (cfg->precision != MOE_BF16) {
     const BwdBufs bb{W_gate, W_up, W_down, dyp, xperm, h, poff, counts, mtile, order, slot_pad,
                      row_slot, w_row, w, idx, wrt, dh, aw, dwp, dl, dlt, scratch, dx,
                      dW_gate, dW_up, dW_down, ws, wflags,
-                     L.prepared ? const_cast<void*>(cfg->prepared_weights) : nullptr};
+                     L.prepared ? const_cast<void*>(cfg->prepared_weights) : nullptr,
+                     x_tok, x_tok_sf};
     MOE_TRY(backward_expert_gemms_mx(L, sms, s, fl, st, bb));
   } else {
     // B2-B4: down dgrad with the SwiGLU backward and router-weight partials

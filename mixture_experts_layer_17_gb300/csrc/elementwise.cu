@@ -158,70 +158,6 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ src, const int* 
   }
 }
 
-// gather_rows_kernel plus the MXFP8 copy along H: each 32-element block of
-// the token's row is quantised once (E4M3, E8M0 scale; 4 lanes per block)
-// and written to every slot's padded row of dstq, with the scale byte at the
-// row's place in the scale atoms of its expert's m-tile:
-// atom (mtile_off[e] + local / 128) * (H / 128) + h / 128, row local % 128.
-__global__ void gather_rows_mx_kernel(const uint16_t* __restrict__ src,
-                                      const int* __restrict__ slot_row,
-                                      const int* __restrict__ idx, const int* __restrict__ poff,
-                                      const int* __restrict__ mtile_off,
-                                      uint16_t* __restrict__ dst, uint8_t* __restrict__ dstq,
-                                      uint8_t* __restrict__ sf, int64_t T, int H, int k) {
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const int lane = threadIdx.x & 31;
-  int64_t rows[16];
-  int64_t atom_row[16];   // atom index of the slot's m-tile at column 0
-  int rin[16];            // row inside that m-tile
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    rows[j] = 0;
-    atom_row[j] = 0;
-    rin[j] = 0;
-    if (j < k) {
-      const int pr = slot_row[t * k + j];
-      const int e = idx[t * k + j];
-      const int local = pr - poff[e];
-      rows[j] = pr;
-      atom_row[j] = static_cast<int64_t>(mtile_off[e] + (local >> 7)) * (H >> 7);
-      rin[j] = local & 127;
-    }
-  }
-  const uint16_t* s = src + t * H;
-  const int nchunks = H >> 3;   // 8 elements per lane and step; H is a multiple of 256
-#pragma unroll 2
-  for (int c = lane; c < nchunks; c += 32) {
-    const uint4 v = ld_global_nc_v4(s + c * 8);
-    float f[8];
-    unpack_bf16x2(v.x, f[0], f[1]);
-    unpack_bf16x2(v.y, f[2], f[3]);
-    unpack_bf16x2(v.z, f[4], f[5]);
-    unpack_bf16x2(v.w, f[6], f[7]);
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    const int X = mx_exponent(amax);
-    const float inv = ldexpf(1.0f, -X);
-    const uint32_t q0 = to_e4m3x4(f[0], f[1], f[2], f[3], inv);
-    const uint32_t q1 = to_e4m3x4(f[4], f[5], f[6], f[7], inv);
-    const int blk = c >> 2;   // 32-element block along H
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (j < k) {
-        st_global_v4(dst + rows[j] * H + c * 8, v.x, v.y, v.z, v.w);
-        *reinterpret_cast<uint2*>(dstq + rows[j] * H + c * 8) = make_uint2(q0, q1);
-        if ((lane & 3) == 0)
-          sf[(atom_row[j] + (blk >> 2)) * 512 + sf_atom_offset(rin[j], blk & 3)] =
-              static_cast<uint8_t>(X + 127);
-      }
-    }
-  }
-}
-
 // Zeroes the tail rows [poff[e] + counts[e], poff[e+1]) of every expert's
 // padded segment of a [rows, H] bf16 matrix (one block per expert).
 __global__ void zero_pad_rows_kernel(uint16_t* __restrict__ m, const int* __restrict__ poff,
@@ -393,15 +329,6 @@ cudaError_t launch_zero_pad_rows(uint16_t* m, const int* poff, const int* counts
 cudaError_t launch_gather_rows(const uint16_t* src, const int* slot_row, uint16_t* dst,
                                int64_t T, int H, int k, cudaStream_t s) {
   gather_rows_kernel<<<blocks_for(T, 8), 256, 0, s>>>(src, slot_row, dst, T, H, k);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_gather_rows_mx(const uint16_t* src, const int* slot_row, const int* idx,
-                                  const int* poff, const int* mtile_off, uint16_t* dst,
-                                  uint8_t* dstq, uint8_t* sf, int64_t T, int H, int k,
-                                  cudaStream_t s) {
-  gather_rows_mx_kernel<<<blocks_for(T, 8), 256, 0, s>>>(src, slot_row, idx, poff, mtile_off, dst,
-                                                         dstq, sf, T, H, k);
   return cudaGetLastError();
 }
 

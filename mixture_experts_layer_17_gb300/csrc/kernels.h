@@ -47,6 +47,13 @@ cudaError_t launch_quant_cols_weights(const uint16_t* src, int E, int R, int C, 
                                       uint8_t* sf, cudaStream_t s);
 cudaError_t launch_quant_cols_gate_up(const uint16_t* W_gate, const uint16_t* W_up, int E, int H,
                                       int F, uint8_t* dst, uint8_t* sf, cudaStream_t s);
+// Dispatch of an activation [T, C] straight into its two MXFP8 copies: along
+// the tokens (token layout, 128-row expert segments) and along C (padded
+// permuted rows); no bf16 copy is written.
+cudaError_t launch_dispatch_quant(const uint16_t* src, const int* perm_token, const int* offsets,
+                                  const int* poff, const int* counts, const int* mtile_off,
+                                  int64_t max_ktiles, int E, int C, uint8_t* dst_t, uint8_t* sf_t,
+                                  uint8_t* dst_r, uint8_t* sf_r, cudaStream_t s);
 cudaError_t launch_quant_cols_tokens(const uint16_t* src, int64_t max_ktiles, int C, uint8_t* dst,
                                      uint8_t* sf, const int* poff, const int* counts,
                                      const int* mtile_off, int E, cudaStream_t s);
@@ -65,12 +72,6 @@ cudaError_t launch_zero_pad_rows(uint16_t* m, const int* poff, const int* counts
                                  cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t* src, const int* slot_row, uint16_t* dst,
                                int64_t T, int H, int k, cudaStream_t s);
-// launch_gather_rows plus the MXFP8 copy of every row along H (padded rows,
-// scale atoms of the expert m-tiles); idx = the slot's expert
-cudaError_t launch_gather_rows_mx(const uint16_t* src, const int* slot_row, const int* idx,
-                                  const int* poff, const int* mtile_off, uint16_t* dst,
-                                  uint8_t* dstq, uint8_t* sf, int64_t T, int H, int k,
-                                  cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* scratch, uint16_t* y, int64_t T, int H, int k,
                            cudaStream_t s);
 cudaError_t launch_router_bwd(const float* dw_part, int nparts, const int* slot_row,

@@ -187,6 +187,112 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(
   }
 }
 
+// Dispatch of an activation [T, C] (x, dY) straight into both MXFP8 copies the
+// expert GEMMs read, one 128-row k-tile of the token layout x 128 columns per
+// CTA.  The k-tile's rows are the expert's tokens (perm_token of the unpadded
+// permuted layout), gathered into shared memory; rows past the expert's count
+// are zero.  Then
+//   along the tokens (unless dst_t is null): the E4M3 tile at token-layout
+//     rows 128*kg + i with its scale atom kg * (C/128) + ct (as
+//     quant_cols_kernel<kColsTokens>);
+//   along C: E4M3 rows at the padded rows poff[e] + 128*g + i that lie inside
+//     the expert's padded segment, scale atom (mtile_off[e] + g) * (C/128) + ct
+//     (as quant_rows_kernel<kRowsPermuted>); a warp per row, 8 lanes per block.
+__global__ void __launch_bounds__(kColThreads) dispatch_quant_kernel(
+    const uint16_t* __restrict__ src, const int* __restrict__ perm_token,
+    const int* __restrict__ offsets, const int* __restrict__ poff, const int* __restrict__ counts,
+    const int* __restrict__ mtile_off, int E, int C, uint8_t* __restrict__ dst_t,
+    uint8_t* __restrict__ sf_t, uint8_t* __restrict__ dst_r, uint8_t* __restrict__ sf_r) {
+  __shared__ __align__(16) uint16_t tile[128][128];
+  __shared__ __align__(16) uint8_t qtile[128][128];
+  const int kg = blockIdx.x;
+  const int ct = blockIdx.y;
+  const int tid = threadIdx.x;
+  if (kg >= __ldg(mtile_off + E)) return;   // the grid is sized for the worst case
+  int lo = 0, hi = E - 1;                    // largest e with mtile_off[e] <= kg
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(mtile_off + mid) <= kg) lo = mid; else hi = mid - 1;
+  }
+  const int e = lo;
+  const int g = kg - __ldg(mtile_off + e);
+  const int local0 = 128 * g;
+  const int valid = min(128, __ldg(counts + e) - local0);
+  const int seg = min(128, __ldg(poff + e + 1) - __ldg(poff + e) - local0);
+  const int* toks = perm_token + __ldg(offsets + e) + local0;
+  // gather: 16 threads per row, 16 bytes each
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int chunk = tid + kColThreads * i;
+    const int row = chunk >> 4;
+    const int c8 = (chunk & 15) * 8;
+    uint4 u = make_uint4(0, 0, 0, 0);
+    if (row < valid) {
+      const int64_t tok = __ldg(toks + row);
+      u = ld_global_nc_v4(src + tok * C + ct * 128 + c8);
+    }
+    *reinterpret_cast<uint4*>(&tile[row][c8]) = u;
+  }
+  __syncthreads();
+  // along the tokens (dst_t may be null: not wanted): unit = (column c, 32-row block kb)
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if (dst_t == nullptr) break;
+    const int c = tid & 127;
+    const int kb = (tid >> 7) + 2 * i;
+    float v[32];
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      v[j] = __uint_as_float(static_cast<uint32_t>(tile[kb * 32 + j][c]) << 16);
+      amax = fmaxf(amax, fabsf(v[j]));
+    }
+    const int X = mx_exponent(amax);
+    const float inv = ldexpf(1.0f, -X);
+    sf_t[(static_cast<int64_t>(kg) * (C >> 7) + ct) * 512 + sf_atom_offset(c, kb)] =
+        static_cast<uint8_t>(X + 127);
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      const uint32_t q = to_e4m3x4(v[j], v[j + 1], v[j + 2], v[j + 3], inv);
+      qtile[kb * 32 + j][c] = static_cast<uint8_t>(q);
+      qtile[kb * 32 + j + 1][c] = static_cast<uint8_t>(q >> 8);
+      qtile[kb * 32 + j + 2][c] = static_cast<uint8_t>(q >> 16);
+      qtile[kb * 32 + j + 3][c] = static_cast<uint8_t>(q >> 24);
+    }
+  }
+  // along C: a warp per row of the padded segment, 4 columns per lane
+  {
+    const int warp = tid >> 5, lane = tid & 31;
+    const int64_t prow0 = static_cast<int64_t>(__ldg(poff + e)) + local0;
+    uint8_t* sfr = sf_r + (static_cast<int64_t>(__ldg(mtile_off + e) + g) * (C >> 7) + ct) * 512;
+#pragma unroll 1
+    for (int row = warp; row < seg; row += kColThreads / 32) {
+      const uint2 u = *reinterpret_cast<const uint2*>(&tile[row][4 * lane]);
+      float v[4];
+      unpack_bf16x2(u.x, v[0], v[1]);
+      unpack_bf16x2(u.y, v[2], v[3]);
+      float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+      for (int m = 1; m < 8; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+      const int X = mx_exponent(amax);
+      *reinterpret_cast<uint32_t*>(dst_r + (prow0 + row) * C + ct * 128 + 4 * lane) =
+          to_e4m3x4(v[0], v[1], v[2], v[3], ldexpf(1.0f, -X));
+      if ((lane & 7) == 0) sfr[sf_atom_offset(row, lane >> 3)] = static_cast<uint8_t>(X + 127);
+    }
+  }
+  __syncthreads();
+  if (dst_t == nullptr) return;
+  // the along-tokens tile leaves as whole rows
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int chunk = tid + kColThreads * i;
+    const int row = chunk >> 3;
+    const int c16 = (chunk & 7) * 16;
+    const uint4 q = *reinterpret_cast<const uint4*>(&qtile[row][c16]);
+    st_global_v4(dst_t + (128ll * kg + row) * C + ct * 128 + c16, q.x, q.y, q.z, q.w);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_quant_rows_dense(const uint16_t* src, int64_t R, int C, uint8_t* dst,
@@ -226,6 +332,16 @@ cudaError_t launch_quant_cols_tokens(const uint16_t* src, int64_t max_ktiles, in
   dim3 grid(static_cast<unsigned>(max_ktiles), static_cast<unsigned>(C / 128));
   quant_cols_kernel<kColsTokens><<<grid, kColThreads, 0, s>>>(src, nullptr, 0, C, dst, sf, poff, counts,
                                                      mtile_off, E);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_quant(const uint16_t* src, const int* perm_token, const int* offsets,
+                                  const int* poff, const int* counts, const int* mtile_off,
+                                  int64_t max_ktiles, int E, int C, uint8_t* dst_t, uint8_t* sf_t,
+                                  uint8_t* dst_r, uint8_t* sf_r, cudaStream_t s) {
+  dim3 grid(static_cast<unsigned>(max_ktiles), static_cast<unsigned>(C / 128));
+  dispatch_quant_kernel<<<grid, kColThreads, 0, s>>>(src, perm_token, offsets, poff, counts,
+                                                      mtile_off, E, C, dst_t, sf_t, dst_r, sf_r);
   return cudaGetLastError();
 }
 

@@ -60,10 +60,13 @@ def test_recompute_is_bit_identical(precision, shape):
     sh, inp = _inputs(shape, precision)
     keep = MoeLayer(sh.T, sh.H, sh.F, sh.E, sh.top_k, precision)
     rec = MoeLayer(sh.T, sh.H, sh.F, sh.E, sh.top_k, precision, flags=libmoe.MOE_FLAG_RECOMPUTE)
-    # ctx loses x_perm [Pa, H] and h [Pa, 2F] (Pa = P + 64 E rows, bf16)
+    # ctx loses h [Pa, 2F] (Pa = P + 64 E rows, bf16) and x: x_perm [Pa, H] bf16,
+    # or in mxfp8 x along the tokens [128 mt, H] E4M3 with its scale atoms
     Pa = sh.P + 64 * sh.E
+    mt = (sh.P + 127) // 128 + sh.E
+    x_bytes = 128 * mt * sh.H + mt * (sh.H // 128) * 512 if precision == "mxfp8" else 2 * Pa * sh.H
     saved = keep.ctx.numel() - rec.ctx.numel()
-    assert 2 * Pa * (sh.H + 2 * sh.F) <= saved <= 2 * Pa * (sh.H + 2 * sh.F) + 512
+    assert x_bytes + 4 * Pa * sh.F <= saved <= x_bytes + 4 * Pa * sh.F + 768
     y0, g0 = _run(keep, inp)
     args = _weights(inp)
     y1 = rec.forward(*args, inp["logit_bias"])
