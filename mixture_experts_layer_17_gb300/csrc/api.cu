@@ -827,7 +827,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     MOE_TRY(run("gate_up_dgrad_scatter_mx", s, fl, [&] { return launch_gate_up_dgrad_mx(a, grid, s); }));
   }
   MOE_TRY(run("unpermute_dx", s, fl, [&] {
-    return launch_unpermute(b.scratch, b.dl, b.idx, b.wrt, b.dx, L.T, L.H, L.k, s);
+    return launch_unpermute(b.scratch, b.dl, b.idx, b.wrt, b.dx, L.T, L.H, L.k, L.E, sms, s);
   }));
   // B8: gate/up wgrad over the padded token layout
   if (!x_ready) {
@@ -1285,7 +1285,7 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
       }
     }
     MOE_TRY(run("unpermute_dx", s, fl, [&] {
-      return launch_unpermute(scratch, dl, idx, wrt, dx, L.T, L.H, L.k, s);
+      return launch_unpermute(scratch, dl, idx, wrt, dx, L.T, L.H, L.k, L.E, sms, s);
     }));
     // B8: gate/up wgrad over the padded token segments
     {

@@ -368,14 +368,18 @@ MOE_DEV uint32_t idesc_with_sf_id(uint32_t idesc, uint32_t sf_id) {
 
 // OCP MX shared exponent of a block with absolute maximum amax:
 // floor(log2(amax)) - 8 (8 = exponent of E4M3's largest power of two),
-// clamped to E8M0's [-127, 127]; an all-zero block takes -127.
+// clamped to E8M0's [-127, 127]; an all-zero block takes -127.  For a finite
+// normal amax, floor(log2(amax)) is its IEEE biased exponent field minus 127;
+// a subnormal amax (field 0) lies below 2^-126 and clamps to -127 as well.
 MOE_DEV int mx_exponent(float amax) {
   if (!(amax > 0.f)) return -127;
-  int e;
-  frexpf(amax, &e);            // amax = m * 2^e, m in [0.5, 1)
-  const int x = (e - 1) - 8;
+  const int x = ((__float_as_int(amax) >> 23) & 0xff) - 127 - 8;
   return x < -127 ? -127 : (x > 127 ? 127 : x);
 }
+
+// 2^-X as an fp32 bit pattern, for the X that mx_exponent returns for finite
+// blocks (X <= 119, so the biased exponent 127 - X stays in [8, 254])
+MOE_DEV float mx_inv_scale(int X) { return __int_as_float((127 - X) << 23); }
 
 // Four fp32 values scaled by 2^-X, rounded to nearest even E4M3 with
 // saturation to +-448, packed little-endian into one word.

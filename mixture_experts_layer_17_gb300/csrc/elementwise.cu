@@ -3,6 +3,8 @@
 // (dispatch of x and dY), the k-way combine, the router softmax/top-k
 // backward, the un-permute with the router's input gradient, and two small
 // transposes.  Every index result is deterministic.
+#include <algorithm>
+
 #include "kernels.h"
 
 namespace moe {
@@ -240,23 +242,58 @@ __global__ void router_bwd_kernel(const float* __restrict__ dw_part, int nparts,
 // dx[t] = sum_j scratch[t*k + j] + sum_j dl[t, j] * W_r^T[idx[t, j]]
 // (the expert input gradients plus the router's input gradient dl · W_r^T,
 // whose only non-zero terms are the k selected experts).
-__global__ void unpermute_kernel(const uint16_t* __restrict__ scratch, const float* __restrict__ dl,
-                                 const int* __restrict__ idx, const uint16_t* __restrict__ WrT,
-                                 uint16_t* __restrict__ dx, int64_t T, int H, int k) {
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int cpr = H >> 3;
-  if (i >= T * cpr) return;
-  const int64_t t = i / cpr;
-  const int c = static_cast<int>(i - t * cpr) * 8;
-  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  const uint16_t* base = scratch + t * k * H + c;
-  for (int j = 0; j < k; ++j) {
-    add_bf16x8(ld_global_nc_v4(base + static_cast<int64_t>(j) * H), acc);
-    const int e = idx[t * k + j];
-    add_bf16x8(ld_global_nc_v4(WrT + static_cast<int64_t>(e) * H + c), acc, dl[t * k + j]);
+// A CTA owns a CW-column slice of dx and first copies that slice of W_r^T for
+// every expert (E x CW bf16, at most 64 KB) into shared memory, so the k
+// router terms of a chunk come from shared memory instead of L2.  Each warp
+// walks tokens, CW/8 lanes per token and 16 bytes per lane: all k slot loads
+// are issued before the sums (the first token's before the copy), and the
+// sums keep the order of the plain definition (slot j's expert gradient,
+// then its router term).
+template <int CW, int KMAX>
+__global__ void __launch_bounds__(256) unpermute_kernel(
+    const uint16_t* __restrict__ scratch, const float* __restrict__ dl,
+    const int* __restrict__ idx, const uint16_t* __restrict__ WrT, uint16_t* __restrict__ dx,
+    int64_t T, int H, int k, int E) {
+  extern __shared__ __align__(16) uint16_t wr_s[];   // [E][CW]
+  constexpr int kChunks = CW / 8;                    // 16-byte chunks per row = lanes per token
+  constexpr int kTokPerWarp = 32 / kChunks;
+  const int c0 = blockIdx.x * CW;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int cl = (lane % kChunks) * 8;
+  const int64_t step = static_cast<int64_t>(gridDim.y) * (blockDim.x >> 5) * kTokPerWarp;
+  const int64_t t0 = (static_cast<int64_t>(blockIdx.y) * (blockDim.x >> 5) + warp) * kTokPerWarp +
+                     lane / kChunks;
+  // the first token's slot loads are in flight while the slice of W_r^T is copied
+  uint4 v[KMAX];
+  if (t0 < T) {
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (j < k) v[j] = ld_global_nc_v4(scratch + (t0 * k + j) * H + c0 + cl);
   }
-  st_global_v4(dx + t * H + c, pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-               pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+  for (int i = threadIdx.x; i < E * kChunks; i += blockDim.x) {
+    const int e = i / kChunks, c = (i % kChunks) * 8;
+    *reinterpret_cast<uint4*>(wr_s + e * CW + c) =
+        ld_global_nc_v4(WrT + static_cast<int64_t>(e) * H + c0 + c);
+  }
+  __syncthreads();
+  for (int64_t t = t0; t < T; t += step) {
+    if (t != t0) {
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (j < k) v[j] = ld_global_nc_v4(scratch + (t * k + j) * H + c0 + cl);
+    }
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (j < k) {
+        add_bf16x8(v[j], acc);
+        const int e = __ldg(idx + t * k + j);
+        add_bf16x8(*reinterpret_cast<const uint4*>(wr_s + e * CW + cl), acc, __ldg(dl + t * k + j));
+      }
+    }
+    st_global_v4(dx + t * H + c0 + cl, pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                 pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+  }
 }
 
 // ---------------------------------------------------------------- B10: dW_r
@@ -346,12 +383,52 @@ cudaError_t launch_router_bwd(const float* dw_part, int nparts, const int* slot_
   return cudaGetLastError();
 }
 
-cudaError_t launch_unpermute(const uint16_t* scratch, const float* dl, const int* idx,
-                             const uint16_t* WrT, uint16_t* dx, int64_t T, int H, int k,
-                             cudaStream_t s) {
-  unpermute_kernel<<<blocks_for(T * (H / 8), 256), 256, 0, s>>>(scratch, dl, idx, WrT, dx, T, H,
-                                                                k);
+namespace {
+
+// grid: H / CW column slices x token groups, one wave of resident CTAs
+template <int CW, int KMAX>
+cudaError_t launch_unpermute_cw(const uint16_t* scratch, const float* dl, const int* idx,
+                                const uint16_t* WrT, uint16_t* dx, int64_t T, int H, int k, int E,
+                                int sms, cudaStream_t s) {
+  constexpr int kSmem = 65536;
+  static unsigned long long configured = 0ull;
+  static int per_sm[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(configured & bit)) {
+    e = cudaFuncSetAttribute(unpermute_kernel<CW, KMAX>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm[dev & 63], unpermute_kernel<CW, KMAX>,
+                                                      256, kSmem);
+    if (e != cudaSuccess) return e;
+    configured |= bit;
+  }
+  const int slices = H / CW;
+  const int64_t tok_per_cta = 8 * (32 / (CW / 8));
+  const int64_t want = static_cast<int64_t>(std::max(per_sm[dev & 63], 1)) * (sms > 0 ? sms : 1) / slices;
+  const int64_t groups = std::max<int64_t>(1, std::min<int64_t>(want, (T + tok_per_cta - 1) / tok_per_cta));
+  dim3 grid(static_cast<unsigned>(slices), static_cast<unsigned>(groups));
+  unpermute_kernel<CW, KMAX><<<grid, 256, static_cast<size_t>(E) * CW * 2, s>>>(
+      scratch, dl, idx, WrT, dx, T, H, k, E);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_unpermute(const uint16_t* scratch, const float* dl, const int* idx,
+                             const uint16_t* WrT, uint16_t* dx, int64_t T, int H, int k, int E,
+                             int sms, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  // E <= 256 and H % 256 == 0: E x CW x 2 bytes <= 64 KB and CW divides H
+  if (E <= 128) {
+    return k <= 8 ? launch_unpermute_cw<256, 8>(scratch, dl, idx, WrT, dx, T, H, k, E, sms, s)
+                  : launch_unpermute_cw<256, 16>(scratch, dl, idx, WrT, dx, T, H, k, E, sms, s);
+  }
+  return k <= 8 ? launch_unpermute_cw<128, 8>(scratch, dl, idx, WrT, dx, T, H, k, E, sms, s)
+                : launch_unpermute_cw<128, 16>(scratch, dl, idx, WrT, dx, T, H, k, E, sms, s);
 }
 
 cudaError_t launch_wr_reduce(const float* part, int S, int E, int H, void* dWr, bool accum_f32,

@@ -78,8 +78,8 @@ cudaError_t launch_router_bwd(const float* dw_part, int nparts, const int* slot_
                               const float* w, const int* idx, int64_t T, int k, float* dl,
                               uint16_t* dlT, int64_t T_pad, cudaStream_t s);
 cudaError_t launch_unpermute(const uint16_t* scratch, const float* dl, const int* idx,
-                             const uint16_t* WrT, uint16_t* dx, int64_t T, int H, int k,
-                             cudaStream_t s);
+                             const uint16_t* WrT, uint16_t* dx, int64_t T, int H, int k, int E,
+                             int sms, cudaStream_t s);
 cudaError_t launch_wr_reduce(const float* part, int S, int E, int H, void* dWr, bool accum_f32,
                              cudaStream_t s);
 

@@ -64,7 +64,7 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, int64_t R, i
 #pragma unroll
     for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
     const int X = mx_exponent(amax);
-    const float inv = ldexpf(1.0f, -X);
+    const float inv = mx_inv_scale(X);
     uint32_t w[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) w[i] = to_e4m3x4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], inv);
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(
       amax = fmaxf(amax, fabsf(v[j]));
     }
     const int X = mx_exponent(amax);
-    const float inv = ldexpf(1.0f, -X);
+    const float inv = mx_inv_scale(X);
     sf[atom * 512 + sf_atom_offset(c, kb)] = static_cast<uint8_t>(X + 127);
 #pragma unroll
     for (int j = 0; j < 32; j += 4) {
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(
 //     quant_cols_kernel<kColsTokens>);
 //   along C: E4M3 rows at the padded rows poff[e] + 128*g + i that lie inside
 //     the expert's padded segment, scale atom (mtile_off[e] + g) * (C/128) + ct
-//     (as quant_rows_kernel<kRowsPermuted>); a warp per row, 8 lanes per block.
+//     (as quant_rows_kernel<kRowsPermuted>).
 __global__ void __launch_bounds__(kColThreads) dispatch_quant_kernel(
     const uint16_t* __restrict__ src, const int* __restrict__ perm_token,
     const int* __restrict__ offsets, const int* __restrict__ poff, const int* __restrict__ counts,
@@ -234,50 +234,56 @@ __global__ void __launch_bounds__(kColThreads) dispatch_quant_kernel(
     *reinterpret_cast<uint4*>(&tile[row][c8]) = u;
   }
   __syncthreads();
-  // along the tokens (dst_t may be null: not wanted): unit = (column c, 32-row block kb)
+  // along the tokens (dst_t may be null: not wanted): a thread takes the
+  // column pair (2 cp, 2 cp + 1) of 32-row block kb; |max| of each column by
+  // bf16x2 max (exact), E4M3 written as byte pairs of one row
+  if (dst_t != nullptr) {
+    const int cp = tid & 63;
+    const int kb = tid >> 6;
+    __nv_bfloat162 amax2 = __float2bfloat162_rn(0.f);
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    if (dst_t == nullptr) break;
-    const int c = tid & 127;
-    const int kb = (tid >> 7) + 2 * i;
-    float v[32];
-    float amax = 0.f;
+    for (int j = 0; j < 32; ++j)
+      amax2 = __hmax2(amax2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&tile[kb * 32 + j][2 * cp])));
+    const int X0 = mx_exponent(__low2float(amax2));
+    const int X1 = mx_exponent(__high2float(amax2));
+    const float inv0 = mx_inv_scale(X0), inv1 = mx_inv_scale(X1);
+    uint8_t* sft = sf_t + (static_cast<int64_t>(kg) * (C >> 7) + ct) * 512;
+    sft[sf_atom_offset(2 * cp, kb)] = static_cast<uint8_t>(X0 + 127);
+    sft[sf_atom_offset(2 * cp + 1, kb)] = static_cast<uint8_t>(X1 + 127);
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
-      v[j] = __uint_as_float(static_cast<uint32_t>(tile[kb * 32 + j][c]) << 16);
-      amax = fmaxf(amax, fabsf(v[j]));
-    }
-    const int X = mx_exponent(amax);
-    const float inv = ldexpf(1.0f, -X);
-    sf_t[(static_cast<int64_t>(kg) * (C >> 7) + ct) * 512 + sf_atom_offset(c, kb)] =
-        static_cast<uint8_t>(X + 127);
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      const uint32_t q = to_e4m3x4(v[j], v[j + 1], v[j + 2], v[j + 3], inv);
-      qtile[kb * 32 + j][c] = static_cast<uint8_t>(q);
-      qtile[kb * 32 + j + 1][c] = static_cast<uint8_t>(q >> 8);
-      qtile[kb * 32 + j + 2][c] = static_cast<uint8_t>(q >> 16);
-      qtile[kb * 32 + j + 3][c] = static_cast<uint8_t>(q >> 24);
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[kb * 32 + j][2 * cp]);
+      const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+      *reinterpret_cast<__nv_fp8x2_storage_t*>(&qtile[kb * 32 + j][2 * cp]) =
+          __nv_cvt_float2_to_fp8x2(make_float2(lo * inv0, hi * inv1), __NV_SATFINITE, __NV_E4M3);
     }
   }
-  // along C: a warp per row of the padded segment, 4 columns per lane
+  // along C: 16 lanes per row (8 columns each, 4 lanes per 32-column block),
+  // two rows per warp step
   {
     const int warp = tid >> 5, lane = tid & 31;
+    const int half = lane >> 4, c8 = (lane & 15) * 8;
     const int64_t prow0 = static_cast<int64_t>(__ldg(poff + e)) + local0;
     uint8_t* sfr = sf_r + (static_cast<int64_t>(__ldg(mtile_off + e) + g) * (C >> 7) + ct) * 512;
 #pragma unroll 1
-    for (int row = warp; row < seg; row += kColThreads / 32) {
-      const uint2 u = *reinterpret_cast<const uint2*>(&tile[row][4 * lane]);
-      float v[4];
+    for (int row = 2 * warp + half; row < seg; row += kColThreads / 16) {
+      const uint4 u = *reinterpret_cast<const uint4*>(&tile[row][c8]);
+      float v[8];
       unpack_bf16x2(u.x, v[0], v[1]);
       unpack_bf16x2(u.y, v[2], v[3]);
-      float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+      unpack_bf16x2(u.z, v[4], v[5]);
+      unpack_bf16x2(u.w, v[6], v[7]);
+      float amax = 0.f;
 #pragma unroll
-      for (int m = 1; m < 8; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
       const int X = mx_exponent(amax);
-      *reinterpret_cast<uint32_t*>(dst_r + (prow0 + row) * C + ct * 128 + 4 * lane) =
-          to_e4m3x4(v[0], v[1], v[2], v[3], ldexpf(1.0f, -X));
-      if ((lane & 7) == 0) sfr[sf_atom_offset(row, lane >> 3)] = static_cast<uint8_t>(X + 127);
+      const float inv = mx_inv_scale(X);
+      const uint2 q = make_uint2(to_e4m3x4(v[0], v[1], v[2], v[3], inv),
+                                 to_e4m3x4(v[4], v[5], v[6], v[7], inv));
+      *reinterpret_cast<uint2*>(dst_r + (prow0 + row) * C + ct * 128 + c8) = q;
+      if ((lane & 3) == 0) sfr[sf_atom_offset(row, (lane & 15) >> 2)] = static_cast<uint8_t>(X + 127);
     }
   }
   __syncthreads();

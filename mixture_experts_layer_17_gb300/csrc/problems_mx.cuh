@@ -23,7 +23,7 @@ MOE_DEV void mx_block_store(const float (&v)[32], uint8_t* dst, uint8_t* scale) 
 #pragma unroll
   for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
   const int X = mx_exponent(amax);
-  const float inv = ldexpf(1.0f, -X);
+  const float inv = mx_inv_scale(X);
   uint32_t w[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) w[i] = to_e4m3x4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], inv);
@@ -161,7 +161,7 @@ struct GateUpFwdMXProblem {
 #pragma unroll
       for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
       const int X = mx_exponent(amax);
-      const float inv = ldexpf(1.0f, -X);
+      const float inv = mx_inv_scale(X);
       uint32_t w[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) w[i] = to_e4m3x4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], inv);

@@ -66,6 +66,8 @@ SWEEP = [
     (129, 256, 512, 256, 16, 15),   # E = 256, top-16: router N = 256
     (1, 256, 128, 8, 2, 16),        # a single token: two rows in two experts
     (100, 256, 128, 1, 1, 17),      # one expert, top-1: a plain SwiGLU FFN, w = 1, dW_r = 0
+    (200, 256, 128, 64, 12, 18),    # top-12 of 64 experts
+    (150, 512, 128, 160, 6, 19),    # E = 160 > 128 experts, top-6
 ]
 
 
