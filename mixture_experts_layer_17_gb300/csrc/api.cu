@@ -323,7 +323,7 @@ Layout make_layout(const moe_config_t& c, int sms) {
 
   Carver b;
   L.b_status = b.take(sizeof(DeviceStatus));
-  L.b_dyp = b.take(2 * Pa * H);
+  if (c.precision == MOE_BF16) L.b_dyp = b.take(2 * Pa * H);   // MXFP8 dispatches dY to E4M3
   L.b_dh = b.take(2 * Pa * 2 * F);
   L.b_aw = b.take(2 * Pa * F);
   L.b_dwp = b.take(sizeof(float) * Pa * L.nparts);
@@ -363,8 +363,10 @@ Layout make_layout(const moe_config_t& c, int sms) {
     L.bs_awt = b.take(mt * (F / 128) * 512);
     L.bq_dyt = b.take(Pp * H);
     L.bs_dyt = b.take(mt * (H / 128) * 512);
-    L.bq_xt = b.take(Pp * H);
-    L.bs_xt = b.take(mt * (H / 128) * 512);
+    if (c.precision == MOE_FP8_BWD || L.recompute) {   // else x along tokens is in ctx
+      L.bq_xt = b.take(Pp * H);
+      L.bs_xt = b.take(mt * (H / 128) * 512);
+    }
     L.bq_dht = b.take(Pp * 2 * F);
     L.bs_dht = b.take(mt * (2 * F / 128) * 512);
   }
@@ -684,7 +686,7 @@ struct BwdBufs {
   void* ws;
   uint32_t wflags;                   // kGemmAccumF32 or 0, for the weight gradients
   void* wq;                          // prepared MXFP8 weights, or nullptr
-  const uint8_t *xt, *sxt;           // x along the tokens already in E4M3, or nullptr
+  const uint8_t *xt, *sxt;           // x along the tokens in E4M3 with its scale atoms
 };
 
 // B2-B9 in MXFP8 (precision mxfp8 and fp8_bwd): every expert GEMM of the
@@ -710,9 +712,8 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
   uint8_t* sawt = at<uint8_t>(ws, L.bs_awt);
   uint8_t* dyt = at<uint8_t>(ws, L.bq_dyt);
   uint8_t* sdyt = at<uint8_t>(ws, L.bs_dyt);
-  const bool x_ready = b.xt != nullptr;
-  uint8_t* xt = x_ready ? const_cast<uint8_t*>(b.xt) : at<uint8_t>(ws, L.bq_xt);
-  uint8_t* sxt = x_ready ? const_cast<uint8_t*>(b.sxt) : at<uint8_t>(ws, L.bs_xt);
+  const uint8_t* xt = b.xt;
+  const uint8_t* sxt = b.sxt;
   uint8_t* dht = at<uint8_t>(ws, L.bq_dht);
   uint8_t* sdht = at<uint8_t>(ws, L.bs_dht);
   const uint64_t Pp = 128ull * static_cast<uint64_t>(L.mt_max);
@@ -830,12 +831,6 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     return launch_unpermute(b.scratch, b.dl, b.idx, b.wrt, b.dx, L.T, L.H, L.k, L.E, sms, s);
   }));
   // B8: gate/up wgrad over the padded token layout
-  if (!x_ready) {
-    MOE_TRY(run("mx_quant_x_tokens", s, fl, [&] {
-      return launch_quant_cols_tokens(b.xperm, L.mt_max, L.H, xt, sxt, b.offsets, b.counts,
-                                      b.mtile, L.E, s);
-    }));
-  }
   MOE_TRY(run("mx_quant_dh_tokens", s, fl, [&] {
     return launch_quant_cols_tokens(b.dh, L.mt_max, 2 * L.F, dht, sdht, b.offsets, b.counts,
                                     b.mtile, L.E, s);
@@ -1021,10 +1016,9 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
                                    at<uint8_t>(ws, L.fq_x), at<uint8_t>(ws, L.fs_x), s);
     }));
   } else {
-    MOE_TRY(run("gather_x", s, fl,
-                [&] { return launch_gather_rows(x, slot_pad, xperm, L.T, L.H, L.k, s); }));
-    MOE_TRY(run("zero_pad_rows_x", s, fl,
-                [&] { return launch_zero_pad_rows(xperm, poff, counts, L.E, L.H, s); }));
+    MOE_TRY(run("gather_x", s, fl, [&] {
+      return launch_gather_rows(x, slot_pad, xperm, L.T, L.H, L.k, poff, counts, L.E, s);
+    }));
   }
 
   if (cfg->precision == MOE_MXFP8) {
@@ -1104,13 +1098,17 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
   const uint16_t* wrt = at<uint16_t>(ctx, L.c_wrt);
   const uint16_t* xperm = L.recompute ? at<uint16_t>(ws, L.b_xperm) : at<uint16_t>(ctx, L.c_xperm);
   const uint16_t* h = L.recompute ? at<uint16_t>(ws, L.b_h) : at<uint16_t>(ctx, L.c_h);
-  // mxfp8: x along the tokens comes from the forward's dispatch (ctx) or from
-  // the recompute dispatch below (ws); fp8_bwd quantises it from x_perm
+  // x along the tokens in E4M3 for the gate/up wgrad: mxfp8 has it from the
+  // forward's dispatch (ctx) or from the recompute dispatch below (ws);
+  // fp8_bwd (bf16 forward) dispatches x into ws with the dY dispatch
   const uint8_t* x_tok = nullptr;
   const uint8_t* x_tok_sf = nullptr;
-  if (cfg->precision == MOE_MXFP8) {
-    x_tok = L.recompute ? at<uint8_t>(ws, L.bq_xt) : at<uint8_t>(ctx, L.c_xt);
-    x_tok_sf = L.recompute ? at<uint8_t>(ws, L.bs_xt) : at<uint8_t>(ctx, L.c_sxt);
+  if (cfg->precision == MOE_MXFP8 && !L.recompute) {
+    x_tok = at<uint8_t>(ctx, L.c_xt);
+    x_tok_sf = at<uint8_t>(ctx, L.c_sxt);
+  } else if (cfg->precision != MOE_BF16) {
+    x_tok = at<uint8_t>(ws, L.bq_xt);
+    x_tok_sf = at<uint8_t>(ws, L.bs_xt);
   }
   uint16_t* dyp = at<uint16_t>(ws, L.b_dyp);
   uint16_t* dh = at<uint16_t>(ws, L.b_dh);
@@ -1136,10 +1134,9 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
                                      at<uint8_t>(ws, L.bs_rx), s);
       }));
     } else {
-      MOE_TRY(run("recompute_gather_x", s, fl,
-                  [&] { return launch_gather_rows(x, slot_pad, xp, L.T, L.H, L.k, s); }));
-      MOE_TRY(run("recompute_zero_pad_rows_x", s, fl,
-                  [&] { return launch_zero_pad_rows(xp, poff, counts, L.E, L.H, s); }));
+      MOE_TRY(run("recompute_gather_x", s, fl, [&] {
+        return launch_gather_rows(x, slot_pad, xp, L.T, L.H, L.k, poff, counts, L.E, s);
+      }));
     }
     if (cfg->precision == MOE_MXFP8) {
       MxGateUpBufs q{at<uint8_t>(ws, L.bq_rx), at<uint8_t>(ws, L.bs_rx),
@@ -1162,6 +1159,14 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
 
   // B1: dispatch dY to the padded expert-major rows (segment tails zeroed:
   // they are K rows of the down weight gradient)
+  if (cfg->precision == MOE_FP8_BWD) {
+    // x along the tokens only (the bf16 forward kept x_perm, not this copy)
+    MOE_TRY(run("dispatch_x_tokens_mx", s, fl, [&] {
+      return launch_dispatch_quant(x, at<int>(ctx, L.c_perm), at<int>(ctx, L.c_offsets), poff,
+                                   counts, mtile, L.mt_max, L.E, L.H, at<uint8_t>(ws, L.bq_xt),
+                                   at<uint8_t>(ws, L.bs_xt), nullptr, nullptr, s);
+    }));
+  }
   if (cfg->precision != MOE_BF16) {
     // MXFP8: dY dispatched straight into its two E4M3 copies (along H for the
     // down dgrad, along the tokens for the down wgrad); no bf16 dY_perm
@@ -1172,10 +1177,9 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
                                    at<uint8_t>(ws, L.bs_dy), s);
     }));
   } else {
-    MOE_TRY(run("gather_dy", s, fl,
-                [&] { return launch_gather_rows(dY, slot_pad, dyp, L.T, L.H, L.k, s); }));
-    MOE_TRY(run("zero_pad_rows_dy", s, fl,
-                [&] { return launch_zero_pad_rows(dyp, poff, counts, L.E, L.H, s); }));
+    MOE_TRY(run("gather_dy", s, fl, [&] {
+      return launch_gather_rows(dY, slot_pad, dyp, L.T, L.H, L.k, poff, counts, L.E, s);
+    }));
   }
 
   if (cfg->precision != MOE_BF16) {

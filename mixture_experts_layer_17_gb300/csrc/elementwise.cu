@@ -140,9 +140,26 @@ __global__ void permute_kernel(const int* __restrict__ idx, const float* __restr
 // ---------------------------------------------------------------- F6/B1: dispatch
 
 // dst[slot_row[t, j]] = src[t] for every slot j: one warp per token reads the
-// token's row once (16-byte vectors) and writes its k copies.
+// token's row once (16-byte vectors) and writes its k copies.  The E blocks
+// after the token blocks zero the tail rows [poff[e] + counts[e], poff[e+1])
+// of each expert's padded segment (one block per expert); no token row lies
+// there.
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ src, const int* __restrict__ slot_row,
-                                   uint16_t* __restrict__ dst, int64_t T, int H, int k) {
+                                   uint16_t* __restrict__ dst, int64_t T, int H, int k,
+                                   const int* __restrict__ poff, const int* __restrict__ counts,
+                                   unsigned token_blocks) {
+  if (blockIdx.x >= token_blocks) {
+    const int e = static_cast<int>(blockIdx.x - token_blocks);
+    const int64_t r0 = static_cast<int64_t>(__ldg(poff + e)) + __ldg(counts + e);
+    const int64_t r1 = __ldg(poff + e + 1);
+    const int cpr = H >> 3;
+    for (int64_t i = threadIdx.x; i < (r1 - r0) * cpr; i += blockDim.x) {
+      const int64_t row = r0 + i / cpr;
+      const int c = static_cast<int>(i % cpr) * 8;
+      st_global_v4(dst + row * H + c, 0u, 0u, 0u, 0u);
+    }
+    return;
+  }
   const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
   const int lane = threadIdx.x & 31;
@@ -157,21 +174,6 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ src, const int* 
 #pragma unroll
     for (int j = 0; j < 16; ++j)
       if (j < k) st_global_v4(dst + rows[j] + c * 8, v.x, v.y, v.z, v.w);
-  }
-}
-
-// Zeroes the tail rows [poff[e] + counts[e], poff[e+1]) of every expert's
-// padded segment of a [rows, H] bf16 matrix (one block per expert).
-__global__ void zero_pad_rows_kernel(uint16_t* __restrict__ m, const int* __restrict__ poff,
-                                     const int* __restrict__ counts, int H) {
-  const int e = blockIdx.x;
-  const int64_t r0 = static_cast<int64_t>(poff[e]) + counts[e];
-  const int64_t r1 = poff[e + 1];
-  const int cpr = H >> 3;
-  for (int64_t i = threadIdx.x; i < (r1 - r0) * cpr; i += blockDim.x) {
-    const int64_t row = r0 + i / cpr;
-    const int c = static_cast<int>(i % cpr) * 8;
-    st_global_v4(m + row * H + c, 0u, 0u, 0u, 0u);
   }
 }
 
@@ -357,15 +359,13 @@ cudaError_t launch_permute(const int* idx, const float* w, const int* block_base
   return cudaGetLastError();
 }
 
-cudaError_t launch_zero_pad_rows(uint16_t* m, const int* poff, const int* counts, int E, int H,
-                                 cudaStream_t s) {
-  zero_pad_rows_kernel<<<E, 256, 0, s>>>(m, poff, counts, H);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_gather_rows(const uint16_t* src, const int* slot_row, uint16_t* dst,
-                               int64_t T, int H, int k, cudaStream_t s) {
-  gather_rows_kernel<<<blocks_for(T, 8), 256, 0, s>>>(src, slot_row, dst, T, H, k);
+                               int64_t T, int H, int k, const int* poff, const int* counts, int E,
+                               cudaStream_t s) {
+  const unsigned token_blocks = blocks_for(T, 8);
+  if (token_blocks + E == 0) return cudaSuccess;
+  gather_rows_kernel<<<token_blocks + static_cast<unsigned>(E), 256, 0, s>>>(
+      src, slot_row, dst, T, H, k, poff, counts, token_blocks);
   return cudaGetLastError();
 }
 

@@ -68,10 +68,11 @@ cudaError_t launch_permute(const int* idx, const float* w, const int* block_base
                            const int* offsets, const int* poff, int64_t T, int k, int E,
                            int* perm_token, int* slot_row, int* slot_pad, int* row_slot,
                            float* w_row, cudaStream_t s);
-cudaError_t launch_zero_pad_rows(uint16_t* m, const int* poff, const int* counts, int E, int H,
-                                 cudaStream_t s);
+// dst[slot_row[t, j]] = src[t] for every slot, and the tail rows of each
+// expert's padded segment ([poff[e] + counts[e], poff[e+1])) zeroed
 cudaError_t launch_gather_rows(const uint16_t* src, const int* slot_row, uint16_t* dst,
-                               int64_t T, int H, int k, cudaStream_t s);
+                               int64_t T, int H, int k, const int* poff, const int* counts, int E,
+                               cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* scratch, uint16_t* y, int64_t T, int H, int k,
                            cudaStream_t s);
 cudaError_t launch_router_bwd(const float* dw_part, int nparts, const int* slot_row,

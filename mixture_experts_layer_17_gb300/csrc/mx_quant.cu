@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(
 //   along the tokens (unless dst_t is null): the E4M3 tile at token-layout
 //     rows 128*kg + i with its scale atom kg * (C/128) + ct (as
 //     quant_cols_kernel<kColsTokens>);
-//   along C: E4M3 rows at the padded rows poff[e] + 128*g + i that lie inside
+//   along C (unless dst_r is null): E4M3 rows at the padded rows poff[e] + 128*g + i that lie inside
 //     the expert's padded segment, scale atom (mtile_off[e] + g) * (C/128) + ct
 //     (as quant_rows_kernel<kRowsPermuted>).
 __global__ void __launch_bounds__(kColThreads) dispatch_quant_kernel(
@@ -258,9 +258,9 @@ __global__ void __launch_bounds__(kColThreads) dispatch_quant_kernel(
           __nv_cvt_float2_to_fp8x2(make_float2(lo * inv0, hi * inv1), __NV_SATFINITE, __NV_E4M3);
     }
   }
-  // along C: 16 lanes per row (8 columns each, 4 lanes per 32-column block),
-  // two rows per warp step
-  {
+  // along C (unless dst_r is null): 16 lanes per row (8 columns each, 4 lanes
+  // per 32-column block), two rows per warp step
+  if (dst_r != nullptr) {
     const int warp = tid >> 5, lane = tid & 31;
     const int half = lane >> 4, c8 = (lane & 15) * 8;
     const int64_t prow0 = static_cast<int64_t>(__ldg(poff + e)) + local0;
