@@ -72,7 +72,8 @@ EncodeTiledFn encode_fn() {
 // stride; boxes of box_rows x box_cols (box_cols * 2 = 128 bytes) with the
 // 128-byte swizzle.  Reads outside the matrix return zeros.
 bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
-              uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows) {
+              uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -80,7 +81,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -730,7 +731,11 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     if (!make_map_u8(&a.mapA, dyq, L.H, L.Pa, L.H) ||
         !make_map_u8(&a.mapB0, wdh, L.H, static_cast<uint64_t>(L.E) * L.F, L.H))
       return MOE_ERR_CUDA;
-    a.mapB1 = a.mapB0;
+    // h [Pa, 2F] in 32 x 32 boxes with the 64-byte swizzle: the epilogue's TMA
+    // loads of the saved pre-activations into its staging buffers
+    if (!make_map(&a.mapB1, b.h, 2ull * L.F, L.Pa, 4ull * L.F, 32, 32,
+                  CU_TENSOR_MAP_SWIZZLE_64B))
+      return MOE_ERR_CUDA;
     a.K = L.H;
     a.N = L.F;
     a.n_tiles = L.F / L.mx_dgrad_bn;

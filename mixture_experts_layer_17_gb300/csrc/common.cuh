@@ -30,6 +30,7 @@ enum : int {
   kWaitEpiTmemFull = 4,
   kWaitInjected = 5,
   kWaitDrain = 6,
+  kWaitEpiLoad = 7,   // an epilogue's own TMA load of an operand it reads
 };
 
 constexpr int kStatusTimeout = 5;  // == MOE_ERR_TIMEOUT

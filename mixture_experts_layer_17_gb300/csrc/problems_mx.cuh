@@ -247,13 +247,35 @@ struct DownDgradMXProblem {
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
   static constexpr bool kMX = true;
-  // kStaged: dh_gate, dh_up and w*a leave through three 2 KB stages per warp
-  static constexpr size_t kExtraSmem = kStaged ? 8 * 3 * kStage64WarpBytes : 0;
+  // kStaged: each epilogue warp owns three 2 KB buffers (1024-byte aligned,
+  // hence up to 1 KB of lead-in) and an mbarrier.  Per 32-column step, TMA
+  // brings the warp's 32 rows of h_gate and h_up into the first two (64-byte
+  // swizzle, the stage64 layout) and the threads read their rows from there;
+  // then dh_gate, dh_up and w*a are staged in the three buffers and leave as
+  // whole 64-byte row pieces.
+  static constexpr size_t kStageBytes = 8 * 3 * kStage64WarpBytes;
+  static constexpr size_t kExtraSmem = kStaged ? 1024 + kStageBytes + 8 * sizeof(uint64_t) : 0;
   static constexpr int kEpiGroups = 2;
+  // two steps per warp and tile keep the parity of each warp's barrier in
+  // step with the step index from one tile to the next
+  static_assert(!kStaged || (BN / 2 / 32) % 2 == 0, "an even number of h steps per tile");
+
+  MOE_DEV static uint8_t* stage_base(uint8_t* extra) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(extra) + 1023) &
+                                      ~static_cast<uintptr_t>(1023));
+  }
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
   MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile_mx(a, t, BN); }
-  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t* extra) {
+    if constexpr (kStaged) {
+      if (threadIdx.x == 0) {
+        uint64_t* bars = reinterpret_cast<uint64_t*>(stage_base(extra) + kStageBytes);
+        for (int w = 0; w < 8; ++w) mbar_init(bars + w, 1);
+        fence_mbar_init();
+      }
+    }
+  }
   MOE_DEV static void load_mx(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
                               uint8_t* sB, uint8_t* sSF, uint64_t* bar) {
     const int k0 = kb * 128;
@@ -275,7 +297,10 @@ struct DownDgradMXProblem {
     const bool valid = r < ti.rows;
     const bool pad = !valid && r < ti.rows_pad;
     const int lane = r & 31;
-    uint8_t* st = kStaged ? extra + (group * 4 + (r >> 5)) * 3 * kStage64WarpBytes : nullptr;
+    const int wslot = group * 4 + (r >> 5);
+    uint8_t* st = kStaged ? stage_base(extra) + wslot * 3 * kStage64WarpBytes : nullptr;
+    uint64_t* hbar = kStaged ? reinterpret_cast<uint64_t*>(stage_base(extra) + kStageBytes) + wslot
+                             : nullptr;
     const int64_t row = static_cast<int64_t>(ti.m0) + ((valid || pad) ? r : 0);
     const int F = a.ld0;
     const int c0 = group * kHalf;
@@ -290,13 +315,48 @@ struct DownDgradMXProblem {
 #pragma unroll 1
     for (int c = c0; c < c0 + kHalf; c += 32) {
       float g[32];
-      tmem_ld32(taddr + c, g);
+      if constexpr (kStaged) {
+        // the warp's 32 rows of h_gate and h_up for columns [c, c + 32) into
+        // the first two buffers; every lane's earlier accesses to them are
+        // ordered before the asynchronous writes
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int y = ti.m0 + (r & ~31);
+          mbar_arrive_expect_tx(hbar, 2 * kStage64WarpBytes);
+          tma_load_2d(st, &a.mapB1, ti.n0 + c, y, hbar);
+          tma_load_2d(st + kStage64WarpBytes, &a.mapB1, F + ti.n0 + c, y, hbar);
+        }
+        tmem_ld32(taddr + c, g);
+        const int never = 0;   // this wait is cut short only by its time limit
+        if (!mbar_wait_bounded(hbar, static_cast<uint32_t>(((c - c0) >> 5) & 1), &never,
+                               a.wait_limit_ns))
+          record_timeout(a.status, kWaitEpiLoad);
+      } else {
+        tmem_ld32(taddr + c, g);
+      }
       if (valid) {
         float hg[32], hu[32], dhg[32], dhu[32], awv[32];
-        load_bf16x16(h + c, *reinterpret_cast<float(*)[16]>(hg));
-        load_bf16x16(h + c + 16, *reinterpret_cast<float(*)[16]>(hg + 16));
-        load_bf16x16(h + F + c, *reinterpret_cast<float(*)[16]>(hu));
-        load_bf16x16(h + F + c + 16, *reinterpret_cast<float(*)[16]>(hu + 16));
+        if constexpr (kStaged) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 ug = *reinterpret_cast<const uint4*>(st + stage64_off(lane, q));
+            const uint4 uu = *reinterpret_cast<const uint4*>(st + kStage64WarpBytes + stage64_off(lane, q));
+            unpack_bf16x2(ug.x, hg[8 * q + 0], hg[8 * q + 1]);
+            unpack_bf16x2(ug.y, hg[8 * q + 2], hg[8 * q + 3]);
+            unpack_bf16x2(ug.z, hg[8 * q + 4], hg[8 * q + 5]);
+            unpack_bf16x2(ug.w, hg[8 * q + 6], hg[8 * q + 7]);
+            unpack_bf16x2(uu.x, hu[8 * q + 0], hu[8 * q + 1]);
+            unpack_bf16x2(uu.y, hu[8 * q + 2], hu[8 * q + 3]);
+            unpack_bf16x2(uu.z, hu[8 * q + 4], hu[8 * q + 5]);
+            unpack_bf16x2(uu.w, hu[8 * q + 6], hu[8 * q + 7]);
+          }
+        } else {
+          load_bf16x16(h + c, *reinterpret_cast<float(*)[16]>(hg));
+          load_bf16x16(h + c + 16, *reinterpret_cast<float(*)[16]>(hg + 16));
+          load_bf16x16(h + F + c, *reinterpret_cast<float(*)[16]>(hu));
+          load_bf16x16(h + F + c + 16, *reinterpret_cast<float(*)[16]>(hu + 16));
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float s = sigmoidf_fast(hg[i]);
