@@ -1203,6 +1203,11 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
                     L.pair_down_dgrad ? 128 : L.dgrad_bn))
         return MOE_ERR_CUDA;
       a.mapB1 = a.mapB0;
+      // CTA pairs: h [Pa, 2F] in 32 x 32 boxes with the 64-byte swizzle, for the
+      // epilogue's TMA loads of the saved pre-activations
+      if (L.pair_down_dgrad && !make_map(&a.mapB1, h, 2ull * L.F, L.Pa, 4ull * L.F, 32, 32,
+                                         CU_TENSOR_MAP_SWIZZLE_64B))
+        return MOE_ERR_CUDA;
       a.K = L.H;
       a.N = L.F;
       a.n_tiles = L.F / L.dgrad_bn;

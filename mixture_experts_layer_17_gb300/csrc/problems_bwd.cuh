@@ -19,21 +19,43 @@ namespace moe {
 //   out0 = dh bf16 [P, 2F];  out1 = aw bf16 [P, F];
 //   out2 = dw_part f32 [P, 2 * n_tiles] (one partial per n-tile and column half)
 //   ld0 = F;  K = H;  n_tiles = F / BN;  b_group_rows = F
+//   mapB1 (kStaged) = h [P, 2F] in 32 x 32 boxes with the 64-byte swizzle
 // ------------------------------------------------------------------------
 template <int BN_, bool kStaged = false>
 struct DownDgradProblem {
   static constexpr int BN = BN_;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
-  // kStaged: dh_gate, dh_up and w*a leave through three 2 KB stages per
-  // epilogue warp as whole half-lines (the CTA-pair version, which has the
-  // shared memory for them at five stages)
-  static constexpr size_t kExtraSmem = kStaged ? 8 * 3 * kStage64WarpBytes : 0;
+  // kStaged (the CTA-pair version, which has the shared memory for it at five
+  // stages): each epilogue warp owns three 2 KB buffers (1024-byte aligned,
+  // hence up to 1 KB of lead-in) and an mbarrier.  Per 32-column step, TMA
+  // brings the warp's 32 rows of h_gate and h_up into the first two (64-byte
+  // swizzle, the stage64 layout) and every thread keeps its row of both as
+  // packed words; dh_gate, dh_up and w*a are then staged in the three
+  // buffers and leave as whole 64-byte row pieces.
+  static constexpr size_t kStageBytes = 8 * 3 * kStage64WarpBytes;
+  static constexpr size_t kExtraSmem = kStaged ? 1024 + kStageBytes + 8 * sizeof(uint64_t) : 0;
   static constexpr int kEpiGroups = 2;
+  // an even number of steps per warp and tile keeps the parity of each
+  // warp's barrier in step with the step index from one tile to the next
+  static_assert(!kStaged || (BN / 2 / 32) % 2 == 0, "an even number of h steps per tile");
+
+  MOE_DEV static uint8_t* stage_base(uint8_t* extra) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(extra) + 1023) &
+                                      ~static_cast<uintptr_t>(1023));
+  }
 
   MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles(a); }
   MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile(a, t, BN); }
-  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t* extra) {
+    if constexpr (kStaged) {
+      if (threadIdx.x == 0) {
+        uint64_t* bars = reinterpret_cast<uint64_t*>(stage_base(extra) + kStageBytes);
+        for (int w = 0; w < 8; ++w) mbar_init(bars + w, 1);
+        fence_mbar_init();
+      }
+    }
+  }
   MOE_DEV static void load(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
                            uint8_t* sB, uint64_t* bar) {
     const int k0 = kb * kBK;
@@ -41,18 +63,114 @@ struct DownDgradProblem {
     tma_load_2d(sB, &a.mapB0, k0, ti.e * a.b_group_rows + ti.n0, bar);
   }
   MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
-  // One thread = one row, one column half.  The global loads of the saved h
-  // for chunk c + 16 are issued before chunk c is computed, so their latency
-  // overlaps the arithmetic and stores of chunk c.
+  // SwiGLU backward of 16 columns: g, the saved h (gate and up, packed) ->
+  // dh_gate, dh_up, w*a; dw accumulates sum g * a
+  MOE_DEV static void swiglu_bwd16(const float* g, const uint32_t* gw, const uint32_t* uw, float w,
+                                   float& dw, float* dhg, float* dhu, float* awv) {
+    float hg[16], hu[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      unpack_bf16x2(gw[i], hg[2 * i], hg[2 * i + 1]);
+      unpack_bf16x2(uw[i], hu[2 * i], hu[2 * i + 1]);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float s = sigmoidf_fast(hg[i]);
+      const float silu = hg[i] * s;
+      const float act = silu * hu[i];
+      dw = fmaf(g[i], act, dw);
+      const float da = w * g[i];
+      dhg[i] = da * hu[i] * s * (1.0f + hg[i] * (1.0f - s));
+      dhu[i] = da * silu;
+      awv[i] = w * act;
+    }
+  }
+
+  // kStaged: one thread = one row, one column half, 32 columns per step
+  MOE_DEV static void epilogue_staged(const GemmArgs& a, const TileInfo& ti, uint32_t taddr,
+                                      int r, int group, uint8_t* extra) {
+    constexpr int kHalf = BN / 2;
+    const bool valid = r < ti.rows;
+    const bool pad = !valid && r < ti.rows_pad;
+    const int lane = r & 31;
+    const int wslot = group * 4 + (r >> 5);
+    uint8_t* st = stage_base(extra) + wslot * 3 * kStage64WarpBytes;
+    uint64_t* hbar = reinterpret_cast<uint64_t*>(stage_base(extra) + kStageBytes) + wslot;
+    const int64_t row = static_cast<int64_t>(ti.m0) + ((valid || pad) ? r : 0);
+    const int F = a.ld0;
+    const int c0 = group * kHalf;
+    __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(a.out0) + row * 2 * F + ti.n0;
+    __nv_bfloat16* aw = static_cast<__nv_bfloat16*>(a.out1) + row * F + ti.n0;
+    const float w = valid ? __ldg(static_cast<const float*>(a.in1) + row) : 0.f;
+    const int never = 0;   // the h waits are cut short only by their time limit
+    float dw = 0.f;
+#pragma unroll 1
+    for (int c = c0; c < c0 + kHalf; c += 32) {
+      // the warp's 32 rows of h_gate and h_up for columns [c, c + 32) into the
+      // first two buffers; every lane's earlier accesses to them are ordered
+      // before the asynchronous writes
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int y = ti.m0 + (r & ~31);
+        mbar_arrive_expect_tx(hbar, 2 * kStage64WarpBytes);
+        tma_load_2d(st, &a.mapB1, ti.n0 + c, y, hbar);
+        tma_load_2d(st + kStage64WarpBytes, &a.mapB1, F + ti.n0 + c, y, hbar);
+      }
+      if (!mbar_wait_bounded(hbar, static_cast<uint32_t>(((c - c0) >> 5) & 1), &never,
+                             a.wait_limit_ns))
+        record_timeout(a.status, kWaitEpiLoad);
+      uint32_t gw[16], uw[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 ug = *reinterpret_cast<const uint4*>(st + stage64_off(lane, q));
+        const uint4 uu =
+            *reinterpret_cast<const uint4*>(st + kStage64WarpBytes + stage64_off(lane, q));
+        gw[4 * q] = ug.x; gw[4 * q + 1] = ug.y; gw[4 * q + 2] = ug.z; gw[4 * q + 3] = ug.w;
+        uw[4 * q] = uu.x; uw[4 * q + 1] = uu.y; uw[4 * q + 2] = uu.z; uw[4 * q + 3] = uu.w;
+      }
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float g[16];
+        tmem_ld16(taddr + c + 16 * half, g);
+        tmem_ld_wait();
+        float dhg[16], dhu[16], awv[16];
+        if (valid) {
+          swiglu_bwd16(g, gw + 8 * half, uw + 8 * half, w, dw, dhg, dhu, awv);
+        } else {
+          // zeros for the padded rows (and for rows nobody writes)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) dhg[i] = dhu[i] = awv[i] = 0.f;
+        }
+        stage64_bf16x16(st, lane, half, dhg);
+        stage64_bf16x16(st + kStage64WarpBytes, lane, half, dhu);
+        stage64_bf16x16(st + 2 * kStage64WarpBytes, lane, half, awv);
+      }
+      const bool w_row = valid || pad;
+      stage64_flush(st, lane, w_row ? dh + c : nullptr, false);
+      stage64_flush(st + kStage64WarpBytes, lane, w_row ? dh + F + c : nullptr, false);
+      stage64_flush(st + 2 * kStage64WarpBytes, lane, w_row ? aw + c : nullptr, false);
+    }
+    // one router-weight partial per (row, n-tile, column half)
+    if (valid)
+      static_cast<float*>(a.out2)[row * (a.n_tiles * kEpiGroups) + (ti.n0 / BN) * kEpiGroups +
+                                  group] = dw;
+  }
+
+  // Unstaged (single-CTA tiles): one thread = one row, one column half.  The
+  // global loads of the saved h for chunk c + 16 are issued before chunk c is
+  // computed, so their latency overlaps the arithmetic and stores of chunk c.
   MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
                                int group, uint8_t* extra) {
+    if constexpr (kStaged) {
+      epilogue_staged(a, ti, taddr, r, group, extra);
+      return;
+    }
     constexpr int kHalf = BN / 2;
     const bool valid = r < ti.rows;
     // rows past the expert's tokens but inside its padded segment: dh and w*a
     // are weight-gradient operands there, so they must read as zero
     const bool pad = !valid && r < ti.rows_pad;
-    const int lane = r & 31;
-    uint8_t* st = kStaged ? extra + (group * 4 + (r >> 5)) * 3 * kStage64WarpBytes : nullptr;
     const int64_t row = static_cast<int64_t>(ti.m0) + ((valid || pad) ? r : 0);
     const int F = a.ld0;
     const int c0 = group * kHalf;
@@ -81,43 +199,13 @@ struct DownDgradProblem {
       tmem_ld16(taddr + c, g);
       tmem_ld_wait();
       if (valid) {
-        float hg[16], hu[16], dhg[16], dhu[16], awv[16];
+        float dhg[16], dhu[16], awv[16];
         const uint32_t gw[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
         const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          unpack_bf16x2(gw[i], hg[2 * i], hg[2 * i + 1]);
-          unpack_bf16x2(uw[i], hu[2 * i], hu[2 * i + 1]);
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float s = sigmoidf_fast(hg[i]);
-          const float silu = hg[i] * s;
-          const float act = silu * hu[i];
-          dw = fmaf(g[i], act, dw);
-          const float da = w * g[i];
-          dhg[i] = da * hu[i] * s * (1.0f + hg[i] * (1.0f - s));
-          dhu[i] = da * silu;
-          awv[i] = w * act;
-        }
-        if constexpr (kStaged) {
-          const int q = ((c - c0) >> 4) & 1;
-          stage64_bf16x16(st, lane, q, dhg);
-          stage64_bf16x16(st + kStage64WarpBytes, lane, q, dhu);
-          stage64_bf16x16(st + 2 * kStage64WarpBytes, lane, q, awv);
-        } else {
-          store_bf16x16(dh + c, dhg);
-          store_bf16x16(dh + F + c, dhu);
-          store_bf16x16(aw + c, awv);
-        }
-      } else if (kStaged) {
-        // zeros for the padded rows (and for rows nobody writes)
-        const int q = ((c - c0) >> 4) & 1;
-        const float z[16] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f,
-                             0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        stage64_bf16x16(st, lane, q, z);
-        stage64_bf16x16(st + kStage64WarpBytes, lane, q, z);
-        stage64_bf16x16(st + 2 * kStage64WarpBytes, lane, q, z);
+        swiglu_bwd16(g, gw, uw, w, dw, dhg, dhu, awv);
+        store_bf16x16(dh + c, dhg);
+        store_bf16x16(dh + F + c, dhu);
+        store_bf16x16(aw + c, awv);
       } else if (pad) {
         st_global_v4(dh + c, 0u, 0u, 0u, 0u);
         st_global_v4(dh + c + 8, 0u, 0u, 0u, 0u);
@@ -125,15 +213,6 @@ struct DownDgradProblem {
         st_global_v4(dh + F + c + 8, 0u, 0u, 0u, 0u);
         st_global_v4(aw + c, 0u, 0u, 0u, 0u);
         st_global_v4(aw + c + 8, 0u, 0u, 0u, 0u);
-      }
-      if constexpr (kStaged) {
-        if (((c - c0) >> 4) & 1) {             // 32 columns staged: flush the three outputs
-          const int c32 = c - 16;
-          const bool w_row = valid || pad;
-          stage64_flush(st, lane, w_row ? dh + c32 : nullptr, false);
-          stage64_flush(st + kStage64WarpBytes, lane, w_row ? dh + F + c32 : nullptr, false);
-          stage64_flush(st + 2 * kStage64WarpBytes, lane, w_row ? aw + c32 : nullptr, false);
-        }
       }
     }
     // one router-weight partial per (row, n-tile, column half)
