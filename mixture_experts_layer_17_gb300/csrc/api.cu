@@ -277,7 +277,7 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.f_a = f.take(2 * Pa * F);
   L.f_scratch = f.take(2 * P * H);
   if (L.recompute) {
-    L.f_xperm = f.take(2 * Pa * H);
+    if (c.precision != MOE_MXFP8) L.f_xperm = f.take(2 * Pa * H);   // mxfp8 dispatches to E4M3
     L.f_h = f.take(2 * Pa * 2 * F);
   }
   L.mt_max = (L.P + kBM - 1) / kBM + L.E;
@@ -333,7 +333,7 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.b_scratch = b.take(2 * P * H);
   L.b_wrp = b.take(sizeof(float) * L.wr_split * E * H);
   if (L.recompute) {
-    L.b_xperm = b.take(2 * Pa * H);
+    if (c.precision != MOE_MXFP8) L.b_xperm = b.take(2 * Pa * H);   // mxfp8 dispatches to E4M3
     L.b_h = b.take(2 * Pa * 2 * F);
     if (c.precision == MOE_MXFP8) {
       L.bq_rx = b.take(Pa * H);
@@ -561,23 +561,17 @@ moe_status_t gate_up_fwd_bf16(const Layout& L, int sms, cudaStream_t s, uint32_t
 // E4M3 operands and scale atoms of the MXFP8 gate/up GEMM
 struct MxGateUpBufs {
   uint8_t *xq, *sx, *aq, *sa, *wgu, *swgu;
-  bool x_ready = false;   // xq / sx already written by the fused gather
   bool w_ready = false;   // wgu / swgu prepared by moe_prepare_weights
 };
 
-// F7 + F8 in MXFP8: quantise x_perm along H and W_gate / W_up along H
-// (interleaved per 128 columns), then the block-scaled gate/up GEMM with
-// SwiGLU whose epilogue writes h and quantises a along F from fp32.
+// F7 + F8 in MXFP8: x along H comes quantised from the dispatch (xq / sx);
+// W_gate / W_up along H (interleaved per 128 columns) are quantised here
+// unless prepared, then the block-scaled gate/up GEMM with SwiGLU whose
+// epilogue writes h and quantises a along F from fp32.
 moe_status_t gate_up_fwd_mx(const Layout& L, int sms, cudaStream_t s, uint32_t fl,
-                            DeviceStatus* st, const uint16_t* xperm, const uint16_t* W_gate,
-                            const uint16_t* W_up, const int* offsets, const int* counts,
-                            const int* mtile, uint16_t* h, const MxGateUpBufs& q,
-                            bool recompute) {
-  if (!q.x_ready) {
-    MOE_TRY(run(recompute ? "recompute_mx_quant_x" : "mx_quant_x", s, fl, [&] {
-      return launch_quant_rows_permuted(xperm, L.Pa, L.H, q.xq, q.sx, offsets, mtile, L.E, s);
-    }));
-  }
+                            DeviceStatus* st, const uint16_t* W_gate, const uint16_t* W_up,
+                            const int* offsets, const int* counts, const int* mtile, uint16_t* h,
+                            const MxGateUpBufs& q, bool recompute) {
   if (!q.w_ready) {
     MOE_TRY(run(recompute ? "recompute_mx_quant_w_gate_up" : "mx_quant_w_gate_up", s, fl, [&] {
       return launch_quant_cols_gate_up(W_gate, W_up, L.E, L.H, L.F, q.wgu, q.swgu, s);
@@ -616,16 +610,12 @@ moe_status_t gate_up_fwd_mx(const Layout& L, int sms, cudaStream_t s, uint32_t f
 // F7 + F8 and F9 in MXFP8: the gate/up part above, then W_down quantised
 // along F and the block-scaled down GEMM with the weighted scatter.
 moe_status_t forward_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t fl,
-                              DeviceStatus* st, const uint16_t* xperm, const uint16_t* W_gate,
-                              const uint16_t* W_up, const uint16_t* W_down, const int* offsets,
-                              const int* counts, const int* mtile, const float* w_row,
-                              const int* row_slot,
-                              uint16_t* act, uint16_t* h, uint16_t* scratch, void* ws,
-                              void* wq) {
-  (void)act;
+                              DeviceStatus* st, const uint16_t* W_gate, const uint16_t* W_up,
+                              const uint16_t* W_down, const int* offsets, const int* counts,
+                              const int* mtile, const float* w_row, const int* row_slot,
+                              uint16_t* h, uint16_t* scratch, void* ws, void* wq) {
   MxGateUpBufs q{at<uint8_t>(ws, L.fq_x), at<uint8_t>(ws, L.fs_x), at<uint8_t>(ws, L.fq_a),
                  at<uint8_t>(ws, L.fs_a), nullptr, nullptr};
-  q.x_ready = true;   // moe_forward's gather quantised x_perm along H
   if (wq != nullptr) {
     q.wgu = at<uint8_t>(wq, L.q_gu_h);
     q.swgu = at<uint8_t>(wq, L.qs_gu_h);
@@ -638,7 +628,7 @@ moe_status_t forward_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t
   uint8_t* sa = q.sa;
   uint8_t* wd = wq != nullptr ? at<uint8_t>(wq, L.q_d_f) : at<uint8_t>(ws, L.fq_wd);
   uint8_t* swd = wq != nullptr ? at<uint8_t>(wq, L.qs_d_f) : at<uint8_t>(ws, L.fs_wd);
-  MOE_TRY(gate_up_fwd_mx(L, sms, s, fl, st, xperm, W_gate, W_up, offsets, counts, mtile, h, q,
+  MOE_TRY(gate_up_fwd_mx(L, sms, s, fl, st, W_gate, W_up, offsets, counts, mtile, h, q,
                          false));
   if (wq == nullptr) {
     MOE_TRY(run("mx_quant_w_down_f", s, fl, [&] {
@@ -1027,9 +1017,8 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
   }
 
   if (cfg->precision == MOE_MXFP8) {
-    MOE_TRY(forward_gemms_mx(L, sms, s, fl, st, xperm, W_gate, W_up, W_down, poff, counts,
-                             mtile, w_row, row_slot, act, h, scratch, ws,
-                             const_cast<void*>(cfg->prepared_weights)));
+    MOE_TRY(forward_gemms_mx(L, sms, s, fl, st, W_gate, W_up, W_down, poff, counts, mtile, w_row,
+                             row_slot, h, scratch, ws, const_cast<void*>(cfg->prepared_weights)));
   } else {
     // F7 + F8: gate/up GEMM with SwiGLU
     MOE_TRY(gate_up_fwd_bf16(L, sms, s, fl, st, xperm, W_gate, W_up, poff, counts, mtile, mtile2,
@@ -1147,14 +1136,13 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
       MxGateUpBufs q{at<uint8_t>(ws, L.bq_rx), at<uint8_t>(ws, L.bs_rx),
                      at<uint8_t>(ws, L.bq_ra), at<uint8_t>(ws, L.bs_ra),
                      at<uint8_t>(ws, L.bq_rwgu), at<uint8_t>(ws, L.bs_rwgu)};
-      q.x_ready = true;
       if (L.prepared) {
         void* wq = const_cast<void*>(cfg->prepared_weights);
         q.wgu = at<uint8_t>(wq, L.q_gu_h);
         q.swgu = at<uint8_t>(wq, L.qs_gu_h);
         q.w_ready = true;
       }
-      MOE_TRY(gate_up_fwd_mx(L, sms, s, fl, st, xp, W_gate, W_up, poff, counts, mtile, hh, q,
+      MOE_TRY(gate_up_fwd_mx(L, sms, s, fl, st, W_gate, W_up, poff, counts, mtile, hh, q,
                              true));
     } else {
       MOE_TRY(gate_up_fwd_bf16(L, sms, s, fl, st, xp, W_gate, W_up, poff, counts, mtile, mtile2,

@@ -40,9 +40,6 @@ cudaError_t launch_dense_mx256(const GemmArgs& a, int grid, cudaStream_t s);
 // MXFP8 quantisers (mx_quant.cu): E4M3 data + 512-byte scale atoms
 cudaError_t launch_quant_rows_dense(const uint16_t* src, int64_t R, int C, uint8_t* dst,
                                     uint8_t* sf, cudaStream_t s);
-cudaError_t launch_quant_rows_permuted(const uint16_t* src, int64_t P, int C, uint8_t* dst,
-                                       uint8_t* sf, const int* offsets, const int* mtile_off,
-                                       int E, cudaStream_t s);
 cudaError_t launch_quant_cols_weights(const uint16_t* src, int E, int R, int C, uint8_t* dst,
                                       uint8_t* sf, cudaStream_t s);
 cudaError_t launch_quant_cols_gate_up(const uint16_t* W_gate, const uint16_t* W_up, int E, int H,

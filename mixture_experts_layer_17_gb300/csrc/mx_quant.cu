@@ -13,40 +13,17 @@ namespace moe {
 namespace {
 
 // --------------------------------------------------------------------------
-// Along the contiguous dimension (K-major operand [R, C], K = C).
-//   kRowsDense:    atom group of row = row / 128, r = row % 128 (weights).
-//   kRowsPermuted: rows of the padded expert-major layout (offsets = padded
-//                  segment starts); the atom group is the row's grouped-GEMM
-//                  m-tile, mtile_off[e] + (row - offsets[e]) / 128, and r its
-//                  row inside that tile.
+// Along the contiguous dimension (K-major operand [R, C], K = C; weights):
+// the atom group of a row is row / 128, its row in the atom row % 128.
 // Atom index = group * (C / 128) + k / 128.  One warp per row.
 // --------------------------------------------------------------------------
-enum RowMode { kRowsDense = 0, kRowsPermuted = 1 };
-
-template <int MODE>
 __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, int64_t R, int C,
-                                  uint8_t* __restrict__ dst, uint8_t* __restrict__ sf,
-                                  const int* __restrict__ offsets,
-                                  const int* __restrict__ mtile_off, int E) {
+                                  uint8_t* __restrict__ dst, uint8_t* __restrict__ sf) {
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= R) return;
   const int lane = threadIdx.x & 31;
-  int64_t group;
-  int r;
-  if (MODE == kRowsDense) {
-    group = row >> 7;
-    r = static_cast<int>(row & 127);
-  } else {
-    if (row >= __ldg(offsets + E)) return;   // rows past the last padded segment
-    int lo = 0, hi = E - 1;     // largest e with offsets[e] <= row
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(offsets + mid) <= row) lo = mid; else hi = mid - 1;
-    }
-    const int64_t local = row - __ldg(offsets + lo);
-    group = __ldg(mtile_off + lo) + (local >> 7);
-    r = static_cast<int>(local & 127);
-  }
+  const int64_t group = row >> 7;
+  const int r = static_cast<int>(row & 127);
   const int KT = C >> 7;
   const uint16_t* s = src + row * C;
   uint8_t* d = dst + row * C;
@@ -93,6 +70,46 @@ enum ColMode { kColsWeights = 0, kColsGateUp = 1, kColsTokens = 2 };
 
 constexpr int kColThreads = 256;
 
+// Expert of k-tile kg: the largest e with mtile_off[e] <= kg, or -1 for a
+// k-tile past mtile_off[E] (the grids are sized for the worst case).  The
+// E + 1 prefix entries stay in L1 after the first block on an SM.
+__device__ __forceinline__ int ktile_expert(const int* __restrict__ mtile_off, int E, int kg) {
+  if (kg >= __ldg(mtile_off + E)) return -1;
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(mtile_off + mid) <= kg) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// The 128 x 128 bf16 tile quantised along its rows' direction (blocks of 32
+// rows per column) into qtile, scales into the 512-byte atom sfa: 256
+// threads, thread t takes the column pair (2 (t % 64), 2 (t % 64) + 1) of
+// 32-row block t / 64.  |max| of each column by a bf16x2 max (exact); the
+// E4M3 values are written as byte pairs of one row.
+__device__ __forceinline__ void quant_tile_cols(const uint16_t (&tile)[128][128],
+                                                uint8_t (&qtile)[128][128], uint8_t* sfa) {
+  const int cp = threadIdx.x & 63;
+  const int kb = threadIdx.x >> 6;
+  __nv_bfloat162 amax2 = __float2bfloat162_rn(0.f);
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    amax2 = __hmax2(amax2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&tile[kb * 32 + j][2 * cp])));
+  const int X0 = mx_exponent(__low2float(amax2));
+  const int X1 = mx_exponent(__high2float(amax2));
+  const float inv0 = mx_inv_scale(X0), inv1 = mx_inv_scale(X1);
+  sfa[sf_atom_offset(2 * cp, kb)] = static_cast<uint8_t>(X0 + 127);
+  sfa[sf_atom_offset(2 * cp + 1, kb)] = static_cast<uint8_t>(X1 + 127);
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[kb * 32 + j][2 * cp]);
+    const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+    *reinterpret_cast<__nv_fp8x2_storage_t*>(&qtile[kb * 32 + j][2 * cp]) =
+        __nv_cvt_float2_to_fp8x2(make_float2(lo * inv0, hi * inv1), __NV_SATFINITE, __NV_E4M3);
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(
     const uint16_t* __restrict__ src0, const uint16_t* __restrict__ src1, int R, int C_in,
@@ -112,12 +129,8 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(
   int valid;                           // valid rows of this K-tile
   int64_t atom;
   if (MODE == kColsTokens) {
-    if (kg >= __ldg(mtile_off + E)) return;   // the grid is sized for the worst case
-    int lo = 0, hi = E - 1;            // largest e with mtile_off[e] <= kg
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(mtile_off + mid) <= kg) lo = mid; else hi = mid - 1;
-    }
+    const int lo = ktile_expert(mtile_off, E, kg);
+    if (lo < 0) return;
     const int g = kg - __ldg(mtile_off + lo);
     src_row0 = static_cast<int64_t>(__ldg(offsets + lo)) + 128 * g;
     valid = min(128, __ldg(counts + lo) - 128 * g);
@@ -151,30 +164,8 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(
     *reinterpret_cast<uint4*>(&tile[row][c8]) = u;
   }
   __syncthreads();
-  // convert: unit = (column c, 32-row block kb)
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int c = tid & 127;
-    const int kb = (tid >> 7) + 2 * i;
-    float v[32];
-    float amax = 0.f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      v[j] = __uint_as_float(static_cast<uint32_t>(tile[kb * 32 + j][c]) << 16);
-      amax = fmaxf(amax, fabsf(v[j]));
-    }
-    const int X = mx_exponent(amax);
-    const float inv = mx_inv_scale(X);
-    sf[atom * 512 + sf_atom_offset(c, kb)] = static_cast<uint8_t>(X + 127);
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      const uint32_t q = to_e4m3x4(v[j], v[j + 1], v[j + 2], v[j + 3], inv);
-      qtile[kb * 32 + j][c] = static_cast<uint8_t>(q);
-      qtile[kb * 32 + j + 1][c] = static_cast<uint8_t>(q >> 8);
-      qtile[kb * 32 + j + 2][c] = static_cast<uint8_t>(q >> 16);
-      qtile[kb * 32 + j + 3][c] = static_cast<uint8_t>(q >> 24);
-    }
-  }
+  // convert: a thread takes the column pair (2 cp, 2 cp + 1) of 32-row block kb
+  quant_tile_cols(tile, qtile, sf + atom * 512);
   __syncthreads();
   // store: 8 threads per 128-byte output row
 #pragma unroll
@@ -197,7 +188,7 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(
 //     quant_cols_kernel<kColsTokens>);
 //   along C (unless dst_r is null): E4M3 rows at the padded rows poff[e] + 128*g + i that lie inside
 //     the expert's padded segment, scale atom (mtile_off[e] + g) * (C/128) + ct
-//     (as quant_rows_kernel<kRowsPermuted>).
+//     (the layout the grouped-M GEMMs read along K).
 __global__ void __launch_bounds__(kColThreads) dispatch_quant_kernel(
     const uint16_t* __restrict__ src, const int* __restrict__ perm_token,
     const int* __restrict__ offsets, const int* __restrict__ poff, const int* __restrict__ counts,
@@ -208,13 +199,8 @@ __global__ void __launch_bounds__(kColThreads) dispatch_quant_kernel(
   const int kg = blockIdx.x;
   const int ct = blockIdx.y;
   const int tid = threadIdx.x;
-  if (kg >= __ldg(mtile_off + E)) return;   // the grid is sized for the worst case
-  int lo = 0, hi = E - 1;                    // largest e with mtile_off[e] <= kg
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(mtile_off + mid) <= kg) lo = mid; else hi = mid - 1;
-  }
-  const int e = lo;
+  const int e = ktile_expert(mtile_off, E, kg);
+  if (e < 0) return;
   const int g = kg - __ldg(mtile_off + e);
   const int local0 = 128 * g;
   const int valid = min(128, __ldg(counts + e) - local0);
@@ -237,27 +223,7 @@ __global__ void __launch_bounds__(kColThreads) dispatch_quant_kernel(
   // along the tokens (dst_t may be null: not wanted): a thread takes the
   // column pair (2 cp, 2 cp + 1) of 32-row block kb; |max| of each column by
   // bf16x2 max (exact), E4M3 written as byte pairs of one row
-  if (dst_t != nullptr) {
-    const int cp = tid & 63;
-    const int kb = tid >> 6;
-    __nv_bfloat162 amax2 = __float2bfloat162_rn(0.f);
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      amax2 = __hmax2(amax2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&tile[kb * 32 + j][2 * cp])));
-    const int X0 = mx_exponent(__low2float(amax2));
-    const int X1 = mx_exponent(__high2float(amax2));
-    const float inv0 = mx_inv_scale(X0), inv1 = mx_inv_scale(X1);
-    uint8_t* sft = sf_t + (static_cast<int64_t>(kg) * (C >> 7) + ct) * 512;
-    sft[sf_atom_offset(2 * cp, kb)] = static_cast<uint8_t>(X0 + 127);
-    sft[sf_atom_offset(2 * cp + 1, kb)] = static_cast<uint8_t>(X1 + 127);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[kb * 32 + j][2 * cp]);
-      const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
-      *reinterpret_cast<__nv_fp8x2_storage_t*>(&qtile[kb * 32 + j][2 * cp]) =
-          __nv_cvt_float2_to_fp8x2(make_float2(lo * inv0, hi * inv1), __NV_SATFINITE, __NV_E4M3);
-    }
-  }
+  if (dst_t != nullptr) quant_tile_cols(tile, qtile, sf_t + (static_cast<int64_t>(kg) * (C >> 7) + ct) * 512);
   // along C (unless dst_r is null): 16 lanes per row (8 columns each, 4 lanes
   // per 32-column block), two rows per warp step
   if (dst_r != nullptr) {
@@ -303,16 +269,7 @@ __global__ void __launch_bounds__(kColThreads) dispatch_quant_kernel(
 
 cudaError_t launch_quant_rows_dense(const uint16_t* src, int64_t R, int C, uint8_t* dst,
                                     uint8_t* sf, cudaStream_t s) {
-  quant_rows_kernel<kRowsDense><<<static_cast<unsigned>((R + 7) / 8), 256, 0, s>>>(
-      src, R, C, dst, sf, nullptr, nullptr, 0);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_quant_rows_permuted(const uint16_t* src, int64_t P, int C, uint8_t* dst,
-                                       uint8_t* sf, const int* offsets, const int* mtile_off,
-                                       int E, cudaStream_t s) {
-  quant_rows_kernel<kRowsPermuted><<<static_cast<unsigned>((P + 7) / 8), 256, 0, s>>>(
-      src, P, C, dst, sf, offsets, mtile_off, E);
+  quant_rows_kernel<<<static_cast<unsigned>((R + 7) / 8), 256, 0, s>>>(src, R, C, dst, sf);
   return cudaGetLastError();
 }
 
