@@ -83,6 +83,12 @@ __device__ __forceinline__ int ktile_expert(const int* __restrict__ mtile_off, i
   return lo;
 }
 
+// Shared-memory tiles of 128 rows x 128 bf16 columns hold their 16-byte
+// chunks swizzled: logical chunk c of row r sits at c ^ ((c >> 3) << 1) ^ (r & 1).
+// Row-wise 16-byte stores, column-pair reads and the (row, 32-column block)
+// reads of the quantiser along C are all free of bank conflicts that way.
+__device__ __forceinline__ int tile_chunk(int row, int c) { return c ^ ((c >> 3) << 1) ^ (row & 1); }
+
 // The 128 x 128 bf16 tile quantised along its rows' direction (blocks of 32
 // rows per column) into qtile, scales into the 512-byte atom sfa: 256
 // threads, thread t takes the column pair (2 (t % 64), 2 (t % 64) + 1) of
@@ -95,7 +101,8 @@ __device__ __forceinline__ void quant_tile_cols(const uint16_t (&tile)[128][128]
   __nv_bfloat162 amax2 = __float2bfloat162_rn(0.f);
 #pragma unroll
   for (int j = 0; j < 32; ++j)
-    amax2 = __hmax2(amax2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(&tile[kb * 32 + j][2 * cp])));
+    amax2 = __hmax2(amax2, __habs2(*reinterpret_cast<const __nv_bfloat162*>(
+                               &tile[kb * 32 + j][tile_chunk(kb * 32 + j, cp >> 2) * 8 + (2 * cp & 7)])));
   const int X0 = mx_exponent(__low2float(amax2));
   const int X1 = mx_exponent(__high2float(amax2));
   const float inv0 = mx_inv_scale(X0), inv1 = mx_inv_scale(X1);
@@ -103,7 +110,8 @@ __device__ __forceinline__ void quant_tile_cols(const uint16_t (&tile)[128][128]
   sfa[sf_atom_offset(2 * cp + 1, kb)] = static_cast<uint8_t>(X1 + 127);
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(&tile[kb * 32 + j][2 * cp]);
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(
+        &tile[kb * 32 + j][tile_chunk(kb * 32 + j, cp >> 2) * 8 + (2 * cp & 7)]);
     const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
     *reinterpret_cast<__nv_fp8x2_storage_t*>(&qtile[kb * 32 + j][2 * cp]) =
         __nv_cvt_float2_to_fp8x2(make_float2(lo * inv0, hi * inv1), __NV_SATFINITE, __NV_E4M3);
@@ -161,7 +169,7 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(
       }
       u = ld_global_nc_v4(src + (src_row0 + row) * C_in + col);
     }
-    *reinterpret_cast<uint4*>(&tile[row][c8]) = u;
+    *reinterpret_cast<uint4*>(&tile[row][tile_chunk(row, c8 >> 3) * 8]) = u;
   }
   __syncthreads();
   // convert: a thread takes the column pair (2 cp, 2 cp + 1) of 32-row block kb
@@ -217,39 +225,45 @@ __global__ void __launch_bounds__(kColThreads) dispatch_quant_kernel(
       const int64_t tok = __ldg(toks + row);
       u = ld_global_nc_v4(src + tok * C + ct * 128 + c8);
     }
-    *reinterpret_cast<uint4*>(&tile[row][c8]) = u;
+    *reinterpret_cast<uint4*>(&tile[row][tile_chunk(row, c8 >> 3) * 8]) = u;
   }
   __syncthreads();
   // along the tokens (dst_t may be null: not wanted): a thread takes the
   // column pair (2 cp, 2 cp + 1) of 32-row block kb; |max| of each column by
   // bf16x2 max (exact), E4M3 written as byte pairs of one row
   if (dst_t != nullptr) quant_tile_cols(tile, qtile, sf_t + (static_cast<int64_t>(kg) * (C >> 7) + ct) * 512);
-  // along C (unless dst_r is null): 16 lanes per row (8 columns each, 4 lanes
-  // per 32-column block), two rows per warp step
+  // along C (unless dst_r is null): a lane takes one 32-column block of a
+  // row (no shuffles), four lanes per row, eight rows per warp step
   if (dst_r != nullptr) {
     const int warp = tid >> 5, lane = tid & 31;
-    const int half = lane >> 4, c8 = (lane & 15) * 8;
+    const int blk = lane & 3;
     const int64_t prow0 = static_cast<int64_t>(__ldg(poff + e)) + local0;
     uint8_t* sfr = sf_r + (static_cast<int64_t>(__ldg(mtile_off + e) + g) * (C >> 7) + ct) * 512;
+    uint8_t* dr = dst_r + prow0 * C + ct * 128 + blk * 32;
 #pragma unroll 1
-    for (int row = 2 * warp + half; row < seg; row += kColThreads / 16) {
-      const uint4 u = *reinterpret_cast<const uint4*>(&tile[row][c8]);
-      float v[8];
-      unpack_bf16x2(u.x, v[0], v[1]);
-      unpack_bf16x2(u.y, v[2], v[3]);
-      unpack_bf16x2(u.z, v[4], v[5]);
-      unpack_bf16x2(u.w, v[6], v[7]);
+    for (int row = 8 * warp + (lane >> 2); row < seg; row += kColThreads / 4) {
+      float v[32];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u =
+            *reinterpret_cast<const uint4*>(&tile[row][tile_chunk(row, 4 * blk + q) * 8]);
+        unpack_bf16x2(u.x, v[8 * q + 0], v[8 * q + 1]);
+        unpack_bf16x2(u.y, v[8 * q + 2], v[8 * q + 3]);
+        unpack_bf16x2(u.z, v[8 * q + 4], v[8 * q + 5]);
+        unpack_bf16x2(u.w, v[8 * q + 6], v[8 * q + 7]);
+      }
       float amax = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
       const int X = mx_exponent(amax);
       const float inv = mx_inv_scale(X);
-      const uint2 q = make_uint2(to_e4m3x4(v[0], v[1], v[2], v[3], inv),
-                                 to_e4m3x4(v[4], v[5], v[6], v[7], inv));
-      *reinterpret_cast<uint2*>(dst_r + (prow0 + row) * C + ct * 128 + c8) = q;
-      if ((lane & 3) == 0) sfr[sf_atom_offset(row, (lane & 15) >> 2)] = static_cast<uint8_t>(X + 127);
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = to_e4m3x4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], inv);
+      uint8_t* d = dr + static_cast<int64_t>(row) * C;
+      st_global_v4(d, w[0], w[1], w[2], w[3]);
+      st_global_v4(d + 16, w[4], w[5], w[6], w[7]);
+      sfr[sf_atom_offset(row, blk)] = static_cast<uint8_t>(X + 127);
     }
   }
   __syncthreads();
