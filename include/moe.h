@@ -87,16 +87,18 @@ typedef enum {
                                          checkpointing is the training setting of
                                          the end-to-end runs in "Os Números..." on
                                          bitsgeniais.com.br): ctx keeps only the
-                                         routing and permutation; the permuted
-                                         input x_perm and the pre-activations h
-                                         live in the forward workspace instead,
-                                         and moe_backward dispatches x again and
+                                         routing and permutation; the dispatched
+                                         input and the pre-activations h live in
+                                         the forward workspace instead, and
+                                         moe_backward dispatches x again and
                                          recomputes h with the gate/up GEMM (in
                                          the forward's precision) before the
                                          backward GEMMs.  ctx_bytes shrinks by
-                                         (T*top_k + 64*E) * (H + 2F) * 2 bytes;
-                                         forward and backward must both be given
-                                         the flag                                 */
+                                         h, (T*top_k + 64*E) * 2F * 2 bytes, and
+                                         x: x_perm, (T*top_k + 64*E) * H * 2
+                                         bytes, or in mxfp8 its E4M3 copy along
+                                         the tokens with the scales; forward and
+                                         backward must both be given the flag     */
 
 typedef struct {
   int64_t T;           /* tokens                                   */
@@ -155,7 +157,7 @@ moe_status_t moe_route(const moe_config_t* cfg, const moe_bf16_t* x, const moe_b
 
 /* Forward pass: y[t] = sum_j topk_w[t,j] * (silu(x_t W_gate[e]) * (x_t W_up[e])) W_down[e],
  * e = topk_idx[t,j] (y in bf16, fp32 accumulation).  Writes ctx (routing,
- * permutation, the permuted input and the pre-activations) for moe_backward;
+ * permutation, the dispatched input and the pre-activations) for moe_backward;
  * ctx must stay unmodified until the matching backward call.  logit_bias may
  * be NULL.  ws: at least fwd_ws bytes; ctx: at least ctx_bytes. */
 moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe_bf16_t* W_r,
