@@ -64,7 +64,7 @@ typedef enum {
   MOE_ERR_CUDA = 4,                 /* a CUDA runtime call failed           */
   MOE_ERR_TIMEOUT = 5,              /* a device-side bounded wait ran out   */
   MOE_ERR_UNSUPPORTED_DEVICE = 6,   /* not an sm_103 GPU                    */
-  MOE_ERR_NOT_IMPLEMENTED = 7       /* reserved: a feature this build lacks */
+  MOE_ERR_NOT_IMPLEMENTED = 7       /* reserved: a feature this library version lacks */
 } moe_status_t;
 
 /* flags */
