@@ -81,8 +81,9 @@ typedef enum {
 #define MOE_FLAG_CTA_PAIRS_ON   0x8u  /* use CTA-pair 256-row tiles (cta_group::2)
                                          wherever the shape allows; by default,
                                          when experts average >= 512 rows, pairs
-                                         run every expert GEMM (the down dgrad when
-                                         F is a multiple of 256)                  */
+                                         run every expert GEMM, and from 256 rows
+                                         the two bf16 dgrads (the down dgrad when F
+                                         is a multiple of 256)                    */
 #define MOE_FLAG_RECOMPUTE      0x10u /* activation checkpointing (full activation
                                          checkpointing is the training setting of
                                          the end-to-end runs in "Os Números..." on

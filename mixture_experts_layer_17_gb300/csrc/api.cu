@@ -227,19 +227,23 @@ Layout make_layout(const moe_config_t& c, int sms) {
   // of a grouped-M GEMM wastes more rows at the end of each expert.  Measured
   // on the 235B shape (1024 rows per expert), pairs win for every expert GEMM
   // once the epilogue stores go through shared memory (the down dgrad's, at
-  // five stages, by 12%; the gate/up forward's by 4.5%); with ~256 rows per
-  // expert they lose everywhere.  MOE_FLAG_CTA_PAIRS_ON / _OFF override.
+  // five stages, by 12%; the gate/up forward's by 4.5%).  With 256 rows per
+  // expert (the 30B shape) only the two dgrads still gain (2-4%); the wgrads,
+  // whose K is then 4 k-blocks per expert, lose 36%, and the forward GEMMs
+  // break even.  MOE_FLAG_CTA_PAIRS_ON / _OFF override.
   const bool pairs_on = (c.flags & MOE_FLAG_CTA_PAIRS_ON) != 0;
   const bool pairs_off = (c.flags & MOE_FLAG_CTA_PAIRS_OFF) != 0;
   const bool bf = c.precision != MOE_MXFP8;        // bf16 forward GEMMs
   const bool bb = c.precision == MOE_BF16;         // bf16 backward GEMMs
   const bool big = L.P >= 512ll * L.E;             // experts average >= 512 rows
+  const bool mid = L.P >= 256ll * L.E;             // experts average >= 256 rows
   const bool can_pair = sms >= 2;                    // an SM budget of 1 runs single CTAs
   const bool pp = can_pair && !pairs_off && (pairs_on || big);
+  const bool pp_dgrad = can_pair && !pairs_off && (pairs_on || mid);
   L.pair_gu_fwd = bf && pp;
   L.pair_down_fwd = bf && pp;
-  L.pair_down_dgrad = bb && pp && (L.F % 256 == 0);
-  L.pair_gu_dgrad = bb && pp;
+  L.pair_down_dgrad = bb && pp_dgrad && (L.F % 256 == 0);
+  L.pair_gu_dgrad = bb && pp_dgrad;
   L.pair_down_wgrad = bb && pp && (L.F % 256 == 0);
   L.pair_gu_wgrad = bb && pp;
   L.recompute = (c.flags & MOE_FLAG_RECOMPUTE) != 0;
