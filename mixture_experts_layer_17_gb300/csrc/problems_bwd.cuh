@@ -27,18 +27,19 @@ struct DownDgradProblem {
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
   // kStaged (the CTA-pair version, which has the shared memory for it at five
-  // stages): each epilogue warp owns three 2 KB buffers (1024-byte aligned,
-  // hence up to 1 KB of lead-in) and an mbarrier.  Per 32-column step, TMA
-  // brings the warp's 32 rows of h_gate and h_up into the first two (64-byte
-  // swizzle, the stage64 layout) and every thread keeps its row of both as
-  // packed words; dh_gate, dh_up and w*a are then staged in the three
-  // buffers and leave as whole 64-byte row pieces.
-  static constexpr size_t kStageBytes = 8 * 3 * kStage64WarpBytes;
-  static constexpr size_t kExtraSmem = kStaged ? 1024 + kStageBytes + 8 * sizeof(uint64_t) : 0;
+  // stages): each epilogue warp owns two pairs of 2 KB buffers (1024-byte
+  // aligned, hence up to 1 KB of lead-in) and an mbarrier per pair.  Per
+  // 32-column step, TMA brings the warp's 32 rows of h_gate and h_up into one
+  // pair (64-byte swizzle, the stage64 layout) while the step before works
+  // out of the other; every thread keeps its row of both as packed words,
+  // then dh_gate and dh_up, and after them w*a, are staged in the step's pair
+  // and leave as whole 64-byte row pieces.
+  static constexpr size_t kStageBytes = 8 * 4 * kStage64WarpBytes;
+  static constexpr size_t kExtraSmem = kStaged ? 1024 + kStageBytes + 16 * sizeof(uint64_t) : 0;
   static constexpr int kEpiGroups = 2;
-  // an even number of steps per warp and tile keeps the parity of each
-  // warp's barrier in step with the step index from one tile to the next
-  static_assert(!kStaged || (BN / 2 / 32) % 2 == 0, "an even number of h steps per tile");
+  // four steps per warp and tile use each pair twice, so the parity of its
+  // barrier follows the step index in every tile
+  static_assert(!kStaged || (BN / 2 / 32) % 4 == 0, "a multiple of four h steps per tile");
 
   MOE_DEV static uint8_t* stage_base(uint8_t* extra) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(extra) + 1023) &
@@ -51,7 +52,7 @@ struct DownDgradProblem {
     if constexpr (kStaged) {
       if (threadIdx.x == 0) {
         uint64_t* bars = reinterpret_cast<uint64_t*>(stage_base(extra) + kStageBytes);
-        for (int w = 0; w < 8; ++w) mbar_init(bars + w, 1);
+        for (int w = 0; w < 16; ++w) mbar_init(bars + w, 1);
         fence_mbar_init();
       }
     }
@@ -90,34 +91,41 @@ struct DownDgradProblem {
   MOE_DEV static void epilogue_staged(const GemmArgs& a, const TileInfo& ti, uint32_t taddr,
                                       int r, int group, uint8_t* extra) {
     constexpr int kHalf = BN / 2;
+    constexpr int kSteps = kHalf / 32;
     const bool valid = r < ti.rows;
     const bool pad = !valid && r < ti.rows_pad;
     const int lane = r & 31;
     const int wslot = group * 4 + (r >> 5);
-    uint8_t* st = stage_base(extra) + wslot * 3 * kStage64WarpBytes;
-    uint64_t* hbar = reinterpret_cast<uint64_t*>(stage_base(extra) + kStageBytes) + wslot;
+    uint8_t* buf = stage_base(extra) + wslot * 4 * kStage64WarpBytes;
+    uint64_t* hbar = reinterpret_cast<uint64_t*>(stage_base(extra) + kStageBytes) + 2 * wslot;
     const int64_t row = static_cast<int64_t>(ti.m0) + ((valid || pad) ? r : 0);
     const int F = a.ld0;
     const int c0 = group * kHalf;
+    const int y = ti.m0 + (r & ~31);
     __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(a.out0) + row * 2 * F + ti.n0;
     __nv_bfloat16* aw = static_cast<__nv_bfloat16*>(a.out1) + row * F + ti.n0;
     const float w = valid ? __ldg(static_cast<const float*>(a.in1) + row) : 0.f;
     const int never = 0;   // the h waits are cut short only by their time limit
-    float dw = 0.f;
-#pragma unroll 1
-    for (int c = c0; c < c0 + kHalf; c += 32) {
-      // the warp's 32 rows of h_gate and h_up for columns [c, c + 32) into the
-      // first two buffers; every lane's earlier accesses to them are ordered
-      // before the asynchronous writes
+    // h_gate and h_up of step s (columns c0 + 32 s ..) into pair s & 1; every
+    // lane's earlier accesses to that pair are ordered before the writes
+    auto load_h = [&](int step) {
+      uint8_t* pp = buf + (step & 1) * 2 * kStage64WarpBytes;
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        const int y = ti.m0 + (r & ~31);
-        mbar_arrive_expect_tx(hbar, 2 * kStage64WarpBytes);
-        tma_load_2d(st, &a.mapB1, ti.n0 + c, y, hbar);
-        tma_load_2d(st + kStage64WarpBytes, &a.mapB1, F + ti.n0 + c, y, hbar);
+        mbar_arrive_expect_tx(hbar + (step & 1), 2 * kStage64WarpBytes);
+        tma_load_2d(pp, &a.mapB1, ti.n0 + c0 + 32 * step, y, hbar + (step & 1));
+        tma_load_2d(pp + kStage64WarpBytes, &a.mapB1, F + ti.n0 + c0 + 32 * step, y,
+                    hbar + (step & 1));
       }
-      if (!mbar_wait_bounded(hbar, static_cast<uint32_t>(((c - c0) >> 5) & 1), &never,
+    };
+    float dw = 0.f;
+    load_h(0);
+#pragma unroll 1
+    for (int step = 0; step < kSteps; ++step) {
+      const int c = c0 + 32 * step;
+      uint8_t* st = buf + (step & 1) * 2 * kStage64WarpBytes;
+      if (!mbar_wait_bounded(hbar + (step & 1), static_cast<uint32_t>(step >> 1) & 1u, &never,
                              a.wait_limit_ns))
         record_timeout(a.status, kWaitEpiLoad);
       uint32_t gw[16], uw[16];
@@ -129,6 +137,9 @@ struct DownDgradProblem {
         gw[4 * q] = ug.x; gw[4 * q + 1] = ug.y; gw[4 * q + 2] = ug.z; gw[4 * q + 3] = ug.w;
         uw[4 * q] = uu.x; uw[4 * q + 1] = uu.y; uw[4 * q + 2] = uu.z; uw[4 * q + 3] = uu.w;
       }
+      // the next step's h is on its way while this one computes and stores
+      if (step + 1 < kSteps) load_h(step + 1);
+      uint32_t awp[16];   // w*a of the step's 32 columns, packed bf16
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         float g[16];
@@ -144,12 +155,17 @@ struct DownDgradProblem {
         }
         stage64_bf16x16(st, lane, half, dhg);
         stage64_bf16x16(st + kStage64WarpBytes, lane, half, dhu);
-        stage64_bf16x16(st + 2 * kStage64WarpBytes, lane, half, awv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) awp[8 * half + i] = pack_bf16x2(awv[2 * i], awv[2 * i + 1]);
       }
       const bool w_row = valid || pad;
       stage64_flush(st, lane, w_row ? dh + c : nullptr, false);
       stage64_flush(st + kStage64WarpBytes, lane, w_row ? dh + F + c : nullptr, false);
-      stage64_flush(st + 2 * kStage64WarpBytes, lane, w_row ? aw + c : nullptr, false);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(st + stage64_off(lane, q)) =
+            make_uint4(awp[4 * q], awp[4 * q + 1], awp[4 * q + 2], awp[4 * q + 3]);
+      stage64_flush(st, lane, w_row ? aw + c : nullptr, false);
     }
     // one router-weight partial per (row, n-tile, column half)
     if (valid)
