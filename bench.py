@@ -107,6 +107,7 @@ def stored_traffic(kernel: str, workload: str):
 # ncu kernel name (template argument) -> the label the library's profiler uses
 NCU_LABELS = [
     ("WgradMXProblem<true>", "gate_up_wgrad_mx"), ("WgradMXProblem<false>", "down_wgrad_mx"),
+    ("WgradMXProblem<1>", "gate_up_wgrad_mx"), ("WgradMXProblem<0>", "down_wgrad_mx"),
     ("GateUpFwdMXProblem", "gate_up_gemm_swiglu_mx"), ("DownFwdMXProblem", "down_gemm_scatter_mx"),
     ("DownDgradMXProblem", "down_dgrad_swiglu_bwd_mx"),
     ("GateUpDgradMXProblem", "gate_up_dgrad_scatter_mx"),
