@@ -365,22 +365,13 @@ def test_mx_segments_restart_blocks_per_expert():
     assert np.max(np.abs(out[:40] - v[:40])) < 0.2
 
 
-def test_mxfp8_forward_is_close_to_exact_and_equals_manual_quantisation():
+def test_mxfp8_forward_is_close_to_exact_and_fp8_bwd_forward_is_exact():
     rng = np.random.default_rng(17)
     x, W_r, Wg, Wu, Wd, dY = _rand_layer(rng, 32, 64, 32, 3, 2, std=0.1)
     exact = mo.forward(x, W_r, Wg, Wu, Wd, 2)
     q = mo.forward(x, W_r, Wg, Wu, Wd, 2, precision="mxfp8")
     rel = np.linalg.norm(q["y"] - exact["y"]) / np.linalg.norm(exact["y"])
     assert 1e-4 < rel < 0.1
-    # expert 0 by hand: x rows quantised along H, weights along H, a along F
-    e = 0
-    r0, r1 = exact["offsets"][e], exact["offsets"][e + 1]
-    xe = x[exact["perm_token"][r0:r1]]
-    xq = mo.mx_round_trip(xe, 1)
-    hg = xq @ mo.mx_round_trip(Wg[e], 0)
-    hu = xq @ mo.mx_round_trip(Wu[e], 0)
-    o = mo.mx_round_trip(mo.swiglu(hg, hu), 1) @ mo.mx_round_trip(Wd[e], 0)
-    np.testing.assert_allclose(q["o"][r0:r1], o, rtol=1e-13, atol=1e-13)
     # fp8_bwd leaves the forward exact
     fb = mo.forward(x, W_r, Wg, Wu, Wd, 2, precision="fp8_bwd")
     np.testing.assert_array_equal(fb["y"], exact["y"])
@@ -389,6 +380,188 @@ def test_mxfp8_forward_is_close_to_exact_and_equals_manual_quantisation():
     for name in ("dx", "dW_gate", "dW_up", "dW_down"):
         rel = np.linalg.norm(gb[name] - ge[name]) / np.linalg.norm(ge[name])
         assert 1e-4 < rel < 0.1, name
+
+
+# ----------------------------------------------------------------- MXFP8 block axes
+#
+# Which axis each GEMM operand is blocked along is a reading (E8M0 scales per
+# 32 elements along the GEMM's reduction dimension K).  The mathematics fixes
+# a pin for it: with blocks along K, multiplying one M-row of the A operand
+# (or one N-column of B) by 2^j moves only that row's (column's) scale
+# exponents by j and leaves its E4M3 codes unchanged, so exactly that row
+# (column) of the product scales by 2^j and every other element stays
+# bit-identical.  Blocks along any other axis mix the scaled row with its
+# neighbours and break both halves of the statement.  Every quantisation
+# point of the oracle is covered by one of the pins below.
+
+MX_SHAPE = (96, 64, 64, 3, 2)    # T, H, F, E, k: 50-80 rows per expert, 2 blocks along H and F
+
+
+def _mx_layer(seed):
+    return _rand_layer(np.random.default_rng(seed), *MX_SHAPE, std=0.1)
+
+
+def _token_rows(fwd, t):
+    """Mask of the permuted rows that hold token t."""
+    return fwd["perm_token"] == t
+
+
+@pytest.mark.parametrize("j", [4, -3])
+def test_mx_forward_activation_blocks_run_along_k(j):
+    """x along H (gate/up GEMM) and a along F (down GEMM): scaling token t's
+    input scales its rows of h exactly and leaves every other token's rows of
+    h and o, and every other token's output, bit-identical."""
+    x, W_r, Wg, Wu, Wd, _ = _mx_layer(40)
+    t = 7
+    base = mo.forward(x, W_r, Wg, Wu, Wd, 2, precision="mxfp8")
+    x2 = x.copy()
+    x2[t] *= 2.0 ** j
+    got = mo.forward(x2, W_r, Wg, Wu, Wd, 2, precision="mxfp8")
+    assert np.array_equal(got["idx"], base["idx"])    # logits scale exactly: same routing
+    rows = _token_rows(base, t)
+    for name in ("h_gate", "h_up"):
+        np.testing.assert_array_equal(got[name][rows], base[name][rows] * 2.0 ** j)
+        np.testing.assert_array_equal(got[name][~rows], base[name][~rows])
+    np.testing.assert_array_equal(got["o"][~rows], base["o"][~rows])
+    assert not np.array_equal(got["o"][rows], base["o"][rows])
+    keep = np.arange(x.shape[0]) != t
+    np.testing.assert_array_equal(got["y"][keep], base["y"][keep])
+
+
+@pytest.mark.parametrize("which", ["gate", "up"])
+def test_mx_forward_gate_up_weight_blocks_run_along_h(which):
+    """W_gate / W_up along H: scaling column f of one expert's weight scales
+    exactly that column of its rows of h and nothing else."""
+    x, W_r, Wg, Wu, Wd, _ = _mx_layer(41)
+    e, f, j = 1, 37, 3
+    base = mo.forward(x, W_r, Wg, Wu, Wd, 2, precision="mxfp8")
+    W2 = (Wg if which == "gate" else Wu).copy()
+    W2[e][:, f] *= 2.0 ** j
+    args = (W2, Wu) if which == "gate" else (Wg, W2)
+    got = mo.forward(x, W_r, *args, Wd, 2, precision="mxfp8")
+    r0, r1 = base["offsets"][e], base["offsets"][e + 1]
+    name, other = ("h_gate", "h_up") if which == "gate" else ("h_up", "h_gate")
+    want = base[name].copy()
+    want[r0:r1, f] *= 2.0 ** j
+    np.testing.assert_array_equal(got[name], want)
+    np.testing.assert_array_equal(got[other], base[other])
+
+
+def test_mx_forward_down_weight_blocks_run_along_f():
+    """W_down along F: scaling column c of one expert's W_down scales exactly
+    that column of its rows of o and nothing else."""
+    x, W_r, Wg, Wu, Wd, _ = _mx_layer(42)
+    e, c, j = 2, 21, 3
+    base = mo.forward(x, W_r, Wg, Wu, Wd, 2, precision="mxfp8")
+    Wd2 = Wd.copy()
+    Wd2[e][:, c] *= 2.0 ** j
+    got = mo.forward(x, W_r, Wg, Wu, Wd2, 2, precision="mxfp8")
+    r0, r1 = base["offsets"][e], base["offsets"][e + 1]
+    want = base["o"].copy()
+    want[r0:r1, c] *= 2.0 ** j
+    np.testing.assert_array_equal(got["o"], want)
+
+
+@pytest.mark.parametrize("precision", ["mxfp8", "fp8_bwd"])
+@pytest.mark.parametrize("j", [3, -4])
+def test_mx_backward_dgrad_activation_blocks_run_along_k(precision, j):
+    """dY along H (down dgrad) and dh along F (gate/up dgrad): scaling token
+    t's upstream gradient scales its dx exactly and leaves every other token's
+    dx bit-identical."""
+    x, W_r, Wg, Wu, Wd, dY = _mx_layer(43)
+    t = 11
+    g0 = mo.backward(x, W_r, Wg, Wu, Wd, 2, dY, precision=precision)
+    dY2 = dY.copy()
+    dY2[t] *= 2.0 ** j
+    g1 = mo.backward(x, W_r, Wg, Wu, Wd, 2, dY2, precision=precision)
+    np.testing.assert_array_equal(g1["dx"][t], g0["dx"][t] * 2.0 ** j)
+    keep = np.arange(x.shape[0]) != t
+    np.testing.assert_array_equal(g1["dx"][keep], g0["dx"][keep])
+    np.testing.assert_array_equal(g1["dw"][t], g0["dw"][t] * 2.0 ** j)
+
+
+@pytest.mark.parametrize("precision", ["mxfp8", "fp8_bwd"])
+def test_mx_backward_down_weight_and_dh_token_blocks(precision):
+    """W_down along H (down dgrad) and dh along the expert's tokens (gate/up
+    wgrad): scaling row f of one expert's W_down scales exactly column f of
+    its dW_gate and dW_up; every other element of both stays bit-identical."""
+    x, W_r, Wg, Wu, Wd, dY = _mx_layer(44)
+    e, f, j = 0, 45, 2
+    g0 = mo.backward(x, W_r, Wg, Wu, Wd, 2, dY, precision=precision)
+    Wd2 = Wd.copy()
+    Wd2[e][f, :] *= 2.0 ** j
+    g1 = mo.backward(x, W_r, Wg, Wu, Wd2, 2, dY, precision=precision)
+    for name in ("dW_gate", "dW_up"):
+        want = g0[name].copy()
+        want[e][:, f] *= 2.0 ** j
+        np.testing.assert_array_equal(g1[name], want)
+
+
+@pytest.mark.parametrize("precision", ["mxfp8", "fp8_bwd"])
+def test_mx_backward_down_wgrad_a_operand_token_blocks(precision):
+    """w*a along the expert's tokens (down wgrad): scaling column f of one
+    expert's W_up scales column f of its a exactly, hence exactly row f of its
+    dW_down, and leaves every other row of dW_down bit-identical."""
+    x, W_r, Wg, Wu, Wd, dY = _mx_layer(45)
+    e, f, j = 1, 9, 3
+    g0 = mo.backward(x, W_r, Wg, Wu, Wd, 2, dY, precision=precision)
+    Wu2 = Wu.copy()
+    Wu2[e][:, f] *= 2.0 ** j
+    g1 = mo.backward(x, W_r, Wg, Wu2, Wd, 2, dY, precision=precision)
+    want = g0["dW_down"].copy()
+    want[e][f, :] *= 2.0 ** j
+    np.testing.assert_array_equal(g1["dW_down"], want)
+
+
+@pytest.mark.parametrize("precision", ["mxfp8", "fp8_bwd"])
+def test_mx_backward_down_wgrad_dy_token_blocks(precision):
+    """dY along the expert's tokens (down wgrad): scaling column c of dY for
+    every token scales exactly column c of every expert's dW_down."""
+    x, W_r, Wg, Wu, Wd, dY = _mx_layer(46)
+    c, j = 50, -3
+    g0 = mo.backward(x, W_r, Wg, Wu, Wd, 2, dY, precision=precision)
+    dY2 = dY.copy()
+    dY2[:, c] *= 2.0 ** j
+    g1 = mo.backward(x, W_r, Wg, Wu, Wd, 2, dY2, precision=precision)
+    want = g0["dW_down"].copy()
+    want[:, :, c] *= 2.0 ** j
+    np.testing.assert_array_equal(g1["dW_down"], want)
+
+
+@pytest.mark.parametrize("precision", ["mxfp8", "fp8_bwd"])
+def test_mx_backward_gate_up_dgrad_weight_blocks_run_along_f(precision):
+    """W_gate and W_up along F (gate/up dgrad), with the forward held fixed:
+    scaling row h of one expert's W_gate and W_up scales exactly column h of
+    its rows of dx and nothing else."""
+    x, W_r, Wg, Wu, Wd, dY = _mx_layer(47)
+    e, h, j = 2, 33, 2
+    fwd = mo.forward(x, W_r, Wg, Wu, Wd, 2, precision=precision)
+    b0 = mo.expert_backward(e, fwd, x, dY, Wg, Wu, Wd, precision)
+    Wg2, Wu2 = Wg.copy(), Wu.copy()
+    Wg2[e][h, :] *= 2.0 ** j
+    Wu2[e][h, :] *= 2.0 ** j
+    b1 = mo.expert_backward(e, fwd, x, dY, Wg2, Wu2, Wd, precision)
+    want = b0["dx_row"].copy()
+    want[:, h] *= 2.0 ** j
+    np.testing.assert_array_equal(b1["dx_row"], want)
+
+
+@pytest.mark.parametrize("precision", ["mxfp8", "fp8_bwd"])
+def test_mx_backward_gate_up_wgrad_x_token_blocks(precision):
+    """x along the expert's tokens (gate/up wgrad), with the forward held
+    fixed: scaling column h of x scales exactly row h of the expert's dW_gate
+    and dW_up and nothing else."""
+    x, W_r, Wg, Wu, Wd, dY = _mx_layer(48)
+    e, h, j = 0, 14, 3
+    fwd = mo.forward(x, W_r, Wg, Wu, Wd, 2, precision=precision)
+    b0 = mo.expert_backward(e, fwd, x, dY, Wg, Wu, Wd, precision)
+    x2 = x.copy()
+    x2[:, h] *= 2.0 ** j
+    b1 = mo.expert_backward(e, fwd, x2, dY, Wg, Wu, Wd, precision)
+    for name in ("dW_gate", "dW_up"):
+        want = b0[name].copy()
+        want[h, :] *= 2.0 ** j
+        np.testing.assert_array_equal(b1[name], want)
 
 
 @pytest.mark.parametrize("precision", ["mxfp8", "fp8_bwd"])
