@@ -57,13 +57,25 @@ def gemm_flops_all(sh):
 FP8_OVER_BF16 = 2.0
 
 
-def tensor_peak(name, peaks):
-    """(peak TFLOP/s, source) for a GEMM kernel: MXFP8 kernels take the measured
-    bf16 sustained peak times the nominal fp8:bf16 ratio."""
+def bf16_peak(peaks, clk):
+    """(TFLOP/s, kind) of the measured bf16 GEMM peak that matches the clocks
+    sampled in the timed region: the burst figure when the median SM clock
+    under load is within 5% of the maximum, else the sustained (power-capped)
+    figure."""
+    med, mx = (clk or {}).get("sm_mhz"), (clk or {}).get("sm_max_mhz")
+    if med is not None and mx and med >= 0.95 * mx:
+        return peaks["bf16_tflops"], "burst"
+    return peaks["bf16_tflops_sustained"], "sustained"
+
+
+def tensor_peak(name, peaks, clk):
+    """(peak TFLOP/s, source) for a GEMM kernel: the bf16 peak chosen by the
+    clocks, and for MXFP8 kernels that peak times the nominal fp8:bf16 ratio."""
+    tf, kind = bf16_peak(peaks, clk)
     if name.endswith("_mx"):
-        return (peaks["bf16_tflops_sustained"] * FP8_OVER_BF16,
-                f"{peaks['source']} bf16 sustained x {FP8_OVER_BF16:g} (nominal fp8:bf16)")
-    return peaks["bf16_tflops_sustained"], f"{peaks['source']} bf16 sustained"
+        return tf * FP8_OVER_BF16, (f"{peaks['source']} bf16 {kind} x {FP8_OVER_BF16:g} "
+                                    f"(nominal fp8:bf16)")
+    return tf, f"{peaks['source']} bf16 {kind}"
 
 
 # algorithmic bytes per launch of the memory-bound kernels
@@ -168,6 +180,66 @@ def layer_flops(sh):
     fwd = 6 * sh.P * sh.H * sh.F + 2 * sh.T * sh.H * sh.E
     bwd = 12 * sh.P * sh.H * sh.F + 4 * sh.T * sh.H * sh.E
     return fwd, bwd
+
+
+def expert_router_flops(sh):
+    """(expert GEMM FLOPs, router GEMM FLOPs) of the forward and of the backward."""
+    fe, fr = 6 * sh.P * sh.H * sh.F, 2 * sh.T * sh.H * sh.E
+    return (fe, fr), (2 * fe, 2 * fr)
+
+
+def layer_peak_frac(sh, achieved_ms, peaks, clk):
+    """The step against the tensor-core roofline of its precision: the time
+    every GEMM would take at the measured peak (bf16 peak chosen by the
+    clocks; MXFP8 GEMMs at FP8_OVER_BF16 times it; the router GEMMs are bf16
+    in every precision) divided by the measured step time."""
+    tf, kind = bf16_peak(peaks, clk)
+    (fe, fr), (be, br) = expert_router_flops(sh)
+    fwd_rate = tf * (FP8_OVER_BF16 if sh.precision == "mxfp8" else 1.0)
+    bwd_rate = tf * (FP8_OVER_BF16 if sh.precision in ("mxfp8", "fp8_bwd") else 1.0)
+    ideal_ms = ((fe / fwd_rate + be / bwd_rate) + (fr + br) / tf) / 1e9
+    return {"frac": ideal_ms / achieved_ms, "ideal_ms": ideal_ms,
+            "peak": f"{peaks['source']} bf16 {kind} {tf:.1f} TFLOP/s"
+                    + (f", MXFP8 GEMMs at x{FP8_OVER_BF16:g}" if sh.precision != "bf16" else "")}
+
+
+def summarize_kernels(prof, sh, peaks, clk):
+    """Per-kernel launches, mean time, share, achieved rate and fraction of
+    roofline from the library's live CUDA-event records, and the roofline
+    object of the kernel with the largest total time."""
+    flops = gemm_flops_all(sh)
+    byts = kernel_bytes(sh)
+    kernels = {name: {"launches": n, "avg_ms": ms / max(n, 1), "share": None}
+               for name, (n, ms) in prof.items()}
+    ktotal = sum(v["avg_ms"] * v["launches"] for v in kernels.values())
+    for v in kernels.values():
+        v["share"] = v["avg_ms"] * v["launches"] / ktotal if ktotal else None
+    dom = max(kernels, key=lambda n: kernels[n]["avg_ms"] * kernels[n]["launches"])
+    if dom in flops:
+        ach = flops[dom] / (kernels[dom]["avg_ms"] * 1e-3) / 1e12
+        peak, src = tensor_peak(dom, peaks, clk)
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak,
+                "unit": "TFLOP/s", "frac": ach / peak, "traffic": stored_traffic(dom, sh.name),
+                "peak_source": src, "sm_mhz_median": clk.get("sm_mhz"),
+                "sm_max_mhz": clk.get("sm_max_mhz")}
+    else:
+        ach = byts.get(dom, 0) / (kernels[dom]["avg_ms"] * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                "frac": ach / peak, "traffic": stored_traffic(dom, sh.name),
+                "peak_source": f"{peaks['source']} hbm"}
+    per_kernel = {}
+    for name, v in sorted(kernels.items(), key=lambda kv: -kv[1]["share"]):
+        d = {"launches": v["launches"], "avg_ms": round(v["avg_ms"], 4),
+             "share": round(v["share"], 4)}
+        if name in flops:
+            d["tflops"] = round(flops[name] / (v["avg_ms"] * 1e-3) / 1e12, 1)
+            d["frac_of_peak"] = round(d["tflops"] / tensor_peak(name, peaks, clk)[0], 3)
+        if name in byts:
+            d["gbs"] = round(byts[name] / (v["avg_ms"] * 1e-3) / 1e9, 1)
+            d["frac_hbm"] = round(d["gbs"] / peaks["hbm_gbs"], 3)
+        per_kernel[name] = d
+    return per_kernel, roof
 
 
 def load_peaks():
@@ -481,37 +553,8 @@ def run_ours(args, sh, world, rank, local):
     assert layer.device_status("fwd") == 0 and layer.device_status("bwd") == 0
 
     fwd_fl, bwd_fl = layer_flops(sh)
-    flops = gemm_flops_all(sh)
-    byts = kernel_bytes(sh)
     peaks = load_peaks()
-    kernels = {name: {"launches": n, "avg_ms": ms / max(n, 1), "share": None}
-               for name, (n, ms) in prof.items()}
-    ktotal = sum(v["avg_ms"] * v["launches"] for v in kernels.values())
-    for v in kernels.values():
-        v["share"] = v["avg_ms"] * v["launches"] / ktotal if ktotal else None
-    dom = max(kernels, key=lambda n: kernels[n]["avg_ms"] * kernels[n]["launches"])
-    if dom in flops:
-        ach = flops[dom] / (kernels[dom]["avg_ms"] * 1e-3) / 1e12
-        peak, src = tensor_peak(dom, peaks)
-        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak,
-                "unit": "TFLOP/s", "frac": ach / peak, "traffic": stored_traffic(dom, sh.name),
-                "peak_source": src}
-    else:
-        ach = byts.get(dom, 0) / (kernels[dom]["avg_ms"] * 1e-3) / 1e9
-        peak = peaks["hbm_gbs"]
-        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
-                "frac": ach / peak, "traffic": stored_traffic(dom, sh.name), "peak_source": f"{peaks['source']} hbm"}
-    per_kernel = {}
-    for name, v in sorted(kernels.items(), key=lambda kv: -kv[1]["share"]):
-        d = {"launches": v["launches"], "avg_ms": round(v["avg_ms"], 4),
-             "share": round(v["share"], 4)}
-        if name in flops:
-            d["tflops"] = round(flops[name] / (v["avg_ms"] * 1e-3) / 1e12, 1)
-            d["frac_of_peak"] = round(d["tflops"] / tensor_peak(name, peaks)[0], 3)
-        if name in byts:
-            d["gbs"] = round(byts[name] / (v["avg_ms"] * 1e-3) / 1e9, 1)
-            d["frac_hbm"] = round(d["gbs"] / peaks["hbm_gbs"], 3)
-        per_kernel[name] = d
+    per_kernel, roof = summarize_kernels(prof, sh, peaks, clk)
 
     tokens_per_s = world * sh.T / (ms_per_step * 1e-3)
     line = {
@@ -542,8 +585,7 @@ def run_ours(args, sh, world, rank, local):
         "bwd_ms": bwd_ms,
         "full_layer_ms": 2 * fwd_ms + bwd_ms,
         "full_layer_tflops": (2 * fwd_fl + bwd_fl) / ((2 * fwd_ms + bwd_ms) * 1e-3) / 1e12,
-        "frac_bf16_sustained": (fwd_fl + bwd_fl) / (ms_per_step * 1e-3) / 1e12
-        / peaks["bf16_tflops_sustained"],
+        "layer_frac_of_peak": layer_peak_frac(sh, ms_per_step, peaks, clk),
         "clocks": clk,
         "e2e": {"value": world * sh.T / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * hx.numel() * 2, "d2h_bytes_per_step": 2 * hx.numel() * 2,
@@ -554,29 +596,148 @@ def run_ours(args, sh, world, rank, local):
         "roofline": roof,
         "kernels": per_kernel,
     }
+    if world == 1 and not args.no_configs and args.shape is None:
+        line["configs"] = run_configs(args, dev, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sh, inp, args.cpu_budget)
     return line
 
 
+# ------------------------------------------------------------------ the other workloads
+
+# Every Qwen3-shaped workload besides the headline one, timed in the same
+# process after it: (workload, weights quantised once by moe_prepare_weights)
+CONFIG_RUNS = [("qwen3_30b", False), ("qwen3_30b_skew", False), ("qwen3_235b_mxfp8", False),
+               ("qwen3_235b_mxfp8", True), ("qwen3_235b_fp8_bwd", False),
+               ("qwen3_235b_mxfp8_skew", False)]
+
+
+def time_config(name, prepared, dev, steps, warmup, peaks, flags, max_sms):
+    """W warm-up steps, then K timed fwd+bwd steps of one workload (inputs
+    resident in HBM), with the library's per-kernel events live; returns the
+    workload's entry of the ``configs`` object."""
+    from mixture_experts_layer_17_gb300 import MoeLayer, moe_profile_enable, moe_profile_read
+    sh = si.shape(name)
+    inp = si.make_inputs(sh, dev)
+    layer = MoeLayer(sh.T, sh.H, sh.F, sh.E, sh.top_k, sh.precision, flags=flags, device=dev,
+                     max_sms=max_sms)
+    W = (inp["W_r"], inp["W_gate"], inp["W_up"], inp["W_down"])
+    grads = {"dx": torch.empty_like(inp["x"]), "dW_r": torch.empty_like(W[0]),
+             "dW_gate": torch.empty_like(W[1]), "dW_up": torch.empty_like(W[2]),
+             "dW_down": torch.empty_like(W[3])}
+    y = torch.empty_like(inp["x"])
+    prepare_ms = None
+    if prepared:
+        layer.prepare_weights(W[1], W[2], W[3])
+        torch.cuda.synchronize()
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record()
+        layer.prepare_weights(W[1], W[2], W[3])
+        p1.record()
+        torch.cuda.synchronize()
+        prepare_ms = p0.elapsed_time(p1)
+    for _ in range(warmup):
+        layer.forward(inp["x"], *W, inp["logit_bias"], y=y)
+        layer.backward(inp["x"], *W, inp["dY"], grads=grads)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    clocks = ClockSampler(dev.index or 0)
+    moe_profile_read()
+    moe_profile_enable(True)
+    clocks.start()
+    time.sleep(0.5)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        layer.forward(inp["x"], *W, inp["logit_bias"], y=y)
+        ev[i][1].record(stream)
+        layer.backward(inp["x"], *W, inp["dY"], grads=grads)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    moe_profile_enable(False)
+    prof = moe_profile_read()
+    assert layer.device_status("fwd") == 0 and layer.device_status("bwd") == 0
+    total = ev[0][0].elapsed_time(ev[-1][2])
+    ms = total / steps
+    fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    fwd_fl, bwd_fl = layer_flops(sh)
+    per_kernel, roof = summarize_kernels(prof, sh, peaks, clk)
+    out = {"workload": name, "precision": sh.precision, "T": sh.T, "H": sh.H, "F": sh.F,
+           "E": sh.E, "top_k": sh.top_k, "steps": steps, "warmup": warmup,
+           "ms_per_step": ms, "tokens_per_s": sh.T / (ms * 1e-3),
+           "tflops": (fwd_fl + bwd_fl) / (ms * 1e-3) / 1e12,
+           "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "full_layer_ms": 2 * fwd_ms + bwd_ms,
+           "full_layer_tflops": (2 * fwd_fl + bwd_fl) / ((2 * fwd_ms + bwd_ms) * 1e-3) / 1e12,
+           "layer_frac_of_peak": layer_peak_frac(sh, ms, peaks, clk),
+           "dominant_kernel": {k: roof[k] for k in ("kernel", "bound", "achieved", "peak",
+                                                     "unit", "frac", "peak_source")},
+           "clocks": clk,
+           "kernels": {k: {"avg_ms": v["avg_ms"], "share": v["share"],
+                           **({"frac_of_peak": v["frac_of_peak"]} if "frac_of_peak" in v else {}),
+                           **({"frac_hbm": v["frac_hbm"]} if "frac_hbm" in v else {})}
+                       for k, v in per_kernel.items()}}
+    if prepared:
+        out["prepared_weights"] = (f"MXFP8 weights quantised once by moe_prepare_weights "
+                                   f"({prepare_ms:.3f} ms, outside the step)")
+    if sh.skew:
+        c = layer.route(inp["x"], W[0], inp["logit_bias"], with_logits=False)["counts"]
+        c = c.double().cpu()
+        out["expert_load"] = {"zero_experts": int((c == 0).sum()),
+                              "max_over_mean": float(c.max() / c.mean()),
+                              "min_over_mean": float(c.min() / c.mean())}
+    del layer, inp, grads, y
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_configs(args, dev, peaks):
+    """The ``configs`` object: every other Qwen3-shaped workload."""
+    out = {"tiny": "parity case only (T=128, H=256, F=128, E=8, top-2): its fp32 draws are "
+                   "rounded to bf16 for the GPU, and it is compared with the oracle element by "
+                   "element in the tests, not timed"}
+    for name, prepared in CONFIG_RUNS:
+        key = name + ("_prepared" if prepared else "")
+        out[key] = time_config(name, prepared, dev, args.config_steps, 3, peaks, args.flags,
+                               args.max_sms)
+    return out
+
+
 # ------------------------------------------------------------------ reference arm
 
+# seconds of oracle work the K timed steps of the reference arm share
+REF_BUDGET_S = 150.0
+
+
 def run_reference(args, sh, world, rank):
-    """The CPU oracle timed on the host cores, each step a bounded sample."""
+    """The CPU oracle timed on the host cores, each step a bounded sample.
+
+    The oracle's cost per call is a fixed part (every expert a sample touches
+    has its weights widened to fp64 and its weight-gradient blocks formed)
+    plus a part linear in the tokens.  Two probe calls fit that cost, and each
+    timed step then runs the largest sample whose predicted time is its share
+    of REF_BUDGET_S (4 to 30 s), so the fixed part is amortised as it is in
+    the cpu_baseline leg.  The W warm-up steps (untimed) run 8 tokens."""
     if rank != 0:
         return None
     inp = si.make_inputs(sh, "cpu")
     inp_cpu = host_copy_for_oracle(inp)
-    n = 8
-    dt = oracle_sample_time(sh, inp_cpu, n)
-    per_step_budget = max(1.0, args.cpu_budget / max(1, args.steps + args.warmup))
-    n = max(8, min(sh.T, int(n * per_step_budget / max(dt, 1e-3))))
+    n1, n2 = min(64, sh.T), min(256, sh.T)
+    t1 = oracle_sample_time(sh, inp_cpu, n1)
+    t2 = oracle_sample_time(sh, inp_cpu, n2)
+    per_tok = max((t2 - t1) / (n2 - n1), 1e-6) if n2 > n1 else t2 / n2
+    fixed = max(t1 - n1 * per_tok, 0.0)
+    per_step = min(30.0, max(4.0, REF_BUDGET_S / max(1, args.steps)))
+    n = max(8, min(sh.T, int((per_step - fixed) / per_tok)))
     for _ in range(args.warmup):
-        oracle_sample_time(sh, inp_cpu, n)
+        oracle_sample_time(sh, inp_cpu, min(8, sh.T))
     times = [oracle_sample_time(sh, inp_cpu, n) for _ in range(args.steps)]
     sec = sum(times) / len(times)
     value = n / sec
-    sample = f"first {n} of {sh.T} tokens of {sh.name} per step: route + fwd + full bwd, numpy fp64"
+    sample = (f"first {n} of {sh.T} tokens of {sh.name} per timed step: route + fwd + full "
+              f"bwd, numpy fp64 (sample sized from probe calls on {n1} and {n2} tokens: "
+              f"{fixed:.2f} s fixed + {per_tok * 1e3:.2f} ms per token)")
     return {
         "impl": "reference",
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -610,6 +771,10 @@ def main():
     ap.add_argument("--prepared-weights", action="store_true",
                     help="MXFP8: quantise the weights once before the timed steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other Qwen3-shaped workloads (the configs object)")
+    ap.add_argument("--config-steps", type=int, default=10,
+                    help="timed steps of each workload in the configs object")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
     ap.add_argument("--record-traffic", default=None, metavar="NCU_CSV",
                     help="store per-launch DRAM bytes from an ncu CSV for --workload and exit")

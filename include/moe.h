@@ -149,7 +149,15 @@ moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* fwd_ws,
  *                   (ascending token within an expert);
  *   slot_row[t,j] = row of (t, j) in that layout.
  * logit_bias [E] fp32 and logits may be NULL.  Every integer output is
- * deterministic.  ws: at least fwd_ws bytes. */
+ * deterministic.  ws: at least fwd_ws bytes.
+ * Non-finite inputs: a NaN logit (for instance from a NaN or Inf in a row of
+ * x) ranks as -inf in the selection, so every slot still gets a valid expert
+ * id; a token whose logits are all NaN or -inf is routed to experts
+ * 0 .. top_k-1 with NaN weights, and its outputs (and every weight gradient
+ * it reaches) are NaN, while other tokens' results are unaffected.  Should an
+ * expert id outside [0, E) ever reach the permutation, that (token, slot) is
+ * skipped and the status word records MOE_ERR_INVALID_ARG (moe_get_device_status);
+ * no kernel indexes with it. */
 moe_status_t moe_route(const moe_config_t* cfg, const moe_bf16_t* x, const moe_bf16_t* W_r,
                        const float* logit_bias, float* logits, int32_t* topk_idx,
                        float* topk_w, int32_t* counts, int32_t* offsets,
@@ -234,13 +242,16 @@ moe_status_t moe_gemm_bf16(int64_t M, int64_t N, int64_t K, const moe_bf16_t* A,
  * Its scratch is a fixed array of MOE_NOALLOC_SCRATCH_BYTES inside the
  * library; every GPU that loads the library holds that array until the
  * process exits.  A configuration that needs more scratch than that is
- * rejected with MOE_ERR_WORKSPACE_TOO_SMALL before anything is queued (at
- * E = 128, H = 4096, top_k = 8 the limit is about T = 75,000 tokens).
+ * rejected with MOE_ERR_WORKSPACE_TOO_SMALL before anything is queued.  The
+ * scratch takes 2*E*H bytes (the router weight transposed), about
+ * 4*(3*top_k + 2*E/128) bytes per token (the permuted-row maps and the
+ * per-tile expert histograms) and 512*E bytes of segment padding: at E = 128,
+ * H = 4096, top_k = 8 that allows at most T = 69,904 tokens.
  * The call allocates no device memory and calls no allocating routine.
  *
  * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  All calls share the one array and it keeps the last call's
+ * device and context, with that device current); make that first call before
+ * any stream capture.  All calls share the one array and it keeps the last call's
  * contents: calls whose GPU work overlaps (on different streams, or from
  * different host threads) race on it and must be serialised by the caller.
  * device_status (nullable, 4 bytes of device memory) receives the call's
@@ -265,7 +276,9 @@ moe_status_t moe_gemm_mxfp8(int64_t M, int64_t N, int64_t K, const moe_bf16_t* A
 
 /* Reads the device status word of a workspace after the work queued on
  * `stream` has finished (this call synchronises the stream).  Returns
- * MOE_OK, MOE_ERR_TIMEOUT, or MOE_ERR_CUDA if the read itself failed. */
+ * MOE_OK, MOE_ERR_TIMEOUT (a bounded wait ran out), MOE_ERR_INVALID_ARG (a
+ * device-side index check failed: an id or row outside its array was
+ * skipped instead of used), or MOE_ERR_CUDA if the read itself failed. */
 moe_status_t moe_get_device_status(const void* ws, moe_stream_t stream);
 
 /* Human-readable name of a status code (static string). */

@@ -500,7 +500,7 @@ moe_status_t run_routing(const moe_config_t& c, const Layout& L, const RouteBufs
   }));
   MOE_TRY(run("permute", s, c.flags, [&] {
     return launch_permute(b.idx, b.w, b.base, b.offsets, b.poff, L.T, L.k, L.E, b.perm, b.slot,
-                          b.slot_pad, b.row_slot, b.w_row, s);
+                          b.slot_pad, b.row_slot, b.w_row, b.st, s);
   }));
   return MOE_OK;
 }
@@ -1518,23 +1518,64 @@ namespace {
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
 
+// The array's device address, cached per device together with the unique id
+// of the context it was looked up in: after a device reset (a new primary
+// context, the module loaded again) the id differs and the address is looked
+// up again instead of being reused.
+struct NoallocAddr {
+  unsigned long long ctx_id = 0;
+  void* addr = nullptr;
+};
 std::mutex g_noalloc_mu;
-void* g_noalloc_addr[64] = {};
+NoallocAddr g_noalloc_addr[64];
 
-// Device address of g_noalloc_scratch on the current device (looked up on
-// first use, with that device current).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (0 if it has none yet).
+moe_status_t current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (get_current == nullptr || get_id == nullptr) return MOE_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return MOE_ERR_CUDA;
+  *id = 0;
+  if (ctx != nullptr && get_id(ctx, id) != CUDA_SUCCESS) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+// Device address of g_noalloc_scratch on the current device: looked up with
+// cudaGetSymbolAddress (the array's name is only a host-side stand-in) on the
+// first call in a context, with that device current, then reused.
 moe_status_t noalloc_scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (dev < 0 || dev >= 64) return MOE_ERR_UNSUPPORTED_DEVICE;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_addr[dev] == nullptr) {
+  unsigned long long id = 0;
+  MOE_TRY(current_context_id(&id));
+  NoallocAddr& c = g_noalloc_addr[dev];
+  if (c.addr == nullptr || id == 0 || c.ctx_id != id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
       return MOE_ERR_CUDA;
-    g_noalloc_addr[dev] = p;
+    MOE_TRY(current_context_id(&id));   // the lookup has made the context current
+    c.ctx_id = id;
+    c.addr = p;
   }
-  *out = g_noalloc_addr[dev];
+  *out = c.addr;
   return MOE_OK;
 }
 

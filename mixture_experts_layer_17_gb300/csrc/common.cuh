@@ -17,9 +17,10 @@ namespace moe {
 // Device status word layout (first 256 bytes of every workspace).
 struct DeviceStatus {
   int code;        // moe_status_t of the first device-side failure, 0 if none
-  int where;       // which wait ran out (kWait* below)
+  int where;       // which wait ran out or which check failed (kWait* / kCheck* below)
   int block;       // blockIdx.x of the CTA that recorded it
-  int pad[61];
+  int index;       // failed index checks: the offending value
+  int pad[60];
 };
 static_assert(sizeof(DeviceStatus) == 256, "status block is 256 bytes");
 
@@ -31,15 +32,38 @@ enum : int {
   kWaitInjected = 5,
   kWaitDrain = 6,
   kWaitEpiLoad = 7,   // an epilogue's own TMA load of an operand it reads
+  // index checks: an expert id, row or token outside its array is recorded
+  // (and the access skipped) instead of being used
+  kCheckRouterExpert = 16,   // router epilogue: selected expert id
+  kCheckPermuteExpert = 17,  // permutation: expert id of a (token, slot)
+  kCheckGatherRow = 18,      // dispatch: destination row of a token copy
+  kCheckScatterRow = 19,     // scatter epilogues: (token, slot) row of a permuted row
+  kCheckUnpermuteExpert = 20,// un-permute: expert id of a (token, slot)
+  kCheckGatherToken = 21,    // gathered operand loads: token of a permuted row
 };
 
-constexpr int kStatusTimeout = 5;  // == MOE_ERR_TIMEOUT
+constexpr int kStatusInvalidArg = 1;  // == MOE_ERR_INVALID_ARG
+constexpr int kStatusTimeout = 5;     // == MOE_ERR_TIMEOUT
 
 MOE_DEV void record_timeout(DeviceStatus* st, int where) {
   if (st != nullptr && atomicCAS(&st->code, 0, kStatusTimeout) == 0) {
     st->where = where;
     st->block = blockIdx.x;
   }
+}
+
+// A failed index check: the first one is kept (code MOE_ERR_INVALID_ARG).
+MOE_DEV void record_bad_index(DeviceStatus* st, int where, long long value) {
+  if (st != nullptr && atomicCAS(&st->code, 0, kStatusInvalidArg) == 0) {
+    st->where = where;
+    st->block = blockIdx.x;
+    st->index = static_cast<int>(value);
+  }
+}
+
+// v in [0, n): the unsigned compare also rejects negative values
+MOE_DEV bool in_range(long long v, long long n) {
+  return static_cast<unsigned long long>(v) < static_cast<unsigned long long>(n);
 }
 
 // ---------------------------------------------------------------- misc

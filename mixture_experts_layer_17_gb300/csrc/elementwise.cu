@@ -106,25 +106,36 @@ __global__ void scan_kernel(const int* __restrict__ hist, int ntiles, int E,
 // global memory, so rows are expert-major with ascending token inside an
 // expert.  The same row shifted to the expert's padded segment (slot_pad) is
 // the row the kernels use internally.
+// An expert id outside [0, E) (which the router never writes) is recorded in
+// the status word and its (token, slot) skipped rather than used as an index.
 __global__ void permute_kernel(const int* __restrict__ idx, const float* __restrict__ w,
                                const int* __restrict__ block_base,
                                const int* __restrict__ offsets, const int* __restrict__ poff,
                                int64_t T, int k, int E, int* __restrict__ perm_token,
                                int* __restrict__ slot_row, int* __restrict__ slot_pad,
-                               int* __restrict__ row_slot, float* __restrict__ w_row) {
+                               int* __restrict__ row_slot, float* __restrict__ w_row,
+                               DeviceStatus* st) {
   __shared__ unsigned mask[4][256];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < 4 * 256; i += blockDim.x) (&mask[0][0])[i] = 0u;
   __syncthreads();
   const int64_t t = static_cast<int64_t>(blockIdx.x) * 128 + tid;
   const bool valid = t < T;
-  if (valid)
-    for (int j = 0; j < k; ++j) atomicOr(&mask[warp][idx[t * k + j]], 1u << lane);
+  if (valid) {
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[t * k + j];
+      if (in_range(e, E))
+        atomicOr(&mask[warp][e], 1u << lane);
+      else
+        record_bad_index(st, kCheckPermuteExpert, e);
+    }
+  }
   __syncthreads();
   if (!valid) return;
   const unsigned lt = (1u << lane) - 1u;
   for (int j = 0; j < k; ++j) {
     const int e = idx[t * k + j];
+    if (!in_range(e, E)) continue;
     int before = __popc(mask[warp][e] & lt);
     for (int q = 0; q < warp; ++q) before += __popc(mask[q][e]);
     const int r = block_base[static_cast<int64_t>(blockIdx.x) * E + e] + before;
@@ -352,10 +363,10 @@ cudaError_t launch_scan(const int* hist, int ntiles, int E, int* counts, int* of
 cudaError_t launch_permute(const int* idx, const float* w, const int* block_base,
                            const int* offsets, const int* poff, int64_t T, int k, int E,
                            int* perm_token, int* slot_row, int* slot_pad, int* row_slot,
-                           float* w_row, cudaStream_t s) {
+                           float* w_row, DeviceStatus* st, cudaStream_t s) {
   permute_kernel<<<blocks_for(T, 128), 128, 0, s>>>(idx, w, block_base, offsets, poff, T, k, E,
                                                     perm_token, slot_row, slot_pad, row_slot,
-                                                    w_row);
+                                                    w_row, st);
   return cudaGetLastError();
 }
 

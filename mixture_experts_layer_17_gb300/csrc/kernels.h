@@ -64,7 +64,7 @@ cudaError_t launch_scan(const int* hist, int ntiles, int E, int* counts, int* of
 cudaError_t launch_permute(const int* idx, const float* w, const int* block_base,
                            const int* offsets, const int* poff, int64_t T, int k, int E,
                            int* perm_token, int* slot_row, int* slot_pad, int* row_slot,
-                           float* w_row, cudaStream_t s);
+                           float* w_row, DeviceStatus* st, cudaStream_t s);
 // dst[slot_row[t, j]] = src[t] for every slot, and the tail rows of each
 // expert's padded segment ([poff[e] + counts[e], poff[e+1])) zeroed
 cudaError_t launch_gather_rows(const uint16_t* src, const int* slot_row, uint16_t* dst,

@@ -231,7 +231,10 @@ struct RouterProblem {
           float l = v[i];
           if (bias != nullptr) l += __ldg(bias + e);
           v[i] = l;
-          insert(topv, topi, k, l, e);
+          // a NaN logit (a token whose input holds NaN or Inf) ranks as -inf:
+          // every slot then still receives a valid expert id, the lower ids
+          // first by the tie rule
+          insert(topv, topi, k, isnan(l) ? -INFINITY : l, e);
         }
       }
       if (valid && logits != nullptr) {
@@ -263,6 +266,8 @@ struct RouterProblem {
       }
     }
     if (group == 0 && valid) {
+      // m = -inf only when every logit of the token is -inf or NaN; the
+      // weights are then NaN, as the softmax over such logits is
       const float m = topv[0];
       float ex[kMaxK];
       float sum = 0.f;
@@ -279,7 +284,10 @@ struct RouterProblem {
         if (j < k) {
           idx_out[j] = topi[j];
           w_out[j] = ex[j] * inv;
-          atomicAdd(hist + topi[j], 1);
+          if (in_range(topi[j], E))
+            atomicAdd(hist + topi[j], 1);
+          else
+            record_bad_index(a.status, kCheckRouterExpert, topi[j]);
         }
       }
     }

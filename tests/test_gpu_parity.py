@@ -137,3 +137,34 @@ def test_repeat_calls_are_deterministic():
     for k in a:
         if a[k] is not None:
             assert np.array_equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("mode", sorted(PAIR_MODES))
+def test_nan_token_is_routed_to_valid_experts(mode):
+    """A token whose input row is NaN has NaN logits, which rank as -inf: it
+    goes to experts 0 .. k-1 (the lower ids, by the tie rule) with NaN
+    weights, as the oracle's stable sort of NaN logits also decides.  The
+    call completes with a clean device status, and every other token's
+    results, and the weight gradients of the experts the NaN token did not
+    reach, match the oracle."""
+    sh = si.custom_shape(300, 256, 256, 16, 4, seed=11)   # the sweep's first shape
+    inp = si.make_inputs(sh, "cuda")
+    t_nan, k = 77, sh.top_k
+    inp["x"][t_nan] = float("nan")
+    out = run_layer(sh, inp, flags=PAIR_MODES[mode])     # asserts a clean device status
+    assert np.array_equal(out["topk_idx"][t_nan], np.arange(k))
+    assert np.all(np.isnan(out["topk_w"][t_nan]))
+    x, W_r, Wg, Wu, Wd, dY = (f64(inp[n]) for n in ("x", "W_r", "W_gate", "W_up", "W_down", "dY"))
+    ref = mo.backward(x, W_r, Wg, Wu, Wd, k, dY)
+    fwd = ref["fwd"]
+    for name, want in (("topk_idx", fwd["idx"]), ("counts", fwd["counts"]),
+                       ("offsets", fwd["offsets"]), ("perm_token", fwd["perm_token"]),
+                       ("slot_row", fwd["slot_row"])):
+        assert np.array_equal(out[name], want), name
+    keep = np.arange(sh.T) != t_nan
+    assert np.all(np.isnan(out["y"][t_nan]))
+    assert rel_fro(out["y"][keep], fwd["y"][keep]) <= BF16_TOL
+    assert rel_fro(out["dx"][keep], ref["dx"][keep]) <= BF16_TOL
+    for e in range(k, sh.E):
+        for name in ("dW_gate", "dW_up", "dW_down"):
+            assert rel_fro(out[name][e], ref[name][e]) <= BF16_TOL, (name, e)

@@ -64,7 +64,8 @@ def test_route_noalloc_matches_route_on_two_calls_in_a_row():
 
 def test_route_noalloc_rejects_configurations_beyond_its_scratch():
     from mixture_experts_layer_17_gb300 import libmoe
-    # about 72 bytes of scratch per token at top_k = 8: 200k tokens exceed 8 MiB
+    # about 104 bytes of scratch per token at top_k = 8 (at most 69,904 tokens fit in
+    # 8 MiB at this shape): 200k tokens are rejected
     cfg = libmoe.make_config(200_000, 4096, 1536, 128, 8)
     x = torch.zeros(16, dtype=torch.bfloat16, device="cuda")   # never read: rejected first
     outs = [torch.zeros(16, dtype=torch.int32, device="cuda") for _ in range(8)]
