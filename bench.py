@@ -90,6 +90,24 @@ def kernel_bytes(sh):
     }
 
 
+def gemm_bytes(sh):
+    """Algorithmic DRAM bytes per launch of each bf16 expert GEMM: every
+    operand read once and every output written once (2 bytes per element).
+    With ~256 rows per expert (the 30B shape) the weight bytes alone put these
+    GEMMs near the ridge of the roofline, so the bench reports whichever of the
+    FLOP time and the byte time is larger."""
+    P, H, F, E = sh.P, sh.H, sh.F, sh.E
+    W1, W2 = 2 * E * H * F * 2, E * F * H * 2      # [W_gate | W_up], W_down
+    return {
+        "gate_up_gemm_swiglu": P * H * 2 + W1 + P * 2 * F * 2 + P * F * 2,
+        "down_gemm_scatter": P * F * 2 + W2 + P * H * 2,
+        "down_dgrad_swiglu_bwd": P * H * 2 + W2 + P * 2 * F * 2 + P * 2 * F * 2 + P * F * 2,
+        "down_wgrad": P * F * 2 + P * H * 2 + W2,
+        "gate_up_dgrad_scatter": P * 2 * F * 2 + W1 + P * H * 2,
+        "gate_up_wgrad": P * H * 2 + P * 2 * F * 2 + W1,
+    }
+
+
 def csrc_hash() -> str:
     """Hash of the kernel sources: a stored ncu traffic figure is only used
     while the kernels it was taken on are unchanged."""
@@ -198,9 +216,21 @@ def layer_peak_frac(sh, achieved_ms, peaks, clk):
     fwd_rate = tf * (FP8_OVER_BF16 if sh.precision == "mxfp8" else 1.0)
     bwd_rate = tf * (FP8_OVER_BF16 if sh.precision in ("mxfp8", "fp8_bwd") else 1.0)
     ideal_ms = ((fe / fwd_rate + be / bwd_rate) + (fr + br) / tf) / 1e9
-    return {"frac": ideal_ms / achieved_ms, "ideal_ms": ideal_ms,
-            "peak": f"{peaks['source']} bf16 {kind} {tf:.1f} TFLOP/s"
-                    + (f", MXFP8 GEMMs at x{FP8_OVER_BF16:g}" if sh.precision != "bf16" else "")}
+    out = {"frac": ideal_ms / achieved_ms, "ideal_ms": ideal_ms,
+           "peak": f"{peaks['source']} bf16 {kind} {tf:.1f} TFLOP/s"
+                   + (f", MXFP8 GEMMs at x{FP8_OVER_BF16:g}" if sh.precision != "bf16" else "")}
+    if sh.precision == "bf16":
+        # the step's roofline with both roofs: every expert GEMM at the larger
+        # of its FLOP time and its algorithmic-byte time, the router GEMMs at
+        # their FLOP time, the memory-bound kernels at their byte time
+        fl, gb, kb = gemm_flops(sh), gemm_bytes(sh), kernel_bytes(sh)
+        hbm = peaks["hbm_gbs"] * 1e9
+        t = sum(max(fl[k] / (tf * 1e12), gb[k] / hbm) for k in gb)
+        t += (fl["router_gemm_topk"] + fl["router_wgrad"]) / (tf * 1e12)
+        t += sum(kb.values()) / hbm
+        out["roofline_ms"] = t * 1e3
+        out["frac_of_roofline"] = t * 1e3 / achieved_ms
+    return out
 
 
 def summarize_kernels(prof, sh, peaks, clk):
@@ -209,19 +239,38 @@ def summarize_kernels(prof, sh, peaks, clk):
     object of the kernel with the largest total time."""
     flops = gemm_flops_all(sh)
     byts = kernel_bytes(sh)
+    gbyts = gemm_bytes(sh) if sh.precision == "bf16" else {}
     kernels = {name: {"launches": n, "avg_ms": ms / max(n, 1), "share": None}
                for name, (n, ms) in prof.items()}
     ktotal = sum(v["avg_ms"] * v["launches"] for v in kernels.values())
     for v in kernels.values():
         v["share"] = v["avg_ms"] * v["launches"] / ktotal if ktotal else None
     dom = max(kernels, key=lambda n: kernels[n]["avg_ms"] * kernels[n]["launches"])
-    if dom in flops:
+
+    def hbm_bound(name):
+        # a bf16 expert GEMM whose algorithmic bytes take longer at the HBM
+        # peak than its FLOPs at the tensor peak
+        if name not in gbyts:
+            return False
+        return gbyts[name] / (peaks["hbm_gbs"] * 1e9) > \
+            flops[name] / (tensor_peak(name, peaks, clk)[0] * 1e12)
+
+    if dom in flops and not hbm_bound(dom):
         ach = flops[dom] / (kernels[dom]["avg_ms"] * 1e-3) / 1e12
         peak, src = tensor_peak(dom, peaks, clk)
         roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peak,
                 "unit": "TFLOP/s", "frac": ach / peak, "traffic": stored_traffic(dom, sh.name),
                 "peak_source": src, "sm_mhz_median": clk.get("sm_mhz"),
                 "sm_max_mhz": clk.get("sm_max_mhz")}
+    elif dom in flops:
+        ach = gbyts[dom] / (kernels[dom]["avg_ms"] * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                "frac": ach / peak, "traffic": stored_traffic(dom, sh.name),
+                "peak_source": f"{peaks['source']} hbm (algorithmic bytes above the tensor "
+                               f"time at this shape)",
+                "tensor_frac": flops[dom] / (kernels[dom]["avg_ms"] * 1e-3) / 1e12
+                / tensor_peak(dom, peaks, clk)[0]}
     else:
         ach = byts.get(dom, 0) / (kernels[dom]["avg_ms"] * 1e-3) / 1e9
         peak = peaks["hbm_gbs"]
@@ -235,6 +284,10 @@ def summarize_kernels(prof, sh, peaks, clk):
         if name in flops:
             d["tflops"] = round(flops[name] / (v["avg_ms"] * 1e-3) / 1e12, 1)
             d["frac_of_peak"] = round(d["tflops"] / tensor_peak(name, peaks, clk)[0], 3)
+        if name in gbyts:
+            d["gbs"] = round(gbyts[name] / (v["avg_ms"] * 1e-3) / 1e9, 1)
+            d["frac_hbm"] = round(d["gbs"] / peaks["hbm_gbs"], 3)
+            d["bound"] = "hbm" if hbm_bound(name) else "tensor"
         if name in byts:
             d["gbs"] = round(byts[name] / (v["avg_ms"] * 1e-3) / 1e9, 1)
             d["frac_hbm"] = round(d["gbs"] / peaks["hbm_gbs"], 3)

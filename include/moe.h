@@ -79,11 +79,14 @@ typedef enum {
 #define MOE_FLAG_CTA_PAIRS_OFF  0x4u  /* run every expert GEMM on single-CTA 128-row
                                          tiles                                    */
 #define MOE_FLAG_CTA_PAIRS_ON   0x8u  /* use CTA-pair 256-row tiles (cta_group::2)
-                                         wherever the shape allows; by default,
-                                         when experts average >= 512 rows, pairs
-                                         run every expert GEMM, and from 256 rows
-                                         the two bf16 dgrads (the down dgrad when F
-                                         is a multiple of 256)                    */
+                                         wherever the shape allows, the MXFP8
+                                         GEMMs included (block-scaled pairs; the
+                                         MXFP8 down dgrad stays single-CTA); by
+                                         default, when experts average >= 512
+                                         rows, pairs run every bf16 expert GEMM,
+                                         and from 256 rows the two bf16 dgrads
+                                         (the down dgrad when F is a multiple of
+                                         256), and the MXFP8 GEMMs run single-CTA */
 #define MOE_FLAG_RECOMPUTE      0x10u /* activation checkpointing (full activation
                                          checkpointing is the training setting of
                                          the end-to-end runs in "Os Números..." on
@@ -269,7 +272,9 @@ moe_status_t moe_route_noalloc(const moe_config_t* cfg, const moe_bf16_t* x,
  * sum_k A_q(m, k) B_q(n, k) with fp32 accumulation.  Limits: M >= 1; N and K
  * multiples of 128.  Workspace: call with ws = NULL to receive the size in
  * *ws_bytes; otherwise *ws_bytes is the workspace size (256-byte aligned).
- * Used to test the engine's MXFP8 path in isolation. */
+ * Used to test the engine's MXFP8 path in isolation: N a multiple of 256 runs
+ * the CTA-pair kernel (256 x 256 tiles, block-scaled cta_group::2 MMAs),
+ * other N the single-CTA one (128 x 128 tiles). */
 moe_status_t moe_gemm_mxfp8(int64_t M, int64_t N, int64_t K, const moe_bf16_t* A,
                             const moe_bf16_t* B, float* D, void* ws, size_t* ws_bytes,
                             moe_stream_t stream);

@@ -100,6 +100,21 @@ bool make_map_u8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// An array of 512-byte MXFP8 scale atoms as a 2-D u32 tensor [atoms, 128]
+// with one-atom boxes: CTA pairs load atoms by TMA (the peer's loads complete
+// on the leader's barrier).  Atom rows past `atoms` read as zeros.
+bool make_map_atoms(CUtensorMap* m, const void* base, uint64_t atoms) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {128, atoms};
+  cuuint64_t strides[1] = {512};
+  cuuint32_t box[2] = {128, 1};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------- profiling
 
 struct Pending {
@@ -181,6 +196,9 @@ struct Layout {
   int64_t T, P, T_pad;
   int64_t Pa;        // rows of the padded internal layout: P + 64 * E (64-row aligned segments)
   bool pair_gu_fwd, pair_down_fwd, pair_down_dgrad, pair_gu_dgrad, pair_down_wgrad, pair_gu_wgrad;
+  // MXFP8 GEMMs on CTA pairs (block-scaled cta_group::2); the down dgrad,
+  // bound by its epilogue, stays on single-CTA tiles
+  bool mx_pair_gu_fwd, mx_pair_down_fwd, mx_pair_gu_dgrad, mx_pair_down_wgrad, mx_pair_gu_wgrad;
   int H, F, E, k;
   int ntiles;        // router tiles of 128 tokens
   int router_bn;     // N of the router GEMM (power of two >= E, >= 16)
@@ -246,6 +264,19 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.pair_gu_dgrad = bb && pp_dgrad;
   L.pair_down_wgrad = bb && pp && (L.F % 256 == 0);
   L.pair_gu_wgrad = bb && pp;
+  // MXFP8 GEMMs run as CTA pairs only on request (MOE_FLAG_CTA_PAIRS_ON):
+  // their 256-column tiles keep one TMEM accumulator beside the scale
+  // factors, and at the 235B shape the pair versions measured 4-9% slower
+  // than the single-CTA ones (the accumulator's hand-over waits on both
+  // CTAs' epilogues)
+  const bool mf = c.precision == MOE_MXFP8;        // MXFP8 forward GEMMs
+  const bool mb = c.precision != MOE_BF16;         // MXFP8 backward GEMMs
+  const bool mxp = can_pair && pairs_on;
+  L.mx_pair_gu_fwd = mf && mxp;
+  L.mx_pair_down_fwd = mf && mxp;
+  L.mx_pair_gu_dgrad = mb && mxp;
+  L.mx_pair_down_wgrad = mb && mxp && (L.F % 256 == 0);
+  L.mx_pair_gu_wgrad = mb && mxp;
   L.recompute = (c.flags & MOE_FLAG_RECOMPUTE) != 0;
   L.prepared = c.precision != MOE_BF16 && c.prepared_weights != nullptr;
   L.ntiles = static_cast<int>((L.T + kBM - 1) / kBM);
@@ -574,8 +605,9 @@ struct MxGateUpBufs {
 // epilogue writes h and quantises a along F from fp32.
 moe_status_t gate_up_fwd_mx(const Layout& L, int sms, cudaStream_t s, uint32_t fl,
                             DeviceStatus* st, const uint16_t* W_gate, const uint16_t* W_up,
-                            const int* offsets, const int* counts, const int* mtile, uint16_t* h,
-                            const MxGateUpBufs& q, bool recompute) {
+                            const int* offsets, const int* counts, const int* mtile,
+                            const int* mtile2, uint16_t* h, const MxGateUpBufs& q,
+                            bool recompute) {
   if (!q.w_ready) {
     MOE_TRY(run(recompute ? "recompute_mx_quant_w_gate_up" : "mx_quant_w_gate_up", s, fl, [&] {
       return launch_quant_cols_gate_up(W_gate, W_up, L.E, L.H, L.F, q.wgu, q.swgu, s);
@@ -588,12 +620,13 @@ moe_status_t gate_up_fwd_mx(const Layout& L, int sms, cudaStream_t s, uint32_t f
   a.mapB1 = a.mapB0;
   a.K = L.H;
   a.N = 2 * L.F;
-  a.n_tiles = 2 * L.F / 256;   // 128 x 256 tiles
+  a.n_tiles = 2 * L.F / 256;   // 128 x 256 tiles (pairs: 256 x 256)
   a.num_groups = L.E;
   a.b_group_rows = L.H;
   a.offsets = offsets;
   a.counts = counts;
   a.mtile_off = mtile;
+  a.mtile2_off = mtile2;
   a.out0 = q.aq;    // a quantised to E4M3 in the epilogue
   a.out1 = h;
   a.out2 = q.sa;    // its scale atoms
@@ -606,9 +639,17 @@ moe_status_t gate_up_fwd_mx(const Layout& L, int sms, cudaStream_t s, uint32_t f
     a.flags = kGemmInjectWait;
     a.wait_limit_ns = kTestWaitNs;
   }
+  const char* label = recompute ? "recompute_gate_up_gemm_swiglu_mx" : "gate_up_gemm_swiglu_mx";
+  if (L.mx_pair_gu_fwd) {
+    if (!make_map_atoms(&a.mapSFA, q.sx, static_cast<uint64_t>(L.mt_max) * (L.H / 128)) ||
+        !make_map_atoms(&a.mapSFB, q.swgu,
+                        static_cast<uint64_t>(L.E) * (2 * L.F / 128) * (L.H / 128)))
+      return MOE_ERR_CUDA;
+    const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, sms);
+    return run(label, s, fl, [&] { return launch_gate_up_fwd_mx_pair(a, grid, s); });
+  }
   const int grid = grid_for(((L.P + kBM - 1) / kBM + L.E) * a.n_tiles, sms);
-  return run(recompute ? "recompute_gate_up_gemm_swiglu_mx" : "gate_up_gemm_swiglu_mx", s, fl,
-             [&] { return launch_gate_up_fwd_mx(a, grid, s); });
+  return run(label, s, fl, [&] { return launch_gate_up_fwd_mx(a, grid, s); });
 }
 
 // F7 + F8 and F9 in MXFP8: the gate/up part above, then W_down quantised
@@ -616,8 +657,9 @@ moe_status_t gate_up_fwd_mx(const Layout& L, int sms, cudaStream_t s, uint32_t f
 moe_status_t forward_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t fl,
                               DeviceStatus* st, const uint16_t* W_gate, const uint16_t* W_up,
                               const uint16_t* W_down, const int* offsets, const int* counts,
-                              const int* mtile, const float* w_row, const int* row_slot,
-                              uint16_t* h, uint16_t* scratch, void* ws, void* wq) {
+                              const int* mtile, const int* mtile2, const float* w_row,
+                              const int* row_slot, uint16_t* h, uint16_t* scratch, void* ws,
+                              void* wq) {
   MxGateUpBufs q{at<uint8_t>(ws, L.fq_x), at<uint8_t>(ws, L.fs_x), at<uint8_t>(ws, L.fq_a),
                  at<uint8_t>(ws, L.fs_a), nullptr, nullptr};
   if (wq != nullptr) {
@@ -632,7 +674,7 @@ moe_status_t forward_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t
   uint8_t* sa = q.sa;
   uint8_t* wd = wq != nullptr ? at<uint8_t>(wq, L.q_d_f) : at<uint8_t>(ws, L.fq_wd);
   uint8_t* swd = wq != nullptr ? at<uint8_t>(wq, L.qs_d_f) : at<uint8_t>(ws, L.fs_wd);
-  MOE_TRY(gate_up_fwd_mx(L, sms, s, fl, st, W_gate, W_up, offsets, counts, mtile, h, q,
+  MOE_TRY(gate_up_fwd_mx(L, sms, s, fl, st, W_gate, W_up, offsets, counts, mtile, mtile2, h, q,
                          false));
   if (wq == nullptr) {
     MOE_TRY(run("mx_quant_w_down_f", s, fl, [&] {
@@ -647,22 +689,34 @@ moe_status_t forward_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t
     a.mapB1 = a.mapB0;
     a.K = L.F;
     a.N = L.H;
-    a.n_tiles = L.H / 256;   // 128 x 256 tiles
+    a.n_tiles = L.H / 256;   // 128 x 256 tiles (pairs: 256 x 256)
     a.num_groups = L.E;
     a.b_group_rows = L.F;
     a.offsets = offsets;
     a.counts = counts;
     a.mtile_off = mtile;
+    a.mtile2_off = mtile2;
     a.in0 = w_row;
     a.in1 = row_slot;
     a.out0 = scratch;
     a.ld0 = L.H;
+    a.T = L.T;           // the scatter's rows are (token, slot) pairs: T * top_k of them
+    a.top_k = L.k;
     a.sfA = sa;
     a.kt_a = L.F / 128;
     a.sfB0 = swd;
     a.kt_b = L.F / 128;
-    const int grid = grid_for(((L.P + kBM - 1) / kBM + L.E) * a.n_tiles, sms);
-    MOE_TRY(run("down_gemm_scatter_mx", s, fl, [&] { return launch_down_fwd_mx(a, grid, s); }));
+    if (L.mx_pair_down_fwd) {
+      if (!make_map_atoms(&a.mapSFA, sa, static_cast<uint64_t>(L.mt_max) * (L.F / 128)) ||
+          !make_map_atoms(&a.mapSFB, swd, static_cast<uint64_t>(L.E) * (L.H / 128) * (L.F / 128)))
+        return MOE_ERR_CUDA;
+      const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, sms);
+      MOE_TRY(run("down_gemm_scatter_mx", s, fl,
+                  [&] { return launch_down_fwd_mx_pair(a, grid, s); }));
+    } else {
+      const int grid = grid_for(((L.P + kBM - 1) / kBM + L.E) * a.n_tiles, sms);
+      MOE_TRY(run("down_gemm_scatter_mx", s, fl, [&] { return launch_down_fwd_mx(a, grid, s); }));
+    }
   }
   return MOE_OK;
 }
@@ -670,7 +724,7 @@ moe_status_t forward_gemms_mx(const Layout& L, int sms, cudaStream_t s, uint32_t
 
 struct BwdBufs {
   const uint16_t *W_gate, *W_up, *W_down, *dyp, *xperm, *h;
-  const int *offsets, *counts, *mtile, *order, *slot, *row_slot;   // offsets: padded starts
+  const int *offsets, *counts, *mtile, *mtile2, *order, *slot, *row_slot;   // offsets: padded starts
   const float *w_row, *w;
   const int* idx;
   const uint16_t* wrt;
@@ -761,7 +815,8 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
   // B9: router softmax / top-k backward
   if (cudaMemsetAsync(b.dlt, 0, 2ull * L.E * L.T_pad, s) != cudaSuccess) return MOE_ERR_CUDA;
   MOE_TRY(run("router_bwd", s, fl, [&] {
-    return launch_router_bwd(b.dwp, L.nparts, b.slot, b.w, b.idx, L.T, L.k, b.dl, b.dlt, L.T_pad, s);
+    return launch_router_bwd(b.dwp, L.nparts, b.slot, b.w, b.idx, L.T, L.k, L.E, L.Pa, b.dl, b.dlt,
+                             L.T_pad, st, s);
   }));
   // B5: down wgrad over the padded token layout
   MOE_TRY(run("mx_quant_aw_tokens", s, fl, [&] {
@@ -778,7 +833,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     a.M = L.F;
     a.N = L.H;
     a.m_tiles = L.F / 128;
-    a.n_tiles = L.H / 256;   // 128 x 256 tiles
+    a.n_tiles = L.H / 256;   // 128 x 256 tiles (pairs: 256 x 256)
     a.num_groups = L.E;
     a.offsets = b.offsets;
     a.counts = b.counts;
@@ -788,8 +843,18 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     a.ld0 = L.H;
     a.sfA = sawt;
     a.sfB0 = sdyt;
-    const int grid = grid_for(static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles, sms);
-    MOE_TRY(run("down_wgrad_mx", s, fl, [&] { return launch_down_wgrad_mx(a, grid, s); }));
+    if (L.mx_pair_down_wgrad) {
+      a.m_tiles = L.F / 256;
+      a.kt_a = L.F / 128;     // A's atoms per token k-tile
+      if (!make_map_atoms(&a.mapSFA, sawt, static_cast<uint64_t>(L.mt_max) * (L.F / 128)) ||
+          !make_map_atoms(&a.mapSFB, sdyt, static_cast<uint64_t>(L.mt_max) * (L.H / 128)))
+        return MOE_ERR_CUDA;
+      const int grid = grid_for_pairs(static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles, sms);
+      MOE_TRY(run("down_wgrad_mx", s, fl, [&] { return launch_down_wgrad_mx_pair(a, grid, s); }));
+    } else {
+      const int grid = grid_for(static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles, sms);
+      MOE_TRY(run("down_wgrad_mx", s, fl, [&] { return launch_down_wgrad_mx(a, grid, s); }));
+    }
   }
   // B6 + B7: gate/up dgrad, then the un-permute
   if (!prep) {
@@ -818,16 +883,30 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     a.in1 = b.row_slot;
     a.out0 = b.scratch;
     a.ld0 = L.H;
+    a.T = L.T;           // the scatter's rows are (token, slot) pairs: T * top_k of them
+    a.top_k = L.k;
     a.sfA = sdh;
     a.kt_a = 2 * L.F / 128;
     a.sfB0 = swg;
     a.sfB1 = swu;
     a.kt_b = L.F / 128;
-    const int grid = grid_for(mtiles * a.n_tiles, sms);
-    MOE_TRY(run("gate_up_dgrad_scatter_mx", s, fl, [&] { return launch_gate_up_dgrad_mx(a, grid, s); }));
+    a.mtile2_off = b.mtile2;
+    if (L.mx_pair_gu_dgrad) {
+      const uint64_t w_atoms = static_cast<uint64_t>(L.E) * (L.H / 128) * (L.F / 128);
+      if (!make_map_atoms(&a.mapSFA, sdh, static_cast<uint64_t>(L.mt_max) * (2 * L.F / 128)) ||
+          !make_map_atoms(&a.mapSFB, swg, w_atoms) || !make_map_atoms(&a.mapSFB1, swu, w_atoms))
+        return MOE_ERR_CUDA;
+      const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, sms);
+      MOE_TRY(run("gate_up_dgrad_scatter_mx", s, fl,
+                  [&] { return launch_gate_up_dgrad_mx_pair(a, grid, s); }));
+    } else {
+      const int grid = grid_for(mtiles * a.n_tiles, sms);
+      MOE_TRY(run("gate_up_dgrad_scatter_mx", s, fl,
+                  [&] { return launch_gate_up_dgrad_mx(a, grid, s); }));
+    }
   }
   MOE_TRY(run("unpermute_dx", s, fl, [&] {
-    return launch_unpermute(b.scratch, b.dl, b.idx, b.wrt, b.dx, L.T, L.H, L.k, L.E, sms, s);
+    return launch_unpermute(b.scratch, b.dl, b.idx, b.wrt, b.dx, L.T, L.H, L.k, L.E, sms, st, s);
   }));
   // B8: gate/up wgrad over the padded token layout
   MOE_TRY(run("mx_quant_dh_tokens", s, fl, [&] {
@@ -844,7 +923,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     a.M = L.H;
     a.N = 2 * L.F;
     a.m_tiles = L.H / 128;
-    a.n_tiles = 2 * L.F / 256;   // 128 x 256 tiles
+    a.n_tiles = 2 * L.F / 256;   // 128 x 256 tiles (pairs: 256 x 256)
     a.num_groups = L.E;
     a.offsets = b.offsets;
     a.counts = b.counts;
@@ -855,8 +934,19 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     a.ld0 = L.F;
     a.sfA = sxt;
     a.sfB0 = sdht;
-    const int grid = grid_for(static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles, sms);
-    MOE_TRY(run("gate_up_wgrad_mx", s, fl, [&] { return launch_gate_up_wgrad_mx(a, grid, s); }));
+    if (L.mx_pair_gu_wgrad) {
+      a.m_tiles = L.H / 256;
+      a.kt_a = L.H / 128;     // A's atoms per token k-tile
+      if (!make_map_atoms(&a.mapSFA, sxt, static_cast<uint64_t>(L.mt_max) * (L.H / 128)) ||
+          !make_map_atoms(&a.mapSFB, sdht, static_cast<uint64_t>(L.mt_max) * (2 * L.F / 128)))
+        return MOE_ERR_CUDA;
+      const int grid = grid_for_pairs(static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles, sms);
+      MOE_TRY(run("gate_up_wgrad_mx", s, fl,
+                  [&] { return launch_gate_up_wgrad_mx_pair(a, grid, s); }));
+    } else {
+      const int grid = grid_for(static_cast<int64_t>(L.E) * a.m_tiles * a.n_tiles, sms);
+      MOE_TRY(run("gate_up_wgrad_mx", s, fl, [&] { return launch_gate_up_wgrad_mx(a, grid, s); }));
+    }
   }
   return MOE_OK;
 }
@@ -1016,13 +1106,14 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
     }));
   } else {
     MOE_TRY(run("gather_x", s, fl, [&] {
-      return launch_gather_rows(x, slot_pad, xperm, L.T, L.H, L.k, poff, counts, L.E, s);
+      return launch_gather_rows(x, slot_pad, xperm, L.T, L.H, L.k, poff, counts, L.E, L.Pa, st, s);
     }));
   }
 
   if (cfg->precision == MOE_MXFP8) {
-    MOE_TRY(forward_gemms_mx(L, sms, s, fl, st, W_gate, W_up, W_down, poff, counts, mtile, w_row,
-                             row_slot, h, scratch, ws, const_cast<void*>(cfg->prepared_weights)));
+    MOE_TRY(forward_gemms_mx(L, sms, s, fl, st, W_gate, W_up, W_down, poff, counts, mtile, mtile2,
+                             w_row, row_slot, h, scratch, ws,
+                             const_cast<void*>(cfg->prepared_weights)));
   } else {
     // F7 + F8: gate/up GEMM with SwiGLU
     MOE_TRY(gate_up_fwd_bf16(L, sms, s, fl, st, xperm, W_gate, W_up, poff, counts, mtile, mtile2,
@@ -1047,6 +1138,8 @@ moe_status_t moe_forward(const moe_config_t* cfg, const moe_bf16_t* x, const moe
       a.in1 = row_slot;
       a.out0 = scratch;
       a.ld0 = L.H;
+      a.T = L.T;           // the scatter's rows are (token, slot) pairs: T * top_k of them
+      a.top_k = L.k;
       if (L.pair_down_fwd) {
         const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, sms);
         MOE_TRY(run("down_gemm_scatter", s, fl, [&] { return launch_down_fwd_pair(a, grid, s); }));
@@ -1133,7 +1226,7 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
       }));
     } else {
       MOE_TRY(run("recompute_gather_x", s, fl, [&] {
-        return launch_gather_rows(x, slot_pad, xp, L.T, L.H, L.k, poff, counts, L.E, s);
+        return launch_gather_rows(x, slot_pad, xp, L.T, L.H, L.k, poff, counts, L.E, L.Pa, st, s);
       }));
     }
     if (cfg->precision == MOE_MXFP8) {
@@ -1146,7 +1239,7 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
         q.swgu = at<uint8_t>(wq, L.qs_gu_h);
         q.w_ready = true;
       }
-      MOE_TRY(gate_up_fwd_mx(L, sms, s, fl, st, W_gate, W_up, poff, counts, mtile, hh, q,
+      MOE_TRY(gate_up_fwd_mx(L, sms, s, fl, st, W_gate, W_up, poff, counts, mtile, mtile2, hh, q,
                              true));
     } else {
       MOE_TRY(gate_up_fwd_bf16(L, sms, s, fl, st, xp, W_gate, W_up, poff, counts, mtile, mtile2,
@@ -1175,12 +1268,12 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
     }));
   } else {
     MOE_TRY(run("gather_dy", s, fl, [&] {
-      return launch_gather_rows(dY, slot_pad, dyp, L.T, L.H, L.k, poff, counts, L.E, s);
+      return launch_gather_rows(dY, slot_pad, dyp, L.T, L.H, L.k, poff, counts, L.E, L.Pa, st, s);
     }));
   }
 
   if (cfg->precision != MOE_BF16) {
-    const BwdBufs bb{W_gate, W_up, W_down, dyp, xperm, h, poff, counts, mtile, order, slot_pad,
+    const BwdBufs bb{W_gate, W_up, W_down, dyp, xperm, h, poff, counts, mtile, mtile2, order, slot_pad,
                      row_slot, w_row, w, idx, wrt, dh, aw, dwp, dl, dlt, scratch, dx,
                      dW_gate, dW_up, dW_down, ws, wflags,
                      L.prepared ? const_cast<void*>(cfg->prepared_weights) : nullptr,
@@ -1232,7 +1325,8 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
     // B9: router softmax / top-k backward
     if (cudaMemsetAsync(dlt, 0, 2ull * L.E * L.T_pad, s) != cudaSuccess) return MOE_ERR_CUDA;
     MOE_TRY(run("router_bwd", s, fl, [&] {
-      return launch_router_bwd(dwp, L.nparts, slot_pad, w, idx, L.T, L.k, dl, dlt, L.T_pad, s);
+      return launch_router_bwd(dwp, L.nparts, slot_pad, w, idx, L.T, L.k, L.E, L.Pa, dl, dlt,
+                               L.T_pad, st, s);
     }));
     // B5: down wgrad over the padded token segments
     {
@@ -1282,6 +1376,8 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
       a.in1 = row_slot;
       a.out0 = scratch;
       a.ld0 = L.H;
+      a.T = L.T;           // the scatter's rows are (token, slot) pairs: T * top_k of them
+      a.top_k = L.k;
       if (L.pair_gu_dgrad) {
         const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, sms);
         MOE_TRY(run("gate_up_dgrad_scatter", s, fl, [&] { return launch_gate_up_dgrad_pair(a, grid, s); }));
@@ -1291,7 +1387,7 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
       }
     }
     MOE_TRY(run("unpermute_dx", s, fl, [&] {
-      return launch_unpermute(scratch, dl, idx, wrt, dx, L.T, L.H, L.k, L.E, sms, s);
+      return launch_unpermute(scratch, dl, idx, wrt, dx, L.T, L.H, L.k, L.E, sms, st, s);
     }));
     // B8: gate/up wgrad over the padded token segments
     {
@@ -1447,11 +1543,13 @@ moe_status_t moe_gemm_mxfp8(int64_t M, int64_t N, int64_t K, const moe_bf16_t* A
   a.kt_a = static_cast<int>(kt);
   a.sfB0 = sb;
   a.kt_b = static_cast<int>(kt);
-  if (N % 256 == 0) {   // 128 x 256 tiles
+  if (N % 256 == 0 && d.sms >= 2) {   // 256 x 256 CTA-pair tiles
+    if (!make_map_atoms(&a.mapSFA, sa, mt * kt) || !make_map_atoms(&a.mapSFB, sb, nt * kt))
+      return MOE_ERR_CUDA;
     a.n_tiles = static_cast<int>(N / 256);
-    const int64_t tiles = static_cast<int64_t>(mt) * a.n_tiles;
+    const int64_t tiles = static_cast<int64_t>((M + 255) / 256) * a.n_tiles;
     return run("dense_gemm_mx", s, 0,
-               [&] { return launch_dense_mx256(a, grid_for(tiles, d.sms), s); });
+               [&] { return launch_dense_mx_pair(a, grid_for_pairs(tiles, d.sms), s); });
   }
   a.n_tiles = static_cast<int>(nt);
   const int64_t tiles = static_cast<int64_t>(mt * nt);

@@ -37,9 +37,9 @@ enum : int {
   kCheckRouterExpert = 16,   // router epilogue: selected expert id
   kCheckPermuteExpert = 17,  // permutation: expert id of a (token, slot)
   kCheckGatherRow = 18,      // dispatch: destination row of a token copy
+  kCheckRouterRow = 21,      // router backward: permuted row of a (token, slot)
   kCheckScatterRow = 19,     // scatter epilogues: (token, slot) row of a permuted row
-  kCheckUnpermuteExpert = 20,// un-permute: expert id of a (token, slot)
-  kCheckGatherToken = 21,    // gathered operand loads: token of a permuted row
+  kCheckUnpermuteExpert = 20,// un-permute / router backward: expert id of a (token, slot)
 };
 
 constexpr int kStatusInvalidArg = 1;  // == MOE_ERR_INVALID_ARG
@@ -65,6 +65,24 @@ MOE_DEV void record_bad_index(DeviceStatus* st, int where, long long value) {
 MOE_DEV bool in_range(long long v, long long n) {
   return static_cast<unsigned long long>(v) < static_cast<unsigned long long>(n);
 }
+
+// Index checks of the debug build (compiled with -DMOE_DEVICE_CHECKS): a
+// value outside [0, n) is recorded in the status word and `on_fail` runs
+// (skipping the access) instead of the value being used.  Without the flag
+// the check compiles to nothing: the library writes every index it reads.
+#ifdef MOE_DEVICE_CHECKS
+#define MOE_CHECK_INDEX(st, where, v, n, on_fail)                  \
+  do {                                                             \
+    if (!::moe::in_range((v), (n))) {                              \
+      ::moe::record_bad_index((st), (where), (v));                 \
+      on_fail;                                                     \
+    }                                                              \
+  } while (0)
+#else
+#define MOE_CHECK_INDEX(st, where, v, n, on_fail) \
+  do {                                            \
+  } while (0)
+#endif
 
 // ---------------------------------------------------------------- misc
 
@@ -300,7 +318,11 @@ MOE_DEV void load_bf16x16(const void* p, float (&v)[16]) {
   unpack_bf16x2(b.w, v[14], v[15]);
 }
 
-MOE_DEV float sigmoidf_fast(float z) { return 1.0f / (1.0f + __expf(-z)); }
+// Logistic function for the SwiGLU epilogues: CUDA's fast exponential and
+// fast division (a reciprocal approximation, a few ulp; 1 / inf gives 0 and
+// the limits at +-inf are exact), ample for bf16 and E4M3 outputs and far
+// cheaper than an IEEE division in epilogues that are instruction-bound.
+MOE_DEV float sigmoidf_fast(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 // p[i] += v[i] for 16 fp32 values at p (16-byte aligned); loads issued first
 MOE_DEV void accum_f32x16(void* p, const float (&v)[16]) {
@@ -468,6 +490,29 @@ MOE_DEV void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, ui
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// sf_copy_to_tmem for a CTA pair, issued by the leader: the atom at this
+// shared-memory offset goes to the same TMEM columns of the pair.
+MOE_DEV void sf_copy_to_tmem_pair(uint32_t tmem_col_addr, const void* smem_atom) {
+  const uint64_t desc = static_cast<uint64_t>((smem_u32(smem_atom) & 0x3FFFFu) >> 4) |
+                        (static_cast<uint64_t>(128u >> 4) << 16) |
+                        (static_cast<uint64_t>(128u >> 4) << 32) | (1ull << 46);
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(tmem_col_addr), "l"(desc)
+               : "memory");
+}
+
+// M = 256 block-scaled MMA over a CTA pair (operand halves as in
+// mma_bf16_pair; scale factors in TMEM as the problem places them).
+MOE_DEV void mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
 

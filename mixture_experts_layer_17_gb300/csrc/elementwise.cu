@@ -158,7 +158,7 @@ __global__ void permute_kernel(const int* __restrict__ idx, const float* __restr
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ src, const int* __restrict__ slot_row,
                                    uint16_t* __restrict__ dst, int64_t T, int H, int k,
                                    const int* __restrict__ poff, const int* __restrict__ counts,
-                                   unsigned token_blocks) {
+                                   unsigned token_blocks, int64_t Pa, DeviceStatus* st) {
   if (blockIdx.x >= token_blocks) {
     const int e = static_cast<int>(blockIdx.x - token_blocks);
     const int64_t r0 = static_cast<int64_t>(__ldg(poff + e)) + __ldg(counts + e);
@@ -176,7 +176,14 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ src, const int* 
   const int lane = threadIdx.x & 31;
   int64_t rows[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) rows[j] = (j < k) ? static_cast<int64_t>(slot_row[t * k + j]) * H : 0;
+  for (int j = 0; j < 16; ++j) {
+    rows[j] = -1;   // no copy
+    if (j < k) {
+      const int r = slot_row[t * k + j];
+      rows[j] = static_cast<int64_t>(r) * H;
+      MOE_CHECK_INDEX(st, kCheckGatherRow, r, Pa, rows[j] = -1);
+    }
+  }
   const uint16_t* s = src + t * H;
   const int nchunks = H >> 3;
 #pragma unroll 4
@@ -184,7 +191,7 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ src, const int* 
     const uint4 v = ld_global_nc_v4(s + c * 8);
 #pragma unroll
     for (int j = 0; j < 16; ++j)
-      if (j < k) st_global_v4(dst + rows[j] + c * 8, v.x, v.y, v.z, v.w);
+      if (j < k && rows[j] >= 0) st_global_v4(dst + rows[j] + c * 8, v.x, v.y, v.z, v.w);
   }
 }
 
@@ -220,8 +227,9 @@ __global__ void combine_kernel(const uint16_t* __restrict__ scratch, uint16_t* _
 // at the selected logits); dlT[e, t] = dl for the dense router weight GEMM.
 __global__ void router_bwd_kernel(const float* __restrict__ dw_part, int nparts,
                                   const int* __restrict__ slot_row, const float* __restrict__ w,
-                                  const int* __restrict__ idx, int64_t T, int k,
-                                  float* __restrict__ dl, uint16_t* __restrict__ dlT, int64_t T_pad) {
+                                  const int* __restrict__ idx, int64_t T, int k, int E, int64_t Pa,
+                                  float* __restrict__ dl, uint16_t* __restrict__ dlT, int64_t T_pad,
+                                  DeviceStatus* st) {
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= T) return;
   float dwv[16], wv[16];
@@ -233,7 +241,10 @@ __global__ void router_bwd_kernel(const float* __restrict__ dw_part, int nparts,
     if (j < k) {
       const int64_t r = slot_row[t * k + j];
       float d = 0.f;
-      for (int n = 0; n < nparts; ++n) d += dw_part[r * nparts + n];
+      bool ok = true;
+      MOE_CHECK_INDEX(st, kCheckRouterRow, r, Pa, ok = false);
+      if (ok)
+        for (int n = 0; n < nparts; ++n) d += dw_part[r * nparts + n];
       dwv[j] = d;
       wv[j] = w[t * k + j];
       s = fmaf(wv[j], d, s);
@@ -245,7 +256,9 @@ __global__ void router_bwd_kernel(const float* __restrict__ dw_part, int nparts,
       const float g = wv[j] * (dwv[j] - s);
       dl[t * k + j] = g;
       __nv_bfloat16 b = __float2bfloat16_rn(g);
-      dlT[static_cast<int64_t>(idx[t * k + j]) * T_pad + t] = *reinterpret_cast<uint16_t*>(&b);
+      const int e = idx[t * k + j];
+      MOE_CHECK_INDEX(st, kCheckUnpermuteExpert, e, E, continue);
+      dlT[static_cast<int64_t>(e) * T_pad + t] = *reinterpret_cast<uint16_t*>(&b);
     }
   }
 }
@@ -266,7 +279,7 @@ template <int CW, int KMAX>
 __global__ void __launch_bounds__(256) unpermute_kernel(
     const uint16_t* __restrict__ scratch, const float* __restrict__ dl,
     const int* __restrict__ idx, const uint16_t* __restrict__ WrT, uint16_t* __restrict__ dx,
-    int64_t T, int H, int k, int E) {
+    int64_t T, int H, int k, int E, DeviceStatus* st) {
   extern __shared__ __align__(16) uint16_t wr_s[];   // [E][CW]
   constexpr int kChunks = CW / 8;                    // 16-byte chunks per row = lanes per token
   constexpr int kTokPerWarp = 32 / kChunks;
@@ -301,6 +314,7 @@ __global__ void __launch_bounds__(256) unpermute_kernel(
       if (j < k) {
         add_bf16x8(v[j], acc);
         const int e = __ldg(idx + t * k + j);
+        MOE_CHECK_INDEX(st, kCheckUnpermuteExpert, e, E, continue);
         add_bf16x8(*reinterpret_cast<const uint4*>(wr_s + e * CW + cl), acc, __ldg(dl + t * k + j));
       }
     }
@@ -372,11 +386,11 @@ cudaError_t launch_permute(const int* idx, const float* w, const int* block_base
 
 cudaError_t launch_gather_rows(const uint16_t* src, const int* slot_row, uint16_t* dst,
                                int64_t T, int H, int k, const int* poff, const int* counts, int E,
-                               cudaStream_t s) {
+                               int64_t Pa, DeviceStatus* st, cudaStream_t s) {
   const unsigned token_blocks = blocks_for(T, 8);
   if (token_blocks + E == 0) return cudaSuccess;
   gather_rows_kernel<<<token_blocks + static_cast<unsigned>(E), 256, 0, s>>>(
-      src, slot_row, dst, T, H, k, poff, counts, token_blocks);
+      src, slot_row, dst, T, H, k, poff, counts, token_blocks, Pa, st);
   return cudaGetLastError();
 }
 
@@ -387,10 +401,11 @@ cudaError_t launch_combine(const uint16_t* scratch, uint16_t* y, int64_t T, int 
 }
 
 cudaError_t launch_router_bwd(const float* dw_part, int nparts, const int* slot_row,
-                              const float* w, const int* idx, int64_t T, int k, float* dl,
-                              uint16_t* dlT, int64_t T_pad, cudaStream_t s) {
+                              const float* w, const int* idx, int64_t T, int k, int E, int64_t Pa,
+                              float* dl, uint16_t* dlT, int64_t T_pad, DeviceStatus* st,
+                              cudaStream_t s) {
   router_bwd_kernel<<<blocks_for(T, 128), 128, 0, s>>>(dw_part, nparts, slot_row, w, idx, T, k,
-                                                       dl, dlT, T_pad);
+                                                       E, Pa, dl, dlT, T_pad, st);
   return cudaGetLastError();
 }
 
@@ -400,7 +415,7 @@ namespace {
 template <int CW, int KMAX>
 cudaError_t launch_unpermute_cw(const uint16_t* scratch, const float* dl, const int* idx,
                                 const uint16_t* WrT, uint16_t* dx, int64_t T, int H, int k, int E,
-                                int sms, cudaStream_t s) {
+                                int sms, DeviceStatus* st, cudaStream_t s) {
   constexpr int kSmem = 65536;
   static unsigned long long configured = 0ull;
   static int per_sm[64] = {};
@@ -423,7 +438,7 @@ cudaError_t launch_unpermute_cw(const uint16_t* scratch, const float* dl, const 
   const int64_t groups = std::max<int64_t>(1, std::min<int64_t>(want, (T + tok_per_cta - 1) / tok_per_cta));
   dim3 grid(static_cast<unsigned>(slices), static_cast<unsigned>(groups));
   unpermute_kernel<CW, KMAX><<<grid, 256, static_cast<size_t>(E) * CW * 2, s>>>(
-      scratch, dl, idx, WrT, dx, T, H, k, E);
+      scratch, dl, idx, WrT, dx, T, H, k, E, st);
   return cudaGetLastError();
 }
 
@@ -431,15 +446,15 @@ cudaError_t launch_unpermute_cw(const uint16_t* scratch, const float* dl, const 
 
 cudaError_t launch_unpermute(const uint16_t* scratch, const float* dl, const int* idx,
                              const uint16_t* WrT, uint16_t* dx, int64_t T, int H, int k, int E,
-                             int sms, cudaStream_t s) {
+                             int sms, DeviceStatus* st, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   // E <= 256 and H % 256 == 0: E x CW x 2 bytes <= 64 KB and CW divides H
   if (E <= 128) {
-    return k <= 8 ? launch_unpermute_cw<256, 8>(scratch, dl, idx, WrT, dx, T, H, k, E, sms, s)
-                  : launch_unpermute_cw<256, 16>(scratch, dl, idx, WrT, dx, T, H, k, E, sms, s);
+    return k <= 8 ? launch_unpermute_cw<256, 8>(scratch, dl, idx, WrT, dx, T, H, k, E, sms, st, s)
+                  : launch_unpermute_cw<256, 16>(scratch, dl, idx, WrT, dx, T, H, k, E, sms, st, s);
   }
-  return k <= 8 ? launch_unpermute_cw<128, 8>(scratch, dl, idx, WrT, dx, T, H, k, E, sms, s)
-                : launch_unpermute_cw<128, 16>(scratch, dl, idx, WrT, dx, T, H, k, E, sms, s);
+  return k <= 8 ? launch_unpermute_cw<128, 8>(scratch, dl, idx, WrT, dx, T, H, k, E, sms, st, s)
+                : launch_unpermute_cw<128, 16>(scratch, dl, idx, WrT, dx, T, H, k, E, sms, st, s);
 }
 
 cudaError_t launch_wr_reduce(const float* part, int S, int E, int H, void* dWr, bool accum_f32,

@@ -34,6 +34,12 @@ struct GemmArgs {
   CUtensorMap mapA;
   CUtensorMap mapB0;
   CUtensorMap mapB1;
+  // MXFP8 CTA pairs: the scale atoms of A and B as [atoms, 128] u32 tensors
+  // (one-atom boxes), loaded by TMA so that the peer's copies complete on the
+  // leader's barrier
+  CUtensorMap mapSFA;
+  CUtensorMap mapSFB;
+  CUtensorMap mapSFB1;   // the second B operand's atoms (gate/up dgrad: W_up)
   int M;               // dense: output rows; grouped-K / split-K: output rows per group
   int N;               // output columns
   int K;               // reduction length (dense, grouped-M, split-K)
@@ -324,6 +330,27 @@ struct StageCfg<P, true, false> {
   static constexpr int kAccBufs = BN == 256 ? 1 : 2;
 };
 
+// CTA pair, MXFP8: per CTA a stage holds its 128 rows of A and BN/2 rows of
+// B (K = 128 E4M3 each) and the scale atoms the problem loads (P::kSFAtoms
+// of 512 bytes: A's first, then B's); one 256-column accumulator per CTA,
+// scales at TMEM column 256 + 4 * kSFAtoms * stage.
+template <class P>
+struct StageCfg<P, true, true> {
+  static constexpr int BN = P::BN;
+  static_assert(BN == 256, "MXFP8 CTA-pair tiles are 256 x 256");
+  static constexpr uint32_t kABytes = kBM * 128;
+  static constexpr uint32_t kBBytes = (BN / 2) * 128;
+  static constexpr uint32_t kSFBytes = 512 * P::kSFAtoms;
+  static constexpr int kFit =
+      static_cast<int>((232448 - 1024 - 256 - P::kExtraSmem) / (kABytes + kBBytes + kSFBytes));
+  static constexpr int kStages = 6 < kFit ? 6 : kFit;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kSFCol0 = 256;
+  static constexpr uint32_t kSFStride = 4 * P::kSFAtoms;
+  static_assert(kSFCol0 + kSFStride * kStages <= kTmemCols, "scale slots exceed TMEM");
+  static constexpr int kAccBufs = 1;
+};
+
 template <class P>
 constexpr size_t gemm_smem_bytes() {
   using C = StageCfg<P>;
@@ -341,7 +368,7 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
   constexpr uint32_t kB = C::kBBytes;
   constexpr uint32_t kSF = C::kSFBytes;
   constexpr bool kPair = IsPair<P>::value;
-  constexpr uint32_t kIdesc = kMX ? make_idesc_mxf8(kBM, BN, P::kAMN, P::kBMN)
+  constexpr uint32_t kIdesc = kMX ? make_idesc_mxf8(kPair ? 2 * kBM : kBM, BN, P::kAMN, P::kBMN)
                                   : make_idesc_bf16(kPair ? 2 * kBM : kBM, BN, P::kAMN, P::kBMN);
 
   extern __shared__ uint8_t smem_raw[];
@@ -417,7 +444,12 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
             ok = false;
             break;
           }
-          if constexpr (kPair) {
+          if constexpr (kPair && kMX) {
+            // both halves and their scale atoms complete on the leader's full barrier
+            if (rank == 0) mbar_arrive_expect_tx(full_bar + stage, 2 * (kA + kB + kSF));
+            P::load_mx_pair(args, ti, kb, static_cast<int>(rank), sA + stage * kA,
+                            sB + stage * kB, sSF + stage * kSF, map_to_rank(full_bar + stage, 0));
+          } else if constexpr (kPair) {
             // both halves complete on the leader's full barrier
             if (rank == 0) mbar_arrive_expect_tx(full_bar + stage, 2 * (kA + kB));
             P::load_pair(args, ti, kb, static_cast<int>(rank), sA + stage * kA, sB + stage * kB,
@@ -480,7 +512,33 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
           ok = false;
           break;
         }
-        if constexpr (kMX) {
+        if constexpr (kMX && kPair) {
+          if (lane == 0) {
+            tc_fence_after();
+            // the stage's scale atoms -> the pair's TMEM (the problem's slot
+            // layout: A's atom at sf_t, B's from sf_t + 4), then four K = 32
+            // block-scaled M = 256 MMAs
+            const uint32_t sf_t = tmem_base + C::kSFCol0 + C::kSFStride * stage;
+#pragma unroll
+            for (int i = 0; i < P::kSFAtoms; ++i)
+              sf_copy_to_tmem_pair(sf_t + 4 * i, sSF + stage * kSF + 512 * i);
+            const uint32_t a_base = smem_u32(sA + stage * kA);
+            const uint32_t b_base = smem_u32(sB + stage * kB);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t adesc =
+                  P::kAMN ? make_smem_desc(a_base + k * 4096, 16384, 1024)
+                          : make_smem_desc(a_base + k * 32, 16, 1024);
+              const uint64_t bdesc =
+                  P::kBMN ? make_smem_desc(b_base + k * 4096, 16384, 1024)
+                          : make_smem_desc(b_base + k * 32, 16, 1024);
+              mma_mxf8_pair(d_tmem, adesc, bdesc, idesc_with_sf_id(kIdesc, k), sf_t, sf_t + 4,
+                            (kb > 0 || k > 0) ? 1u : 0u);
+            }
+            mma_commit_pair(empty_bar + stage, 0x3);   // frees the stage in both CTAs
+            committed_any = true;
+          }
+        } else if constexpr (kMX) {
           if (lane == 0) {
             tc_fence_after();
             // scales of this stage -> TMEM (4-column aligned slots), then four
@@ -573,8 +631,10 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
     for (int t = t_first; t < num_tiles; t += t_step) {
       TileInfo ti = P::tile(args, t);
       if constexpr (kPair) {
-        // this CTA owns rows [128 * rank, 128 * rank + 128) of the pair's tile
+        // this CTA owns rows [128 * rank, 128 * rank + 128) of the pair's tile,
+        // its 128-row m-tile within the group being 2 * (pair m-tile) + rank
         ti.m0 += 128 * static_cast<int>(rank);
+        ti.mt = 2 * ti.mt + static_cast<int>(rank);
         ti.rows = max(0, min(kBM, ti.rows - 128 * static_cast<int>(rank)));
         ti.rows_pad = max(0, min(kBM, ti.rows_pad - 128 * static_cast<int>(rank)));
       }
@@ -605,7 +665,12 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
         P::epilogue_load(args, ti, taddr, r, group, f);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar + acc);
+        if (lane == 0) {
+          if (kPair && rank != 0)
+            mbar_arrive_remote(map_to_rank(tempty_bar + acc, 0));
+          else
+            mbar_arrive(tempty_bar + acc);
+        }
         P::epilogue_store(args, ti, r, group, f, extra);
       } else {
         P::epilogue(args, ti, taddr, r, group, extra);

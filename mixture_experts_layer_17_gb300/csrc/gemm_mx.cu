@@ -25,8 +25,5 @@ cudaError_t launch_gate_up_wgrad_mx(const GemmArgs& a, int grid, cudaStream_t s)
 cudaError_t launch_dense_mx(const GemmArgs& a, int grid, cudaStream_t s) {
   return launch_gemm<DenseMXProblem>(a, grid, s);
 }
-cudaError_t launch_dense_mx256(const GemmArgs& a, int grid, cudaStream_t s) {
-  return launch_gemm<DenseMX256Problem>(a, grid, s);
-}
 
 }  // namespace moe

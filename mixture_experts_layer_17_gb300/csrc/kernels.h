@@ -35,7 +35,13 @@ cudaError_t launch_gate_up_dgrad_mx(const GemmArgs& a, int grid, cudaStream_t s)
 cudaError_t launch_down_wgrad_mx(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_gate_up_wgrad_mx(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_dense_mx(const GemmArgs& a, int grid, cudaStream_t s);
-cudaError_t launch_dense_mx256(const GemmArgs& a, int grid, cudaStream_t s);
+// MXFP8 CTA-pair GEMMs (grid must be even)
+cudaError_t launch_gate_up_fwd_mx_pair(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_down_fwd_mx_pair(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_gate_up_dgrad_mx_pair(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_down_wgrad_mx_pair(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_gate_up_wgrad_mx_pair(const GemmArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_dense_mx_pair(const GemmArgs& a, int grid, cudaStream_t s);
 
 // MXFP8 quantisers (mx_quant.cu): E4M3 data + 512-byte scale atoms
 cudaError_t launch_quant_rows_dense(const uint16_t* src, int64_t R, int C, uint8_t* dst,
@@ -69,15 +75,16 @@ cudaError_t launch_permute(const int* idx, const float* w, const int* block_base
 // expert's padded segment ([poff[e] + counts[e], poff[e+1])) zeroed
 cudaError_t launch_gather_rows(const uint16_t* src, const int* slot_row, uint16_t* dst,
                                int64_t T, int H, int k, const int* poff, const int* counts, int E,
-                               cudaStream_t s);
+                               int64_t Pa, DeviceStatus* st, cudaStream_t s);
 cudaError_t launch_combine(const uint16_t* scratch, uint16_t* y, int64_t T, int H, int k,
                            cudaStream_t s);
 cudaError_t launch_router_bwd(const float* dw_part, int nparts, const int* slot_row,
-                              const float* w, const int* idx, int64_t T, int k, float* dl,
-                              uint16_t* dlT, int64_t T_pad, cudaStream_t s);
+                              const float* w, const int* idx, int64_t T, int k, int E, int64_t Pa,
+                              float* dl, uint16_t* dlT, int64_t T_pad, DeviceStatus* st,
+                              cudaStream_t s);
 cudaError_t launch_unpermute(const uint16_t* scratch, const float* dl, const int* idx,
                              const uint16_t* WrT, uint16_t* dx, int64_t T, int H, int k, int E,
-                             int sms, cudaStream_t s);
+                             int sms, DeviceStatus* st, cudaStream_t s);
 cudaError_t launch_wr_reduce(const float* part, int S, int E, int H, void* dWr, bool accum_f32,
                              cudaStream_t s);
 

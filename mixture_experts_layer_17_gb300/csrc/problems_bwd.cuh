@@ -277,6 +277,7 @@ struct GateUpDgradProblem {
     if (valid) {
       const int slot = __ldg(static_cast<const int*>(a.in1) + row);
       dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 + ti.n0;
+      MOE_CHECK_INDEX(a.status, kCheckScatterRow, slot, a.T * a.top_k, dst = nullptr);
     }
 #pragma unroll 1
     for (int c0 = group * (BN / 2); c0 < (group + 1) * (BN / 2); c0 += 64) {

@@ -218,6 +218,7 @@ struct DownFwdMXProblem {
       const int slot = __ldg(static_cast<const int*>(a.in1) + row);
       dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 + ti.n0 +
             128 * group;
+      MOE_CHECK_INDEX(a.status, kCheckScatterRow, slot, a.T * a.top_k, dst = nullptr);
     }
 #pragma unroll
     for (int i = 0; i < 128; ++i) f.v[i] *= w;
@@ -464,6 +465,7 @@ struct GateUpDgradMXProblem {
       const int slot = __ldg(static_cast<const int*>(a.in1) + row);
       dst = static_cast<__nv_bfloat16*>(a.out0) + static_cast<int64_t>(slot) * a.ld0 + ti.n0 +
             128 * group;
+      MOE_CHECK_INDEX(a.status, kCheckScatterRow, slot, a.T * a.top_k, dst = nullptr);
     }
 #pragma unroll
     for (int c = 0; c < 128; c += 32) {
@@ -600,53 +602,6 @@ struct DenseMXProblem {
                        __float_as_uint(v[i + 2]), __float_as_uint(v[i + 3]));
       }
     }
-  }
-};
-
-// Dense MXFP8 GEMM with 128 x 256 tiles (N a multiple of 256): as
-// DenseMXProblem, B atoms (n-tile of 128 rows) * kt + k-tile, two per stage;
-// one accumulator, released as soon as the epilogue holds its fragment.
-struct DenseMX256Problem {
-  static constexpr int BN = 256;
-  static constexpr bool kAMN = false;
-  static constexpr bool kBMN = false;
-  static constexpr bool kMX = true;
-  static constexpr size_t kExtraSmem = 0;
-  static constexpr int kEpiGroups = 2;
-  struct Frag {
-    float v[128];
-  };
-
-  MOE_DEV static int num_tiles(const GemmArgs& a) { return dense_num_tiles(a); }
-  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) {
-    TileInfo ti = dense_tile(a, t, BN);
-    ti.num_kb = (a.K + 127) / 128;
-    return ti;
-  }
-  MOE_DEV static void init_extra(const GemmArgs&, uint8_t*) {}
-  MOE_DEV static void load_mx(const GemmArgs& a, const TileInfo& ti, int kb, uint8_t* sA,
-                              uint8_t* sB, uint8_t* sSF, uint64_t* bar) {
-    tma_load_2d(sA, &a.mapA, kb * 128, ti.m0, bar);
-    load_b256_kmajor(&a.mapB0, kb * 128, ti.n0, sB, bar);
-    const int64_t nt = ti.n0 / 128;
-    bulk_load(sSF, sf_atom(a.sfA, static_cast<int64_t>(ti.mt) * a.kt_a + kb), 512, bar);
-    bulk_load(sSF + 512, sf_atom(a.sfB0, nt * a.kt_b + kb), 512, bar);
-    bulk_load(sSF + 1024, sf_atom(a.sfB0, (nt + 1) * a.kt_b + kb), 512, bar);
-  }
-  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
-  MOE_DEV static void epilogue_load(const GemmArgs&, const TileInfo&, uint32_t taddr, int,
-                                    int group, Frag& f) {
-    tmem_ld128(taddr + 128 * group, f.v);
-  }
-  MOE_DEV static void epilogue_store(const GemmArgs& a, const TileInfo& ti, int r, int group,
-                                     const Frag& f, uint8_t*) {
-    if (r >= ti.rows) return;
-    float* p = static_cast<float*>(a.out0) + (static_cast<int64_t>(ti.m0) + r) * a.ld0 + ti.n0 +
-               128 * group;
-#pragma unroll
-    for (int i = 0; i < 128; i += 4)
-      st_global_v4(p + i, __float_as_uint(f.v[i]), __float_as_uint(f.v[i + 1]),
-                   __float_as_uint(f.v[i + 2]), __float_as_uint(f.v[i + 3]));
   }
 };
 

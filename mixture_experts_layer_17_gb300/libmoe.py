@@ -52,11 +52,14 @@ _lib: Optional[ctypes.CDLL] = None
 _vp, _sz, _i64, _i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int64, ctypes.c_int
 
 
-def load(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Loads libmoe.so (built by __graft_entry__.build()); raises if absent."""
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Loads libmoe.so (built by __graft_entry__.build()), or the library that
+    LIBMOE_PATH names (such as the index-checking debug build); raises if absent."""
     global _lib
     if _lib is not None:
         return _lib
+    if path is None:
+        path = os.environ.get("LIBMOE_PATH") or LIB_PATH
     if not os.path.exists(path):
         raise RuntimeError(f"libmoe.so not found at {path}; build it with "
                            "`python -c 'import __graft_entry__ as g; g.build()'`")

@@ -45,12 +45,17 @@ def test_dense_mxfp8_gemm_matches_oracle_quantisation(M, N, K):
     assert err < 1e-5, err
 
 
-def _layer_case(sh, precision, bias=None):
+# expert GEMMs on single-CTA tiles, or on CTA-pair 256-row tiles (block-scaled
+# cta_group::2 MMAs) wherever the shape allows
+PAIR_MODES = {"single": 0x4, "pairs": 0x8}
+
+
+def _layer_case(sh, precision, bias=None, flags=0):
     sh = si.custom_shape(sh[0], sh[1], sh[2], sh[3], sh[4], seed=sh[5], precision=precision)
     inp = si.make_inputs(sh, "cuda")
     if bias is not None:
         inp["logit_bias"] = bias.cuda()
-    out = run_layer(sh, inp)
+    out = run_layer(sh, inp, flags=flags)
     check_route_properties(out, sh.T, sh.E, sh.top_k)
     args = [f64(inp[k]) for k in ("x", "W_r", "W_gate", "W_up", "W_down")]
     ref = mo.backward(*args, sh.top_k, f64(inp["dY"]), logit_bias=f64(inp["logit_bias"]),
@@ -75,9 +80,10 @@ MX_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("shape", MX_SHAPES)
-def test_layer_mxfp8(shape):
-    out, ref, errs, errs_exact = _layer_case(shape, "mxfp8")
+@pytest.mark.parametrize("mode", sorted(PAIR_MODES))
+@pytest.mark.parametrize("shape", MX_SHAPES + [(1500, 512, 512, 6, 2, 56)])
+def test_layer_mxfp8(shape, mode):
+    out, ref, errs, errs_exact = _layer_case(shape, "mxfp8", flags=PAIR_MODES[mode])
     for name, e in errs.items():
         if name == "dW_r" and shape[4] == 1:
             continue
@@ -90,19 +96,22 @@ def test_layer_mxfp8(shape):
             assert np.all(out[name][e] == 0.0)
 
 
+@pytest.mark.parametrize("mode", sorted(PAIR_MODES))
 @pytest.mark.parametrize("shape", MX_SHAPES[:2])
-def test_layer_fp8_bwd(shape):
-    out, ref, errs, errs_exact = _layer_case(shape, "fp8_bwd")
+def test_layer_fp8_bwd(shape, mode):
+    out, ref, errs, errs_exact = _layer_case(shape, "fp8_bwd", flags=PAIR_MODES[mode])
     assert errs["y"] <= BF16_TOL                 # the forward is bf16
     for name, e in errs.items():
         assert e <= MX_TOL, (name, e)
     assert errs["dW_gate"] < 0.5 * errs_exact["dW_gate"]
 
 
-def test_layer_mxfp8_with_empty_experts():
+@pytest.mark.parametrize("mode", sorted(PAIR_MODES))
+def test_layer_mxfp8_with_empty_experts(mode):
     bias = torch.zeros(12)
     bias[[2, 9]] = -30.0
-    out, ref, errs, _ = _layer_case((256, 256, 256, 12, 2, 54), "mxfp8", bias=bias)
+    out, ref, errs, _ = _layer_case((256, 256, 256, 12, 2, 54), "mxfp8", bias=bias,
+                                    flags=PAIR_MODES[mode])
     assert ref["fwd"]["counts"][2] == 0 and ref["fwd"]["counts"][9] == 0
     for name, e in errs.items():
         assert e <= MX_TOL, (name, e)

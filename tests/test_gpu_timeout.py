@@ -4,7 +4,7 @@ limit.  The kernel must give up, record MOE_ERR_TIMEOUT in the workspace
 status word, free its tensor memory and return, leaving the context usable.
 Run on the single-CTA bf16 kernels, on CTA pairs (where each CTA of a pair
 gives up on its own and both still meet at the closing cluster barrier) and on
-the MXFP8 kernels."""
+the MXFP8 kernels, single-CTA and paired."""
 
 import numpy as np
 import pytest
@@ -17,7 +17,8 @@ from oracle import moe_oracle as mo
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("precision,extra", [("bf16", 0), ("bf16", "pairs"), ("mxfp8", 0)])
+@pytest.mark.parametrize("precision,extra", [("bf16", 0), ("bf16", "pairs"), ("mxfp8", 0),
+                                             ("mxfp8", "pairs")])
 def test_bounded_wait_times_out_and_context_survives(precision, extra):
     from mixture_experts_layer_17_gb300 import MoeLayer, libmoe
     sh = si.custom_shape(384, 256, 256, 8, 2, seed=31)
