@@ -154,11 +154,15 @@ _BYTE_UNITS = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "KB": 1e3, "
                "GB": 1e9}
 
 
-def record_traffic(csv_path: str, workload: str, command: str, path: str = None) -> dict:
+def record_traffic(csv_path: str, workload: str, command: str, path: str = None,
+                   scale: float = 1.0, captured_on: str = None) -> dict:
     """Fold an ncu CSV (metrics dram__bytes_read.sum and dram__bytes_write.sum,
     one row per launch and metric) into profiles/dram_traffic.json: bytes per
     launch for each library kernel of ``workload``, stamped with the hash of
-    the kernel sources they were taken on."""
+    the kernel sources they were taken on.  A capture taken on a smaller case
+    of the same per-expert shape (``captured_on``) is scaled to ``workload``
+    by ``scale``, the ratio of the units the two process (every term of the
+    traffic grows with them)."""
     import csv
     rows = []
     with open(csv_path) as fh:
@@ -185,9 +189,12 @@ def record_traffic(csv_path: str, workload: str, command: str, path: str = None)
     h = csrc_hash()
     for lab in labels:
         vals = [v for (l2, _), v in per_launch.items() if l2 == lab]
-        table[f"{lab}@{workload}"] = {"bytes_per_launch": sum(vals) / len(vals),
-                                      "launches": len(vals), "csrc_hash": h,
-                                      "command": command}
+        rec = {"bytes_per_launch": scale * sum(vals) / len(vals), "launches": len(vals),
+               "csrc_hash": h, "command": command}
+        if captured_on:
+            rec["captured_on"] = captured_on
+            rec["scale"] = scale
+        table[f"{lab}@{workload}"] = rec
     with open(path, "w") as fh:
         json.dump(table, fh, indent=1, sort_keys=True)
         fh.write("\n")
@@ -833,9 +840,15 @@ def main():
                     help="store per-launch DRAM bytes from an ncu CSV for --workload and exit")
     ap.add_argument("--traffic-command", default="",
                     help="the ncu command line the CSV came from (stored beside the figures)")
+    ap.add_argument("--traffic-scale", type=float, default=1.0,
+                    help="scale a smaller capture's bytes to --workload (ratio of the units)")
+    ap.add_argument("--traffic-captured-on", default=None,
+                    help="the shape the capture was taken on, when it is not --workload")
     args = ap.parse_args()
     if args.record_traffic:
-        print(json.dumps(record_traffic(args.record_traffic, args.workload, args.traffic_command)))
+        print(json.dumps(record_traffic(args.record_traffic, args.workload, args.traffic_command,
+                                        scale=args.traffic_scale,
+                                        captured_on=args.traffic_captured_on)))
         return
     args.warmup = max(args.warmup, 3)
     if args.shape:
