@@ -244,9 +244,9 @@ Layout make_layout(const moe_config_t& c, int sms) {
   // stages fit and the operand-latency lookahead grows by half; a pair tile
   // of a grouped-M GEMM wastes more rows at the end of each expert.  Measured
   // on the 235B shape (1024 rows per expert), pairs win for every expert GEMM
-  // once the epilogue stores go through shared memory (the down dgrad's, at
-  // five stages, by 12%; the gate/up forward's by 4.5%).  With 256 rows per
-  // expert (the 30B shape) only the two dgrads still gain (2-4%); the wgrads,
+  // once the epilogue stores go through shared memory (the down dgrad's by
+  // 12%; the gate/up forward's by 4.5%).  With 256 rows per expert (the 30B
+  // shape) only the two dgrads still gain (2-4%); the wgrads,
   // whose K is then 4 k-blocks per expert, lose 36%, and the forward GEMMs
   // break even.  MOE_FLAG_CTA_PAIRS_ON / _OFF override.
   const bool pairs_on = (c.flags & MOE_FLAG_CTA_PAIRS_ON) != 0;

@@ -26,20 +26,22 @@ struct DownDgradProblem {
   static constexpr int BN = BN_;
   static constexpr bool kAMN = false;
   static constexpr bool kBMN = false;
-  // kStaged (the CTA-pair version, which has the shared memory for it at five
-  // stages): each epilogue warp owns two pairs of 2 KB buffers (1024-byte
-  // aligned, hence up to 1 KB of lead-in) and an mbarrier per pair.  Per
-  // 32-column step, TMA brings the warp's 32 rows of h_gate and h_up into one
-  // pair (64-byte swizzle, the stage64 layout) while the step before works
-  // out of the other; every thread keeps its row of both as packed words,
-  // then dh_gate and dh_up, and after them w*a, are staged in the step's pair
-  // and leave as whole 64-byte row pieces.
-  static constexpr size_t kStageBytes = 8 * 4 * kStage64WarpBytes;
-  static constexpr size_t kExtraSmem = kStaged ? 1024 + kStageBytes + 16 * sizeof(uint64_t) : 0;
+  // kStaged (the CTA-pair version): each epilogue warp owns one pair of 2 KB
+  // buffers (1024-byte aligned, hence up to 1 KB of lead-in) and an mbarrier.
+  // Per 32-column step, TMA brings the warp's 32 rows of h_gate and h_up into
+  // the pair (64-byte swizzle, the stage64 layout); every thread keeps its row
+  // of both as packed words, then dh_gate and dh_up, and after them w*a, are
+  // staged in the same pair and leave as whole 64-byte row pieces, after
+  // which the next step's h is loaded.  One pair per warp (32 KB in all)
+  // leaves room for six operand stages; a second pair, to load the next h
+  // during the step, would cost a stage, and measured 2% slower at the 235B
+  // shape (the h wait is under a sixth of the epilogue's time per tile).
+  static constexpr size_t kStageBytes = 8 * 2 * kStage64WarpBytes;
+  static constexpr size_t kExtraSmem = kStaged ? 1024 + kStageBytes + 8 * sizeof(uint64_t) : 0;
   static constexpr int kEpiGroups = 2;
-  // four steps per warp and tile use each pair twice, so the parity of its
+  // an even number of steps per warp and tile, so the parity of the warp's
   // barrier follows the step index in every tile
-  static_assert(!kStaged || (BN / 2 / 32) % 4 == 0, "a multiple of four h steps per tile");
+  static_assert(!kStaged || (BN / 2 / 32) % 2 == 0, "an even number of h steps per tile");
 
   MOE_DEV static uint8_t* stage_base(uint8_t* extra) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(extra) + 1023) &
@@ -52,7 +54,7 @@ struct DownDgradProblem {
     if constexpr (kStaged) {
       if (threadIdx.x == 0) {
         uint64_t* bars = reinterpret_cast<uint64_t*>(stage_base(extra) + kStageBytes);
-        for (int w = 0; w < 16; ++w) mbar_init(bars + w, 1);
+        for (int w = 0; w < 8; ++w) mbar_init(bars + w, 1);
         fence_mbar_init();
       }
     }
@@ -96,8 +98,8 @@ struct DownDgradProblem {
     const bool pad = !valid && r < ti.rows_pad;
     const int lane = r & 31;
     const int wslot = group * 4 + (r >> 5);
-    uint8_t* buf = stage_base(extra) + wslot * 4 * kStage64WarpBytes;
-    uint64_t* hbar = reinterpret_cast<uint64_t*>(stage_base(extra) + kStageBytes) + 2 * wslot;
+    uint8_t* buf = stage_base(extra) + wslot * 2 * kStage64WarpBytes;
+    uint64_t* hbar = reinterpret_cast<uint64_t*>(stage_base(extra) + kStageBytes) + wslot;
     const int64_t row = static_cast<int64_t>(ti.m0) + ((valid || pad) ? r : 0);
     const int F = a.ld0;
     const int c0 = group * kHalf;
@@ -106,17 +108,15 @@ struct DownDgradProblem {
     __nv_bfloat16* aw = static_cast<__nv_bfloat16*>(a.out1) + row * F + ti.n0;
     const float w = valid ? __ldg(static_cast<const float*>(a.in1) + row) : 0.f;
     const int never = 0;   // the h waits are cut short only by their time limit
-    // h_gate and h_up of step s (columns c0 + 32 s ..) into pair s & 1; every
-    // lane's earlier accesses to that pair are ordered before the writes
+    // h_gate and h_up of step s (columns c0 + 32 s ..) into the warp's pair;
+    // every lane's earlier accesses to the pair are ordered before the writes
     auto load_h = [&](int step) {
-      uint8_t* pp = buf + (step & 1) * 2 * kStage64WarpBytes;
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(hbar + (step & 1), 2 * kStage64WarpBytes);
-        tma_load_2d(pp, &a.mapB1, ti.n0 + c0 + 32 * step, y, hbar + (step & 1));
-        tma_load_2d(pp + kStage64WarpBytes, &a.mapB1, F + ti.n0 + c0 + 32 * step, y,
-                    hbar + (step & 1));
+        mbar_arrive_expect_tx(hbar, 2 * kStage64WarpBytes);
+        tma_load_2d(buf, &a.mapB1, ti.n0 + c0 + 32 * step, y, hbar);
+        tma_load_2d(buf + kStage64WarpBytes, &a.mapB1, F + ti.n0 + c0 + 32 * step, y, hbar);
       }
     };
     float dw = 0.f;
@@ -124,8 +124,8 @@ struct DownDgradProblem {
 #pragma unroll 1
     for (int step = 0; step < kSteps; ++step) {
       const int c = c0 + 32 * step;
-      uint8_t* st = buf + (step & 1) * 2 * kStage64WarpBytes;
-      if (!mbar_wait_bounded(hbar + (step & 1), static_cast<uint32_t>(step >> 1) & 1u, &never,
+      uint8_t* st = buf;
+      if (!mbar_wait_bounded(hbar, static_cast<uint32_t>(step) & 1u, &never,
                              a.wait_limit_ns))
         record_timeout(a.status, kWaitEpiLoad);
       uint32_t gw[16], uw[16];
@@ -137,8 +137,6 @@ struct DownDgradProblem {
         gw[4 * q] = ug.x; gw[4 * q + 1] = ug.y; gw[4 * q + 2] = ug.z; gw[4 * q + 3] = ug.w;
         uw[4 * q] = uu.x; uw[4 * q + 1] = uu.y; uw[4 * q + 2] = uu.z; uw[4 * q + 3] = uu.w;
       }
-      // the next step's h is on its way while this one computes and stores
-      if (step + 1 < kSteps) load_h(step + 1);
       uint32_t awp[16];   // w*a of the step's 32 columns, packed bf16
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -166,6 +164,7 @@ struct DownDgradProblem {
         *reinterpret_cast<uint4*>(st + stage64_off(lane, q)) =
             make_uint4(awp[4 * q], awp[4 * q + 1], awp[4 * q + 2], awp[4 * q + 3]);
       stage64_flush(st, lane, w_row ? aw + c : nullptr, false);
+      if (step + 1 < kSteps) load_h(step + 1);
     }
     // one router-weight partial per (row, n-tile, column half)
     if (valid)
