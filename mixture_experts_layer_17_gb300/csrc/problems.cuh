@@ -184,20 +184,23 @@ struct RouterProblem {
   }
   MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
 
-  // (cv, ci) into the list ordered by (-logit, expert id)
+  // (cv, ci) into the list ordered by (-logit, expert id), the last entry
+  // falling off.  Its position p (the number of entries that stay ahead of it)
+  // comes from k independent comparisons, and every slot then takes its new
+  // entry by a select: no chain of compare-and-swap steps through the list.
   MOE_DEV static void insert(float (&topv)[kMaxK], int (&topi)[kMaxK], int k, float cv, int ci) {
+    unsigned ahead = 0u;
 #pragma unroll
-    for (int s = 0; s < kMaxK; ++s) {
+    for (int s = 0; s < kMaxK; ++s)
+      if (s < k && ((topv[s] > cv) || (topv[s] == cv && topi[s] < ci))) ahead |= 1u << s;
+    const int p = __popc(ahead);   // the list is sorted: the entries ahead are a prefix
+#pragma unroll
+    for (int s = kMaxK - 1; s >= 0; --s) {
       if (s < k) {
-        const bool better = (cv > topv[s]) || (cv == topv[s] && ci < topi[s]);
-        if (better) {
-          const float tv = topv[s];
-          const int tt = topi[s];
-          topv[s] = cv;
-          topi[s] = ci;
-          cv = tv;
-          ci = tt;
-        }
+        const float pv = s > 0 ? topv[s > 0 ? s - 1 : 0] : cv;
+        const int pi = s > 0 ? topi[s > 0 ? s - 1 : 0] : ci;
+        topv[s] = s > p ? pv : (s == p ? cv : topv[s]);
+        topi[s] = s > p ? pi : (s == p ? ci : topi[s]);
       }
     }
   }
