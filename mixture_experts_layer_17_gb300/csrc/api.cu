@@ -199,6 +199,8 @@ struct Layout {
   // MXFP8 GEMMs on CTA pairs (block-scaled cta_group::2); the down dgrad,
   // bound by its epilogue, stays on single-CTA tiles
   bool mx_pair_gu_fwd, mx_pair_down_fwd, mx_pair_gu_dgrad, mx_pair_down_wgrad, mx_pair_gu_wgrad;
+  // MXFP8 down dgrad on 256 x 192 CTA-pair tiles (two accumulators per CTA)
+  bool mx_pair_down_dgrad;
   int H, F, E, k;
   int ntiles;        // router tiles of 128 tokens
   int router_bn;     // N of the router GEMM (power of two >= E, >= 16)
@@ -228,6 +230,7 @@ struct Layout {
   // prepared MXFP8 weights (moe_prepare_weights): every orientation the GEMMs read
   bool prepared;
   size_t q_gu_h, qs_gu_h, q_d_f, qs_d_f, q_g_f, qs_g_f, q_u_f, qs_u_f, q_d_h, qs_d_h, q_total;
+  size_t qs_d_h192;   // W_down's scales along H in 192-row blocks (F a multiple of 192)
 };
 
 Layout make_layout(const moe_config_t& c, int sms) {
@@ -277,6 +280,8 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.mx_pair_gu_dgrad = mb && mxp;
   L.mx_pair_down_wgrad = mb && mxp && (L.F % 256 == 0);
   L.mx_pair_gu_wgrad = mb && mxp;
+  // the down dgrad's 256 x 192 pair tiles keep two accumulators
+  L.mx_pair_down_dgrad = mb && can_pair && !pairs_off && (L.F % 192 == 0);
   L.recompute = (c.flags & MOE_FLAG_RECOMPUTE) != 0;
   L.prepared = c.precision != MOE_BF16 && c.prepared_weights != nullptr;
   L.ntiles = static_cast<int>((L.T + kBM - 1) / kBM);
@@ -285,7 +290,7 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.mx_dgrad_bn = 128;
   // one router-weight partial per n-tile and epilogue column half (the bf16
   // and MXFP8 down dgrads both use 256-wide tiles when F allows)
-  L.nparts = (L.F / (bb ? L.dgrad_bn : L.mx_dgrad_bn)) * 2;
+  L.nparts = (L.F / (bb ? L.dgrad_bn : (L.mx_pair_down_dgrad ? 192 : L.mx_dgrad_bn))) * 2;
   L.wr_mtiles = (L.E + kBM - 1) / kBM;
   L.wr_ntiles = L.H / 256;
   const int total_kb = static_cast<int>((L.T + kBK - 1) / kBK);
@@ -389,7 +394,8 @@ Layout make_layout(const moe_config_t& c, int sms) {
     L.bs_dh = b.take(mt * (2 * F / 128) * 512);
     if (!L.prepared) {
       L.bq_wdh = b.take(E * F * H);
-      L.bs_wdh = b.take(E * (F / 128) * (H / 128) * 512);
+      L.bs_wdh = L.mx_pair_down_dgrad ? b.take(E * (F / 192) * 2 * (H / 128) * 512)
+                                      : b.take(E * (F / 128) * (H / 128) * 512);
       L.bq_wg = b.take(E * H * F);
       L.bs_wg = b.take(E * (H / 128) * (F / 128) * 512);
       L.bq_wu = b.take(E * H * F);
@@ -419,6 +425,9 @@ Layout make_layout(const moe_config_t& c, int sms) {
   L.qs_u_f = q.take(E * (H / 128) * (F / 128) * 512);
   L.q_d_h = q.take(E * F * H);
   L.qs_d_h = q.take(E * (F / 128) * (H / 128) * 512);
+  // both layouts of W_down's scales along H, so that the flags of a call may
+  // differ from those of the preparation
+  L.qs_d_h192 = (F % 192 == 0) ? q.take(E * (F / 192) * 2 * (H / 128) * 512) : 0;
   L.q_total = q.off;
   (void)T;
   return L;
@@ -750,7 +759,8 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
   uint8_t* sdy = at<uint8_t>(ws, L.bs_dy);
   const bool prep = b.wq != nullptr;
   uint8_t* wdh = prep ? at<uint8_t>(b.wq, L.q_d_h) : at<uint8_t>(ws, L.bq_wdh);
-  uint8_t* swdh = prep ? at<uint8_t>(b.wq, L.qs_d_h) : at<uint8_t>(ws, L.bs_wdh);
+  uint8_t* swdh = prep ? at<uint8_t>(b.wq, L.mx_pair_down_dgrad ? L.qs_d_h192 : L.qs_d_h)
+                       : at<uint8_t>(ws, L.bs_wdh);
   uint8_t* dhq = at<uint8_t>(ws, L.bq_dh);
   uint8_t* sdh = at<uint8_t>(ws, L.bs_dh);
   uint8_t* wg = prep ? at<uint8_t>(b.wq, L.q_g_f) : at<uint8_t>(ws, L.bq_wg);
@@ -771,13 +781,16 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
   // B2-B4: down dgrad (dY was dispatched straight into its E4M3 copies)
   if (!prep) {
     MOE_TRY(run("mx_quant_w_down_h", s, fl, [&] {
-      return launch_quant_rows_dense(b.W_down, static_cast<int64_t>(L.E) * L.F, L.H, wdh, swdh, s);
+      return launch_quant_rows_dense(b.W_down, static_cast<int64_t>(L.E) * L.F, L.H, wdh,
+                                     L.mx_pair_down_dgrad ? nullptr : swdh, s,
+                                     L.mx_pair_down_dgrad ? swdh : nullptr);
     }));
   }
   {
     GemmArgs a = base_args(st, fl);
     if (!make_map_u8(&a.mapA, dyq, L.H, L.Pa, L.H) ||
-        !make_map_u8(&a.mapB0, wdh, L.H, static_cast<uint64_t>(L.E) * L.F, L.H))
+        !make_map_u8(&a.mapB0, wdh, L.H, static_cast<uint64_t>(L.E) * L.F, L.H,
+                     L.mx_pair_down_dgrad ? 96 : 128))
       return MOE_ERR_CUDA;
     // h [Pa, 2F] in 32 x 32 boxes with the 64-byte swizzle: the epilogue's TMA
     // loads of the saved pre-activations into its staging buffers
@@ -786,7 +799,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
       return MOE_ERR_CUDA;
     a.K = L.H;
     a.N = L.F;
-    a.n_tiles = L.F / L.mx_dgrad_bn;
+    a.n_tiles = L.F / (L.mx_pair_down_dgrad ? 192 : L.mx_dgrad_bn);
     a.num_groups = L.E;
     a.b_group_rows = L.F;
     a.offsets = b.offsets;
@@ -808,9 +821,20 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
       a.flags = kGemmInjectWait;
       a.wait_limit_ns = kTestWaitNs;
     }
-    const int grid = grid_for(mtiles * a.n_tiles, sms);
-    MOE_TRY(run("down_dgrad_swiglu_bwd_mx", s, fl,
-                [&] { return launch_down_dgrad_mx(a, grid, s); }));
+    if (L.mx_pair_down_dgrad) {
+      a.mtile2_off = b.mtile2;
+      if (!make_map_atoms(&a.mapSFA, sdy, static_cast<uint64_t>(L.mt_max) * (L.H / 128)) ||
+          !make_map_atoms(&a.mapSFB, swdh,
+                          static_cast<uint64_t>(L.E) * (L.F / 192) * 2 * (L.H / 128)))
+        return MOE_ERR_CUDA;
+      const int grid = grid_for_pairs(grouped_m_pair_bound(L) * a.n_tiles, sms);
+      MOE_TRY(run("down_dgrad_swiglu_bwd_mx", s, fl,
+                  [&] { return launch_down_dgrad_mx_pair(a, grid, s); }));
+    } else {
+      const int grid = grid_for(mtiles * a.n_tiles, sms);
+      MOE_TRY(run("down_dgrad_swiglu_bwd_mx", s, fl,
+                  [&] { return launch_down_dgrad_mx(a, grid, s); }));
+    }
   }
   // B9: router softmax / top-k backward
   if (cudaMemsetAsync(b.dlt, 0, 2ull * L.E * L.T_pad, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -1022,7 +1046,8 @@ moe_status_t moe_prepare_weights(const moe_config_t* cfg, const moe_bf16_t* W_ga
   }));
   return run("prepare_w_down_h", s, fl, [&] {
     return launch_quant_rows_dense(W_down, static_cast<int64_t>(L.E) * L.F, L.H,
-                                   at<uint8_t>(wq, L.q_d_h), at<uint8_t>(wq, L.qs_d_h), s);
+                                   at<uint8_t>(wq, L.q_d_h), at<uint8_t>(wq, L.qs_d_h), s,
+                                   L.F % 192 == 0 ? at<uint8_t>(wq, L.qs_d_h192) : nullptr);
   });
 }
 

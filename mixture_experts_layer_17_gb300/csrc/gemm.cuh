@@ -281,7 +281,8 @@ struct HasFrag<P, std::void_t<typename P::Frag>> : std::true_type {};
 // 8*stage (A) and +4 (B); 256-wide tiles have one accumulator (columns
 // [0, 256), released early by epilogues with a Frag, else after the
 // epilogue) and scales at 256 + 16*stage
-// (A), +4 (B rows 0..127) and +8 (B rows 128..255).  kAccBufs: accumulators.
+// (A), +4 (B rows 0..127) and +8 (B rows 128..255).  kAccBufs: accumulators,
+// kAccStride TMEM columns apart; sf_col(stage): the stage's first scale column.
 template <class P, bool MX = IsMX<P>::value, bool PAIR = IsPair<P>::value>
 struct StageCfg {
   static constexpr int BN = P::BN;
@@ -295,6 +296,7 @@ struct StageCfg {
   static constexpr int kStages = kWant < kFit ? kWant : kFit;
   static constexpr uint32_t kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
   static constexpr int kAccBufs = 2;
+  static constexpr uint32_t kAccStride = BN;
 };
 
 // CTA pair, bf16: per CTA a stage holds its 128 rows of A and BN/2 rows of B
@@ -311,6 +313,7 @@ struct StageCfg<P, false, true> {
   static constexpr int kStages = 6 < kFit ? 6 : kFit;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr int kAccBufs = 2;
+  static constexpr uint32_t kAccStride = BN;
 };
 
 template <class P>
@@ -328,16 +331,21 @@ struct StageCfg<P, true, false> {
   static constexpr uint32_t kSFCol0 = 256;
   static constexpr uint32_t kSFStride = BN == 256 ? 16 : 8;   // TMEM columns per stage
   static constexpr int kAccBufs = BN == 256 ? 1 : 2;
+  static constexpr uint32_t kAccStride = BN;
+  MOE_DEV static uint32_t sf_col(int stage) { return kSFCol0 + kSFStride * stage; }
 };
 
 // CTA pair, MXFP8: per CTA a stage holds its 128 rows of A and BN/2 rows of
 // B (K = 128 E4M3 each) and the scale atoms the problem loads (P::kSFAtoms
-// of 512 bytes: A's first, then B's); one 256-column accumulator per CTA,
-// scales at TMEM column 256 + 4 * kSFAtoms * stage.
+// of 512 bytes: A's first, then B's), copied to 4 * kSFAtoms TMEM columns.
+//   BN = 256: one accumulator (columns [0, 256)), the stages' scales from
+//             column 256 on;
+//   BN = 192: two accumulators (columns [0, 192) and [256, 448)), the stages'
+//             scales in the gaps [192, 256) and [448, 512).
 template <class P>
 struct StageCfg<P, true, true> {
   static constexpr int BN = P::BN;
-  static_assert(BN == 256, "MXFP8 CTA-pair tiles are 256 x 256");
+  static_assert(BN == 256 || BN == 192, "MXFP8 CTA-pair tiles are 256 x 256 or 256 x 192");
   static constexpr uint32_t kABytes = kBM * 128;
   static constexpr uint32_t kBBytes = (BN / 2) * 128;
   static constexpr uint32_t kSFBytes = 512 * P::kSFAtoms;
@@ -345,10 +353,20 @@ struct StageCfg<P, true, true> {
       static_cast<int>((232448 - 1024 - 256 - P::kExtraSmem) / (kABytes + kBBytes + kSFBytes));
   static constexpr int kStages = 6 < kFit ? 6 : kFit;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kSFCol0 = 256;
   static constexpr uint32_t kSFStride = 4 * P::kSFAtoms;
-  static_assert(kSFCol0 + kSFStride * kStages <= kTmemCols, "scale slots exceed TMEM");
-  static constexpr int kAccBufs = 1;
+  static constexpr int kAccBufs = BN == 192 ? 2 : 1;
+  static constexpr uint32_t kAccStride = 256;
+  // scale slots per gap of the 192-wide layout
+  static constexpr int kGapSlots = static_cast<int>((256 - BN) / kSFStride);
+  static_assert(BN == 256 ? 256 + kSFStride * kStages <= kTmemCols : kStages <= 2 * kGapSlots,
+                "scale slots exceed TMEM");
+  MOE_DEV static uint32_t sf_col(int stage) {
+    if constexpr (BN == 256) {
+      return 256 + kSFStride * stage;
+    } else {
+      return stage < kGapSlots ? BN + kSFStride * stage : 256 + BN + kSFStride * (stage - kGapSlots);
+    }
+  }
 };
 
 template <class P>
@@ -504,7 +522,7 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
         break;
       }
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc) * C::kAccStride;
       for (int kb = 0; kb < ti.num_kb; ++kb) {
         if (!mbar_wait_bounded(full_bar + stage, phase, abort_flag, limit)) {
           if (!*abort_flag) record_timeout(args.status, kWaitMmaFull);
@@ -518,7 +536,7 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
             // the stage's scale atoms -> the pair's TMEM (the problem's slot
             // layout: A's atom at sf_t, B's from sf_t + 4), then four K = 32
             // block-scaled M = 256 MMAs
-            const uint32_t sf_t = tmem_base + C::kSFCol0 + C::kSFStride * stage;
+            const uint32_t sf_t = tmem_base + C::sf_col(stage);
 #pragma unroll
             for (int i = 0; i < P::kSFAtoms; ++i)
               sf_copy_to_tmem_pair(sf_t + 4 * i, sSF + stage * kSF + 512 * i);
@@ -543,7 +561,7 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
             tc_fence_after();
             // scales of this stage -> TMEM (4-column aligned slots), then four
             // K = 32 block-scaled MMAs selecting the K-block with sf_id
-            const uint32_t sf_t = tmem_base + C::kSFCol0 + C::kSFStride * stage;
+            const uint32_t sf_t = tmem_base + C::sf_col(stage);
             sf_copy_to_tmem(sf_t, sSF + stage * kSF);
             sf_copy_to_tmem(sf_t + 4, sSF + stage * kSF + 512);
             if constexpr (BN == 256) sf_copy_to_tmem(sf_t + 8, sSF + stage * kSF + 1024);
@@ -657,7 +675,7 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
         break;
       }
       tc_fence_after();
-      const uint32_t taddr = tmem_base + lane_off + static_cast<uint32_t>(acc * BN);
+      const uint32_t taddr = tmem_base + lane_off + static_cast<uint32_t>(acc) * C::kAccStride;
       if constexpr (HasFrag<P>::value) {
         // early release: fragment -> registers, accumulator back to the MMA
         // warp, then the element-wise work and the stores

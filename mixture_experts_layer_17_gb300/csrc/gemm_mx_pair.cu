@@ -22,5 +22,8 @@ cudaError_t launch_gate_up_wgrad_mx_pair(const GemmArgs& a, int grid, cudaStream
 cudaError_t launch_dense_mx_pair(const GemmArgs& a, int grid, cudaStream_t s) {
   return launch_gemm<DenseMXPairProblem>(a, grid, s);
 }
+cudaError_t launch_down_dgrad_mx_pair(const GemmArgs& a, int grid, cudaStream_t s) {
+  return launch_gemm<DownDgradMXPairProblem>(a, grid, s);
+}
 
 }  // namespace moe

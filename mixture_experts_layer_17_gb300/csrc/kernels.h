@@ -42,10 +42,14 @@ cudaError_t launch_gate_up_dgrad_mx_pair(const GemmArgs& a, int grid, cudaStream
 cudaError_t launch_down_wgrad_mx_pair(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_gate_up_wgrad_mx_pair(const GemmArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_dense_mx_pair(const GemmArgs& a, int grid, cudaStream_t s);
+// 256 x 192 tiles, two accumulators per CTA (F a multiple of 192)
+cudaError_t launch_down_dgrad_mx_pair(const GemmArgs& a, int grid, cudaStream_t s);
 
-// MXFP8 quantisers (mx_quant.cu): E4M3 data + 512-byte scale atoms
+// MXFP8 quantisers (mx_quant.cu): E4M3 data + 512-byte scale atoms.  Rows
+// quantiser: sf (128-row atoms) and/or sf192 (192-row blocks of two atoms, R
+// a multiple of 192), each written when not null.
 cudaError_t launch_quant_rows_dense(const uint16_t* src, int64_t R, int C, uint8_t* dst,
-                                    uint8_t* sf, cudaStream_t s);
+                                    uint8_t* sf, cudaStream_t s, uint8_t* sf192 = nullptr);
 cudaError_t launch_quant_cols_weights(const uint16_t* src, int E, int R, int C, uint8_t* dst,
                                       uint8_t* sf, cudaStream_t s);
 cudaError_t launch_quant_cols_gate_up(const uint16_t* W_gate, const uint16_t* W_up, int E, int H,

@@ -13,17 +13,25 @@ namespace moe {
 namespace {
 
 // --------------------------------------------------------------------------
-// Along the contiguous dimension (K-major operand [R, C], K = C; weights):
-// the atom group of a row is row / 128, its row in the atom row % 128.
-// Atom index = group * (C / 128) + k / 128.  One warp per row.
+// Along the contiguous dimension (K-major operand [R, C], K = C; weights).
+// One warp per row.  Two scale layouts, each written when its pointer is set:
+//   sf:    128-row atoms: atom (row / 128) * (C / 128) + k / 128, atom row
+//          row % 128;
+//   sf192: 192-row blocks of two atoms (rows 0..127 of the block, then rows
+//          128..191 in the first 64 rows of the second; its other 64 rows are
+//          never read): atom ((row / 192) * 2 + half) * (C / 128) + k / 128.
 // --------------------------------------------------------------------------
 __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, int64_t R, int C,
-                                  uint8_t* __restrict__ dst, uint8_t* __restrict__ sf) {
+                                  uint8_t* __restrict__ dst, uint8_t* __restrict__ sf,
+                                  uint8_t* __restrict__ sf192) {
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= R) return;
   const int lane = threadIdx.x & 31;
   const int64_t group = row >> 7;
   const int r = static_cast<int>(row & 127);
+  const int64_t b192 = row / 192;
+  const int r192 = static_cast<int>(row - 192 * b192);
+  const int64_t group192 = 2 * b192 + (r192 >> 7);
   const int KT = C >> 7;
   const uint16_t* s = src + row * C;
   uint8_t* d = dst + row * C;
@@ -47,7 +55,11 @@ __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, int64_t R, i
     for (int i = 0; i < 8; ++i) w[i] = to_e4m3x4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], inv);
     st_global_v4(d + b * 32, w[0], w[1], w[2], w[3]);
     st_global_v4(d + b * 32 + 16, w[4], w[5], w[6], w[7]);
-    sf[(group * KT + (b >> 2)) * 512 + sf_atom_offset(r, b & 3)] = static_cast<uint8_t>(X + 127);
+    if (sf != nullptr)
+      sf[(group * KT + (b >> 2)) * 512 + sf_atom_offset(r, b & 3)] = static_cast<uint8_t>(X + 127);
+    if (sf192 != nullptr)
+      sf192[(group192 * KT + (b >> 2)) * 512 + sf_atom_offset(r192 & 127, b & 3)] =
+          static_cast<uint8_t>(X + 127);
   }
 }
 
@@ -282,8 +294,9 @@ __global__ void __launch_bounds__(kColThreads) dispatch_quant_kernel(
 }  // namespace
 
 cudaError_t launch_quant_rows_dense(const uint16_t* src, int64_t R, int C, uint8_t* dst,
-                                    uint8_t* sf, cudaStream_t s) {
-  quant_rows_kernel<<<static_cast<unsigned>((R + 7) / 8), 256, 0, s>>>(src, R, C, dst, sf);
+                                    uint8_t* sf, cudaStream_t s, uint8_t* sf192) {
+  if (sf192 != nullptr && R % 192 != 0) return cudaErrorInvalidValue;
+  quant_rows_kernel<<<static_cast<unsigned>((R + 7) / 8), 256, 0, s>>>(src, R, C, dst, sf, sf192);
   return cudaGetLastError();
 }
 

@@ -129,6 +129,152 @@ struct WgradMXPairProblem : WgradMXProblem<kGateUp> {
   }
 };
 
+// B2-B4 in MXFP8 on CTA pairs with 256 x 192 tiles (N = 192 divides F for
+// the Qwen3-shaped layers): two accumulators per CTA fit beside the scale
+// slots, so a tile's epilogue overlaps the next tile's MMAs.  Per stage CTA
+// `rank` loads its 128 rows of dY (along H), rows n0 + 96 * rank of W_down
+// (K-major) and three scale atoms: its own A atom and both atoms of the
+// tile's 192 B rows.  W_down's scales come in 192-row blocks of two atoms
+// (rows 0..127, then rows 128..191 in the first 64 rows of the second atom):
+// atom ((expert * F/192 + n-tile) * 2 + half) * (H/128) + k-tile.
+// Epilogue: the SwiGLU backward of DownDgradProblem's staged epilogue (one
+// pair of 2 KB buffers per warp, h by TMA), plus dh quantised to E4M3 along F
+// from fp32 (out3 / out4, as in DownDgradMXProblem); 96 columns per warpgroup
+// and tile, i.e. three 32-column steps.
+struct DownDgradMXPairProblem {
+  static constexpr int BN = 192;
+  static constexpr bool kAMN = false;
+  static constexpr bool kBMN = false;
+  static constexpr bool kMX = true;
+  static constexpr bool kPair = true;
+  static constexpr int kSFAtoms = 3;
+  static constexpr size_t kStageBytes = 8 * 2 * kStage64WarpBytes;
+  static constexpr size_t kExtraSmem = 1024 + kStageBytes + 8 * sizeof(uint64_t);
+  static constexpr int kEpiGroups = 2;
+  static constexpr int kSteps = BN / 2 / 32;
+
+  MOE_DEV static uint8_t* stage_base(uint8_t* extra) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(extra) + 1023) &
+                                      ~static_cast<uintptr_t>(1023));
+  }
+  MOE_DEV static int num_tiles(const GemmArgs& a) { return grouped_m_num_tiles_pair(a); }
+  MOE_DEV static TileInfo tile(const GemmArgs& a, int t) { return grouped_m_tile_pair_mx(a, t, BN); }
+  MOE_DEV static void init_extra(const GemmArgs&, uint8_t* extra) {
+    if (threadIdx.x == 0) {
+      uint64_t* bars = reinterpret_cast<uint64_t*>(stage_base(extra) + kStageBytes);
+      for (int w = 0; w < 8; ++w) mbar_init(bars + w, 1);
+      fence_mbar_init();
+    }
+  }
+  MOE_DEV static void load_mx_pair(const GemmArgs& a, const TileInfo& ti, int kb, int rank,
+                                   uint8_t* sA, uint8_t* sB, uint8_t* sSF, uint32_t bar) {
+    const int k0 = kb * 128;
+    tma_load_2d_pair(sA, &a.mapA, k0, ti.m0 + kBM * rank, bar);
+    tma_load_2d_pair(sB, &a.mapB0, k0, ti.e * a.b_group_rows + ti.n0 + (BN / 2) * rank, bar);
+    load_atom_pair(sSF, &a.mapSFA, a_atom_row_pair(a, ti, rank) * a.kt_a + kb, bar);
+    const int64_t blk = static_cast<int64_t>(ti.e) * a.n_tiles + ti.n0 / BN;
+    load_atom_pair(sSF + 512, &a.mapSFB, 2 * blk * a.kt_b + kb, bar);
+    load_atom_pair(sSF + 1024, &a.mapSFB, (2 * blk + 1) * a.kt_b + kb, bar);
+  }
+  MOE_DEV static void epilogue_empty(const GemmArgs&, const TileInfo&, int, int, uint8_t*) {}
+  MOE_DEV static void epilogue(const GemmArgs& a, const TileInfo& ti, uint32_t taddr, int r,
+                               int group, uint8_t* extra) {
+    constexpr int kHalf = BN / 2;
+    const bool valid = r < ti.rows;
+    const bool pad = !valid && r < ti.rows_pad;
+    const int lane = r & 31;
+    const int wslot = group * 4 + (r >> 5);
+    uint8_t* buf = stage_base(extra) + wslot * 2 * kStage64WarpBytes;
+    uint64_t* hbar = reinterpret_cast<uint64_t*>(stage_base(extra) + kStageBytes) + wslot;
+    const int64_t row = static_cast<int64_t>(ti.m0) + ((valid || pad) ? r : 0);
+    const int F = a.ld0;
+    const int c0 = group * kHalf;
+    const int y = ti.m0 + (r & ~31);
+    __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(a.out0) + row * 2 * F + ti.n0;
+    __nv_bfloat16* aw = static_cast<__nv_bfloat16*>(a.out1) + row * F + ti.n0;
+    uint8_t* dhq = static_cast<uint8_t*>(a.out3) + row * 2 * F;
+    uint8_t* sfq = static_cast<uint8_t*>(a.out4);
+    const int64_t atom_row = (static_cast<int64_t>(__ldg(a.mtile_off + ti.e)) + ti.mt) * (2 * F / 128);
+    const float w = valid ? __ldg(static_cast<const float*>(a.in1) + row) : 0.f;
+    const int never = 0;   // the h waits are cut short only by their time limit
+    // h_gate and h_up of step s into the warp's pair; every lane's earlier
+    // accesses to the pair are ordered before the asynchronous writes
+    auto load_h = [&](int step) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(hbar, 2 * kStage64WarpBytes);
+        tma_load_2d(buf, &a.mapB1, ti.n0 + c0 + 32 * step, y, hbar);
+        tma_load_2d(buf + kStage64WarpBytes, &a.mapB1, F + ti.n0 + c0 + 32 * step, y, hbar);
+      }
+    };
+    float dw = 0.f;
+    load_h(0);
+#pragma unroll 1
+    for (int step = 0; step < kSteps; ++step) {
+      const int c = c0 + 32 * step;
+      if (!mbar_wait_bounded(hbar, static_cast<uint32_t>(step) & 1u, &never, a.wait_limit_ns))
+        record_timeout(a.status, kWaitEpiLoad);
+      uint32_t gw[16], uw[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 ug = *reinterpret_cast<const uint4*>(buf + stage64_off(lane, q));
+        const uint4 uu =
+            *reinterpret_cast<const uint4*>(buf + kStage64WarpBytes + stage64_off(lane, q));
+        gw[4 * q] = ug.x; gw[4 * q + 1] = ug.y; gw[4 * q + 2] = ug.z; gw[4 * q + 3] = ug.w;
+        uw[4 * q] = uu.x; uw[4 * q + 1] = uu.y; uw[4 * q + 2] = uu.z; uw[4 * q + 3] = uu.w;
+      }
+      float g[32];
+      tmem_ld32(taddr + c, g);
+      float dhg[32], dhu[32];
+      uint32_t awp[16];   // w*a of the step's 32 columns, packed bf16
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float awv[16];
+        if (valid) {
+          DownDgradProblem<256, true>::swiglu_bwd16(g + 16 * half, gw + 8 * half, uw + 8 * half, w,
+                                                    dw, dhg + 16 * half, dhu + 16 * half, awv);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) dhg[16 * half + i] = dhu[16 * half + i] = awv[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) awp[8 * half + i] = pack_bf16x2(awv[2 * i], awv[2 * i + 1]);
+      }
+      stage64_bf16x16(buf, lane, 0, dhg);
+      stage64_bf16x16(buf, lane, 1, dhg + 16);
+      stage64_bf16x16(buf + kStage64WarpBytes, lane, 0, dhu);
+      stage64_bf16x16(buf + kStage64WarpBytes, lane, 1, dhu + 16);
+      const bool w_row = valid || pad;
+      stage64_flush(buf, lane, w_row ? dh + c : nullptr, false);
+      stage64_flush(buf + kStage64WarpBytes, lane, w_row ? dh + F + c : nullptr, false);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(buf + stage64_off(lane, q)) =
+            make_uint4(awp[4 * q], awp[4 * q + 1], awp[4 * q + 2], awp[4 * q + 3]);
+      stage64_flush(buf, lane, w_row ? aw + c : nullptr, false);
+      if (valid) {
+        const int cg = ti.n0 + c;           // gate column; up column = F + cg
+        mx_block_store(dhg, dhq + cg,
+                       sfq + (atom_row + cg / 128) * 512 + sf_atom_offset(r, (cg >> 5) & 3));
+        mx_block_store(dhu, dhq + F + cg,
+                       sfq + (atom_row + (F + cg) / 128) * 512 + sf_atom_offset(r, ((F + cg) >> 5) & 3));
+      }
+      if (step + 1 < kSteps) load_h(step + 1);
+    }
+    if constexpr (kSteps % 2 != 0) {
+      // one more (empty) phase, so that every tile starts at parity 0; every
+      // lane has passed its last wait
+      __syncwarp();
+      if (lane == 0) mbar_arrive(hbar);
+    }
+    // one router-weight partial per (row, n-tile, column half)
+    if (valid)
+      static_cast<float*>(a.out2)[row * (a.n_tiles * kEpiGroups) + (ti.n0 / BN) * kEpiGroups +
+                                  group] = dw;
+  }
+};
+
 // Dense MXFP8 GEMM on 256 x 256 CTA-pair tiles for moe_gemm_mxfp8 (N a
 // multiple of 256): A [M, K] and B [N, K] E4M3, K-major; A's atoms (128-row
 // m-tile * kt + k-tile), B's (128-row n-tile * kt + k-tile); D fp32 [M, N].

@@ -77,6 +77,7 @@ MX_SHAPES = [
     (517, 512, 384, 16, 4, 52),     # F = 3 x 128, several tiles per expert
     (200, 256, 128, 4, 1, 53),      # top-1
     (1, 256, 256, 4, 2, 55),        # a single token
+    (1100, 256, 768, 6, 2, 57),     # F = 4 x 192: the down dgrad's 256 x 192 pair tiles
 ]
 
 
@@ -107,10 +108,11 @@ def test_layer_fp8_bwd(shape, mode):
 
 
 @pytest.mark.parametrize("mode", sorted(PAIR_MODES))
-def test_layer_mxfp8_with_empty_experts(mode):
+@pytest.mark.parametrize("F", [256, 384])
+def test_layer_mxfp8_with_empty_experts(mode, F):
     bias = torch.zeros(12)
     bias[[2, 9]] = -30.0
-    out, ref, errs, _ = _layer_case((256, 256, 256, 12, 2, 54), "mxfp8", bias=bias,
+    out, ref, errs, _ = _layer_case((256, 256, F, 12, 2, 54), "mxfp8", bias=bias,
                                     flags=PAIR_MODES[mode])
     assert ref["fwd"]["counts"][2] == 0 and ref["fwd"]["counts"][9] == 0
     for name, e in errs.items():
