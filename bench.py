@@ -141,6 +141,12 @@ NCU_LABELS = [
     ("GateUpFwdMXProblem", "gate_up_gemm_swiglu_mx"), ("DownFwdMXProblem", "down_gemm_scatter_mx"),
     ("DownDgradMXProblem", "down_dgrad_swiglu_bwd_mx"),
     ("GateUpDgradMXProblem", "gate_up_dgrad_scatter_mx"),
+    ("WgradMXPairProblem<true>", "gate_up_wgrad_mx"), ("WgradMXPairProblem<false>", "down_wgrad_mx"),
+    ("WgradMXPairProblem<1>", "gate_up_wgrad_mx"), ("WgradMXPairProblem<0>", "down_wgrad_mx"),
+    ("GateUpFwdMXPairProblem", "gate_up_gemm_swiglu_mx"),
+    ("DownFwdMXPairProblem", "down_gemm_scatter_mx"),
+    ("DownDgradMXPairProblem", "down_dgrad_swiglu_bwd_mx"),
+    ("GateUpDgradMXPairProblem", "gate_up_dgrad_scatter_mx"),
     ("GateUpWgradProblem", "gate_up_wgrad"), ("DownWgradProblem", "down_wgrad"),
     ("GateUpFwdPairProblem", "gate_up_gemm_swiglu"), ("GateUpFwdProblem", "gate_up_gemm_swiglu"),
     ("DownFwdPairProblem", "down_gemm_scatter"), ("DownFwdProblem", "down_gemm_scatter"),
