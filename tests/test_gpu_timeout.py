@@ -4,7 +4,8 @@ limit.  The kernel must give up, record MOE_ERR_TIMEOUT in the workspace
 status word, free its tensor memory and return, leaving the context usable.
 Run on the single-CTA bf16 kernels, on CTA pairs (where each CTA of a pair
 gives up on its own and both still meet at the closing cluster barrier) and on
-the MXFP8 kernels, single-CTA and paired."""
+the MXFP8 kernels, single-CTA and paired (F = 384 adds the down dgrad's 256 x
+192 pair tiles with two accumulators)."""
 
 import numpy as np
 import pytest
@@ -17,11 +18,12 @@ from oracle import moe_oracle as mo
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("precision,extra", [("bf16", 0), ("bf16", "pairs"), ("mxfp8", 0),
-                                             ("mxfp8", "pairs")])
-def test_bounded_wait_times_out_and_context_survives(precision, extra):
+@pytest.mark.parametrize("precision,extra,F", [("bf16", 0, 256), ("bf16", "pairs", 256),
+                                               ("mxfp8", 0, 256), ("mxfp8", "pairs", 256),
+                                               ("mxfp8", "pairs", 384)])
+def test_bounded_wait_times_out_and_context_survives(precision, extra, F):
     from mixture_experts_layer_17_gb300 import MoeLayer, libmoe
-    sh = si.custom_shape(384, 256, 256, 8, 2, seed=31)
+    sh = si.custom_shape(384, 256, F, 8, 2, seed=31)
     inp = si.make_inputs(sh, "cuda")
     args = (inp["x"], inp["W_r"], inp["W_gate"], inp["W_up"], inp["W_down"])
     flags = libmoe.MOE_FLAG_TEST_TIMEOUT
