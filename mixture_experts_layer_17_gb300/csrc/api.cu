@@ -548,6 +548,13 @@ moe_status_t run_routing(const moe_config_t& c, const Layout& L, const RouteBufs
   return MOE_OK;
 }
 
+// The down dgrads' output maps: dh [Pa, 2F] and w*a [Pa, F] bf16 in 32 x 32
+// boxes with the 64-byte swizzle, the layout their epilogues stage.
+bool make_out_maps(GemmArgs* a, const void* dh, const void* aw, const Layout& L) {
+  return make_map(&a->mapC0, dh, 2ull * L.F, L.Pa, 4ull * L.F, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) &&
+         make_map(&a->mapC1, aw, L.F, L.Pa, 2ull * L.F, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 int64_t grouped_m_tile_bound(const Layout& L) { return (L.P + kBM - 1) / kBM + L.E; }
 int64_t grouped_m_pair_bound(const Layout& L) { return (L.P + 2 * kBM - 1) / (2 * kBM) + L.E; }
 
@@ -826,6 +833,7 @@ moe_status_t backward_expert_gemms_mx(const Layout& L, int sms, cudaStream_t s, 
     }
     if (L.mx_pair_down_dgrad) {
       a.mtile2_off = b.mtile2;
+      if (!make_out_maps(&a, b.dh, b.aw, L)) return MOE_ERR_CUDA;
       if (!make_map_atoms(&a.mapSFA, sdy, static_cast<uint64_t>(L.mt_max) * (L.H / 128)) ||
           !make_map_atoms(&a.mapSFB, swdh,
                           static_cast<uint64_t>(L.E) * (L.F / 192) * 2 * (L.H / 128)))
@@ -1321,6 +1329,8 @@ static moe_status_t backward_impl(const moe_config_t* cfg, const moe_bf16_t* x,
       if (L.pair_down_dgrad && !make_map(&a.mapB1, h, 2ull * L.F, L.Pa, 4ull * L.F, 32, 32,
                                          CU_TENSOR_MAP_SWIZZLE_64B))
         return MOE_ERR_CUDA;
+      // dh [Pa, 2F] and w*a [Pa, F] in the same boxes: the staged outputs' TMA stores
+      if (L.pair_down_dgrad && !make_out_maps(&a, dh, aw, L)) return MOE_ERR_CUDA;
       a.K = L.H;
       a.N = L.F;
       a.n_tiles = L.F / L.dgrad_bn;

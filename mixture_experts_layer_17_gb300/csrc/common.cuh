@@ -171,6 +171,21 @@ MOE_DEV void tma_load_2d(void* smem_dst, const CUtensorMap* map, int32_t c0, int
       : "memory");
 }
 
+// TMA tensor store of one box from shared memory (a bulk async-group
+// operation of the issuing thread): the box at coordinates (c0, c1) of the
+// map's tensor; rows past the tensor's end are not written.
+MOE_DEV void tma_store_2d(const CUtensorMap* map, const void* smem_src, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(smem_src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+// Closes the thread's pending bulk stores into one group.
+MOE_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every committed bulk store of the thread has read its shared
+// memory source (the source may then be rewritten; the global writes complete
+// on their own, at the latest with the kernel).
+MOE_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (tensor cores / TMA) before they read it.
 MOE_DEV void fence_proxy_async_smem() {

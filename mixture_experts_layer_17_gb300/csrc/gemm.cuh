@@ -40,6 +40,9 @@ struct GemmArgs {
   CUtensorMap mapSFA;
   CUtensorMap mapSFB;
   CUtensorMap mapSFB1;   // the second B operand's atoms (gate/up dgrad: W_up)
+  // staged epilogue outputs leaving by TMA stores (the down dgrads' dh and w*a)
+  CUtensorMap mapC0;
+  CUtensorMap mapC1;
   int M;               // dense: output rows; grouped-K / split-K: output rows per group
   int N;               // output columns
   int K;               // reduction length (dense, grouped-M, split-K)

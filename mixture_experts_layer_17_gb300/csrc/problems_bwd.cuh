@@ -31,8 +31,9 @@ struct DownDgradProblem {
   // Per 32-column step, TMA brings the warp's 32 rows of h_gate and h_up into
   // the pair (64-byte swizzle, the stage64 layout); every thread keeps its row
   // of both as packed words, then dh_gate and dh_up, and after them w*a, are
-  // staged in the same pair and leave as whole 64-byte row pieces, after
-  // which the next step's h is loaded.  One pair per warp (32 KB in all)
+  // staged in the same pair and leave by TMA stores (maps mapC0 over dh and
+  // mapC1 over w*a, the same 32 x 32 boxes), after which the next step's h
+  // is loaded.  One pair per warp (32 KB in all)
   // leaves room for six operand stages; a second pair, to load the next h
   // during the step, would cost a stage, and measured 2% slower at the 235B
   // shape (the h wait is under a sixth of the epilogue's time per tile).
@@ -104,8 +105,6 @@ struct DownDgradProblem {
     const int F = a.ld0;
     const int c0 = group * kHalf;
     const int y = ti.m0 + (r & ~31);
-    __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(a.out0) + row * 2 * F + ti.n0;
-    __nv_bfloat16* aw = static_cast<__nv_bfloat16*>(a.out1) + row * F + ti.n0;
     const float w = valid ? __ldg(static_cast<const float*>(a.in1) + row) : 0.f;
     const int never = 0;   // the h waits are cut short only by their time limit
     // h_gate and h_up of step s (columns c0 + 32 s ..) into the warp's pair;
@@ -156,14 +155,32 @@ struct DownDgradProblem {
 #pragma unroll
         for (int i = 0; i < 8; ++i) awp[8 * half + i] = pack_bf16x2(awv[2 * i], awv[2 * i + 1]);
       }
-      const bool w_row = valid || pad;
-      stage64_flush(st, lane, w_row ? dh + c : nullptr, false);
-      stage64_flush(st + kStage64WarpBytes, lane, w_row ? dh + F + c : nullptr, false);
+      // dh_gate and dh_up, then w*a, leave by TMA stores (a.mapC0, a.mapC1: the
+      // stage64 layout is the 64-byte swizzle of a 32 x 32 box).  Segments
+      // are 64-row aligned, so the warp's 32 rows lie wholly inside the
+      // expert's padded segment (valid and padding rows) or wholly outside.
+      const bool slab_in = (r & ~31) < ti.rows_pad;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && slab_in) {
+        tma_store_2d(&a.mapC0, st, ti.n0 + c, y);
+        tma_store_2d(&a.mapC0, st + kStage64WarpBytes, F + ti.n0 + c, y);
+        bulk_commit();
+        bulk_wait_read0();
+      }
+      __syncwarp();
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         *reinterpret_cast<uint4*>(st + stage64_off(lane, q)) =
             make_uint4(awp[4 * q], awp[4 * q + 1], awp[4 * q + 2], awp[4 * q + 3]);
-      stage64_flush(st, lane, w_row ? aw + c : nullptr, false);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && slab_in) {
+        tma_store_2d(&a.mapC1, st, ti.n0 + c, y);
+        bulk_commit();
+        bulk_wait_read0();
+      }
+      __syncwarp();
       if (step + 1 < kSteps) load_h(step + 1);
     }
     // one router-weight partial per (row, n-tile, column half)

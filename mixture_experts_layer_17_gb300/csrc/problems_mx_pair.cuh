@@ -138,9 +138,10 @@ struct WgradMXPairProblem : WgradMXProblem<kGateUp> {
 // (rows 0..127, then rows 128..191 in the first 64 rows of the second atom):
 // atom ((expert * F/192 + n-tile) * 2 + half) * (H/128) + k-tile.
 // Epilogue: the SwiGLU backward of DownDgradProblem's staged epilogue (one
-// pair of 2 KB buffers per warp, h by TMA), plus dh quantised to E4M3 along F
-// from fp32 (out3 / out4, as in DownDgradMXProblem); 96 columns per warpgroup
-// and tile, i.e. three 32-column steps.
+// pair of 2 KB buffers per warp, h by TMA, dh and w*a out by TMA stores
+// through mapC0 / mapC1), plus dh quantised to E4M3 along F from fp32 (out3
+// / out4, as in DownDgradMXProblem); 96 columns per warpgroup and tile, i.e.
+// three 32-column steps.
 struct DownDgradMXPairProblem {
   static constexpr int BN = 192;
   static constexpr bool kAMN = false;
@@ -190,8 +191,6 @@ struct DownDgradMXPairProblem {
     const int F = a.ld0;
     const int c0 = group * kHalf;
     const int y = ti.m0 + (r & ~31);
-    __nv_bfloat16* dh = static_cast<__nv_bfloat16*>(a.out0) + row * 2 * F + ti.n0;
-    __nv_bfloat16* aw = static_cast<__nv_bfloat16*>(a.out1) + row * F + ti.n0;
     uint8_t* dhq = static_cast<uint8_t*>(a.out3) + row * 2 * F;
     uint8_t* sfq = static_cast<uint8_t*>(a.out4);
     const int64_t atom_row = (static_cast<int64_t>(__ldg(a.mtile_off + ti.e)) + ti.mt) * (2 * F / 128);
@@ -245,14 +244,31 @@ struct DownDgradMXPairProblem {
       stage64_bf16x16(buf, lane, 1, dhg + 16);
       stage64_bf16x16(buf + kStage64WarpBytes, lane, 0, dhu);
       stage64_bf16x16(buf + kStage64WarpBytes, lane, 1, dhu + 16);
-      const bool w_row = valid || pad;
-      stage64_flush(buf, lane, w_row ? dh + c : nullptr, false);
-      stage64_flush(buf + kStage64WarpBytes, lane, w_row ? dh + F + c : nullptr, false);
+      // dh_gate and dh_up, then w*a, leave by TMA stores (a.mapC0, a.mapC1);
+      // the warp's 32 rows lie wholly inside the expert's 64-row aligned
+      // padded segment or wholly outside it
+      const bool slab_in = (r & ~31) < ti.rows_pad;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && slab_in) {
+        tma_store_2d(&a.mapC0, buf, ti.n0 + c, y);
+        tma_store_2d(&a.mapC0, buf + kStage64WarpBytes, F + ti.n0 + c, y);
+        bulk_commit();
+        bulk_wait_read0();
+      }
+      __syncwarp();
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         *reinterpret_cast<uint4*>(buf + stage64_off(lane, q)) =
             make_uint4(awp[4 * q], awp[4 * q + 1], awp[4 * q + 2], awp[4 * q + 3]);
-      stage64_flush(buf, lane, w_row ? aw + c : nullptr, false);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && slab_in) {
+        tma_store_2d(&a.mapC1, buf, ti.n0 + c, y);
+        bulk_commit();
+        bulk_wait_read0();
+      }
+      __syncwarp();
       if (valid) {
         const int cg = ti.n0 + c;           // gate column; up column = F + cg
         mx_block_store(dhg, dhq + cg,
