@@ -54,7 +54,10 @@ def _run(layer, inp):
 
 
 @pytest.mark.parametrize("precision", ["bf16", "mxfp8", "fp8_bwd"])
-@pytest.mark.parametrize("shape", [(517, 512, 384, 16, 4, 61), (1024, 512, 256, 8, 4, 62)])
+@pytest.mark.parametrize("shape", [(517, 512, 384, 16, 4, 61), (1024, 512, 256, 8, 4, 62),
+                                   # 367 rows per expert, F = 2 x 192: the MXFP8 down dgrad
+                                   # runs on 256 x 192 CTA pairs
+                                   (1100, 256, 384, 6, 2, 67)])
 def test_recompute_is_bit_identical(precision, shape):
     from mixture_experts_layer_17_gb300 import MoeLayer, libmoe
     sh, inp = _inputs(shape, precision)
@@ -83,11 +86,12 @@ def test_recompute_is_bit_identical(precision, shape):
             assert rel_fro(f64(g1[key]), ref[key]) <= BF16_TOL, key
 
 
-@pytest.mark.parametrize("precision,flags", [("bf16", 0), ("bf16", "pairs"), ("mxfp8", 0)])
-def test_accumulate_into_fp32(precision, flags):
+@pytest.mark.parametrize("precision,flags,F", [("bf16", 0, 256), ("bf16", "pairs", 256),
+                                               ("mxfp8", 0, 256), ("mxfp8", "pairs", 384)])
+def test_accumulate_into_fp32(precision, flags, F):
     from mixture_experts_layer_17_gb300 import MoeLayer, libmoe
     fl = libmoe.MOE_FLAG_CTA_PAIRS_ON if flags == "pairs" else 0
-    sh, inp = _inputs((1024, 512, 256, 12, 4, 63), precision, zero_experts=(3, 7))
+    sh, inp = _inputs((1024, 512, F, 12, 4, 63), precision, zero_experts=(3, 7))
     layer = MoeLayer(sh.T, sh.H, sh.F, sh.E, sh.top_k, precision, flags=fl)
     args = _weights(inp)
     y, g = _run(layer, inp)
@@ -158,16 +162,24 @@ def test_sm_budget_mxfp8_and_recompute_together():
         assert rel_fro(f64(g1[key]), ref[key]) <= MX_TOL, key
 
 
-@pytest.mark.parametrize("precision,extra", [("mxfp8", 0), ("fp8_bwd", 0), ("mxfp8", "recompute")])
+@pytest.mark.parametrize("precision,extra", [("mxfp8", 0), ("fp8_bwd", 0), ("mxfp8", "recompute"),
+                                             ("mxfp8", "pairs"), ("fp8_bwd", "pairs")])
 def test_prepared_weights_are_bit_identical(precision, extra):
     """moe_prepare_weights writes the bytes the calls would quantise
-    themselves, and the calls read them instead of the bf16 weights."""
+    themselves, and the calls read them instead of the bf16 weights.  With
+    CTA pairs (F = 384: the down dgrad's 256 x 192 tiles, which read W_down's
+    scales in 192-row blocks) the weights are prepared under
+    MOE_FLAG_CTA_PAIRS_OFF and used under MOE_FLAG_CTA_PAIRS_ON: the buffer
+    holds both scale layouts."""
     from mixture_experts_layer_17_gb300 import MoeLayer, libmoe
-    fl = libmoe.MOE_FLAG_RECOMPUTE if extra == "recompute" else 0
+    fl = {"recompute": libmoe.MOE_FLAG_RECOMPUTE, "pairs": libmoe.MOE_FLAG_CTA_PAIRS_ON}.get(extra, 0)
     sh, inp = _inputs((517, 512, 384, 16, 4, 66), precision)
     plain = MoeLayer(sh.T, sh.H, sh.F, sh.E, sh.top_k, precision, flags=fl)
     prep = MoeLayer(sh.T, sh.H, sh.F, sh.E, sh.top_k, precision, flags=fl)
+    if extra == "pairs":
+        prep.cfg.flags = libmoe.MOE_FLAG_CTA_PAIRS_OFF
     prep.prepare_weights(inp["W_gate"], inp["W_up"], inp["W_down"])
+    prep.cfg.flags = fl
     y0, g0 = _run(plain, inp)
     y1, g1 = _run(prep, inp)
     assert torch.equal(y0, y1)
