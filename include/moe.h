@@ -297,6 +297,11 @@ const char* moe_status_string(moe_status_t status);
 void moe_profile_enable(int on);
 int moe_profile_read(const char** names, int64_t* launches, double* total_ms, int cap);
 
+/* Restricts the per-kernel timing to the launches labelled `name` (the names
+ * moe_profile_read returns), so that the other launches run without events
+ * between them; NULL times every launch again.  The string is copied. */
+void moe_profile_select(const char* name);
+
 /* Number of kernel launches the library has made in this process. */
 int64_t moe_launch_count(void);
 

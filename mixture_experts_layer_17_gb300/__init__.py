@@ -16,8 +16,8 @@ import torch
 from . import libmoe
 from .libmoe import (MoeConfig, MoeError, make_config, moe_backward,  # noqa: F401
                      moe_backward_accumulate, moe_forward, moe_gemm_bf16, moe_get_device_status, moe_launch_count,
-                     moe_profile_enable, moe_profile_read, moe_route, moe_status_string,
-                     moe_workspace_size)
+                     moe_profile_enable, moe_profile_read, moe_profile_select, moe_route,
+                     moe_status_string, moe_workspace_size)
 
 
 class MoeLayer:

@@ -129,6 +129,7 @@ struct Totals {
 
 std::mutex g_prof_mu;
 bool g_prof_on = false;
+std::string g_prof_only;   // when not empty, only launches with this label are timed
 std::vector<Pending> g_pending;
 std::map<std::string, Totals> g_totals;
 std::vector<std::string> g_names;   // storage behind names handed out by moe_profile_read
@@ -142,7 +143,7 @@ moe_status_t run(const char* name, cudaStream_t s, uint32_t flags, Fn&& fn) {
   bool prof;
   {
     std::lock_guard<std::mutex> lock(g_prof_mu);
-    prof = g_prof_on;
+    prof = g_prof_on && (g_prof_only.empty() || g_prof_only == name);
   }
   if (prof) {
     if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess)
@@ -1607,6 +1608,11 @@ moe_status_t moe_get_device_status(const void* ws, moe_stream_t stream) {
 void moe_profile_enable(int on) {
   std::lock_guard<std::mutex> lock(g_prof_mu);
   g_prof_on = on != 0;
+}
+
+void moe_profile_select(const char* name) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof_only = name != nullptr ? name : "";
 }
 
 int moe_profile_read(const char** names, int64_t* launches, double* total_ms, int cap) {

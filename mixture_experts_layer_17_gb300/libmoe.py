@@ -31,7 +31,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
 # every symbol include/moe.h declares
 EXPORTED = ("moe_workspace_size", "moe_route", "moe_forward", "moe_backward", "moe_gemm_bf16",
             "moe_get_device_status", "moe_status_string", "moe_profile_enable",
-            "moe_profile_read", "moe_launch_count", "moe_route_noalloc", "moe_gemm_mxfp8",
+            "moe_profile_read", "moe_profile_select", "moe_launch_count", "moe_route_noalloc",
+            "moe_gemm_mxfp8",
             "moe_backward_accumulate", "moe_prepared_weights_size", "moe_prepare_weights")
 
 
@@ -77,6 +78,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         "moe_get_device_status": [_vp, _vp],
         "moe_status_string": [_i32],
         "moe_profile_enable": [_i32],
+        "moe_profile_select": [ctypes.c_char_p],
         "moe_profile_read": [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(_i64),
                              ctypes.POINTER(ctypes.c_double), _i32],
         "moe_launch_count": [],
@@ -90,6 +92,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.moe_status_string.restype = ctypes.c_char_p
     lib.moe_launch_count.restype = _i64
     lib.moe_profile_enable.restype = None
+    lib.moe_profile_select.restype = None
     _lib = lib
     return lib
 
@@ -233,6 +236,12 @@ def moe_status_string(code: int) -> str:
 
 def moe_profile_enable(on: bool) -> None:
     load().moe_profile_enable(1 if on else 0)
+
+
+def moe_profile_select(name: Optional[str]) -> None:
+    """Times only the launches labelled `name` while profiling is enabled
+    (None: every launch)."""
+    load().moe_profile_select(None if name is None else name.encode())
 
 
 def moe_profile_read(cap: int = 64) -> Dict[str, Tuple[int, float]]:

@@ -127,3 +127,28 @@ def test_bench_records_ncu_traffic(tmp_path):
     assert got == {"gate_up_gemm_swiglu": (1e6 + 500 + 3e6 + 500) / 2, "gate_up_wgrad": 2001.0}
     stored = json.loads(out.read_text())
     assert stored["gate_up_wgrad@w"]["csrc_hash"] == bench.csrc_hash()
+
+
+def test_bench_times_the_dominant_kernel_live():
+    """The roofline object takes the dominant kernel's mean time from its
+    launches inside the timed region; the table keeps the profiled pass's
+    figure beside it.  Profiling switches need no GPU."""
+    import bench
+    from mixture_experts_layer_17_gb300 import libmoe
+    libmoe.moe_profile_select("gate_up_gemm_swiglu")
+    libmoe.moe_profile_select(None)
+    assert libmoe.moe_profile_read() == {}
+    sh = bench.si.shape("qwen3_235b")
+    peaks = {"hbm_gbs": 6759.2, "bf16_tflops": 1901.5, "bf16_tflops_sustained": 1728.6,
+             "source": "measured"}
+    clk = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0}
+    prof = {"gate_up_gemm_swiglu": (10, 23.0), "down_wgrad": (10, 11.0), "combine": (10, 1.8)}
+    assert bench.dominant_kernel(prof) == "gate_up_gemm_swiglu"
+    live = {"gate_up_gemm_swiglu": (20, 44.0)}
+    per_kernel, roof = bench.summarize_kernels(prof, sh, peaks, clk, live=live)
+    flops = bench.gemm_flops_all(sh)["gate_up_gemm_swiglu"]
+    assert roof["kernel"] == "gate_up_gemm_swiglu"
+    assert abs(roof["achieved"] - flops / 2.2e-3 / 1e12) < 1e-6 * roof["achieved"]
+    assert per_kernel["gate_up_gemm_swiglu"]["avg_ms"] == 2.2
+    assert per_kernel["gate_up_gemm_swiglu"]["avg_ms_profiled_pass"] == 2.3
+    assert "timing" in roof
