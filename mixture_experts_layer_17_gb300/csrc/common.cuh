@@ -186,6 +186,14 @@ MOE_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "mem
 // on their own, at the latest with the kernel).
 MOE_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
+// Programmatic dependent launch: the library launches every kernel with
+// programmatic stream serialization, so a kernel's CTAs may start while the
+// kernel before it in the stream drains.  Each kernel calls this before it
+// touches global memory that an earlier kernel writes or reads; it returns
+// once those kernels have completed and their writes are visible (at once
+// when the launch had no such attribute).
+MOE_DEV void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (tensor cores / TMA) before they read it.
 MOE_DEV void fence_proxy_async_smem() {

@@ -16,6 +16,7 @@ namespace {
 // out[c, r] = in[r, c] for a bf16 matrix [rows, cols]
 __global__ void transpose_bf16_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out,
                                       int rows, int cols) {
+  grid_dependency_wait();
   __shared__ uint16_t tile[32][33];
   const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
@@ -45,6 +46,7 @@ __global__ void scan_kernel(const int* __restrict__ hist, int ntiles, int E,
                             int* __restrict__ poff, int* __restrict__ block_base,
                             int* __restrict__ mtile_off, int* __restrict__ mtile2_off,
                             int* __restrict__ group_order) {
+  grid_dependency_wait();
   __shared__ int s_cnt[256];
   __shared__ int s_off[257];
   __shared__ int s_poff[257];
@@ -115,6 +117,7 @@ __global__ void permute_kernel(const int* __restrict__ idx, const float* __restr
                                int* __restrict__ slot_row, int* __restrict__ slot_pad,
                                int* __restrict__ row_slot, float* __restrict__ w_row,
                                DeviceStatus* st) {
+  grid_dependency_wait();
   __shared__ unsigned mask[4][256];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < 4 * 256; i += blockDim.x) (&mask[0][0])[i] = 0u;
@@ -159,6 +162,7 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ src, const int* 
                                    uint16_t* __restrict__ dst, int64_t T, int H, int k,
                                    const int* __restrict__ poff, const int* __restrict__ counts,
                                    unsigned token_blocks, int64_t Pa, DeviceStatus* st) {
+  grid_dependency_wait();
   if (blockIdx.x >= token_blocks) {
     const int e = static_cast<int>(blockIdx.x - token_blocks);
     const int64_t r0 = static_cast<int64_t>(__ldg(poff + e)) + __ldg(counts + e);
@@ -208,6 +212,7 @@ MOE_DEV void add_bf16x8(const uint4& v, float (&acc)[8], float scale = 1.0f) {
 // y[t] = sum_j scratch[t*k + j]; scratch rows already carry the router weight.
 __global__ void combine_kernel(const uint16_t* __restrict__ scratch, uint16_t* __restrict__ y,
                                int64_t T, int H, int k) {
+  grid_dependency_wait();
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int cpr = H >> 3;
   if (i >= T * cpr) return;
@@ -230,6 +235,7 @@ __global__ void router_bwd_kernel(const float* __restrict__ dw_part, int nparts,
                                   const int* __restrict__ idx, int64_t T, int k, int E, int64_t Pa,
                                   float* __restrict__ dl, uint16_t* __restrict__ dlT, int64_t T_pad,
                                   DeviceStatus* st) {
+  grid_dependency_wait();
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= T) return;
   float dwv[16], wv[16];
@@ -280,6 +286,7 @@ __global__ void __launch_bounds__(256) unpermute_kernel(
     const uint16_t* __restrict__ scratch, const float* __restrict__ dl,
     const int* __restrict__ idx, const uint16_t* __restrict__ WrT, uint16_t* __restrict__ dx,
     int64_t T, int H, int k, int E, DeviceStatus* st) {
+  grid_dependency_wait();
   extern __shared__ __align__(16) uint16_t wr_s[];   // [E][CW]
   constexpr int kChunks = CW / 8;                    // 16-byte chunks per row = lanes per token
   constexpr int kTokPerWarp = 32 / kChunks;
@@ -331,6 +338,7 @@ __global__ void __launch_bounds__(256) unpermute_kernel(
 template <bool kAccum>
 __global__ void wr_reduce_kernel(const float* __restrict__ part, int S, int E, int H,
                                  void* __restrict__ out) {
+  grid_dependency_wait();
   __shared__ float tile[32][33];
   const int h0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
@@ -362,26 +370,22 @@ inline unsigned blocks_for(int64_t n, int per) { return static_cast<unsigned>((n
 cudaError_t launch_transpose_bf16(const uint16_t* in, uint16_t* out, int rows, int cols,
                                   cudaStream_t s) {
   dim3 grid(blocks_for(cols, 32), blocks_for(rows, 32));
-  transpose_bf16_kernel<<<grid, dim3(32, 8), 0, s>>>(in, out, rows, cols);
-  return cudaGetLastError();
+  return launch_pdl(transpose_bf16_kernel, grid, dim3(32, 8), 0, s, in, out, rows, cols);
 }
 
 cudaError_t launch_scan(const int* hist, int ntiles, int E, int* counts, int* offsets,
                         int* poff, int* block_base, int* mtile_off, int* mtile2_off,
                         int* group_order, cudaStream_t s) {
-  scan_kernel<<<1, 256, 0, s>>>(hist, ntiles, E, counts, offsets, poff, block_base, mtile_off,
-                                mtile2_off, group_order);
-  return cudaGetLastError();
+  return launch_pdl(scan_kernel, dim3(1), dim3(256), 0, s, hist, ntiles, E, counts, offsets, poff,
+                    block_base, mtile_off, mtile2_off, group_order);
 }
 
 cudaError_t launch_permute(const int* idx, const float* w, const int* block_base,
                            const int* offsets, const int* poff, int64_t T, int k, int E,
                            int* perm_token, int* slot_row, int* slot_pad, int* row_slot,
                            float* w_row, DeviceStatus* st, cudaStream_t s) {
-  permute_kernel<<<blocks_for(T, 128), 128, 0, s>>>(idx, w, block_base, offsets, poff, T, k, E,
-                                                    perm_token, slot_row, slot_pad, row_slot,
-                                                    w_row, st);
-  return cudaGetLastError();
+  return launch_pdl(permute_kernel, dim3(blocks_for(T, 128)), dim3(128), 0, s, idx, w, block_base,
+                    offsets, poff, T, k, E, perm_token, slot_row, slot_pad, row_slot, w_row, st);
 }
 
 cudaError_t launch_gather_rows(const uint16_t* src, const int* slot_row, uint16_t* dst,
@@ -389,24 +393,22 @@ cudaError_t launch_gather_rows(const uint16_t* src, const int* slot_row, uint16_
                                int64_t Pa, DeviceStatus* st, cudaStream_t s) {
   const unsigned token_blocks = blocks_for(T, 8);
   if (token_blocks + E == 0) return cudaSuccess;
-  gather_rows_kernel<<<token_blocks + static_cast<unsigned>(E), 256, 0, s>>>(
-      src, slot_row, dst, T, H, k, poff, counts, token_blocks, Pa, st);
-  return cudaGetLastError();
+  return launch_pdl(gather_rows_kernel, dim3(token_blocks + static_cast<unsigned>(E)), dim3(256), 0,
+                    s, src, slot_row, dst, T, H, k, poff, counts, token_blocks, Pa, st);
 }
 
 cudaError_t launch_combine(const uint16_t* scratch, uint16_t* y, int64_t T, int H, int k,
                            cudaStream_t s) {
-  combine_kernel<<<blocks_for(T * (H / 8), 256), 256, 0, s>>>(scratch, y, T, H, k);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(blocks_for(T * (H / 8), 256)), dim3(256), 0, s, scratch, y,
+                    T, H, k);
 }
 
 cudaError_t launch_router_bwd(const float* dw_part, int nparts, const int* slot_row,
                               const float* w, const int* idx, int64_t T, int k, int E, int64_t Pa,
                               float* dl, uint16_t* dlT, int64_t T_pad, DeviceStatus* st,
                               cudaStream_t s) {
-  router_bwd_kernel<<<blocks_for(T, 128), 128, 0, s>>>(dw_part, nparts, slot_row, w, idx, T, k,
-                                                       E, Pa, dl, dlT, T_pad, st);
-  return cudaGetLastError();
+  return launch_pdl(router_bwd_kernel, dim3(blocks_for(T, 128)), dim3(128), 0, s, dw_part, nparts,
+                    slot_row, w, idx, T, k, E, Pa, dl, dlT, T_pad, st);
 }
 
 namespace {
@@ -437,9 +439,8 @@ cudaError_t launch_unpermute_cw(const uint16_t* scratch, const float* dl, const 
   const int64_t want = static_cast<int64_t>(std::max(per_sm[dev & 63], 1)) * (sms > 0 ? sms : 1) / slices;
   const int64_t groups = std::max<int64_t>(1, std::min<int64_t>(want, (T + tok_per_cta - 1) / tok_per_cta));
   dim3 grid(static_cast<unsigned>(slices), static_cast<unsigned>(groups));
-  unpermute_kernel<CW, KMAX><<<grid, 256, static_cast<size_t>(E) * CW * 2, s>>>(
-      scratch, dl, idx, WrT, dx, T, H, k, E, st);
-  return cudaGetLastError();
+  return launch_pdl(unpermute_kernel<CW, KMAX>, grid, dim3(256), static_cast<size_t>(E) * CW * 2, s,
+                    scratch, dl, idx, WrT, dx, T, H, k, E, st);
 }
 
 }  // namespace
@@ -461,10 +462,9 @@ cudaError_t launch_wr_reduce(const float* part, int S, int E, int H, void* dWr, 
                              cudaStream_t s) {
   dim3 grid(blocks_for(H, 32), blocks_for(E, 32));
   if (accum_f32)
-    wr_reduce_kernel<true><<<grid, dim3(32, 8), 0, s>>>(part, S, E, H, dWr);
+    return launch_pdl(wr_reduce_kernel<true>, grid, dim3(32, 8), 0, s, part, S, E, H, dWr);
   else
-    wr_reduce_kernel<false><<<grid, dim3(32, 8), 0, s>>>(part, S, E, H, dWr);
-  return cudaGetLastError();
+    return launch_pdl(wr_reduce_kernel<false>, grid, dim3(32, 8), 0, s, part, S, E, H, dWr);
 }
 
 }  // namespace moe

@@ -442,6 +442,9 @@ __global__ void __launch_bounds__(gemm_threads<P>(), 1) gemm_kernel(const __grid
   __syncthreads();
   if constexpr (kPair) cluster_sync();   // the peer's barriers are initialised
   tc_fence_after();
+  // the prologue above overlaps the previous kernel's tail; from here on
+  // global memory is read and written
+  grid_dependency_wait();
   const uint32_t tmem_base = *tmem_holder;
   const int num_tiles = P::num_tiles(args);
   const uint64_t limit = args.wait_limit_ns;

@@ -92,8 +92,29 @@ cudaError_t launch_unpermute(const uint16_t* scratch, const float* dl, const int
 cudaError_t launch_wr_reduce(const float* part, int S, int E, int H, void* dWr, bool accum_f32,
                              cudaStream_t s);
 
+// Launches `kernel` with programmatic stream serialization (see
+// grid_dependency_wait): it may start while the stream's previous kernel
+// drains, and waits for it in its first instructions.
+template <class... KArgs, class... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 // Launches gemm_kernel<P>, raising the dynamic shared-memory limit once per
-// device.
+// device; programmatic stream serialization as launch_pdl.
 template <class P>
 cudaError_t launch_gemm(const GemmArgs& a, int grid, cudaStream_t s) {
   constexpr size_t smem = gemm_smem_bytes<P>();
@@ -116,19 +137,21 @@ cudaError_t launch_gemm(const GemmArgs& a, int grid, cudaStream_t s) {
     cfg.blockDim = dim3(gemm_threads<P>());
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, gemm_kernel<P>, a);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   } else {
-    gemm_kernel<P><<<grid, gemm_threads<P>(), smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(gemm_kernel<P>, dim3(static_cast<unsigned>(grid)), dim3(gemm_threads<P>()),
+                      smem, s, a);
   }
 }
 

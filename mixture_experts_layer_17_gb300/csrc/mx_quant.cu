@@ -24,6 +24,7 @@ namespace {
 __global__ void quant_rows_kernel(const uint16_t* __restrict__ src, int64_t R, int C,
                                   uint8_t* __restrict__ dst, uint8_t* __restrict__ sf,
                                   uint8_t* __restrict__ sf192) {
+  grid_dependency_wait();
   const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= R) return;
   const int lane = threadIdx.x & 31;
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(
     const uint16_t* __restrict__ src0, const uint16_t* __restrict__ src1, int R, int C_in,
     uint8_t* __restrict__ dst, uint8_t* __restrict__ sf, const int* __restrict__ offsets,
     const int* __restrict__ counts, const int* __restrict__ mtile_off, int E) {
+  grid_dependency_wait();
   // One pass: the 128-row x 128-column bf16 tile is read once into shared
   // memory (coalesced 16-byte loads), each thread turns two (column, 32-row
   // block) units into a scale and 32 E4M3 bytes, and the E4M3 tile leaves
@@ -214,6 +216,7 @@ __global__ void __launch_bounds__(kColThreads) dispatch_quant_kernel(
     const int* __restrict__ offsets, const int* __restrict__ poff, const int* __restrict__ counts,
     const int* __restrict__ mtile_off, int E, int C, uint8_t* __restrict__ dst_t,
     uint8_t* __restrict__ sf_t, uint8_t* __restrict__ dst_r, uint8_t* __restrict__ sf_r) {
+  grid_dependency_wait();
   __shared__ __align__(16) uint16_t tile[128][128];
   __shared__ __align__(16) uint8_t qtile[128][128];
   const int kg = blockIdx.x;
@@ -296,33 +299,30 @@ __global__ void __launch_bounds__(kColThreads) dispatch_quant_kernel(
 cudaError_t launch_quant_rows_dense(const uint16_t* src, int64_t R, int C, uint8_t* dst,
                                     uint8_t* sf, cudaStream_t s, uint8_t* sf192) {
   if (sf192 != nullptr && R % 192 != 0) return cudaErrorInvalidValue;
-  quant_rows_kernel<<<static_cast<unsigned>((R + 7) / 8), 256, 0, s>>>(src, R, C, dst, sf, sf192);
-  return cudaGetLastError();
+  return launch_pdl(quant_rows_kernel, dim3(static_cast<unsigned>((R + 7) / 8)), dim3(256), 0, s,
+                    src, R, C, dst, sf, sf192);
 }
 
 cudaError_t launch_quant_cols_weights(const uint16_t* src, int E, int R, int C, uint8_t* dst,
                                       uint8_t* sf, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(E * (R / 128)), static_cast<unsigned>(C / 128));
-  quant_cols_kernel<kColsWeights><<<grid, kColThreads, 0, s>>>(src, nullptr, R, C, dst, sf, nullptr,
-                                                      nullptr, nullptr, E);
-  return cudaGetLastError();
+  return launch_pdl(quant_cols_kernel<kColsWeights>, grid, dim3(kColThreads), 0, s, src, nullptr, R,
+                    C, dst, sf, nullptr, nullptr, nullptr, E);
 }
 
 cudaError_t launch_quant_cols_gate_up(const uint16_t* W_gate, const uint16_t* W_up, int E, int H,
                                       int F, uint8_t* dst, uint8_t* sf, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(E * (H / 128)), static_cast<unsigned>(2 * F / 128));
-  quant_cols_kernel<kColsGateUp><<<grid, kColThreads, 0, s>>>(W_gate, W_up, H, F, dst, sf, nullptr,
-                                                     nullptr, nullptr, E);
-  return cudaGetLastError();
+  return launch_pdl(quant_cols_kernel<kColsGateUp>, grid, dim3(kColThreads), 0, s, W_gate, W_up, H,
+                    F, dst, sf, nullptr, nullptr, nullptr, E);
 }
 
 cudaError_t launch_quant_cols_tokens(const uint16_t* src, int64_t max_ktiles, int C, uint8_t* dst,
                                      uint8_t* sf, const int* poff, const int* counts,
                                      const int* mtile_off, int E, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(max_ktiles), static_cast<unsigned>(C / 128));
-  quant_cols_kernel<kColsTokens><<<grid, kColThreads, 0, s>>>(src, nullptr, 0, C, dst, sf, poff, counts,
-                                                     mtile_off, E);
-  return cudaGetLastError();
+  return launch_pdl(quant_cols_kernel<kColsTokens>, grid, dim3(kColThreads), 0, s, src, nullptr, 0,
+                    C, dst, sf, poff, counts, mtile_off, E);
 }
 
 cudaError_t launch_dispatch_quant(const uint16_t* src, const int* perm_token, const int* offsets,
@@ -330,9 +330,8 @@ cudaError_t launch_dispatch_quant(const uint16_t* src, const int* perm_token, co
                                   int64_t max_ktiles, int E, int C, uint8_t* dst_t, uint8_t* sf_t,
                                   uint8_t* dst_r, uint8_t* sf_r, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(max_ktiles), static_cast<unsigned>(C / 128));
-  dispatch_quant_kernel<<<grid, kColThreads, 0, s>>>(src, perm_token, offsets, poff, counts,
-                                                      mtile_off, E, C, dst_t, sf_t, dst_r, sf_r);
-  return cudaGetLastError();
+  return launch_pdl(dispatch_quant_kernel, grid, dim3(kColThreads), 0, s, src, perm_token, offsets,
+                    poff, counts, mtile_off, E, C, dst_t, sf_t, dst_r, sf_r);
 }
 
 }  // namespace moe
