@@ -78,6 +78,8 @@ MX_SHAPES = [
     (200, 256, 128, 4, 1, 53),      # top-1
     (1, 256, 256, 4, 2, 55),        # a single token
     (1100, 256, 768, 6, 2, 57),     # F = 4 x 192: the down dgrad's 256 x 192 pair tiles
+    (1, 256, 384, 4, 2, 58),        # a single token on 256 x 192 pair tiles (pairs mode)
+    (200, 256, 384, 4, 1, 59),      # top-1 on 256 x 192 pair tiles (pairs mode)
 ]
 
 
